@@ -40,8 +40,9 @@ Readings taken where the pages are silent (each is listed in the design notes):
 7. A segment is invalid (skipped; its rows count as uncovered; a status bit is set) when
    q_len < 0, q_start < 0, q_start + q_len > T, col outside [0, cols), kv_end < 0, or
    when the keys its rows see span more than `rows` store rows (a ring would already
-   have overwritten one of them).  Rows that two valid segments both cover set the
-   overlap bit, and their output is unspecified.
+   have overwritten one of them).  When two valid segments cover a common row, both
+   are overlapping: the overlap bit is set and every row of either segment has an
+   unspecified output.
 
 The arithmetic is fp64 from the exact upcast of the bf16 inputs.
 """
@@ -127,27 +128,40 @@ def visible_interval(seq_info, T: int, causal: bool, window: int, rows: int, col
     """Per packed row: (segment id, lo, hi, status).
 
     seg_id[t] is the index of the valid segment covering row t, UNCOVERED when none
-    does and OVERLAPPED when two or more do.  lo/hi are the row's visible positions
-    (hi <= lo: empty); both are 0 for uncovered and overlapped rows.  status is the OR
-    of every segment's bits plus SEG_OVERLAP.
+    does and OVERLAPPED when t belongs to a segment that shares a row with another
+    valid segment (reading 7).  lo/hi are the row's visible positions (hi <= lo:
+    empty); both are 0 for uncovered and overlapped rows.  status is the OR of every
+    segment's bits plus SEG_OVERLAP.
     """
     seq_info = np.asarray(seq_info, dtype=np.int64).reshape(-1, 4)
     seg_id = np.full(T, UNCOVERED, dtype=np.int64)
     lo = np.zeros(T, dtype=np.int64)
     hi = np.zeros(T, dtype=np.int64)
     status = 0
+    owners = [[] for _ in range(T)]
+    valid = []
     for s, seg in enumerate(seq_info):
         bits = segment_status(seg, T, rows, cols, window)
         status |= bits
         if bits:
             continue
-        q_start, q_len, _, kv_end = (int(x) for x in seg)
+        valid.append(s)
+        q_start, q_len = int(seg[0]), int(seg[1])
+        for t in range(q_start, q_start + q_len):
+            owners[t].append(s)
+    overlapping = set()
+    for t in range(T):
+        if len(owners[t]) > 1:
+            overlapping.update(owners[t])
+    if overlapping:
+        status |= SEG_OVERLAP
+    for s in valid:
+        q_start, q_len, _, kv_end = (int(x) for x in seq_info[s])
         for i in range(q_len):
             t = q_start + i
-            if seg_id[t] != UNCOVERED:
+            if s in overlapping:
                 seg_id[t] = OVERLAPPED
                 lo[t] = hi[t] = 0
-                status |= SEG_OVERLAP
                 continue
             seg_id[t] = s
             lo[t], hi[t] = row_interval(i, q_len, kv_end, causal, window)

@@ -74,10 +74,13 @@ def brute_force(q, K, V, seq_info, causal, W, scale):
             continue
         for i in range(ql):
             owners[qs + i].append(s)
+    overlapping = set()
     for t in range(T):
         if len(owners[t]) > 1:
             status |= 16
-        if len(owners[t]) != 1:
+            overlapping.update(owners[t])
+    for t in range(T):
+        if len(owners[t]) != 1 or owners[t][0] in overlapping:
             continue
         qs, ql, col, ke = seq_info[owners[t][0]]
         p = ke - ql + (t - qs)
@@ -138,8 +141,9 @@ def test_oracle_matches_brute_force_on_tiny_grid(causal, W):
         out, seg_id, status = O.sdpa_varlen(q, K, V, np.array(segs), causal, W, 0.7)
         ref, owners, ref_status = brute_force(q.tolist(), K.tolist(), V.tolist(), segs, causal, W, 0.7)
         assert status == ref_status, (segs, rows, W)
+        overlapping = {s for t in range(T) if len(owners[t]) > 1 for s in owners[t]}
         for t in range(T):
-            if len(owners[t]) > 1:
+            if any(s in overlapping for s in owners[t]):
                 assert seg_id[t] == O.OVERLAPPED
                 continue  # unspecified output
             np.testing.assert_allclose(out[t], np.array(ref[t]), rtol=1e-12, atol=1e-12,
@@ -402,7 +406,7 @@ def _grid_disagrees(monkeypatch_ctx=None):
         if status != ref_status:
             return True
         for t in range(8):
-            if len(owners[t]) == 1 and not np.allclose(out[t], ref[t], rtol=1e-12, atol=1e-12):
+            if seg_id[t] >= 0 and not np.allclose(out[t], ref[t], rtol=1e-12, atol=1e-12):
                 return True
     return False
 
@@ -435,3 +439,14 @@ def test_planted_causal_drop_is_caught(monkeypatch):
     real = O.row_interval
     monkeypatch.setattr(O, "row_interval", lambda i, ql, ke, c, w: real(i, ql, ke, False, w))
     assert _grid_disagrees()
+
+
+def test_overlapping_segments_make_all_their_rows_unspecified():
+    q = np.ones((8, 1, 2))
+    k = np.zeros((4, 2, 1, 2))
+    v = np.ones((4, 2, 1, 2))
+    seq = np.array([[0, 3, 0, 3], [2, 2, 1, 2], [5, 2, 0, 2]])  # first two share row 2
+    out, seg_id, status = O.sdpa_varlen(q, k, v, seq, True, 0, 1.0)
+    assert status == O.SEG_OVERLAP
+    assert list(seg_id) == [-2, -2, -2, -2, -1, 2, 2, -1]
+    assert np.all(out[5:7] == 1.0) and np.all(out[4] == 0) and np.all(out[7] == 0)

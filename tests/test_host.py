@@ -1,0 +1,105 @@
+"""Host-side checks that need no GPU: the library builds/loads, exports every symbol the
+header declares, and rejects bad arguments before making any CUDA call.
+
+Only argument errors that the C interface detects ahead of any CUDA call are exercised
+here (the pointers are fake but never dereferenced); nothing launches a kernel.
+"""
+
+import os
+import re
+
+import pytest
+
+import varlen_gqa_attention_gb300 as pkg
+from varlen_gqa_attention_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "sdpa_varlen.h")
+
+FAKE = 0x10000  # 16-byte aligned, never dereferenced
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(sdpa_[a-z_]+)\s*\(", text)))
+
+
+def test_library_builds_in_tree_and_loads():
+    path = _build.build()
+    assert os.path.exists(path)
+    assert os.path.commonpath([path, ROOT]) == ROOT
+    lib = pkg.library()
+    assert lib.sdpa_version() == 100
+
+
+def test_every_declared_symbol_is_exported():
+    lib = pkg.library()
+    names = _declared_functions()
+    assert set(names) >= {"sdpa_varlen", "sdpa_causal_prefill", "sdpa_varlen_workspace_bytes",
+                          "sdpa_last_error", "sdpa_set_route_policy", "sdpa_version"}
+    for n in names:
+        assert hasattr(lib, n), n
+    assert sorted(pkg.EXPORTS) == sorted(names)
+
+
+def test_status_bits_match_the_oracle_constants():
+    from oracle import sdpa_varlen_oracle as O
+
+    assert (pkg.SEG_BAD_QRANGE, pkg.SEG_BAD_COL, pkg.SEG_BAD_KV, pkg.SEG_SPAN, pkg.SEG_OVERLAP) == \
+        (O.SEG_BAD_QRANGE, O.SEG_BAD_COL, O.SEG_BAD_KV, O.SEG_SPAN, O.SEG_OVERLAP)
+    text = open(HEADER).read()
+    for name, val in (("SDPA_SEG_BAD_QRANGE", 1), ("SDPA_SEG_BAD_COL", 2), ("SDPA_SEG_BAD_KV", 4),
+                      ("SDPA_SEG_SPAN", 8), ("SDPA_SEG_OVERLAP", 16), ("SDPA_DEV_TIMEOUT", 32)):
+        assert re.search(rf"#define {name} {val}\b", text), name
+
+
+def _call(**kw):
+    a = dict(q=FAKE, T=8, Hq=4, D=64, q_rs=256, q_hs=64, k=FAKE, v=FAKE, rows=16, cols=2, Hkv=2,
+             seq=FAKE, S=1, causal=1, window=0, scale=0.125, out=FAKE, o_rs=256, o_hs=64, ws=FAKE,
+             ws_bytes=1 << 30, status=None, stream=None)
+    a.update(kw)
+    lib = pkg.library()
+    code = lib.sdpa_varlen(a["q"], a["T"], a["Hq"], a["D"], a["q_rs"], a["q_hs"], a["k"], a["v"],
+                           a["rows"], a["cols"], a["Hkv"], a["seq"], a["S"], a["causal"], a["window"],
+                           a["scale"], a["out"], a["o_rs"], a["o_hs"], a["ws"], a["ws_bytes"],
+                           a["status"], a["stream"])
+    return code, lib.sdpa_last_error().decode()
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(D=96), 3), (dict(D=0), 3), (dict(Hq=6, Hkv=4), 4), (dict(Hq=256, Hkv=1), 4),
+    (dict(T=-1), 2), (dict(S=-1), 2), (dict(rows=0), 2), (dict(cols=0), 2), (dict(Hkv=0), 2),
+    (dict(window=-3), 8), (dict(scale=float("inf")), 8), (dict(scale=float("nan")), 8),
+    (dict(q=None), 1), (dict(out=None), 1), (dict(seq=None), 1), (dict(ws=None), 7),
+    (dict(q=FAKE + 2), 6), (dict(out=FAKE + 8), 6), (dict(q_rs=250), 5), (dict(o_hs=3), 5),
+    (dict(ws=FAKE + 16), 6),
+])
+def test_bad_arguments_are_rejected_before_any_cuda_call(kw, code):
+    got, msg = _call(**kw)
+    assert got == code, msg
+    assert msg
+
+
+def test_route_policy_is_checked():
+    lib = pkg.library()
+    assert lib.sdpa_set_route_policy(7) == 8
+    assert lib.sdpa_set_route_policy(0) == 0
+
+
+def test_workspace_query_depends_only_on_sizes():
+    a = pkg.workspace_bytes(4096, 16, 2, 128, 1)
+    b = pkg.workspace_bytes(4096, 16, 2, 128, 1)
+    assert a == b and a > 0 and a % 256 == 0
+    assert pkg.workspace_bytes(8192, 16, 2, 128, 1) > a
+    assert pkg.workspace_bytes(16, 16, 3, 128, 1) == 0  # Hq % Hkv != 0
+    assert pkg.workspace_bytes(16, 16, 2, 80, 1) == 0
+
+
+def test_product_path_does_not_import_the_oracle():
+    src_dir = os.path.join(ROOT, "varlen_gqa_attention_gb300")
+    for dirpath, _, files in os.walk(src_dir):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "oracle" not in text.lower().replace("oracles", ""), f

@@ -1,0 +1,226 @@
+"""GPU parity: the CUDA library (through the C interface) against the CPU oracle.
+
+Every test runs on cuda:0 and compares element by element with the fp64 oracle on the same
+seeded inputs (tolerances in tests/parity.py).  Both kernels are checked on every case by
+forcing each route (the auto route sends long segments to the prefill kernel).
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import varlen_gqa_attention_gb300 as pkg
+from oracle import sdpa_varlen_oracle as O
+from workloads import synth
+
+from parity import (assert_matches, check_call, decode_probe, oracle, poison_invisible, probe_call,
+                    run_call)
+
+pytestmark = pytest.mark.gpu
+
+ROUTES = [pkg.ROUTE_AUTO, pkg.ROUTE_SPLITK, pkg.ROUTE_PREFILL]
+
+
+@pytest.fixture(scope="module")
+def dev():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    d = torch.device("cuda:0")
+    torch.cuda.set_device(d)
+    return d
+
+
+@pytest.fixture(params=ROUTES, ids=["auto", "splitk", "prefill"])
+def route(request):
+    pkg.set_route_policy(request.param)
+    yield request.param
+    pkg.set_route_policy(pkg.ROUTE_AUTO)
+
+
+def test_native_library_is_loaded(dev):
+    lib = pkg.library()
+    import varlen_gqa_attention_gb300._build as b
+    maps = open("/proc/self/maps").read()
+    assert b.lib_path() in maps
+    assert lib.sdpa_version() == 100
+
+
+def test_tiny_causal_prefill(dev, route):
+    call = synth.tiny_causal_prefill(seed=0).calls[0]
+    check_call(call, dev, tag="tiny")
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_d64_long_prefill_full(dev, route, seed):
+    call = synth.long_causal_prefill(64, 512, 16384, seed=seed).calls[0]
+    check_call(call, dev, tag=f"d64 seed {seed}")
+
+
+def test_d128_long_prefill_sampled_rows(dev, route):
+    call = synth.long_causal_prefill(128, 4096, 131072, seed=0).calls[0]
+    rows = sorted(set([0, 1, 15, 16, 17, 127, 128, 2047, 2048, 4094, 4095] +
+                      list(np.random.default_rng(0).integers(0, 4096, 20))))
+    check_call(call, dev, rows_subset=rows, tag="d128 sampled")
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_batched_decode_full(dev, route, seed):
+    call = synth.batched_decode(seed=seed).calls[0]
+    check_call(call, dev, tag=f"decode seed {seed}")
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_mixed_step_full(dev, route, seed):
+    wl = synth.mixed_step(seed=seed)
+    T = wl.calls[-1].row_end
+    out = torch.full((T, 32, 128), float("nan"), dtype=torch.bfloat16, device=dev)
+    for c in wl.calls:
+        run_call(c, dev, out=out[c.row_begin:c.row_end])  # each call owns its half
+    torch.cuda.synchronize()
+    for c in wl.calls:
+        ref, seg_id, _ = oracle(c)
+        _, lo, hi, _ = O.visible_interval(c.seq_info, c.T, c.causal, c.window, c.rows, c.cols)
+        assert_matches(out[c.row_begin:c.row_end], ref, seg_id, lo, hi, tag=f"mixed causal={c.causal}")
+
+
+@pytest.mark.parametrize("D", [64, 128, 256])
+@pytest.mark.parametrize("causal,window", [(True, 0), (False, 0), (True, 5), (False, 7), (True, 1)])
+def test_random_tables(dev, route, D, causal, window):
+    rng = np.random.default_rng(D * 100 + window * 3 + int(causal))
+    for trial, (Hq, Hkv) in enumerate([(4, 1), (8, 2), (6, 3), (16, 16)]):
+        rows = int(rng.choice([40, 97, 300]))
+        call = synth.random_call(rng, D=D, Hq=Hq, Hkv=Hkv, T=80, S=6, rows=rows, cols=3,
+                                 causal=causal, window=window, max_q=24, max_kv=320,
+                                 gen_seed=trial + 10 * D)
+        check_call(call, dev, tag=f"D{D} Hq{Hq}/{Hkv} {causal} W{window} rows{rows}")
+
+
+def test_ring_store_long_window(dev, route):
+    # causal window 300 on a 315-row ring (window + max_write - 1), long positions
+    rng = np.random.default_rng(5)
+    call = synth.random_call(rng, D=128, Hq=8, Hkv=2, T=64, S=4, rows=315, cols=5, causal=True,
+                             window=300, max_q=16, max_kv=5000, gen_seed=3)
+    check_call(call, dev, tag="ring")
+
+
+def test_invalid_segments_set_status_and_zero_rows(dev, route):
+    call = synth.random_call(np.random.default_rng(9), D=64, Hq=4, Hkv=2, T=40, S=2, rows=64, cols=2,
+                             causal=True, window=0, max_q=8, max_kv=60, gen_seed=4, allow_gaps=False)
+    bad = np.array([[0, 5, 0, 20],      # valid
+                    [5, 3, 2, 10],      # bad column
+                    [8, -1, 0, 3],      # negative q_len
+                    [9, 4, 1, 65],      # kv_end beyond the 64 rows, no window
+                    [13, 4, 1, -2],     # negative kv_end
+                    [17, 30, 0, 10],    # q range beyond T
+                    [20, 3, 1, 12],     # valid
+                    [22, 2, 0, 5]],     # overlaps the previous one
+                   dtype=np.int32)
+    call.seq_info = bad
+    check_call(call, dev, tag="invalid")
+
+
+def test_nan_in_invisible_cells_changes_no_output_bit(dev, route):
+    wl = synth.batched_decode(seed=1, S=8, rows=2048)
+    call = wl.calls[0]
+    clean = run_call(call, dev).clone()
+    k, v = poison_invisible(call)
+    dirty = run_call(call, dev, k=k.to(dev), v=v.to(dev))
+    torch.cuda.synchronize()
+    assert torch.equal(clean.view(torch.int16), dirty.view(torch.int16))
+    rng = np.random.default_rng(3)
+    call = synth.random_call(rng, D=128, Hq=8, Hkv=2, T=64, S=4, rows=200, cols=5, causal=True,
+                             window=60, max_q=16, max_kv=900, gen_seed=3)
+    clean = run_call(call, dev).clone()
+    k, v = poison_invisible(call)
+    dirty = run_call(call, dev, k=k.to(dev), v=v.to(dev))
+    torch.cuda.synchronize()
+    assert torch.equal(clean.view(torch.int16), dirty.view(torch.int16))
+
+
+@pytest.mark.parametrize("causal,window,rows", [(True, 0, 5000), (True, 37, 52), (False, 0, 5000),
+                                                (False, 23, 40), (True, 200, 215)])
+def test_index_sets_are_bit_exact(dev, route, causal, window, rows):
+    rng = np.random.default_rng(rows + window)
+    max_q = min(40, rows - window + 1) if window else 40
+    call = synth.random_call(rng, D=64, Hq=8, Hkv=2, T=200, S=8, rows=rows, cols=4, causal=causal,
+                             window=window, max_q=max_q, max_kv=min(4000, 3 * rows), gen_seed=1)
+    call.scale = 64.0
+    seg_id, lo, hi, _ = O.visible_interval(call.seq_info, call.T, causal, window, rows, call.cols)
+    for sign in (+1, -1):
+        q, k = probe_call(call, sign)
+        out = run_call(call, dev, q=q.to(dev), k=k.to(dev), v=k.to(dev))
+        torch.cuda.synchronize()
+        got = decode_probe(out)
+        for t in range(call.T):
+            if seg_id[t] == O.UNCOVERED or (seg_id[t] >= 0 and hi[t] <= lo[t]):
+                assert bool((out[t].view(torch.int16) == 0).all()), t
+            elif seg_id[t] >= 0:
+                want = hi[t] - 1 if sign > 0 else lo[t]
+                assert np.all(got[t] == want), (t, sign, got[t], lo[t], hi[t])
+
+
+def test_graph_replay_with_new_lengths(dev, route):
+    T, Hq, Hkv, D, rows, cols, S = 64, 8, 2, 128, 1024, 5, 4
+    rng = np.random.default_rng(11)
+    base = synth.random_call(rng, D=D, Hq=Hq, Hkv=Hkv, T=T, S=S, rows=rows, cols=cols, causal=True,
+                             window=0, max_q=16, max_kv=rows, gen_seed=5)
+    q, k, v = base.q.to(dev), base.k_store.to(dev), base.v_store.to(dev)
+    seq = torch.zeros((S, 4), dtype=torch.int32, device=dev)
+    out = torch.empty((T, Hq, D), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(pkg.workspace_bytes(T, Hq, Hkv, D, S), dtype=torch.uint8, device=dev)
+    seq.copy_(torch.from_numpy(base.seq_info))
+    pkg.sdpa_varlen(q, k, v, seq, causal=True, scale=base.scale, out=out, workspace=ws)  # warm
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        pkg.sdpa_varlen(q, k, v, seq, causal=True, scale=base.scale, out=out, workspace=ws)
+    tables = [
+        np.array([[0, 16, 0, 1000], [16, 1, 1, 5], [20, 9, 2, 9], [40, 3, 4, 3]]),
+        np.array([[3, 1, 3, 1], [4, 0, 0, 0], [10, 16, 1, 700], [30, 12, 0, 12]]),
+        np.array([[0, 8, 4, 1024], [8, 8, 3, 512], [16, 8, 2, 256], [24, 8, 1, 8]]),
+    ]
+    for tab in tables:
+        seq.copy_(torch.from_numpy(tab.astype(np.int32)))
+        out.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        ref, seg_id, _ = O.sdpa_varlen(base.q, base.k_store, base.v_store, tab, True, 0, base.scale)
+        _, lo, hi, _ = O.visible_interval(tab, T, True, 0, rows, cols)
+        assert_matches(out, ref, seg_id, lo, hi, tag=f"replay {tab[:, 1]}")
+
+
+def test_dense_entry_equals_one_segment_call(dev):
+    call = synth.long_causal_prefill(128, 300, 2000, seed=2).calls[0]
+    q, k, v = call.q.to(dev), call.k_store.to(dev), call.v_store.to(dev)
+    a = pkg.sdpa_causal_prefill(q, k[:, 0].contiguous(), v[:, 0].contiguous(), call.scale)
+    b = run_call(call, dev, q=q, k=k, v=v)
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    ref = O.sdpa_causal_prefill(call.q, call.k_store[:, 0], call.v_store[:, 0], call.scale)
+    err = np.abs(a.double().cpu().numpy() - ref)
+    assert err.max() <= 2e-2 and err.mean() <= 2e-3
+
+
+def test_strided_q_and_out(dev, route):
+    call = synth.random_call(np.random.default_rng(4), D=128, Hq=8, Hkv=4, T=48, S=3, rows=256,
+                             cols=3, causal=True, window=0, max_q=16, max_kv=256, gen_seed=8)
+    big = torch.zeros((48, 8, 3 * 128), dtype=torch.bfloat16, device=dev)
+    big[:, :, 128:256] = call.q.to(dev)
+    q = big[:, :, 128:256]
+    ob = torch.zeros((48, 10, 128), dtype=torch.bfloat16, device=dev)
+    out = ob[:, 1:9]
+    run_call(call, dev, q=q, out=out)
+    torch.cuda.synchronize()
+    ref, seg_id, _ = oracle(call)
+    _, lo, hi, _ = O.visible_interval(call.seq_info, call.T, True, 0, call.rows, call.cols)
+    assert_matches(out, ref, seg_id, lo, hi, tag="strided")
+    assert bool((ob[:, 0].view(torch.int16) == 0).all()) and bool((ob[:, 9].view(torch.int16) == 0).all())
+
+
+def test_empty_step_and_zero_segments(dev):
+    call = synth.random_call(np.random.default_rng(1), D=64, Hq=4, Hkv=1, T=16, S=1, rows=32, cols=1,
+                             causal=True, window=0, max_q=4, max_kv=32, gen_seed=1)
+    call.seq_info = np.zeros((0, 4), dtype=np.int32)
+    out = run_call(call, dev)
+    torch.cuda.synchronize()
+    assert bool((out.view(torch.int16) == 0).all())

@@ -1,0 +1,173 @@
+"""Length-aware GQA attention over a per-sequence KV column store, for GB300 (sm_103a).
+
+A thin ctypes binding over ``libsdpa_varlen.so`` (C interface in include/sdpa_varlen.h):
+it only checks tensor dtypes/devices, reads strides and pointers, allocates outputs and
+workspace with torch, and passes the current CUDA stream.  Every step of the computation
+runs in the library's CUDA kernels; there is no other implementation to fall back on, so a
+missing library is an error.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from typing import Optional
+
+import torch
+
+from . import _build
+
+__all__ = [
+    "sdpa_varlen", "sdpa_causal_prefill", "workspace_bytes", "set_route_policy", "library",
+    "SDPA_OK", "SEG_BAD_QRANGE", "SEG_BAD_COL", "SEG_BAD_KV", "SEG_SPAN", "SEG_OVERLAP",
+    "DEV_TIMEOUT", "ROUTE_AUTO", "ROUTE_SPLITK", "ROUTE_PREFILL", "SdpaError",
+]
+
+SDPA_OK = 0
+SEG_BAD_QRANGE, SEG_BAD_COL, SEG_BAD_KV, SEG_SPAN, SEG_OVERLAP, DEV_TIMEOUT = 1, 2, 4, 8, 16, 32
+ROUTE_AUTO, ROUTE_SPLITK, ROUTE_PREFILL = 0, 1, 2
+
+STATUS_NAMES = {
+    0: "SDPA_OK", 1: "SDPA_ERR_NULL", 2: "SDPA_ERR_SHAPE", 3: "SDPA_ERR_HEAD_DIM", 4: "SDPA_ERR_GQA",
+    5: "SDPA_ERR_STRIDE", 6: "SDPA_ERR_ALIGN", 7: "SDPA_ERR_WORKSPACE", 8: "SDPA_ERR_ARG",
+    9: "SDPA_ERR_CUDA",
+}
+
+EXPORTS = [
+    "sdpa_varlen_workspace_bytes", "sdpa_varlen", "sdpa_causal_prefill", "sdpa_set_route_policy",
+    "sdpa_last_error", "sdpa_version",
+]
+
+
+class SdpaError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(f"{STATUS_NAMES.get(code, code)}: {msg}")
+        self.code = code
+
+
+_lib: Optional[ctypes.CDLL] = None
+
+
+def library(build_if_missing: bool = True) -> ctypes.CDLL:
+    """Load libsdpa_varlen.so (building it first when it is missing)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = _build.lib_path()
+    if not os.path.exists(path):
+        if not build_if_missing:
+            raise ImportError(f"{path} is missing; run __graft_entry__.build()")
+        _build.build()
+    lib = ctypes.CDLL(path)
+    c_i64, c_int, c_vp, c_f = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_float
+    lib.sdpa_varlen_workspace_bytes.restype = ctypes.c_size_t
+    lib.sdpa_varlen_workspace_bytes.argtypes = [c_i64, c_int, c_int, c_int, c_int]
+    lib.sdpa_varlen.restype = c_int
+    lib.sdpa_varlen.argtypes = [c_vp, c_i64, c_int, c_int, c_i64, c_i64, c_vp, c_vp, c_i64, c_int,
+                                c_int, c_vp, c_int, c_int, c_int, c_f, c_vp, c_i64, c_i64, c_vp,
+                                ctypes.c_size_t, c_vp, c_vp]
+    lib.sdpa_causal_prefill.restype = c_int
+    lib.sdpa_causal_prefill.argtypes = [c_vp, c_vp, c_vp, c_i64, c_i64, c_int, c_int, c_int, c_f,
+                                        c_vp, c_vp, ctypes.c_size_t, c_vp]
+    lib.sdpa_set_route_policy.restype = c_int
+    lib.sdpa_set_route_policy.argtypes = [c_int]
+    lib.sdpa_last_error.restype = ctypes.c_char_p
+    lib.sdpa_last_error.argtypes = []
+    lib.sdpa_version.restype = c_int
+    lib.sdpa_version.argtypes = []
+    _lib = lib
+    return lib
+
+
+def _check(code: int):
+    if code != SDPA_OK:
+        raise SdpaError(code, library().sdpa_last_error().decode())
+
+
+def workspace_bytes(T: int, Hq: int, Hkv: int, D: int, S: int) -> int:
+    return int(library().sdpa_varlen_workspace_bytes(T, Hq, Hkv, D, S))
+
+
+def set_route_policy(policy: int) -> None:
+    _check(library().sdpa_set_route_policy(policy))
+
+
+def _workspace(nbytes: int, device) -> torch.Tensor:
+    return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+
+
+def _stream_ptr(stream) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def sdpa_varlen(q: torch.Tensor, k_store: torch.Tensor, v_store: torch.Tensor, seq_info: torch.Tensor,
+                *, causal: bool, window: int = 0, scale: Optional[float] = None,
+                out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                status: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """out[T, Hq, D] = length-aware GQA attention of q over the column stores.
+
+    q: bf16 [T, Hq, D] (inner stride 1); k_store, v_store: bf16 [rows, cols, Hkv, D]
+    contiguous; seq_info: int32 [S, 4] contiguous on the same device.  ``status`` (an int32
+    device tensor, optional) receives the OR of the device status bits.
+    """
+    lib = library()
+    if q.dim() != 3 or k_store.dim() != 4 or tuple(v_store.shape) != tuple(k_store.shape):
+        raise ValueError("q must be [T, Hq, D] and the stores [rows, cols, Hkv, D]")
+    for name, t in (("q", q), ("k_store", k_store), ("v_store", v_store)):
+        if t.dtype != torch.bfloat16 or not t.is_cuda:
+            raise ValueError(f"{name} must be a bf16 CUDA tensor")
+    if not (k_store.is_contiguous() and v_store.is_contiguous()):
+        raise ValueError("k_store and v_store must be contiguous")
+    if seq_info.dtype != torch.int32 or not seq_info.is_cuda or not seq_info.is_contiguous():
+        raise ValueError("seq_info must be a contiguous int32 CUDA tensor")
+    T, Hq, D = q.shape
+    rows, cols, Hkv, Dk = k_store.shape
+    if Dk != D:
+        raise ValueError("head dims of q and the stores differ")
+    if q.stride(2) != 1:
+        raise ValueError("q must have unit inner stride")
+    S = seq_info.shape[0] if seq_info.numel() else 0
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty((T, Hq, D), dtype=torch.bfloat16, device=q.device)
+    elif out.dtype != torch.bfloat16 or tuple(out.shape) != (T, Hq, D) or out.stride(2) != 1:
+        raise ValueError("out must be bf16 [T, Hq, D] with unit inner stride")
+    need = workspace_bytes(T, Hq, Hkv, D, S)
+    if workspace is None:
+        workspace = _workspace(need, q.device)
+    st_ptr = status.data_ptr() if status is not None else None
+    code = lib.sdpa_varlen(q.data_ptr(), T, Hq, D, q.stride(0), q.stride(1), k_store.data_ptr(),
+                           v_store.data_ptr(), rows, cols, Hkv, seq_info.data_ptr() if S else None,
+                           S, int(bool(causal)), int(window), float(scale), out.data_ptr(),
+                           out.stride(0), out.stride(1), workspace.data_ptr(), workspace.numel(),
+                           st_ptr, _stream_ptr(stream))
+    _check(code)
+    return out
+
+
+def sdpa_causal_prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: Optional[float] = None,
+                        *, out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                        stream=None) -> torch.Tensor:
+    """Dense causal GQA attention: q [Lq, Hq, D] against k, v [Lkv, Hkv, D], queries being
+    the last Lq positions.  All tensors contiguous bf16 on one CUDA device."""
+    lib = library()
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous() or t.dim() != 3:
+            raise ValueError(f"{name} must be a contiguous 3-d bf16 CUDA tensor")
+    Lq, Hq, D = q.shape
+    Lkv, Hkv, _ = k.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q)
+    need = workspace_bytes(Lq, Hq, Hkv, D, 1)
+    if workspace is None:
+        workspace = _workspace(need, q.device)
+    code = lib.sdpa_causal_prefill(q.data_ptr(), k.data_ptr(), v.data_ptr(), Lq, Lkv, Hq, Hkv, D,
+                                   float(scale), out.data_ptr(), workspace.data_ptr(),
+                                   workspace.numel(), _stream_ptr(stream))
+    _check(code)
+    return out

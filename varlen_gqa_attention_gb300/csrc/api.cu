@@ -1,0 +1,242 @@
+// api.cu - the C interface: argument checks, workspace layout, launches.
+//
+// Every check runs before any CUDA call, so a bad argument never touches the device.  The
+// launches are asynchronous and allocation-free, so a call can be captured in a CUDA graph;
+// the device scheduler reads the segment table when the graph replays.
+#include <atomic>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <mutex>
+
+#include "common.cuh"
+
+namespace sdpa {
+
+static thread_local char g_err[512] = "";
+static std::atomic<int> g_policy{SDPA_ROUTE_AUTO};
+
+static sdpa_status fail(sdpa_status code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+static bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+// Per-device launch facts, measured once.
+struct DevInfo {
+  bool ready = false;
+  int sms = 0;
+  int splitk_per_sm[3] = {0, 0, 0};  // D = 64, 128, 256
+};
+static std::mutex g_mu;
+static DevInfo g_dev[64];
+
+static int d_index(int D) { return D == 64 ? 0 : D == 128 ? 1 : 2; }
+
+static sdpa_status device_info(DevInfo* out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(SDPA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= 64) return fail(SDPA_ERR_CUDA, "device index %d out of range", dev);
+  std::lock_guard<std::mutex> lk(g_mu);
+  DevInfo& di = g_dev[dev];
+  if (!di.ready) {
+    e = cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return fail(SDPA_ERR_CUDA, "SM count: %s", cudaGetErrorString(e));
+    const int Ds[3] = {64, 128, 256};
+    for (int k = 0; k < 3; ++k) {
+      const void* f = splitk_kernel_ptr(Ds[k]);
+      const int smem = splitk_smem_bytes(Ds[k]);
+      e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      if (e != cudaSuccess) return fail(SDPA_ERR_CUDA, "smem attribute: %s", cudaGetErrorString(e));
+      int nb = 0;
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, f, 128, smem);
+      if (e != cudaSuccess) return fail(SDPA_ERR_CUDA, "occupancy: %s", cudaGetErrorString(e));
+      di.splitk_per_sm[k] = nb > 0 ? nb : 1;
+    }
+    di.ready = true;
+  }
+  *out = di;
+  return SDPA_OK;
+}
+
+struct Grids {
+  int64_t splitk, prefill;
+};
+static Grids grids_for(const DevInfo& di, int D) {
+  Grids g;
+  g.splitk = (int64_t)di.sms * di.splitk_per_sm[d_index(D)];
+  g.prefill = di.sms;
+  return g;
+}
+
+static sdpa_status check_common(int64_t T, int Hq, int Hkv, int D, int S, int64_t rows, int cols,
+                                int window, float scale) {
+  if (T < 0 || S < 0 || Hq <= 0 || Hkv <= 0 || rows <= 0 || cols <= 0)
+    return fail(SDPA_ERR_SHAPE, "bad sizes: T=%lld S=%d Hq=%d Hkv=%d rows=%lld cols=%d",
+                (long long)T, S, Hq, Hkv, (long long)rows, cols);
+  if (T > INT32_MAX || rows > INT32_MAX || (int64_t)Hq * T > ((int64_t)1 << 40))
+    return fail(SDPA_ERR_SHAPE, "T or rows beyond 2^31-1");
+  if (D != 64 && D != 128 && D != 256) return fail(SDPA_ERR_HEAD_DIM, "head dim %d not in {64,128,256}", D);
+  if (Hq % Hkv != 0 || Hq / Hkv > 128)
+    return fail(SDPA_ERR_GQA, "Hq=%d is not a multiple of Hkv=%d (group <= 128)", Hq, Hkv);
+  if (window < 0) return fail(SDPA_ERR_ARG, "window %d < 0", window);
+  if (!std::isfinite(scale)) return fail(SDPA_ERR_ARG, "scale is not finite");
+  return SDPA_OK;
+}
+
+static sdpa_status launch_all(const SchedArgs& sa, const AttnArgs& aa, int D, const Grids& g,
+                              cudaStream_t st) {
+  cudaError_t e;
+  {
+    void* args[] = {(void*)&sa};
+    e = cudaLaunchKernel(sched_kernel_ptr(), dim3(1), dim3(kSchedThreads), args, 0, st);
+    if (e != cudaSuccess) return fail(SDPA_ERR_CUDA, "scheduler launch: %s", cudaGetErrorString(e));
+  }
+  {
+    void* args[] = {(void*)&aa};
+    e = cudaLaunchKernel(splitk_kernel_ptr(D), dim3((unsigned)g.splitk), dim3(128), args,
+                         splitk_smem_bytes(D), st);
+    if (e != cudaSuccess) return fail(SDPA_ERR_CUDA, "split-K launch: %s", cudaGetErrorString(e));
+  }
+  if (aa.T > 0) {
+    void* args[] = {(void*)&aa};
+    const int64_t warps = aa.T * aa.Hq;
+    const int64_t blocks = (warps * 32 + 255) / 256;
+    e = cudaLaunchKernel(combine_kernel_ptr(D), dim3((unsigned)blocks), dim3(256), args, 0, st);
+    if (e != cudaSuccess) return fail(SDPA_ERR_CUDA, "combine launch: %s", cudaGetErrorString(e));
+  }
+  return SDPA_OK;
+}
+
+static sdpa_status run(const void* q, int64_t T, int Hq, int D, int64_t q_rs, int64_t q_hs,
+                       const void* k, const void* v, int64_t rows, int cols, int Hkv,
+                       const int32_t* seq_info, int S, const int32_t* inl, int causal, int window,
+                       float scale, void* out, int64_t o_rs, int64_t o_hs, void* ws, size_t ws_bytes,
+                       int32_t* status_dev, void* stream) {
+  g_err[0] = 0;
+  sdpa_status st = check_common(T, Hq, Hkv, D, S, rows, cols, window, scale);
+  if (st) return st;
+  if (!q || !k || !v || !out || (!seq_info && !inl && S > 0))
+    return fail(SDPA_ERR_NULL, "a required pointer is NULL");
+  if (!ws) return fail(SDPA_ERR_WORKSPACE, "workspace is NULL");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(ws) ||
+      (seq_info && !aligned16(seq_info)))
+    return fail(SDPA_ERR_ALIGN, "tensor pointers must be 16-byte aligned");
+  if (q_rs % 8 || q_hs % 8 || o_rs % 8 || o_hs % 8 || q_rs < 0 || q_hs < 0 || o_rs < 0 || o_hs < 0)
+    return fail(SDPA_ERR_STRIDE, "row/head strides must be non-negative multiples of 8 elements");
+  if ((uintptr_t)ws % 256) return fail(SDPA_ERR_ALIGN, "workspace must be 256-byte aligned");
+
+  DevInfo di;
+  if ((st = device_info(&di))) return st;
+  const Grids g = grids_for(di, D);
+  Workspace W;
+  const size_t need = layout_workspace((char*)ws, T, Hq, Hkv, D, S, g.splitk, g.prefill, &W);
+  if (ws_bytes < need)
+    return fail(SDPA_ERR_WORKSPACE, "workspace of %zu bytes, %zu needed", ws_bytes, need);
+
+  SchedArgs sa{};
+  sa.seq_info = seq_info;
+  sa.S = S;
+  sa.use_inline = inl != nullptr;
+  if (inl)
+    for (int i = 0; i < 4; ++i) sa.inl[i] = inl[i];
+  sa.T = T;
+  sa.rows = rows;
+  sa.cols = cols;
+  sa.Hkv = Hkv;
+  sa.group = Hq / Hkv;
+  sa.causal = causal ? 1 : 0;
+  sa.window = window;
+  sa.policy = g_policy.load();
+  sa.prefill_ok = 0;
+  sa.grid[0] = 0;
+  sa.grid[1] = g.splitk;
+  sa.grid[2] = g.prefill;
+  sa.ws = W;
+  sa.status_dev = status_dev;
+
+  AttnArgs aa{};
+  aa.q = (const __nv_bfloat16*)q;
+  aa.q_rs = q_rs;
+  aa.q_hs = q_hs;
+  aa.k = (const __nv_bfloat16*)k;
+  aa.v = (const __nv_bfloat16*)v;
+  aa.rows = rows;
+  aa.cols = cols;
+  aa.Hkv = Hkv;
+  aa.Hq = Hq;
+  aa.group = Hq / Hkv;
+  aa.D = D;
+  aa.causal = sa.causal;
+  aa.window = window;
+  aa.scale_log2 = scale * 1.4426950408889634f;
+  aa.out = (__nv_bfloat16*)out;
+  aa.o_rs = o_rs;
+  aa.o_hs = o_hs;
+  aa.T = T;
+  aa.ws = W;
+  aa.status_dev = status_dev;
+  return launch_all(sa, aa, D, g, (cudaStream_t)stream);
+}
+
+}  // namespace sdpa
+
+using namespace sdpa;
+
+extern "C" {
+
+size_t sdpa_varlen_workspace_bytes(int64_t T, int Hq, int Hkv, int D, int S) {
+  if (T < 0 || S < 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv) return 0;
+  if (D != 64 && D != 128 && D != 256) return 0;
+  DevInfo di;
+  Grids g;
+  if (device_info(&di) == SDPA_OK) {
+    g = grids_for(di, D);
+  } else {
+    g.splitk = 4096;  // no device: a bound above any real grid
+    g.prefill = 1024;
+    g_err[0] = 0;
+  }
+  return layout_workspace(nullptr, T, Hq, Hkv, D, S, g.splitk, g.prefill, nullptr);
+}
+
+sdpa_status sdpa_varlen(const void* q, int64_t T, int Hq, int D, int64_t q_row_stride,
+                        int64_t q_head_stride, const void* k_store, const void* v_store,
+                        int64_t rows, int cols, int Hkv, const int32_t* seq_info, int S,
+                        int causal, int window, float scale, void* out, int64_t o_row_stride,
+                        int64_t o_head_stride, void* workspace, size_t ws_bytes,
+                        int32_t* status_dev, void* stream) {
+  return run(q, T, Hq, D, q_row_stride, q_head_stride, k_store, v_store, rows, cols, Hkv, seq_info,
+             S, nullptr, causal, window, scale, out, o_row_stride, o_head_stride, workspace,
+             ws_bytes, status_dev, stream);
+}
+
+sdpa_status sdpa_causal_prefill(const void* q, const void* k, const void* v, int64_t Lq,
+                                int64_t Lkv, int Hq, int Hkv, int D, float scale, void* out,
+                                void* workspace, size_t ws_bytes, void* stream) {
+  g_err[0] = 0;
+  if (Lq < 0 || Lkv <= 0) return fail(SDPA_ERR_SHAPE, "Lq=%lld Lkv=%lld", (long long)Lq, (long long)Lkv);
+  if (Lq > INT32_MAX || Lkv > INT32_MAX) return fail(SDPA_ERR_SHAPE, "Lq or Lkv beyond 2^31-1");
+  const int32_t seg[4] = {0, (int32_t)Lq, 0, (int32_t)Lkv};
+  const int64_t rs = (int64_t)Hq * D;
+  return run(q, Lq, Hq, D, rs, D, k, v, Lkv, 1, Hkv, nullptr, 1, seg, 1, 0, scale, out, rs, D,
+             workspace, ws_bytes, nullptr, stream);
+}
+
+sdpa_status sdpa_set_route_policy(int policy) {
+  if (policy != SDPA_ROUTE_AUTO && policy != SDPA_ROUTE_SPLITK && policy != SDPA_ROUTE_PREFILL)
+    return fail(SDPA_ERR_ARG, "unknown route policy %d", policy);
+  g_policy.store(policy);
+  return SDPA_OK;
+}
+
+const char* sdpa_last_error(void) { return g_err; }
+
+int sdpa_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,245 @@
+// common.cuh - shared definitions of the sm_103a attention kernels: workspace layout,
+// segment/unit records written by the device scheduler, and small inline-PTX helpers.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/sdpa_varlen.h"
+
+namespace sdpa {
+
+// Rows of one work unit: query rows (t, g) packed as r = i * group + g, so the query
+// heads that share a KV head sit side by side in one tile (GQA packing).
+constexpr int kSplitkRows = 64;    // split-K kernel: 4 warps x 16 rows
+constexpr int kSplitkTile = 64;    // split-K kernel: key positions per tile
+constexpr int kPrefillRows = 128;  // tensor-memory prefill kernel: one 128-lane accumulator
+constexpr int kPrefillTile = 128;  // prefill kernel: key positions per tile
+
+constexpr int kRouteNone = 0;
+constexpr int kRouteSplitk = 1;
+constexpr int kRoutePrefill = 2;
+
+// Per-segment record (the scheduler's view of one seq_info row).
+struct SegRec {
+  int32_t q_start, q_len, col, kv_end;
+  int32_t route;     // kRoute*: none for invalid, overlapping or empty segments
+  int32_t nrb;       // row blocks per KV head (units per KV head)
+  int32_t bits;      // SDPA_SEG_* bits of this segment
+  int32_t pad;
+  int32_t ubase[4];  // per route: units of all earlier segments on that route (monotone in
+                     // the segment index, so a binary search maps a unit to its segment)
+};
+
+// Per-unit record: (segment, KV head, row block) and its stream-K split.
+struct UnitRec {
+  int32_t seg, hk, rb, rows;  // rows = query rows in this unit (<= unit size)
+  int32_t lo, hi;             // key positions the unit's rows see together: [lo, hi)
+  int32_t nslots;             // CTAs that work on the unit (0: no keys; 1: written directly)
+  int32_t g_first;            // first such CTA
+  int32_t ntiles;             // key tiles of the unit
+  int32_t pad;
+  int64_t tile_base;          // first tile of the unit in the flattened tile space
+  int64_t slot_base;          // first partial row of the unit's slots
+};
+
+
+// Scheduler header (int64 words).
+struct SchedHdr {
+  int64_t tiles[3];   // total tiles per route (index = route)
+  int64_t units[3];   // units per route
+  int64_t grid[3];    // CTAs per route (as launched)
+  int64_t status;     // OR of the status bits of this call
+  int64_t pad[4];
+};
+
+struct Workspace {
+  SchedHdr* hdr;
+  SegRec* segs;
+  int32_t* row_seg;     // [T] owning segment or -1
+  int32_t* seg_flag;    // [S] overlap flags
+  UnitRec* units[3];    // [route][U_cap]
+  float2* part_ml[3];   // [route][P_cap] (running max in log2 units, sum)
+  float* part_o[3];     // [route][P_cap * D] unnormalised output
+  int64_t unit_cap[3];
+  int64_t part_cap[3];
+};
+
+__host__ __device__ inline int64_t align_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
+
+// Units a route can produce for T packed rows in S segments (non-overlapping after the
+// scheduler drops overlapping segments): sum_s ceil(q_len_s * group / R) <= T*group/R + S.
+__host__ __device__ inline int64_t unit_cap(int64_t T, int Hq, int Hkv, int S, int rows_per_unit) {
+  int group = Hq / Hkv;
+  return (int64_t)Hkv * ((T * group) / rows_per_unit + (int64_t)S + 1);
+}
+
+// Partial rows: each (unit, CTA) pair that is not the only CTA of its unit writes one slot
+// of `unit rows` rows; there are at most units + CTAs such pairs.
+__host__ __device__ inline int64_t part_cap(int64_t ucap, int64_t grid, int rows_per_unit) {
+  return (ucap + grid + 1) * rows_per_unit;
+}
+
+// Lays the workspace out from `base` (base may be null to only measure). Returns bytes.
+__host__ inline size_t layout_workspace(char* base, int64_t T, int Hq, int Hkv, int D, int S,
+                                        int64_t grid_splitk, int64_t grid_prefill,
+                                        Workspace* ws) {
+  int64_t off = 0;
+  auto take = [&](int64_t bytes) {
+    int64_t o = off;
+    off = align_up(off + bytes, 256);
+    return base ? base + o : nullptr;
+  };
+  Workspace w{};
+  w.hdr = (SchedHdr*)take(sizeof(SchedHdr));
+  w.segs = (SegRec*)take((int64_t)sizeof(SegRec) * (S > 0 ? S : 1));
+  w.row_seg = (int32_t*)take(4 * (T > 0 ? T : 1));
+  w.seg_flag = (int32_t*)take(4 * (S > 0 ? S : 1));
+  const int rpu[3] = {0, kSplitkRows, kPrefillRows};
+  const int64_t grid[3] = {0, grid_splitk, grid_prefill};
+  for (int r = 1; r < 3; ++r) {
+    w.unit_cap[r] = unit_cap(T, Hq, Hkv, S, rpu[r]);
+    w.part_cap[r] = part_cap(w.unit_cap[r], grid[r], rpu[r]);
+    w.units[r] = (UnitRec*)take((int64_t)sizeof(UnitRec) * w.unit_cap[r]);
+    w.part_ml[r] = (float2*)take(8 * w.part_cap[r]);
+    w.part_o[r] = (float*)take(4 * w.part_cap[r] * D);
+  }
+  if (ws) *ws = w;
+  return (size_t)off;
+}
+
+// Arguments shared by the attention kernels and the combine pass.
+struct AttnArgs {
+  const __nv_bfloat16* q;
+  int64_t q_rs, q_hs;  // element strides of q rows and heads
+  const __nv_bfloat16* k;
+  const __nv_bfloat16* v;
+  int64_t rows;        // store rows
+  int cols, Hkv, Hq, group, D;
+  int causal, window;
+  float scale_log2;    // scale * log2(e): scores are kept in base-2 units
+  __nv_bfloat16* out;
+  int64_t o_rs, o_hs;
+  int64_t T;
+  Workspace ws;
+  int32_t* status_dev;
+};
+
+// Arguments of the scheduler kernel.
+struct SchedArgs {
+  const int32_t* seq_info;
+  int S;
+  int use_inline;  // dense entry: one segment passed by value
+  int32_t inl[4];
+  int64_t T, rows;
+  int cols, Hkv, group, causal, window;
+  int policy;      // SDPA_ROUTE_*
+  int prefill_ok;  // prefill kernel available for this call's head dim
+  int64_t grid[3];
+  Workspace ws;
+  int32_t* status_dev;
+};
+
+constexpr int kSchedThreads = 1024;
+
+// Kernel entry points (defined in their own translation units).
+const void* sched_kernel_ptr();
+const void* splitk_kernel_ptr(int D);
+int splitk_smem_bytes(int D);
+const void* combine_kernel_ptr(int D);
+
+// Segment validity (SDPA_SEG_* bits), same rule on host and device.
+__host__ __device__ inline int32_t segment_bits(int64_t q_start, int64_t q_len, int64_t col,
+                                                int64_t kv_end, int64_t T, int64_t rows,
+                                                int64_t cols, int window) {
+  int32_t bits = 0;
+  if (q_len < 0 || q_start < 0 || q_start + q_len > T) bits |= SDPA_SEG_BAD_QRANGE;
+  if (col < 0 || col >= cols) bits |= SDPA_SEG_BAD_COL;
+  if (kv_end < 0) bits |= SDPA_SEG_BAD_KV;
+  if (bits == 0 && q_len > 0 && kv_end > 0) {
+    int64_t span = kv_end;
+    if (window > 0) span = kv_end < q_len + window - 1 ? kv_end : q_len + window - 1;
+    if (span > rows) bits |= SDPA_SEG_SPAN;
+  }
+  return bits;
+}
+
+// Visible key positions of query row i: [lo, hi) (hi <= lo: none).
+struct RowWin {
+  int32_t lo, hi;
+};
+__device__ __forceinline__ RowWin row_window(int i, int q_len, int kv_end, int causal, int window) {
+  int p = kv_end - q_len + i;
+  RowWin w;
+  w.hi = causal ? min(p + 1, kv_end) : kv_end;
+  w.lo = window > 0 ? max(0, p - window + 1) : 0;
+  return w;
+}
+
+// Stream-K partition: CTA g of G owns flattened tiles [g*W/G, (g+1)*W/G).
+__host__ __device__ inline int64_t sk_start(int64_t g, int64_t W, int64_t G) { return g * W / G; }
+// CTA whose range holds tile x.
+__host__ __device__ inline int64_t sk_owner(int64_t x, int64_t W, int64_t G) {
+  return ((x + 1) * G - 1) / W;
+}
+
+// ------------------------------------------------------------------------------------
+// inline PTX helpers
+// ------------------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, bool pred) {
+  int sz = pred ? 16 : 0;  // src-size 0 fills the 16 bytes with zeros
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(sz));
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
+}
+
+__device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                            uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t addr, uint32_t& r0, uint32_t& r1,
+                                                  uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+// D(16x8 f32) += A(16x16 bf16, row) * B(16x8 bf16, col)
+__device__ __forceinline__ void mma_bf16_16816(float* d, const uint32_t* a, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// 2^x on the SFU (PTX ex2.approx; -inf gives +0).
+__device__ __forceinline__ float exp2_approx(float x) {
+  float y;
+  asm volatile("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Swizzled offset (bytes) of 16-byte chunk `c` of row `r` in a tile whose rows are
+// `row_bytes` long: the low three bits of the chunk index are XORed with the row, so
+// eight consecutive rows at one logical chunk hit eight different bank groups.
+__device__ __forceinline__ uint32_t swz(int r, int c, int row_bytes) {
+  return (uint32_t)(r * row_bytes + ((c ^ (r & 7)) << 4));
+}
+
+}  // namespace sdpa

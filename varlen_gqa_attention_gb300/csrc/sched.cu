@@ -1,0 +1,224 @@
+// sched.cu - device-side segment scheduler.
+//
+// Walks the segment table on the device ("[executorch][cuda] Add a length-aware Triton SDPA
+// over per-sequence KV columns", PR description: lengths are read on device, so one captured
+// graph serves any mix of sequence lengths) and turns it into work for the attention kernels:
+//   1. validates each segment (SDPA_SEG_* bits);
+//   2. claims packed rows for valid segments, dropping every segment that shares a row with
+//      another one (SDPA_SEG_OVERLAP);
+//   3. routes each remaining segment to the split-K or the tensor-memory prefill kernel and
+//      cuts it into units (segment, KV head, block of packed (query row, head) rows);
+//   4. counts each unit's key tiles over the union of its rows' visible intervals and lays
+//      all units' tiles end to end; CTA g of a route's persistent grid of G CTAs owns tiles
+//      [g*W/G, (g+1)*W/G) of that line (a stream-K split, so every CTA gets the same amount
+//      of key tiles whatever the length mix), and each (unit, CTA) pair gets a slot of
+//      partial results unless the unit has a single CTA, which then writes `out` itself.
+// One CTA of 1024 threads does all of it; block-wide scans give the prefix sums.
+#include "common.cuh"
+
+namespace sdpa {
+
+
+// Exclusive block scan of one int64 per thread; returns the prefix, writes the total.
+__device__ int64_t block_excl_scan(int64_t v, int64_t* total, int64_t* sh /*[33]*/) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int64_t x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int64_t y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) sh[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int64_t w = lane < (int)(blockDim.x >> 5) ? sh[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int64_t y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    sh[lane] = w;  // inclusive warp totals
+  }
+  __syncthreads();
+  int64_t base = warp > 0 ? sh[warp - 1] : 0;
+  if (total) *total = sh[(blockDim.x >> 5) - 1];
+  __syncthreads();
+  return base + x - v;
+}
+
+// Contiguous range of n items owned by this thread.
+__device__ __forceinline__ void my_range(int64_t n, int64_t* a, int64_t* b) {
+  int64_t per = (n + blockDim.x - 1) / blockDim.x;
+  *a = min(n, per * threadIdx.x);
+  *b = min(n, *a + per);
+}
+
+__device__ __forceinline__ void load_seg(const SchedArgs& A, int s, int32_t* seg) {
+  if (A.use_inline) {
+    seg[0] = A.inl[0]; seg[1] = A.inl[1]; seg[2] = A.inl[2]; seg[3] = A.inl[3];
+  } else {
+    int4 v = reinterpret_cast<const int4*>(A.seq_info)[s];
+    seg[0] = v.x; seg[1] = v.y; seg[2] = v.z; seg[3] = v.w;
+  }
+}
+
+__device__ __forceinline__ int rows_per_unit(int route) {
+  return route == kRoutePrefill ? kPrefillRows : kSplitkRows;
+}
+__device__ __forceinline__ int tile_len(int route) {
+  return route == kRoutePrefill ? kPrefillTile : kSplitkTile;
+}
+
+__global__ void __launch_bounds__(kSchedThreads) sdpa_sched_kernel(SchedArgs A) {
+  __shared__ int64_t sh[33];
+  __shared__ int32_t s_status;
+  __shared__ int64_t s_tot[3];
+  const Workspace& W = A.ws;
+  const int S = A.S;
+  const int64_t T = A.T;
+  if (threadIdx.x == 0) s_status = 0;
+  __syncthreads();
+
+  // 1. validate; clear overlap flags and the row owner map
+  for (int s = threadIdx.x; s < S; s += blockDim.x) {
+    int32_t g[4];
+    load_seg(A, s, g);
+    int32_t bits = segment_bits(g[0], g[1], g[2], g[3], T, A.rows, A.cols, A.window);
+    SegRec r;
+    r.q_start = g[0]; r.q_len = g[1]; r.col = g[2]; r.kv_end = g[3];
+    r.route = kRouteNone; r.nrb = 0; r.bits = bits; r.pad = 0;
+    r.ubase[0] = r.ubase[1] = r.ubase[2] = r.ubase[3] = 0;
+    W.segs[s] = r;
+    W.seg_flag[s] = 0;
+    if (bits) atomicOr(&s_status, bits);
+  }
+  for (int64_t t = threadIdx.x; t < T; t += blockDim.x) W.row_seg[t] = -1;
+  __syncthreads();
+
+  // 2. claim rows; a segment that meets another one marks both
+  for (int s = 0; s < S; ++s) {
+    SegRec r = W.segs[s];
+    if (r.bits) continue;
+    for (int i = threadIdx.x; i < r.q_len; i += blockDim.x) {
+      int old = atomicCAS(&W.row_seg[r.q_start + i], -1, s);
+      if (old != -1) {
+        atomicExch(&W.seg_flag[s], 1);
+        atomicExch(&W.seg_flag[old], 1);
+      }
+    }
+  }
+  __syncthreads();
+
+  // 3. route each live segment and count its units (contiguous segment ranges per thread)
+  int64_t sa, sb;
+  my_range(S, &sa, &sb);
+  int64_t cnt[3] = {0, 0, 0};
+  for (int64_t s = sa; s < sb; ++s) {
+    SegRec r = W.segs[s];
+    if (r.bits == 0 && W.seg_flag[s]) atomicOr(&s_status, SDPA_SEG_OVERLAP);
+    if (r.bits || W.seg_flag[s] || r.q_len == 0) continue;
+    int64_t R = (int64_t)r.q_len * A.group;
+    int route;
+    if (A.policy == SDPA_ROUTE_SPLITK || !A.prefill_ok) route = kRouteSplitk;
+    else if (A.policy == SDPA_ROUTE_PREFILL) route = kRoutePrefill;
+    else route = R >= kPrefillRows ? kRoutePrefill : kRouteSplitk;
+    const int rpu = rows_per_unit(route);
+    const int nrb = (int)((R + rpu - 1) / rpu);
+    W.segs[s].route = route;
+    W.segs[s].nrb = nrb;
+    cnt[route] += (int64_t)A.Hkv * nrb;
+  }
+  int64_t ubase[3];
+  for (int q = 1; q < 3; ++q) {
+    int64_t tot;
+    ubase[q] = block_excl_scan(cnt[q], &tot, sh);
+    // Live segments cover disjoint rows, so tot <= unit_cap; units past the cap (none)
+    // would simply not be generated.
+    if (threadIdx.x == 0) s_tot[q] = min(tot, W.unit_cap[q]);
+  }
+  for (int64_t s = sa; s < sb; ++s) {
+    SegRec r = W.segs[s];
+    for (int q = 1; q < 3; ++q) W.segs[s].ubase[q] = (int32_t)ubase[q];
+    if (r.route != kRouteNone) ubase[r.route] += (int64_t)A.Hkv * r.nrb;
+  }
+  __syncthreads();
+
+  // 4. per route: units, their tiles, the stream-K split and partial slots
+  for (int q = 1; q < 3; ++q) {
+    const int64_t U = s_tot[q];
+    const int rpu = rows_per_unit(q), tl = tile_len(q);
+    UnitRec* units = W.units[q];
+    int64_t ua, ub;
+    my_range(U, &ua, &ub);
+    int64_t my_tiles = 0;
+    for (int64_t u = ua; u < ub; ++u) {
+      // owning segment: the last one whose route-q unit base is <= u
+      int lo = 0, hi = S - 1, s = 0;
+      while (lo <= hi) {
+        int mid = (lo + hi) >> 1;
+        if (W.segs[mid].ubase[q] <= u) { s = mid; lo = mid + 1; } else { hi = mid - 1; }
+      }
+      SegRec g = W.segs[s];
+      UnitRec ur;
+      int64_t j = u - g.ubase[q];
+      ur.seg = s;
+      ur.hk = (int32_t)(j / g.nrb);
+      ur.rb = (int32_t)(j % g.nrb);
+      int64_t R = (int64_t)g.q_len * A.group;
+      int64_t r0 = (int64_t)ur.rb * rpu;
+      ur.rows = (int32_t)min((int64_t)rpu, R - r0);
+      int i0 = (int)(r0 / A.group), i1 = (int)((r0 + ur.rows - 1) / A.group);
+      RowWin w0 = row_window(i0, g.q_len, g.kv_end, A.causal, A.window);
+      RowWin w1 = row_window(i1, g.q_len, g.kv_end, A.causal, A.window);
+      ur.lo = w0.lo;  // lo and hi grow with the query row
+      ur.hi = max(w1.hi, w0.lo);
+      int64_t nt = ur.hi > ur.lo ? ((int64_t)(ur.hi - ur.lo) + tl - 1) / tl : 0;
+      ur.nslots = 0;
+      ur.g_first = 0;
+      ur.ntiles = (int32_t)nt;
+      ur.pad = 0;
+      ur.tile_base = nt;  // the count, until the scan below
+      ur.slot_base = 0;
+      units[u] = ur;
+      my_tiles += nt;
+    }
+    int64_t Wt;
+    int64_t tb = block_excl_scan(my_tiles, &Wt, sh);
+    const int64_t G = A.grid[q];
+    int64_t my_rows = 0;
+    for (int64_t u = ua; u < ub; ++u) {
+      UnitRec ur = units[u];
+      const int64_t nt = ur.tile_base;
+      ur.tile_base = tb;
+      if (nt > 0) {
+        const int64_t g0 = sk_owner(tb, Wt, G), g1 = sk_owner(tb + nt - 1, Wt, G);
+        ur.g_first = (int32_t)g0;
+        ur.nslots = (int32_t)(g1 - g0 + 1);
+        if (ur.nslots > 1) my_rows += (int64_t)ur.nslots * ur.rows;
+      }
+      tb += nt;
+      units[u] = ur;
+    }
+    int64_t Pt;
+    int64_t pb = block_excl_scan(my_rows, &Pt, sh);
+    for (int64_t u = ua; u < ub; ++u) {
+      units[u].slot_base = pb;
+      UnitRec ur = units[u];
+      if (ur.nslots > 1) pb += (int64_t)ur.nslots * ur.rows;
+    }
+    if (threadIdx.x == 0) {
+      W.hdr->tiles[q] = Wt;
+      W.hdr->units[q] = U;
+      W.hdr->grid[q] = G;
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    W.hdr->status = s_status;
+    if (A.status_dev && s_status) atomicOr(A.status_dev, s_status);
+  }
+}
+
+const void* sched_kernel_ptr() { return (const void*)sdpa_sched_kernel; }
+
+}  // namespace sdpa

@@ -1,0 +1,356 @@
+// splitk.cu - split-K attention kernel for short steps (decode, draft blocks, small prefills).
+//
+// "[CUDA] Use Triton TMA for long-context causal prefill" (stack list: hardware-aware
+// online-softmax split-K decode scheduling) and "[executorch][cuda] Add a length-aware Triton
+// SDPA over per-sequence KV columns" (split-K for short steps).
+//
+// A persistent grid (a multiple of the SM count) walks the stream-K tile line the scheduler
+// built: each CTA owns an equal share of key tiles across all units, a unit being
+// (segment, KV head, 64 packed rows r = i * group + g).  Per unit and CTA:
+//   * Q rows and 64-position K/V tiles are staged in shared memory with 16-byte cp.async
+//     (coalesced: a store row of one KV head is D*2 contiguous bytes; ring rows wrap per row),
+//     double buffered so the next tile streams in while this one is used;
+//   * each warp takes 16 packed rows and a slice of the tile: S = Q K^T and O += P V with
+//     bf16 m16n8k16 tensor-core MMAs and fp32 accumulation; with few rows (decode: q_len=1,
+//     group 8) the four warps split the tile's keys instead of the rows;
+//   * online softmax in base 2 with quad shuffles for the row max / sum, masks applied by
+//     select (never by adding), fully masked rows kept finite;
+//   * the warps' slices are merged through shared memory, then the CTA either writes `out`
+//     (it is the unit's only CTA) or a partial (max, sum, unnormalised O) that the combine
+//     pass merges by log-sum-exp.
+#include "common.cuh"
+
+namespace sdpa {
+
+constexpr int kSplitkThreads = 128;
+constexpr int kStages = 2;
+
+template <int D>
+struct SplitkSmem {
+  static constexpr int kRowBytes = D * 2;
+  static constexpr int kQBytes = kSplitkRows * kRowBytes;
+  static constexpr int kTileBytes = kSplitkTile * kRowBytes;
+  static constexpr int kBytes = kQBytes + 2 * kStages * kTileBytes;
+};
+
+template <int D>
+__device__ __forceinline__ void load_kv_tile(const AttnArgs& A, const SegRec& sg, int hk,
+                                             int64_t tile_start, int64_t pos_hi, char* sK,
+                                             char* sV) {
+  constexpr int CH = D / 8;  // 16-byte chunks per store row
+  constexpr int RB = D * 2;
+  const int64_t row_stride = (int64_t)A.cols * A.Hkv * D;
+  const int64_t col_off = ((int64_t)sg.col * A.Hkv + hk) * D;
+  const int64_t base_row = tile_start % A.rows;
+#pragma unroll 4
+  for (int idx = threadIdx.x; idx < kSplitkTile * CH; idx += kSplitkThreads) {
+    const int n = idx / CH, c = idx % CH;
+    const bool ok = tile_start + n < pos_hi;
+    int64_t phys = base_row + n;
+    if (phys >= A.rows) phys -= A.rows;  // valid positions span at most `rows` rows
+    const int64_t off = ok ? phys * row_stride + col_off + c * 8 : 0;
+    const uint32_t so = swz(n, c, RB);
+    cp_async_16(smem_u32(sK + so), A.k + off, ok);
+    cp_async_16(smem_u32(sV + so), A.v + off, ok);
+  }
+}
+
+// One warp's share of a unit: 16 packed rows x a slice of each key tile.
+template <int D, int NCS>
+__device__ __forceinline__ void splitk_unit(const AttnArgs& A, const UnitRec& ur, const SegRec& sg,
+                                            int64_t ta, int64_t tb, int slot, char* smem,
+                                            float2* s_ml) {
+  using S = SplitkSmem<D>;
+  constexpr int RB = S::kRowBytes;
+  constexpr int SW = kSplitkTile / NCS;  // keys per warp slice
+  constexpr int NB = SW / 8;             // n8 blocks per slice
+  constexpr int ND = D / 8;              // n8 blocks of the output
+  char* sQ = smem;
+  char* sK = smem + S::kQBytes;
+  char* sV = sK + kStages * S::kTileBytes;
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int mt = warp / NCS, cs = warp % NCS;
+  const int gq = lane >> 2, tq = lane & 3;
+  const int R = ur.rows;
+  const int64_t r0 = (int64_t)ur.rb * kSplitkRows;
+
+  // key positions of this CTA's share of the unit
+  const int64_t pos_lo = (int64_t)ur.lo + ta * kSplitkTile;
+  const int64_t pos_hi = min((int64_t)ur.lo + tb * kSplitkTile, (int64_t)ur.hi);
+  const int ntiles = (int)(tb - ta);
+
+  // Q rows (packed r -> query row i = r / group, head hk*group + r % group)
+  {
+    constexpr int CH = D / 8;
+    for (int idx = tid; idx < kSplitkRows * CH; idx += kSplitkThreads) {
+      const int rl = idx / CH, c = idx % CH;
+      const bool ok = rl < R;
+      int64_t off = 0;
+      if (ok) {
+        const int64_t r = r0 + rl;
+        const int64_t i = r / A.group;
+        const int h = ur.hk * A.group + (int)(r % A.group);
+        off = (sg.q_start + i) * A.q_rs + (int64_t)h * A.q_hs + c * 8;
+      }
+      cp_async_16(smem_u32(sQ + swz(rl, c, RB)), A.q + off, ok);
+    }
+  }
+  load_kv_tile<D>(A, sg, ur.hk, pos_lo, pos_hi, sK, sV);
+  cp_async_commit();
+
+  // this thread's two rows: local rows mt*16 + gq and +8
+  int32_t rlo[2], rhi[2];
+  bool live[2];
+#pragma unroll
+  for (int e = 0; e < 2; ++e) {
+    const int rl = mt * 16 + gq + 8 * e;
+    live[e] = rl < R;
+    if (live[e]) {
+      const int i = (int)((r0 + rl) / A.group);
+      RowWin w = row_window(i, sg.q_len, sg.kv_end, A.causal, A.window);
+      rlo[e] = (int32_t)max((int64_t)w.lo, pos_lo);
+      rhi[e] = (int32_t)min((int64_t)w.hi, pos_hi);
+    } else {
+      rlo[e] = INT32_MIN;  // padding rows: never stored, Q = 0 keeps them finite
+      rhi[e] = INT32_MAX;
+    }
+  }
+  const int32_t lo_max = max(rlo[0], rlo[1]), hi_min = min(rhi[0], rhi[1]);
+
+  float o[ND][4];
+#pragma unroll
+  for (int nd = 0; nd < ND; ++nd) o[nd][0] = o[nd][1] = o[nd][2] = o[nd][3] = 0.f;
+  float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
+  const float sl2 = A.scale_log2;
+
+  for (int kt = 0; kt < ntiles; ++kt) {
+    if (kt + 1 < ntiles) {
+      const int st = (kt + 1) % kStages;
+      load_kv_tile<D>(A, sg, ur.hk, pos_lo + (int64_t)(kt + 1) * kSplitkTile, pos_hi,
+                      sK + st * S::kTileBytes, sV + st * S::kTileBytes);
+      cp_async_commit();
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
+    }
+    __syncthreads();
+    const char* cK = sK + (kt % kStages) * S::kTileBytes;
+    const char* cV = sV + (kt % kStages) * S::kTileBytes;
+    const int64_t tile0 = pos_lo + (int64_t)kt * kSplitkTile + cs * SW;  // first key of slice
+
+    // S = Q K^T over the slice
+    float s[NB][4];
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb) s[nb][0] = s[nb][1] = s[nb][2] = s[nb][3] = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      uint32_t a[4];
+      ldmatrix_x4(smem_u32(sQ + swz(mt * 16 + (lane & 15), kk * 2 + (lane >> 4), RB)), a[0], a[1],
+                  a[2], a[3]);
+#pragma unroll
+      for (int nb = 0; nb < NB; nb += 2) {
+        uint32_t b0, b1, b2, b3;
+        const int pos = cs * SW + nb * 8 + (lane & 7) + ((lane >> 4) << 3);
+        ldmatrix_x4(smem_u32(cK + swz(pos, kk * 2 + ((lane >> 3) & 1), RB)), b0, b1, b2, b3);
+        mma_bf16_16816(s[nb], a, b0, b1);
+        mma_bf16_16816(s[nb + 1], a, b2, b3);
+      }
+    }
+
+    // mask (select), scale to base 2, online softmax
+    const bool full = tile0 >= lo_max && tile0 + SW <= hi_min;
+    float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int rr = e >> 1;
+        float x = s[nb][e] * sl2;
+        if (!full) {
+          const int64_t j = tile0 + nb * 8 + 2 * tq + (e & 1);
+          const bool vis = !live[rr] || (j >= rlo[rr] && j < rhi[rr]);
+          // padding rows: keys past the share are zero-filled, harmless
+          x = vis ? x : -INFINITY;
+        }
+        s[nb][e] = x;
+        mx[rr] = fmaxf(mx[rr], x);
+      }
+    }
+    float alpha[2], muse[2];
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) {
+      mx[rr] = fmaxf(mx[rr], __shfl_xor_sync(0xffffffffu, mx[rr], 1));
+      mx[rr] = fmaxf(mx[rr], __shfl_xor_sync(0xffffffffu, mx[rr], 2));
+      const float mn = fmaxf(m[rr], mx[rr]);
+      muse[rr] = mn == -INFINITY ? 0.f : mn;
+      alpha[rr] = exp2_approx(m[rr] - muse[rr]);
+      m[rr] = mn;
+    }
+    float ls[2] = {0.f, 0.f};
+#pragma unroll
+    for (int nb = 0; nb < NB; ++nb) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float p = exp2_approx(s[nb][e] - muse[e >> 1]);
+        s[nb][e] = p;
+        ls[e >> 1] += p;
+      }
+    }
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) l[rr] = l[rr] * alpha[rr] + ls[rr];
+#pragma unroll
+    for (int nd = 0; nd < ND; ++nd) {
+      o[nd][0] *= alpha[0];
+      o[nd][1] *= alpha[0];
+      o[nd][2] *= alpha[1];
+      o[nd][3] *= alpha[1];
+    }
+
+    // O += P V
+#pragma unroll
+    for (int k2 = 0; k2 < SW / 16; ++k2) {
+      uint32_t a[4];
+      a[0] = pack_bf16x2(s[2 * k2][0], s[2 * k2][1]);
+      a[1] = pack_bf16x2(s[2 * k2][2], s[2 * k2][3]);
+      a[2] = pack_bf16x2(s[2 * k2 + 1][0], s[2 * k2 + 1][1]);
+      a[3] = pack_bf16x2(s[2 * k2 + 1][2], s[2 * k2 + 1][3]);
+      const int pos = cs * SW + k2 * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
+#pragma unroll
+      for (int nd = 0; nd < ND; nd += 2) {
+        uint32_t b0, b1, b2, b3;
+        ldmatrix_x4_trans(smem_u32(cV + swz(pos, nd + (lane >> 4), RB)), b0, b1, b2, b3);
+        mma_bf16_16816(o[nd], a, b0, b1);
+        mma_bf16_16816(o[nd + 1], a, b2, b3);
+      }
+    }
+    __syncthreads();
+  }
+
+  // row sums over the quad
+#pragma unroll
+  for (int rr = 0; rr < 2; ++rr) {
+    l[rr] += __shfl_xor_sync(0xffffffffu, l[rr], 1);
+    l[rr] += __shfl_xor_sync(0xffffffffu, l[rr], 2);
+  }
+
+  // merge the warps' slices through shared memory (the K/V buffers are free now)
+  float* mo = reinterpret_cast<float*>(sK);  // [4 warps][16 rows][D]
+  {
+    float* mw = mo + warp * 16 * D;
+#pragma unroll
+    for (int nd = 0; nd < ND; ++nd) {
+      const int d = nd * 8 + 2 * tq;
+      *reinterpret_cast<float2*>(mw + gq * D + d) = make_float2(o[nd][0], o[nd][1]);
+      *reinterpret_cast<float2*>(mw + (gq + 8) * D + d) = make_float2(o[nd][2], o[nd][3]);
+    }
+    if (tq == 0) {
+      s_ml[warp * 16 + gq] = make_float2(m[0], l[0]);
+      s_ml[warp * 16 + gq + 8] = make_float2(m[1], l[1]);
+    }
+  }
+  __syncthreads();
+
+  const bool direct = ur.nslots == 1;
+  for (int idx = tid; idx < R * (D / 8); idx += kSplitkThreads) {
+    const int rl = idx / (D / 8), d0 = (idx % (D / 8)) * 8;
+    const int mtr = rl / 16, rin = rl % 16;
+    float M = -INFINITY;
+#pragma unroll
+    for (int c = 0; c < NCS; ++c) M = fmaxf(M, s_ml[(mtr * NCS + c) * 16 + rin].x);
+    const float Mu = M == -INFINITY ? 0.f : M;
+    float L = 0.f, acc[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) acc[k] = 0.f;
+#pragma unroll
+    for (int c = 0; c < NCS; ++c) {
+      const int w = mtr * NCS + c;
+      const float2 ml = s_ml[w * 16 + rin];
+      const float f = exp2_approx(ml.x - Mu);
+      L += ml.y * f;
+      const float* src = mo + (w * 16 + rin) * D + d0;
+      const float4 u0 = *reinterpret_cast<const float4*>(src);
+      const float4 u1 = *reinterpret_cast<const float4*>(src + 4);
+      acc[0] += u0.x * f; acc[1] += u0.y * f; acc[2] += u0.z * f; acc[3] += u0.w * f;
+      acc[4] += u1.x * f; acc[5] += u1.y * f; acc[6] += u1.z * f; acc[7] += u1.w * f;
+    }
+    const int64_t r = r0 + rl;
+    if (direct) {
+      const float inv = L > 0.f ? 1.f / L : 0.f;
+      const int64_t i = r / A.group;
+      const int h = ur.hk * A.group + (int)(r % A.group);
+      uint4 pk;
+      pk.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+      pk.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+      pk.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
+      pk.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
+      *reinterpret_cast<uint4*>(A.out + (sg.q_start + i) * A.o_rs + (int64_t)h * A.o_hs + d0) = pk;
+    } else {
+      const int64_t pi = ur.slot_base + (int64_t)slot * R + rl;
+      if (d0 == 0) A.ws.part_ml[kRouteSplitk][pi] = make_float2(M, L);
+      float* dst = A.ws.part_o[kRouteSplitk] + pi * D + d0;
+      *reinterpret_cast<float4*>(dst) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      *reinterpret_cast<float4*>(dst + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    }
+  }
+  __syncthreads();
+}
+
+template <int D>
+__global__ void __launch_bounds__(kSplitkThreads) sdpa_splitk_kernel(AttnArgs A) {
+  extern __shared__ __align__(128) char smem[];
+  __shared__ float2 s_ml[4 * 16];
+  const SchedHdr* hdr = A.ws.hdr;
+  const int64_t Wt = hdr->tiles[kRouteSplitk];
+  const int64_t U = hdr->units[kRouteSplitk];
+  const int64_t G = gridDim.x;
+  if (Wt == 0) return;
+  int64_t t0 = sk_start(blockIdx.x, Wt, G);
+  const int64_t t1 = sk_start(blockIdx.x + 1, Wt, G);
+  if (t0 >= t1) return;
+  const UnitRec* units = A.ws.units[kRouteSplitk];
+  // first unit holding tile t0: the last unit whose tile_base <= t0
+  int64_t lo = 0, hi = U - 1, u = 0;
+  while (lo <= hi) {
+    const int64_t mid = (lo + hi) >> 1;
+    if (units[mid].tile_base <= t0) { u = mid; lo = mid + 1; } else { hi = mid - 1; }
+  }
+  for (; u < U && t0 < t1; ++u) {
+    const UnitRec ur = units[u];
+    if (ur.ntiles == 0) continue;
+    const int64_t ta = t0 - ur.tile_base;
+    const int64_t tb = min(t1, ur.tile_base + ur.ntiles) - ur.tile_base;
+    if (ta >= tb) continue;
+    const SegRec sg = A.ws.segs[ur.seg];
+    const int slot = (int)(blockIdx.x - ur.g_first);
+    if (ur.rows <= 16)
+      splitk_unit<D, 4>(A, ur, sg, ta, tb, slot, smem, s_ml);
+    else if (ur.rows <= 32)
+      splitk_unit<D, 2>(A, ur, sg, ta, tb, slot, smem, s_ml);
+    else
+      splitk_unit<D, 1>(A, ur, sg, ta, tb, slot, smem, s_ml);
+    t0 = ur.tile_base + tb;
+  }
+}
+
+template __global__ void sdpa_splitk_kernel<64>(AttnArgs);
+template __global__ void sdpa_splitk_kernel<128>(AttnArgs);
+template __global__ void sdpa_splitk_kernel<256>(AttnArgs);
+
+int splitk_smem_bytes(int D) {
+  switch (D) {
+    case 64: return SplitkSmem<64>::kBytes;
+    case 128: return SplitkSmem<128>::kBytes;
+    default: return SplitkSmem<256>::kBytes;
+  }
+}
+
+const void* splitk_kernel_ptr(int D) {
+  switch (D) {
+    case 64: return (const void*)sdpa_splitk_kernel<64>;
+    case 128: return (const void*)sdpa_splitk_kernel<128>;
+    default: return (const void*)sdpa_splitk_kernel<256>;
+  }
+}
+
+}  // namespace sdpa

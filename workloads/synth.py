@@ -50,8 +50,8 @@ class Call:
     q: torch.Tensor  # bf16 [T, Hq, D] (CPU)
     k_store: torch.Tensor  # bf16 [rows, cols, Hkv, D] (CPU)
     v_store: torch.Tensor  # bf16 [rows, cols, Hkv, D] (CPU)
-    # Packed-row range this call owns in a step that several calls share
-    # (a mixed step runs one call per store); rows outside it are left alone.
+    # Packed rows [row_begin, row_end) of the step this call owns (a mixed step runs one
+    # call per store); q and seq_info are relative to row_begin.
     row_begin: int = 0
     row_end: Optional[int] = None
 
@@ -119,7 +119,9 @@ def mixed_step(seed: int = 0, n_target: int = 8, n_draft: int = 8, Hq: int = 32,
     """Sliding-window targets on a ring store plus non-causal draft blocks on a flat store.
 
     Rows [0, T/2) hold the targets, packed from row 0 (the rows after the last
-    target stay uncovered); rows [T/2, T) hold the draft blocks of max_write rows.
+    target stay uncovered); rows [T/2, T) hold the draft blocks of max_write rows.  The
+    step is two calls, one per store, each owning its half of the packed rows: its q is
+    a view of those rows and its q_start values count from the half's first row.
     """
     rng = np.random.default_rng(seed)
     q_len_t = rng.integers(1, max_write + 1, size=n_target)
@@ -138,12 +140,13 @@ def mixed_step(seed: int = 0, n_target: int = 8, n_draft: int = 8, Hq: int = 32,
     for k in range(n_target):
         segs_a.append((start, int(q_len_t[k]), k, int(kv_end_t[k])))
         start += int(q_len_t[k])
-    segs_b = [(half + max_write * k, max_write, k, int(kv_end_d[k])) for k in range(n_draft)]
+    # q_start of each call is relative to the first packed row the call owns
+    segs_b = [(max_write * k, max_write, k, int(kv_end_d[k])) for k in range(n_draft)]
     scale = 1.0 / math.sqrt(D)
-    a = Call(T, Hq, Hkv, D, ring_rows, cols, _seq_info(segs_a), True, window, scale, q, rk, rv,
-             row_begin=0, row_end=half)
-    b = Call(T, Hq, Hkv, D, flat_rows, cols, _seq_info(segs_b), False, 0, scale, q, fk, fv,
-             row_begin=half, row_end=T)
+    a = Call(half, Hq, Hkv, D, ring_rows, cols, _seq_info(segs_a), True, window, scale, q[:half],
+             rk, rv, row_begin=0, row_end=half)
+    b = Call(T - half, Hq, Hkv, D, flat_rows, cols, _seq_info(segs_b), False, 0, scale, q[half:],
+             fk, fv, row_begin=half, row_end=T)
     return Workload("mixed_swa_ring_draft_step", [a, b],
                     f"T={T} Hq={Hq} Hkv={Hkv} D={D}: {n_target} causal W={window} ring segments "
                     f"(rows {ring_rows}) + {n_draft} non-causal {max_write}-row draft blocks")

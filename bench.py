@@ -1,0 +1,401 @@
+"""Benchmark of length-aware GQA attention on one GB300 (replicas on N GPUs).
+
+Prints one JSON line (rank 0).  A step is one pass of the whole path (scheduler, attention
+kernels, combine) over one synthetic batch, inputs resident in HBM.  The workload defaults to
+the long-context causal GQA prefill with D=128, Lq=4096, Lkv=131072, Hq=16, Hkv=2 (the
+D=128 row of the operator table on "[CUDA] Use Triton TMA for long-context causal prefill").
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+value: useful (mask-aware) TFLOP/s for prefill workloads, useful KV GB/s for decode-like
+ones, whole job (all ranks).  The L2 is flushed (a 512 MiB write) between timed steps,
+outside each step's events.  `roofline` reports the dominant kernel, timed with CUDA events
+recorded by the library on the launch stream; `e2e` repeats the measurement through the C
+interface from pinned host buffers (H2D of the step's inputs and D2H of its output inside
+the timed region); `cpu_baseline` times the fp64 CPU oracle on a bounded sample.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOADS = {
+    "tiny": 0, "prefill_d64": 1, "prefill_d128": 2, "decode": 3, "mixed": 4,
+}
+PREFILL_LIKE = {"tiny", "prefill_d64", "prefill_d128"}
+METRIC = "varlen GQA attention TFLOP/s (prefill) & KV GB/s (decode), % of roofline"
+L2_FLUSH_BYTES = 512 << 20
+
+
+def useful_work(call):
+    """(flops, kv_bytes, q_out_bytes) the call must do: 4*D*Hq per (row, visible key) pair,
+    K and V bytes of the union of each valid segment's visible positions, and q/out bytes of
+    the rows valid segments cover."""
+    T, rows, cols, W = call.T, call.rows, call.cols, call.window
+    pairs = 0
+    kv = 0
+    covered = 0
+    owners = np.zeros(T, dtype=np.int64)
+    segs = np.asarray(call.seq_info, dtype=np.int64)
+    ok = []
+    for (qs, ql, col, ke) in segs:
+        bad = ql < 0 or qs < 0 or qs + ql > T or col < 0 or col >= cols or ke < 0
+        if not bad and ql > 0 and ke > 0:
+            span = min(ke, ql + W - 1) if W > 0 else ke
+            bad = span > rows
+        ok.append(not bad)
+        if not bad and ql > 0:
+            owners[qs:qs + ql] += 1
+    for (qs, ql, col, ke), good in zip(segs, ok):
+        if not good or ql <= 0 or (owners[qs:qs + ql] > 1).any():
+            continue
+        p = ke - ql + np.arange(ql)
+        hi = np.minimum(p + 1, ke) if call.causal else np.full(ql, ke)
+        lo = np.maximum(0, p - W + 1) if W > 0 else np.zeros(ql, dtype=np.int64)
+        pairs += int(np.maximum(hi - lo, 0).sum())
+        if ke > 0:
+            span = min(ke, ql + W - 1) if W > 0 else ke
+            kv += span * call.Hkv * call.D * 2 * 2
+        covered += ql
+    return 4 * call.D * call.Hq * pairs, kv, 2 * covered * call.Hq * call.D * 2
+
+
+def read_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return d.get("hbm_gbs", 6800.0), d.get("bf16_tflops", 1900.0), d.get("bf16_tflops_sustained"), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 200 ms during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.reader = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.reader = threading.Thread(target=self._read, daemon=True)
+            self.reader.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.reader.join(timeout=2)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("gloo")
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def cpu_baseline(wl, prefill_like: bool, budget_s: float = 12.0):
+    """Time the fp64 oracle on a bounded sample: the last rows of each call (the heaviest
+    ones under causal masking), as many as fit the time budget."""
+    from oracle import sdpa_varlen_oracle as O
+
+    t0 = time.perf_counter()
+    done_flops = 0
+    done_bytes = 0
+    n_rows = 0
+    for c in wl.calls:
+        seg_id, lo, hi, _ = O.visible_interval(c.seq_info, c.T, c.causal, c.window, c.rows, c.cols)
+        live = [t for t in range(c.T) if seg_id[t] >= 0]
+        step = 8
+        idx = len(live)
+        while idx > 0 and time.perf_counter() - t0 < budget_s / len(wl.calls):
+            rows = live[max(0, idx - step):idx]
+            idx -= step
+            O.sdpa_varlen(c.q, c.k_store, c.v_store, c.seq_info, c.causal, c.window, c.scale, rows_subset=rows)
+            n_rows += len(rows)
+            done_flops += 4 * c.D * c.Hq * int(np.maximum(hi[rows] - lo[rows], 0).sum())
+            # bytes: the visible K/V rows these query rows need (per KV head), once per row block
+            for s in set(int(seg_id[t]) for t in rows):
+                qs, ql, col, ke = (int(x) for x in c.seq_info[s])
+                span = O.needed_span(ql, ke, c.window)
+                done_bytes += span * c.Hkv * c.D * 2 * 2
+    el = time.perf_counter() - t0
+    cores = len(os.sched_getaffinity(0))
+    value = done_flops / el / 1e12 if prefill_like else done_bytes / el / 1e9
+    return {"value": value, "unit": "TFLOP/s" if prefill_like else "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"{n_rows} packed rows (all heads) of {wl.name}, the last rows of each call, "
+                      f"{el:.1f} s of fp64 NumPy on {cores} host cores"}
+
+
+def run_reference(args, wl, world, rank):
+    """The reference arm: the CPU oracle, as it stands, on a bounded sample per step."""
+    if rank != 0:
+        return
+    prefill_like = args.workload in PREFILL_LIKE
+    per_step = max(1.0, min(6.0, 150.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        cpu_baseline(wl, prefill_like, budget_s=per_step)
+    t0 = time.perf_counter()
+    vals = [cpu_baseline(wl, prefill_like, budget_s=per_step) for _ in range(args.steps)]
+    el = time.perf_counter() - t0
+    v = statistics.mean(x["value"] for x in vals)
+    unit = vals[0]["unit"]
+    line = {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": unit, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": wl.name, "description": wl.description},
+        "cpu_baseline": {"value": v, "unit": unit, "cores": vals[0]["cores"], "kind": "oracle",
+                         "sample": vals[0]["sample"]},
+        "e2e": {"value": v, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default="prefill_d128", choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world, rank, local = dist_setup()
+    from workloads import synth
+
+    wl = synth.workload(WORKLOADS[args.workload], seed=args.seed)
+    if args.impl == "reference":
+        run_reference(args, wl, world, rank)
+        return
+
+    import torch
+
+    import varlen_gqa_attention_gb300 as pkg
+
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    prefill_like = args.workload in PREFILL_LIKE
+
+    # device-resident inputs, outputs and workspaces
+    calls = []
+    T_total = max(c.row_end or c.T for c in wl.calls)
+    out = torch.empty((T_total, wl.calls[0].Hq, wl.calls[0].D), dtype=torch.bfloat16, device=dev)
+    for c in wl.calls:
+        d = dict(call=c, q=c.q.to(dev), k=c.k_store.to(dev), v=c.v_store.to(dev),
+                 seq=torch.from_numpy(c.seq_info).to(dev),
+                 ws=torch.empty(pkg.workspace_bytes(c.T, c.Hq, c.Hkv, c.D, len(c.seq_info)),
+                                dtype=torch.uint8, device=dev))
+        d["out"] = out[c.row_begin:(c.row_end or c.T)]
+        calls.append(d)
+    flops = sum(useful_work(c)[0] for c in wl.calls)
+    kv_bytes = sum(useful_work(c)[1] for c in wl.calls)
+    qo_bytes = sum(useful_work(c)[2] for c in wl.calls)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(evs=None):
+        for i, d in enumerate(calls):
+            if evs is not None:
+                pkg.set_timing_events(evs[i])
+            c = d["call"]
+            pkg.sdpa_varlen(d["q"], d["k"], d["v"], d["seq"], causal=c.causal, window=c.window,
+                            scale=c.scale, out=d["out"], workspace=d["ws"])
+        if evs is not None:
+            pkg.set_timing_events(None)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in calls] for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    for k in range(args.steps):
+        flush.fill_(k & 0xFF)  # L2 flush outside the step's events
+        step(ev[k])
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+
+    step_ms = []
+    kern_ms = {"sched": [], "prefill": [], "splitk": [], "combine": []}
+    for k in range(args.steps):
+        tot = 0.0
+        for i in range(len(calls)):
+            e = ev[k][i]
+            tot += e[0].elapsed_time(e[4])
+            kern_ms["sched"].append(e[0].elapsed_time(e[1]))
+            kern_ms["prefill"].append(e[1].elapsed_time(e[2]))
+            kern_ms["splitk"].append(e[2].elapsed_time(e[3]))
+            kern_ms["combine"].append(e[3].elapsed_time(e[4]))
+        step_ms.append(tot)
+    ms = statistics.mean(step_ms)
+    ms_all = max_over_ranks(ms, world)
+    if prefill_like:
+        value = world * flops / (ms_all * 1e-3) / 1e12
+        unit = "TFLOP/s"
+    else:
+        value = world * kv_bytes / (ms_all * 1e-3) / 1e9
+        unit = "GB/s"
+
+    # dominant kernel and its roofline
+    hbm, bf16, bf16_sus, peak_src = read_peaks()
+    means = {k: statistics.mean(v) * len(calls) for k, v in kern_ms.items()}
+    dom = max(("prefill", "splitk"), key=lambda k: means[k])
+    dom_ms = means[dom]
+    if prefill_like:
+        achieved = flops / (dom_ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": bf16, "unit": "TFLOP/s",
+                "frac": achieved / bf16, "traffic": None, "kernel": dom,
+                "peak_source": f"{peak_src} bf16 dense (burst)"}
+    else:
+        alg = kv_bytes + qo_bytes
+        achieved = alg / (dom_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                "frac": achieved / hbm, "traffic": None, "kernel": dom,
+                "peak_source": f"{peak_src} HBM copy"}
+
+    # end to end through the C interface from pinned host buffers
+    host = []
+    h2d = 0
+    for d in calls:
+        c = d["call"]
+        hq, hk, hv = c.q.pin_memory(), c.k_store.pin_memory(), c.v_store.pin_memory()
+        hs = torch.from_numpy(c.seq_info.copy()).pin_memory()
+        host.append((hq, hk, hv, hs))
+        h2d += hq.numel() * 2 + hk.numel() * 2 + hv.numel() * 2 + hs.numel() * 4
+    hout = torch.empty(out.shape, dtype=torch.bfloat16).pin_memory()
+    d2h = hout.numel() * 2
+
+    def e2e_step():
+        for d, (hq, hk, hv, hs) in zip(calls, host):
+            d["q"].copy_(hq, non_blocking=True)
+            d["k"].copy_(hk, non_blocking=True)
+            d["v"].copy_(hv, non_blocking=True)
+            d["seq"].copy_(hs, non_blocking=True)
+            c = d["call"]
+            pkg.sdpa_varlen(d["q"], d["k"], d["v"], d["seq"], causal=c.causal, window=c.window,
+                            scale=c.scale, out=d["out"], workspace=d["ws"])
+        hout.copy_(out, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_ms = []
+    for k in range(args.steps):
+        flush.fill_(k & 0xFF)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms.append(a.elapsed_time(b))
+    e2e = max_over_ranks(statistics.mean(e2e_ms), world)
+    e2e_val = world * (flops if prefill_like else kv_bytes) / (e2e * 1e-3) / (1e12 if prefill_like else 1e9)
+
+    launches = args.steps * len(calls) * 3
+
+    if rank != 0:
+        return
+    base = None
+    if not args.no_cpu_baseline:
+        base = cpu_baseline(wl, prefill_like)
+    vs = None
+    if args.workload == "prefill_d128":
+        vs = value / 160.1  # RTX 5090 Triton TMA, 27.039 ms on this shape (pages' operator table)
+    line = {
+        "metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_all, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": vs, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": wl.name, "description": wl.description, "seed": args.seed,
+                   "l2": "flushed between steps (512 MiB write outside the step's events)",
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "useful_tflop_per_step": flops / 1e12, "kv_gb_per_step": kv_bytes / 1e9},
+        "roofline": roof,
+        "kernel_ms": {k: statistics.mean(v) for k, v in kern_ms.items()},
+        "e2e": {"value": e2e_val, "unit": unit, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e},
+        "gpu_launches": launches,
+        "clocks": clk,
+        "cpu_baseline": base,
+    }
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

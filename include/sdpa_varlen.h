@@ -119,6 +119,13 @@ sdpa_status sdpa_causal_prefill(const void* q, const void* k, const void* v, int
 /* Set the process-wide route policy (SDPA_ROUTE_*).  Returns SDPA_ERR_ARG if unknown. */
 sdpa_status sdpa_set_route_policy(int policy);
 
+/* Timing hook for this thread's next calls.  `events` holds 5 cudaEvent_t handles (or is
+ * NULL to switch the hook off); each call then records them on its stream at the kernel
+ * boundaries: [0] before the scheduler, [1] before the prefill kernel, [2] before the
+ * split-K kernel, [3] before the combine pass, [4] after it.  The caller owns the events.
+ * Returns SDPA_ERR_ARG if n != 5 while events is non-NULL. */
+sdpa_status sdpa_set_timing_events(void* const* events, int n);
+
 /* Message describing the last failure on this thread ("" if none). */
 const char* sdpa_last_error(void);
 

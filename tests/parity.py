@@ -24,8 +24,11 @@ def run_call(call, dev, *, out=None, q=None, k=None, v=None, status=None, seq_ov
     v = call.v_store.to(dev) if v is None else v
     si = call.seq_info if seq_override is None else seq_override
     seq = torch.from_numpy(np.ascontiguousarray(si, dtype=np.int32)).to(dev)
+    # a workspace full of 0xFF bytes (NaN floats, -1 ints): nothing may rely on its contents
+    ws = torch.full((pkg.workspace_bytes(call.T, call.Hq, call.Hkv, call.D, len(si)),), 255,
+                    dtype=torch.uint8, device=dev)
     return pkg.sdpa_varlen(q, k, v, seq, causal=call.causal, window=call.window, scale=call.scale,
-                           out=out, status=status)
+                           out=out, status=status, workspace=ws)
 
 
 def oracle(call, rows_subset=None, seq_override=None, k=None, v=None):

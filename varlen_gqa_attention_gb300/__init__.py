@@ -19,7 +19,8 @@ import torch
 from . import _build
 
 __all__ = [
-    "sdpa_varlen", "sdpa_causal_prefill", "workspace_bytes", "set_route_policy", "library",
+    "sdpa_varlen", "sdpa_causal_prefill", "workspace_bytes", "set_route_policy", "set_timing_events",
+    "library",
     "SDPA_OK", "SEG_BAD_QRANGE", "SEG_BAD_COL", "SEG_BAD_KV", "SEG_SPAN", "SEG_OVERLAP",
     "DEV_TIMEOUT", "ROUTE_AUTO", "ROUTE_SPLITK", "ROUTE_PREFILL", "SdpaError",
 ]
@@ -36,7 +37,7 @@ STATUS_NAMES = {
 
 EXPORTS = [
     "sdpa_varlen_workspace_bytes", "sdpa_varlen", "sdpa_causal_prefill", "sdpa_set_route_policy",
-    "sdpa_last_error", "sdpa_version",
+    "sdpa_set_timing_events", "sdpa_last_error", "sdpa_version",
 ]
 
 
@@ -72,6 +73,8 @@ def library(build_if_missing: bool = True) -> ctypes.CDLL:
                                         c_vp, c_vp, ctypes.c_size_t, c_vp]
     lib.sdpa_set_route_policy.restype = c_int
     lib.sdpa_set_route_policy.argtypes = [c_int]
+    lib.sdpa_set_timing_events.restype = c_int
+    lib.sdpa_set_timing_events.argtypes = [ctypes.POINTER(c_vp), c_int]
     lib.sdpa_last_error.restype = ctypes.c_char_p
     lib.sdpa_last_error.argtypes = []
     lib.sdpa_version.restype = c_int
@@ -91,6 +94,17 @@ def workspace_bytes(T: int, Hq: int, Hkv: int, D: int, S: int) -> int:
 
 def set_route_policy(policy: int) -> None:
     _check(library().sdpa_set_route_policy(policy))
+
+
+def set_timing_events(events) -> None:
+    """Record 5 torch.cuda.Event objects at the kernel boundaries of this thread's next calls
+    (scheduler | prefill | split-K | combine); ``None`` switches the hook off."""
+    lib = library()
+    if events is None:
+        _check(lib.sdpa_set_timing_events(None, 0))
+        return
+    arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
+    _check(lib.sdpa_set_timing_events(arr, len(events)))
 
 
 def _workspace(nbytes: int, device) -> torch.Tensor:

@@ -14,6 +14,12 @@
 namespace sdpa {
 
 static thread_local char g_err[512] = "";
+static thread_local cudaEvent_t g_ev[5] = {nullptr, nullptr, nullptr, nullptr, nullptr};
+static thread_local bool g_ev_on = false;
+
+static cudaError_t mark(int i, cudaStream_t st) {
+  return g_ev_on ? cudaEventRecord(g_ev[i], st) : cudaSuccess;
+}
 static std::atomic<int> g_policy{SDPA_ROUTE_AUTO};
 
 static sdpa_status fail(sdpa_status code, const char* fmt, ...) {
@@ -91,25 +97,30 @@ static sdpa_status check_common(int64_t T, int Hq, int Hkv, int D, int S, int64_
 
 static sdpa_status launch_all(const SchedArgs& sa, const AttnArgs& aa, int D, const Grids& g,
                               cudaStream_t st) {
-  cudaError_t e;
-  {
+  cudaError_t e = mark(0, st);
+  if (e == cudaSuccess) {
     void* args[] = {(void*)&sa};
     e = cudaLaunchKernel(sched_kernel_ptr(), dim3(1), dim3(kSchedThreads), args, 0, st);
     if (e != cudaSuccess) return fail(SDPA_ERR_CUDA, "scheduler launch: %s", cudaGetErrorString(e));
   }
-  {
+  if (e == cudaSuccess) e = mark(1, st);
+  if (e == cudaSuccess) e = mark(2, st);
+  if (e == cudaSuccess) {
     void* args[] = {(void*)&aa};
     e = cudaLaunchKernel(splitk_kernel_ptr(D), dim3((unsigned)g.splitk), dim3(128), args,
                          splitk_smem_bytes(D), st);
     if (e != cudaSuccess) return fail(SDPA_ERR_CUDA, "split-K launch: %s", cudaGetErrorString(e));
   }
-  if (aa.T > 0) {
+  if (e == cudaSuccess) e = mark(3, st);
+  if (e == cudaSuccess && aa.T > 0) {
     void* args[] = {(void*)&aa};
     const int64_t warps = aa.T * aa.Hq;
     const int64_t blocks = (warps * 32 + 255) / 256;
     e = cudaLaunchKernel(combine_kernel_ptr(D), dim3((unsigned)blocks), dim3(256), args, 0, st);
     if (e != cudaSuccess) return fail(SDPA_ERR_CUDA, "combine launch: %s", cudaGetErrorString(e));
   }
+  if (e == cudaSuccess) e = mark(4, st);
+  if (e != cudaSuccess) return fail(SDPA_ERR_CUDA, "timing event: %s", cudaGetErrorString(e));
   return SDPA_OK;
 }
 
@@ -232,6 +243,20 @@ sdpa_status sdpa_set_route_policy(int policy) {
   if (policy != SDPA_ROUTE_AUTO && policy != SDPA_ROUTE_SPLITK && policy != SDPA_ROUTE_PREFILL)
     return fail(SDPA_ERR_ARG, "unknown route policy %d", policy);
   g_policy.store(policy);
+  return SDPA_OK;
+}
+
+sdpa_status sdpa_set_timing_events(void* const* events, int n) {
+  if (!events) {
+    g_ev_on = false;
+    return SDPA_OK;
+  }
+  if (n != 5) return fail(SDPA_ERR_ARG, "timing hook takes 5 events, got %d", n);
+  for (int i = 0; i < 5; ++i) {
+    if (!events[i]) return fail(SDPA_ERR_NULL, "timing event %d is NULL", i);
+    g_ev[i] = (cudaEvent_t)events[i];
+  }
+  g_ev_on = true;
   return SDPA_OK;
 }
 

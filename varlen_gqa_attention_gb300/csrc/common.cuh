@@ -49,7 +49,7 @@ struct UnitRec {
 struct SchedHdr {
   int64_t tiles[3];   // total tiles per route (index = route)
   int64_t units[3];   // units per route
-  int64_t grid[3];    // CTAs per route (as launched)
+  int64_t grid[3];    // working CTAs per route: min(launched grid, tiles)
   int64_t status;     // OR of the status bits of this call
   int64_t pad[4];
 };

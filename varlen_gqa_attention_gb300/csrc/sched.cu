@@ -11,7 +11,8 @@
 //   4. counts each unit's key tiles over the union of its rows' visible intervals and lays
 //      all units' tiles end to end; CTA g of a route's persistent grid of G CTAs owns tiles
 //      [g*W/G, (g+1)*W/G) of that line (a stream-K split, so every CTA gets the same amount
-//      of key tiles whatever the length mix), and each (unit, CTA) pair gets a slot of
+//      of key tiles whatever the length mix; G is capped at W so that no CTA is idle inside
+//      a unit's range), and each (unit, CTA) pair gets a slot of
 //      partial results unless the unit has a single CTA, which then writes `out` itself.
 // One CTA of 1024 threads does all of it; block-wide scans give the prefix sums.
 #include "common.cuh"
@@ -184,7 +185,9 @@ __global__ void __launch_bounds__(kSchedThreads) sdpa_sched_kernel(SchedArgs A) 
     }
     int64_t Wt;
     int64_t tb = block_excl_scan(my_tiles, &Wt, sh);
-    const int64_t G = A.grid[q];
+    // Effective grid: at most one CTA per tile, so every working CTA owns at least one tile
+    // and the CTAs between a unit's first and last owner all work on it (nslots is exact).
+    const int64_t G = min(A.grid[q], max(Wt, (int64_t)1));
     int64_t my_rows = 0;
     for (int64_t u = ua; u < ub; ++u) {
       UnitRec ur = units[u];

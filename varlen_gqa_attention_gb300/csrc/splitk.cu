@@ -303,8 +303,8 @@ __global__ void __launch_bounds__(kSplitkThreads) sdpa_splitk_kernel(AttnArgs A)
   const SchedHdr* hdr = A.ws.hdr;
   const int64_t Wt = hdr->tiles[kRouteSplitk];
   const int64_t U = hdr->units[kRouteSplitk];
-  const int64_t G = gridDim.x;
-  if (Wt == 0) return;
+  const int64_t G = hdr->grid[kRouteSplitk];  // effective grid chosen by the scheduler
+  if (Wt == 0 || (int64_t)blockIdx.x >= G) return;
   int64_t t0 = sk_start(blockIdx.x, Wt, G);
   const int64_t t1 = sk_start(blockIdx.x + 1, Wt, G);
   if (t0 >= t1) return;

@@ -281,6 +281,9 @@ def main():
     torch.cuda.synchronize()
 
     ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in calls] for _ in range(args.steps)]
+    for e in (e for a in ev for b in a for e in b):
+        e.record(stream)  # torch creates the CUDA event on its first record
+    torch.cuda.synchronize()
     clocks = ClockSampler(local)
     clocks.start()
     barrier(world)

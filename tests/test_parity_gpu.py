@@ -142,8 +142,10 @@ def test_nan_in_invisible_cells_changes_no_output_bit(dev, route):
 def test_index_sets_are_bit_exact(dev, route, causal, window, rows):
     rng = np.random.default_rng(rows + window)
     max_q = min(40, rows - window + 1) if window else 40
-    call = synth.random_call(rng, D=64, Hq=8, Hkv=2, T=200, S=8, rows=rows, cols=4, causal=causal,
-                             window=window, max_q=max_q, max_kv=min(4000, 3 * rows), gen_seed=1)
+    # each segment owns its column, so every store cell spells one position
+    call = synth.random_call(rng, D=64, Hq=8, Hkv=2, T=200, S=8, rows=rows, cols=8, causal=causal,
+                             window=window, max_q=max_q, max_kv=min(4000, 3 * rows), gen_seed=1,
+                             distinct_cols=True)
     call.scale = 64.0
     seg_id, lo, hi, _ = O.visible_interval(call.seq_info, call.T, causal, window, rows, call.cols)
     for sign in (+1, -1):

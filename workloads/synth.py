@@ -169,7 +169,7 @@ def workload(index: int, seed: int = 0) -> Workload:
 
 def random_call(rng: np.random.Generator, *, D: int, Hq: int, Hkv: int, T: int, S: int,
                 rows: int, cols: int, causal: bool, window: int, max_q: int, max_kv: int,
-                gen_seed: int, allow_gaps: bool = True) -> Call:
+                gen_seed: int, allow_gaps: bool = True, distinct_cols: bool = False) -> Call:
     """A random segment table over packed rows (with uncovered gaps), for parity sweeps.
 
     Only draws numbers: segments are laid end to end with random gaps and kv_end is
@@ -186,6 +186,8 @@ def random_call(rng: np.random.Generator, *, D: int, Hq: int, Hkv: int, T: int, 
             ql = max(0, T - t)
         ke = int(rng.integers(0, max_kv + 1))
         col = int(rng.integers(0, cols))
+        if distinct_cols:
+            col = s % cols  # one sequence per column
         segs.append((t, ql, col, ke))
         t += ql
     gen = torch.Generator().manual_seed(gen_seed)

@@ -9,6 +9,9 @@
 #include <cstdio>
 #include <mutex>
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "common.cuh"
 
 namespace sdpa {
@@ -37,6 +40,7 @@ struct DevInfo {
   bool ready = false;
   int sms = 0;
   int splitk_per_sm[3] = {0, 0, 0};  // D = 64, 128, 256
+  bool prefill_ok[3] = {false, false, false};
 };
 static std::mutex g_mu;
 static DevInfo g_dev[64];
@@ -63,11 +67,60 @@ static sdpa_status device_info(DevInfo* out) {
       e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, f, 128, smem);
       if (e != cudaSuccess) return fail(SDPA_ERR_CUDA, "occupancy: %s", cudaGetErrorString(e));
       di.splitk_per_sm[k] = nb > 0 ? nb : 1;
+      const void* pf = prefill_kernel_ptr(Ds[k]);
+      e = cudaFuncSetAttribute(pf, cudaFuncAttributeMaxDynamicSharedMemorySize, prefill_smem_bytes(Ds[k]));
+      di.prefill_ok[k] = e == cudaSuccess;
+      if (e != cudaSuccess) cudaGetLastError();  // leave no sticky error; split-K covers it
     }
     di.ready = true;
   }
   *out = di;
   return SDPA_OK;
+}
+
+// cuTensorMapEncodeTiled, fetched from the driver once (no link against libcuda).
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = (PFN_cuTensorMapEncodeTiled_v12000)p;
+    else
+      cudaGetLastError();
+  });
+  return fn;
+}
+
+// TMA descriptors of q [T, Hq, D] (box: 64 dims x group heads x 128/group rows, i.e. one
+// 128-row tile of packed (row, head) pairs) and of the stores [rows, cols, Hkv, D] (box:
+// 64 dims x 1 head x 1 column x `bn` rows), all with 128-byte swizzle.
+static bool make_tensor_maps(const void* q, int64_t T, int Hq, int D, int64_t q_rs, int64_t q_hs,
+                             const void* k, const void* v, int64_t rows, int cols, int Hkv, int group,
+                             int bn, CUtensorMap* mq, CUtensorMap* mk, CUtensorMap* mv) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc || T <= 0 || q_hs <= 0 || q_rs <= 0) return false;
+  const cuuint32_t es[4] = {1, 1, 1, 1};
+  const cuuint64_t qdim[3] = {(cuuint64_t)D, (cuuint64_t)Hq, (cuuint64_t)T};
+  const cuuint64_t qstr[2] = {(cuuint64_t)q_hs * 2, (cuuint64_t)q_rs * 2};
+  const cuuint32_t qbox[3] = {64, (cuuint32_t)group, (cuuint32_t)(kPrefillRows / group)};
+  if (enc(mq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, (void*)q, qdim, qstr, qbox, es,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  const cuuint64_t kdim[4] = {(cuuint64_t)D, (cuuint64_t)Hkv, (cuuint64_t)cols, (cuuint64_t)rows};
+  const cuuint64_t kstr[3] = {(cuuint64_t)D * 2, (cuuint64_t)Hkv * D * 2, (cuuint64_t)cols * Hkv * D * 2};
+  const cuuint32_t kbox[4] = {64, 1, 1, (cuuint32_t)bn};
+  for (int w = 0; w < 2; ++w) {
+    if (enc(w ? mv : mk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, (void*)(w ? v : k), kdim, kstr, kbox, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return false;
+  }
+  return true;
 }
 
 struct Grids {
@@ -95,8 +148,12 @@ static sdpa_status check_common(int64_t T, int Hq, int Hkv, int D, int S, int64_
   return SDPA_OK;
 }
 
+struct TensorMaps {
+  CUtensorMap q, k, v;
+};
+
 static sdpa_status launch_all(const SchedArgs& sa, const AttnArgs& aa, int D, const Grids& g,
-                              cudaStream_t st) {
+                              const TensorMaps& tm, cudaStream_t st) {
   cudaError_t e = mark(0, st);
   if (e == cudaSuccess) {
     void* args[] = {(void*)&sa};
@@ -104,6 +161,12 @@ static sdpa_status launch_all(const SchedArgs& sa, const AttnArgs& aa, int D, co
     if (e != cudaSuccess) return fail(SDPA_ERR_CUDA, "scheduler launch: %s", cudaGetErrorString(e));
   }
   if (e == cudaSuccess) e = mark(1, st);
+  if (e == cudaSuccess && sa.prefill_ok) {
+    void* args[] = {(void*)&aa, (void*)&tm.q, (void*)&tm.k, (void*)&tm.v};
+    e = cudaLaunchKernel(prefill_kernel_ptr(D), dim3((unsigned)g.prefill), dim3(192), args,
+                         prefill_smem_bytes(D), st);
+    if (e != cudaSuccess) return fail(SDPA_ERR_CUDA, "prefill launch: %s", cudaGetErrorString(e));
+  }
   if (e == cudaSuccess) e = mark(2, st);
   if (e == cudaSuccess) {
     void* args[] = {(void*)&aa};
@@ -164,7 +227,13 @@ static sdpa_status run(const void* q, int64_t T, int Hq, int D, int64_t q_rs, in
   sa.causal = causal ? 1 : 0;
   sa.window = window;
   sa.policy = g_policy.load();
-  sa.prefill_ok = 0;
+  TensorMaps tm;
+  const int group = Hq / Hkv;
+  const bool group_fits = group <= kPrefillRows && (kPrefillRows % group) == 0;
+  sa.tile_pf = prefill_tile_keys(D);
+  sa.prefill_ok = di.prefill_ok[d_index(D)] && group_fits &&
+                  make_tensor_maps(q, T, Hq, D, q_rs, q_hs, k, v, rows, cols, Hkv, group, sa.tile_pf,
+                                   &tm.q, &tm.k, &tm.v);
   sa.grid[0] = 0;
   sa.grid[1] = g.splitk;
   sa.grid[2] = g.prefill;
@@ -192,7 +261,7 @@ static sdpa_status run(const void* q, int64_t T, int Hq, int D, int64_t q_rs, in
   aa.T = T;
   aa.ws = W;
   aa.status_dev = status_dev;
-  return launch_all(sa, aa, D, g, (cudaStream_t)stream);
+  return launch_all(sa, aa, D, g, tm, (cudaStream_t)stream);
 }
 
 }  // namespace sdpa

@@ -135,7 +135,8 @@ struct SchedArgs {
   int64_t T, rows;
   int cols, Hkv, group, causal, window;
   int policy;      // SDPA_ROUTE_*
-  int prefill_ok;  // prefill kernel available for this call's head dim
+  int prefill_ok;  // prefill kernel usable for this call (group divides 128, tensor maps made)
+  int tile_pf;     // keys per prefill tile
   int64_t grid[3];
   Workspace ws;
   int32_t* status_dev;
@@ -148,6 +149,9 @@ const void* sched_kernel_ptr();
 const void* splitk_kernel_ptr(int D);
 int splitk_smem_bytes(int D);
 const void* combine_kernel_ptr(int D);
+const void* prefill_kernel_ptr(int D);
+int prefill_smem_bytes(int D);
+int prefill_tile_keys(int D);
 
 // Segment validity (SDPA_SEG_* bits), same rule on host and device.
 __host__ __device__ inline int32_t segment_bits(int64_t q_start, int64_t q_len, int64_t col,

@@ -1,0 +1,469 @@
+// prefill.cu - tensor-memory attention kernel for long segments on sm_103a.
+//
+// "[CUDA] Use Triton TMA for long-context causal prefill" (Summary: TMA-staged tiles,
+// per-head-dim tile configurations, guarded online softmax so fully masked rows stay finite,
+// real output strides) and "[executorch][cuda] Add a length-aware Triton SDPA over
+// per-sequence KV columns" (segments over a column store, causal / window masks, GQA).
+// The pages' Triton design targets SM90 / RTX 5090; this kernel is written for Blackwell's
+// fifth-generation tensor cores instead:
+//
+//   * a persistent grid of one CTA per SM walks the stream-K tile line of the prefill route
+//     (same scheduler output as the split-K kernel): every CTA gets the same number of key
+//     tiles, units being (segment, KV head, 128 packed rows r = i * group + g) - the query
+//     heads sharing a KV head fill the MMA's M dimension together (GQA packing);
+//   * warp 4 (producer) moves Q and K/V tiles with TMA (128-byte swizzle) into a ring of
+//     shared-memory stages; the store is a 4-d tensor [rows, cols, Hkv, D], so a tile of one
+//     column and KV head is one box;
+//   * warp 5 (one thread) issues tcgen05.mma: S = Q K^T into one of two tensor-memory
+//     buffers (fp32, 128 lanes x BN columns), then O += P V into a tensor-memory accumulator;
+//     completion is signalled with tcgen05.commit on mbarriers;
+//   * warps 0-3 (softmax): one thread per row reads its S row from tensor memory, masks by
+//     select (causal, window, piece bounds), keeps a base-2 running max with lazy rescaling
+//     (O is only rescaled when the max grows by more than 2^8), writes P as bf16 into a
+//     swizzled shared-memory tile for the PV MMA, and at the end of a piece normalises O and
+//     writes `out` (the unit's only CTA) or a log-sum-exp partial for the combine pass;
+//   * V rows past the last visible key of a unit are zeroed in shared memory before the PV
+//     MMA, so stale or NaN store cells never meet a zero probability (0 * NaN).
+// Every mbarrier wait is bounded; a wait that gives up sets SDPA_DEV_TIMEOUT and the CTA
+// unwinds, frees its tensor memory and exits.
+#include <cuda.h>
+
+#include "tc.cuh"
+
+namespace sdpa {
+
+template <int D>
+struct PfCfg {
+  static constexpr int BM = kPrefillRows;                 // 128 packed rows
+  static constexpr int BN = D == 256 ? 64 : kPrefillTile;  // keys per tile
+  static constexpr int STAGES = D == 64 ? 4 : 2;
+  static constexpr int NREG = D / 64;                     // 64-element (128-byte) column regions
+  static constexpr int Q_BYTES = BM * D * 2;
+  static constexpr int KV_BYTES = BN * D * 2;             // K (or V) of one stage
+  static constexpr int P_BYTES = BM * BN * 2;
+  static constexpr int S_COL0 = 0;                        // S buffers: columns [b*BN, (b+1)*BN)
+  static constexpr int O_COL = 2 * BN;                    // O: columns [2*BN, 2*BN + D)
+  static constexpr int TMEM_COLS = (2 * BN + D) <= 256 ? 256 : 512;
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_K = OFF_Q + Q_BYTES;
+  static constexpr int OFF_V = OFF_K + STAGES * KV_BYTES;
+  static constexpr int OFF_P = OFF_V + STAGES * KV_BYTES;
+  static constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
+  static constexpr int BAR_BYTES = 256;
+  static constexpr int SMEM = OFF_BAR + BAR_BYTES + 1024;  // + alignment slack
+};
+static_assert(PfCfg<128>::SMEM <= 232448, "prefill D=128 shared memory");
+static_assert(PfCfg<64>::SMEM <= 232448, "prefill D=64 shared memory");
+static_assert(PfCfg<256>::SMEM <= 232448, "prefill D=256 shared memory");
+
+constexpr int kPfThreads = 192;
+
+// barrier slots (8 bytes each) inside the barrier block
+struct PfBars {
+  static constexpr int KV_FULL = 0;    // [4]
+  static constexpr int KV_EMPTY = 4;   // [4]
+  static constexpr int V_READY = 8;    // [4]
+  static constexpr int S_FULL = 12;    // [2]
+  static constexpr int S_FREE = 14;    // [2]
+  static constexpr int P_FULL = 16;    // [2]
+  static constexpr int O_DONE = 18;
+  static constexpr int Q_FULL = 19;
+  static constexpr int Q_EMPTY = 20;
+  static constexpr int DRAIN = 21;
+};
+
+struct PfPiece {
+  UnitRec ur;
+  SegRec sg;
+  int64_t ta, tb;
+  int slot;
+};
+
+__device__ __forceinline__ bool pf_next(const Workspace& W, int64_t& t0, int64_t t1, int64_t& u,
+                                        int64_t U, PfPiece& pc) {
+  while (t0 < t1 && u < U) {
+    const UnitRec ur = W.units[kRoutePrefill][u];
+    if (ur.ntiles == 0 || t0 >= ur.tile_base + ur.ntiles) {
+      ++u;
+      continue;
+    }
+    pc.ur = ur;
+    pc.sg = W.segs[ur.seg];
+    pc.ta = t0 - ur.tile_base;
+    pc.tb = min(t1, ur.tile_base + ur.ntiles) - ur.tile_base;
+    pc.slot = (int)(blockIdx.x - ur.g_first);
+    t0 = ur.tile_base + pc.tb;
+    ++u;
+    return true;
+  }
+  return false;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kPfThreads, 1)
+    sdpa_prefill_kernel(const AttnArgs A, const __grid_constant__ CUtensorMap tmQ,
+                        const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV) {
+  using C = PfCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_abort;
+
+  const SchedHdr* hdr = A.ws.hdr;
+  const int64_t Wt = hdr->tiles[kRoutePrefill];
+  const int64_t U = hdr->units[kRoutePrefill];
+  const int64_t G = hdr->grid[kRoutePrefill];
+  if (Wt == 0 || (int64_t)blockIdx.x >= G) return;  // whole CTA leaves before any setup
+  const int64_t t_begin = sk_start(blockIdx.x, Wt, G), t_end = sk_start(blockIdx.x + 1, Wt, G);
+  if (t_begin >= t_end) return;
+
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t sQ = sbase + C::OFF_Q, sK = sbase + C::OFF_K, sV = sbase + C::OFF_V,
+                 sP = sbase + C::OFF_P, sBar = sbase + C::OFF_BAR;
+  auto bar = [&](int i) { return sBar + 8u * (uint32_t)i; };
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  volatile int* abort = &s_abort;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(bar(PfBars::KV_FULL + s), 1);
+      mbar_init(bar(PfBars::KV_EMPTY + s), 1);
+      mbar_init(bar(PfBars::V_READY + s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(PfBars::S_FULL + b), 1);
+      mbar_init(bar(PfBars::S_FREE + b), 128);
+      mbar_init(bar(PfBars::P_FULL + b), 128);
+    }
+    mbar_init(bar(PfBars::O_DONE), 1);
+    mbar_init(bar(PfBars::Q_FULL), 1);
+    mbar_init(bar(PfBars::Q_EMPTY), 1);
+    mbar_init(bar(PfBars::DRAIN), 1);
+    s_abort = 0;
+    mbar_fence_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(smem_u32(&s_tmem), C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+
+  // first unit holding tile t_begin
+  const UnitRec* units = A.ws.units[kRoutePrefill];
+  int64_t u0 = 0;
+  {
+    int64_t lo = 0, hi = U - 1;
+    while (lo <= hi) {
+      const int64_t mid = (lo + hi) >> 1;
+      if (units[mid].tile_base <= t_begin) { u0 = mid; lo = mid + 1; } else { hi = mid - 1; }
+    }
+  }
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ TMA producer
+    int64_t t0 = t_begin, u = u0;
+    PfPiece pc;
+    uint32_t gt = 0, pi = 0;
+    bool ok = true;
+    while (ok && pf_next(A.ws, t0, t_end, u, U, pc)) {
+      const int hk = pc.ur.hk;
+      if (lane == 0) {
+        ok = mbar_wait(bar(PfBars::Q_EMPTY), (pi & 1) ^ 1, abort);
+        if (ok) {
+          mbar_expect_tx(bar(PfBars::Q_FULL), C::Q_BYTES);
+          const int qrow = pc.sg.q_start + (int)(((int64_t)pc.ur.rb * C::BM) / A.group);
+#pragma unroll
+          for (int c = 0; c < C::NREG; ++c)
+            tma_load_3d(sQ + c * (C::BM * 128), &tmQ, bar(PfBars::Q_FULL), 64 * c, hk * A.group, qrow);
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      const int64_t pos_lo = (int64_t)pc.ur.lo + pc.ta * C::BN;
+      const int64_t pos_hi = min((int64_t)pc.ur.lo + pc.tb * C::BN, (int64_t)pc.ur.hi);
+      const int n = (int)(pc.tb - pc.ta);
+      for (int j = 0; ok && j < n; ++j, ++gt) {
+        const int s = gt % C::STAGES;
+        const uint32_t use = gt / C::STAGES;
+        const int64_t j0 = pos_lo + (int64_t)j * C::BN;
+        const int valid = (int)min((int64_t)C::BN, pos_hi - j0);
+        if (lane == 0) {
+          ok = mbar_wait(bar(PfBars::KV_EMPTY + s), (use & 1) ^ 1, abort);
+          if (ok) {
+            mbar_expect_tx(bar(PfBars::KV_FULL + s), 2 * C::KV_BYTES);
+            const int row0 = (int)(j0 % A.rows);
+#pragma unroll
+            for (int c = 0; c < C::NREG; ++c) {
+              tma_load_4d(sK + s * C::KV_BYTES + c * (C::BN * 128), &tmK, bar(PfBars::KV_FULL + s),
+                          64 * c, hk, pc.sg.col, row0);
+              tma_load_4d(sV + s * C::KV_BYTES + c * (C::BN * 128), &tmV, bar(PfBars::KV_FULL + s),
+                          64 * c, hk, pc.sg.col, row0);
+            }
+          }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        if (valid < C::BN) {
+          // V rows past the last visible key: wait for the tile, then zero them
+          ok = mbar_wait(bar(PfBars::KV_FULL + s), use & 1, abort);
+          ok = __all_sync(0xffffffffu, ok);
+          if (!ok) break;
+          const int bytes = (C::BN - valid) * 128;
+#pragma unroll
+          for (int c = 0; c < C::NREG; ++c) {
+            uint8_t* reg = smem + C::OFF_V + s * C::KV_BYTES + c * (C::BN * 128) + valid * 128;
+            for (int o = lane * 16; o < bytes; o += 32 * 16)
+              *reinterpret_cast<uint4*>(reg + o) = make_uint4(0, 0, 0, 0);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+        }
+        if (lane == 0) mbar_arrive(bar(PfBars::V_READY + s));
+      }
+      ++pi;
+    }
+    // drain: the copies this warp started must land before the CTA can exit (immediate on
+    // the normal path, where the MMA warp already consumed every stage and Q tile)
+    if (lane == 0) {
+      int dummy = 0;
+      const uint32_t first = gt > (uint32_t)C::STAGES ? gt - C::STAGES : 0u;
+      for (uint32_t g = first; g < gt; ++g)
+        mbar_wait(bar(PfBars::KV_FULL + g % C::STAGES), (g / C::STAGES) & 1, &dummy);
+      if (pi > 0) mbar_wait(bar(PfBars::Q_FULL), (pi - 1) & 1, &dummy);
+    }
+    __syncwarp();
+  } else if (warp == 5) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t IDESC_QK = idesc_bf16_f32(128, C::BN, false, false);
+      constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, D, false, true);
+      int64_t t0 = t_begin, u = u0;
+      PfPiece pc;
+      uint32_t gt = 0, pi = 0;
+      bool ok = true;
+      auto issue_s = [&](uint32_t g) -> bool {
+        const int s = g % C::STAGES, b = g & 1;
+        if (!mbar_wait(bar(PfBars::KV_FULL + s), (g / C::STAGES) & 1, abort)) return false;
+        if (!mbar_wait(bar(PfBars::S_FREE + b), ((g >> 1) & 1) ^ 1, abort)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+          const uint64_t a = sdesc_sw128(sQ + (k >> 2) * (C::BM * 128) + (k & 3) * 32, 16, 1024);
+          const uint64_t bd =
+              sdesc_sw128(sK + s * C::KV_BYTES + (k >> 2) * (C::BN * 128) + (k & 3) * 32, 16, 1024);
+          tc_mma_ss(tmem + C::S_COL0 + b * C::BN, a, bd, IDESC_QK, k > 0 ? 1u : 0u);
+        }
+        tc_commit(bar(PfBars::S_FULL + b));
+        return true;
+      };
+      while (ok && pf_next(A.ws, t0, t_end, u, U, pc)) {
+        ok = mbar_wait(bar(PfBars::Q_FULL), pi & 1, abort);
+        if (!ok) break;
+        tc_fence_after();
+        const int n = (int)(pc.tb - pc.ta);
+        ok = issue_s(gt);
+        for (int j = 0; ok && j < n; ++j) {
+          const uint32_t g = gt + j;
+          if (j + 1 < n) {
+            ok = issue_s(g + 1);
+            if (!ok) break;
+          } else {
+            tc_commit(bar(PfBars::Q_EMPTY));  // every S of this piece has been issued
+          }
+          const int b = g & 1, s = g % C::STAGES;
+          ok = mbar_wait(bar(PfBars::P_FULL + b), (g >> 1) & 1, abort) &&
+               mbar_wait(bar(PfBars::V_READY + s), (g / C::STAGES) & 1, abort);
+          if (!ok) break;
+          tc_fence_after();
+#pragma unroll
+          for (int k = 0; k < C::BN / 16; ++k) {
+            const uint64_t a = sdesc_sw128(sP + b * C::P_BYTES + (k >> 2) * (C::BM * 128) + (k & 3) * 32, 16, 1024);
+            const uint64_t bd = sdesc_sw128(sV + s * C::KV_BYTES + k * 16 * 128, C::BN * 128, 1024);
+            tc_mma_ss(tmem + C::O_COL, a, bd, IDESC_PV, (j > 0 || k > 0) ? 1u : 0u);
+          }
+          tc_commit(bar(PfBars::O_DONE));
+          tc_commit(bar(PfBars::KV_EMPTY + s));
+        }
+        gt += n;
+        ++pi;
+      }
+      // drain: wait (bounded) until every MMA this thread issued has finished
+      tc_commit(bar(PfBars::DRAIN));
+      int dummy = 0;
+      mbar_wait(bar(PfBars::DRAIN), 0, &dummy);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax + epilogue
+    const int row = threadIdx.x;  // 0..127 = tensor-memory lane
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const float sl2 = A.scale_log2;
+    int64_t t0 = t_begin, u = u0;
+    PfPiece pc;
+    uint32_t gt = 0;
+    bool ok = true;
+    while (ok && pf_next(A.ws, t0, t_end, u, U, pc)) {
+      const UnitRec& ur = pc.ur;
+      const SegRec& sg = pc.sg;
+      const bool live = row < ur.rows;
+      const int64_t r = (int64_t)ur.rb * C::BM + row;
+      const int qi = (int)(r / A.group);
+      const int64_t pos_lo = (int64_t)ur.lo + pc.ta * C::BN;
+      const int64_t pos_hi = min((int64_t)ur.lo + pc.tb * C::BN, (int64_t)ur.hi);
+      int64_t rlo = 1, rhi = 0;  // padding rows see nothing
+      if (live) {
+        const RowWin w = row_window(qi, sg.q_len, sg.kv_end, A.causal, A.window);
+        rlo = max((int64_t)w.lo, pos_lo);
+        rhi = min((int64_t)w.hi, pos_hi);
+      }
+      const int n = (int)(pc.tb - pc.ta);
+      float m_use = -INFINITY, l = 0.f;
+      for (int j = 0; j < n; ++j) {
+        const uint32_t g = gt + j;
+        const int b = g & 1;
+        ok = mbar_wait(bar(PfBars::S_FULL + b), (g >> 1) & 1, abort);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after();
+        float s[C::BN];
+#pragma unroll
+        for (int c = 0; c < C::BN / 32; ++c) tmem_ld32(tmem + lane_off + C::S_COL0 + b * C::BN + 32 * c, s + 32 * c);
+        tc_fence_before();
+        mbar_arrive(bar(PfBars::S_FREE + b));
+
+        const int64_t j0 = pos_lo + (int64_t)j * C::BN;
+        const bool full = j0 >= rlo && j0 + C::BN <= rhi;
+        float mx = -INFINITY;
+#pragma unroll
+        for (int k = 0; k < C::BN; ++k) {
+          float x = s[k] * sl2;
+          if (!full) x = (j0 + k >= rlo && j0 + k < rhi) ? x : -INFINITY;
+          s[k] = x;
+          mx = fmaxf(mx, x);
+        }
+        const float m_new = fmaxf(m_use, mx);
+        const bool resc = m_new > m_use + 8.f;  // false while nothing is visible
+        const float alpha = resc ? exp2_approx(m_use - m_new) : 1.f;
+        const bool need_o = resc && j > 0 && m_use != -INFINITY;
+        if (__any_sync(0xffffffffu, need_o)) {
+          // O holds P V of earlier tiles: wait for the last PV, then rescale in place
+          ok = mbar_wait(bar(PfBars::O_DONE), (g - 1) & 1, abort);
+          ok = __all_sync(0xffffffffu, ok);
+          if (!ok) break;
+          tc_fence_after();
+          const float f = need_o ? alpha : 1.f;
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            float o[32];
+            tmem_ld32(tmem + lane_off + C::O_COL + 32 * c, o);
+#pragma unroll
+            for (int k = 0; k < 32; ++k) o[k] *= f;
+            tmem_st32(tmem + lane_off + C::O_COL + 32 * c, o);
+          }
+        }
+        if (resc) {
+          m_use = m_new;
+          l *= alpha;
+        }
+        const float mu = m_use == -INFINITY ? 0.f : m_use;
+        float sum = 0.f;
+#pragma unroll
+        for (int k = 0; k < C::BN; ++k) {
+          const float p = exp2_approx(s[k] - mu);
+          s[k] = p;
+          sum += p;
+        }
+        l += sum;
+        // P row (bf16) into the swizzled K-major tile of buffer b
+        uint8_t* prow = smem + C::OFF_P + b * C::P_BYTES + row * 128;
+#pragma unroll
+        for (int c = 0; c < C::BN / 8; ++c) {
+          uint4 v;
+          v.x = pack_bf16x2(s[8 * c + 0], s[8 * c + 1]);
+          v.y = pack_bf16x2(s[8 * c + 2], s[8 * c + 3]);
+          v.z = pack_bf16x2(s[8 * c + 4], s[8 * c + 5]);
+          v.w = pack_bf16x2(s[8 * c + 6], s[8 * c + 7]);
+          *reinterpret_cast<uint4*>(prow + (c >> 3) * (C::BM * 128) + (((c & 7) ^ (row & 7)) << 4)) = v;
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(bar(PfBars::P_FULL + b));
+      }
+      if (!ok) break;
+      gt += n;
+      // epilogue: wait for the last PV, then normalise (direct) or write a partial
+      ok = mbar_wait(bar(PfBars::O_DONE), (gt - 1) & 1, abort);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      const bool direct = ur.nslots == 1;
+      const int h = ur.hk * A.group + (int)(r % A.group);
+      __nv_bfloat16* orow = A.out + ((int64_t)sg.q_start + qi) * A.o_rs + (int64_t)h * A.o_hs;
+      const int64_t pidx = ur.slot_base + (int64_t)pc.slot * ur.rows + row;
+      float* prow = A.ws.part_o[kRoutePrefill] + pidx * D;
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        float o[32];
+        tmem_ld32(tmem + lane_off + C::O_COL + 32 * c, o);
+        if (!live) continue;
+        if (direct) {
+#pragma unroll
+          for (int k = 0; k < 32; k += 8) {
+            uint4 v;
+            v.x = pack_bf16x2(o[k] * inv, o[k + 1] * inv);
+            v.y = pack_bf16x2(o[k + 2] * inv, o[k + 3] * inv);
+            v.z = pack_bf16x2(o[k + 4] * inv, o[k + 5] * inv);
+            v.w = pack_bf16x2(o[k + 6] * inv, o[k + 7] * inv);
+            *reinterpret_cast<uint4*>(orow + 32 * c + k) = v;
+          }
+        } else {
+#pragma unroll
+          for (int k = 0; k < 32; k += 4)
+            *reinterpret_cast<float4*>(prow + 32 * c + k) = make_float4(o[k], o[k + 1], o[k + 2], o[k + 3]);
+        }
+      }
+      if (live && !direct) A.ws.part_ml[kRoutePrefill][pidx] = make_float2(m_use, l);
+      tc_fence_before();
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (threadIdx.x == 0 && s_abort) {
+    atomicOr((int*)&A.ws.hdr->status, SDPA_DEV_TIMEOUT);
+    if (A.status_dev) atomicOr(A.status_dev, SDPA_DEV_TIMEOUT);
+  }
+  if (warp == 5) tmem_dealloc(tmem, C::TMEM_COLS);
+}
+
+template __global__ void sdpa_prefill_kernel<64>(const AttnArgs, const __grid_constant__ CUtensorMap,
+                                                 const __grid_constant__ CUtensorMap,
+                                                 const __grid_constant__ CUtensorMap);
+template __global__ void sdpa_prefill_kernel<128>(const AttnArgs, const __grid_constant__ CUtensorMap,
+                                                  const __grid_constant__ CUtensorMap,
+                                                  const __grid_constant__ CUtensorMap);
+template __global__ void sdpa_prefill_kernel<256>(const AttnArgs, const __grid_constant__ CUtensorMap,
+                                                  const __grid_constant__ CUtensorMap,
+                                                  const __grid_constant__ CUtensorMap);
+
+const void* prefill_kernel_ptr(int D) {
+  switch (D) {
+    case 64: return (const void*)sdpa_prefill_kernel<64>;
+    case 128: return (const void*)sdpa_prefill_kernel<128>;
+    default: return (const void*)sdpa_prefill_kernel<256>;
+  }
+}
+int prefill_smem_bytes(int D) {
+  switch (D) {
+    case 64: return PfCfg<64>::SMEM;
+    case 128: return PfCfg<128>::SMEM;
+    default: return PfCfg<256>::SMEM;
+  }
+}
+int prefill_tile_keys(int D) { return D == 256 ? PfCfg<256>::BN : PfCfg<128>::BN; }
+
+}  // namespace sdpa

@@ -66,8 +66,25 @@ __device__ __forceinline__ void load_seg(const SchedArgs& A, int s, int32_t* seg
 __device__ __forceinline__ int rows_per_unit(int route) {
   return route == kRoutePrefill ? kPrefillRows : kSplitkRows;
 }
-__device__ __forceinline__ int tile_len(int route) {
-  return route == kRoutePrefill ? kPrefillTile : kSplitkTile;
+__device__ __forceinline__ int tile_len(const SchedArgs& A, int route) {
+  return route == kRoutePrefill ? A.tile_pf : kSplitkTile;
+}
+
+// Route of a live segment.  The prefill kernel takes segments that fill at least one
+// 128-row tile and whose visible keys do not wrap around a ring store (a TMA box cannot
+// wrap); everything else, and everything when the prefill kernel is unusable, goes to
+// the split-K kernel.
+__device__ __forceinline__ int route_of(const SchedArgs& A, const SegRec& r) {
+  const int64_t R = (int64_t)r.q_len * A.group;
+  if (A.policy == SDPA_ROUTE_SPLITK || !A.prefill_ok) return kRouteSplitk;
+  if (r.kv_end > 0) {
+    int64_t span = r.kv_end;
+    if (A.window > 0) span = min(span, (int64_t)r.q_len + A.window - 1);
+    const int64_t first = r.kv_end - span;
+    if (first / A.rows != (r.kv_end - 1) / A.rows) return kRouteSplitk;
+  }
+  if (A.policy == SDPA_ROUTE_PREFILL) return kRoutePrefill;
+  return R >= kPrefillRows ? kRoutePrefill : kRouteSplitk;
 }
 
 __global__ void __launch_bounds__(kSchedThreads) sdpa_sched_kernel(SchedArgs A) {
@@ -118,11 +135,8 @@ __global__ void __launch_bounds__(kSchedThreads) sdpa_sched_kernel(SchedArgs A) 
     SegRec r = W.segs[s];
     if (r.bits == 0 && W.seg_flag[s]) atomicOr(&s_status, SDPA_SEG_OVERLAP);
     if (r.bits || W.seg_flag[s] || r.q_len == 0) continue;
-    int64_t R = (int64_t)r.q_len * A.group;
-    int route;
-    if (A.policy == SDPA_ROUTE_SPLITK || !A.prefill_ok) route = kRouteSplitk;
-    else if (A.policy == SDPA_ROUTE_PREFILL) route = kRoutePrefill;
-    else route = R >= kPrefillRows ? kRoutePrefill : kRouteSplitk;
+    const int64_t R = (int64_t)r.q_len * A.group;
+    const int route = route_of(A, r);
     const int rpu = rows_per_unit(route);
     const int nrb = (int)((R + rpu - 1) / rpu);
     W.segs[s].route = route;
@@ -147,7 +161,7 @@ __global__ void __launch_bounds__(kSchedThreads) sdpa_sched_kernel(SchedArgs A) 
   // 4. per route: units, their tiles, the stream-K split and partial slots
   for (int q = 1; q < 3; ++q) {
     const int64_t U = s_tot[q];
-    const int rpu = rows_per_unit(q), tl = tile_len(q);
+    const int rpu = rows_per_unit(q), tl = tile_len(A, q);
     UnitRec* units = W.units[q];
     int64_t ua, ub;
     my_range(U, &ua, &ub);

@@ -20,8 +20,15 @@ static thread_local char g_err[512] = "";
 static thread_local cudaEvent_t g_ev[5] = {nullptr, nullptr, nullptr, nullptr, nullptr};
 static thread_local bool g_ev_on = false;
 
+// Records timing event i on `st`.  Under stream capture the record must become an event
+// node of the graph (cudaEventRecordExternal) so that it fires on every replay.
 static cudaError_t mark(int i, cudaStream_t st) {
-  return g_ev_on ? cudaEventRecord(g_ev[i], st) : cudaSuccess;
+  if (!g_ev_on) return cudaSuccess;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(st, &cs);
+  if (e != cudaSuccess) return e;
+  return cs == cudaStreamCaptureStatusActive ? cudaEventRecordWithFlags(g_ev[i], st, cudaEventRecordExternal)
+                                             : cudaEventRecord(g_ev[i], st);
 }
 static std::atomic<int> g_policy{SDPA_ROUTE_AUTO};
 

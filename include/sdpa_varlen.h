@@ -126,6 +126,33 @@ sdpa_status sdpa_set_route_policy(int policy);
  * Returns SDPA_ERR_ARG if n != 5 while events is non-NULL. */
 sdpa_status sdpa_set_timing_events(void* const* events, int n);
 
+/* Bytes of the device array that sdpa_varlen_splitk_static uses as its scratch (32 MiB).
+ * Every GPU that loads the library holds this array until the process exits. */
+#define SDPA_STATIC_SCRATCH_BYTES (32u << 20)
+
+/*
+ * sdpa_varlen for callers that cannot allocate device memory.  (The pages have no
+ * counterpart: this entry point exists for callers such as a runtime with a fixed memory
+ * plan, a plugin that may not call cudaMalloc, or a binding with no device allocator, which
+ * cannot provide sdpa_varlen's workspace.)
+ *
+ * Arguments and results are those of sdpa_varlen without `workspace`/`ws_bytes`; every
+ * segment runs on the split-K kernel.  The scratch is a file-scope device array of
+ * SDPA_STATIC_SCRATCH_BYTES inside the library; nothing is allocated.  Sizes whose scratch
+ * does not fit return SDPA_ERR_WORKSPACE (sdpa_last_error() says how much they need).
+ * The first call on each device looks up the array's device address (with that device
+ * current) and configures the kernels: make that first call before any stream capture.
+ * All calls on a device share the one array and it keeps the last call's contents; nothing
+ * in it needs to start at zero, but calls that overlap on the GPU (different streams, or
+ * graphs replayed at the same time) race on it and must be serialised by the caller.
+ */
+sdpa_status sdpa_varlen_splitk_static(const void* q, int64_t T, int Hq, int D, int64_t q_row_stride,
+                                      int64_t q_head_stride, const void* k_store, const void* v_store,
+                                      int64_t rows, int cols, int Hkv, const int32_t* seq_info, int S,
+                                      int causal, int window, float scale, void* out,
+                                      int64_t o_row_stride, int64_t o_head_stride, int32_t* status_dev,
+                                      void* stream);
+
 /* Message describing the last failure on this thread ("" if none). */
 const char* sdpa_last_error(void);
 

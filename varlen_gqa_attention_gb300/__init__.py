@@ -37,7 +37,7 @@ STATUS_NAMES = {
 
 EXPORTS = [
     "sdpa_varlen_workspace_bytes", "sdpa_varlen", "sdpa_causal_prefill", "sdpa_set_route_policy",
-    "sdpa_set_timing_events", "sdpa_last_error", "sdpa_version",
+    "sdpa_set_timing_events", "sdpa_last_error", "sdpa_version", "sdpa_varlen_splitk_static",
 ]
 
 
@@ -183,5 +183,34 @@ def sdpa_causal_prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale
     code = lib.sdpa_causal_prefill(q.data_ptr(), k.data_ptr(), v.data_ptr(), Lq, Lkv, Hq, Hkv, D,
                                    float(scale), out.data_ptr(), workspace.data_ptr(),
                                    workspace.numel(), _stream_ptr(stream))
+    _check(code)
+    return out
+
+
+def sdpa_varlen_splitk_static(q: torch.Tensor, k_store: torch.Tensor, v_store: torch.Tensor,
+                              seq_info: torch.Tensor, *, causal: bool, window: int = 0,
+                              scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
+                              status: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """sdpa_varlen for callers that cannot allocate device scratch: the library's own static
+    device array (SDPA_STATIC_SCRATCH_BYTES) serves as the workspace and every segment runs on
+    the split-K kernel.  Pass ``out`` to allocate nothing at all.  Calls must not overlap on
+    the GPU (they share the array); make the first call on a device outside stream capture."""
+    lib = library()
+    fn = lib.sdpa_varlen_splitk_static
+    c_i64, c_int, c_vp, c_f = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_float
+    fn.restype = c_int
+    fn.argtypes = [c_vp, c_i64, c_int, c_int, c_i64, c_i64, c_vp, c_vp, c_i64, c_int, c_int, c_vp,
+                   c_int, c_int, c_int, c_f, c_vp, c_i64, c_i64, c_vp, c_vp]
+    T, Hq, D = q.shape
+    rows, cols, Hkv, _ = k_store.shape
+    S = seq_info.shape[0] if seq_info.numel() else 0
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty((T, Hq, D), dtype=torch.bfloat16, device=q.device)
+    code = fn(q.data_ptr(), T, Hq, D, q.stride(0), q.stride(1), k_store.data_ptr(), v_store.data_ptr(),
+              rows, cols, Hkv, seq_info.data_ptr() if S else None, S, int(bool(causal)), int(window),
+              float(scale), out.data_ptr(), out.stride(0), out.stride(1),
+              status.data_ptr() if status is not None else None, _stream_ptr(stream))
     _check(code)
     return out

@@ -40,6 +40,8 @@ static sdpa_status fail(sdpa_status code, const char* fmt, ...) {
   return code;
 }
 
+void set_last_error(const char* msg) { snprintf(g_err, sizeof(g_err), "%s", msg); }
+
 static bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
 // Per-device launch facts, measured once.

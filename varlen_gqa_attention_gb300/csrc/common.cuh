@@ -152,6 +152,8 @@ const void* combine_kernel_ptr(int D);
 const void* prefill_kernel_ptr(int D);
 int prefill_smem_bytes(int D);
 int prefill_tile_keys(int D);
+// Sets the message sdpa_last_error() returns on this thread.
+void set_last_error(const char* msg);
 
 // Segment validity (SDPA_SEG_* bits), same rule on host and device.
 __host__ __device__ inline int32_t segment_bits(int64_t q_start, int64_t q_len, int64_t col,

@@ -1,0 +1,211 @@
+// noalloc.cu - an entry point for callers that cannot allocate device memory.
+//
+// sdpa_varlen needs a caller-provided workspace.  Some callers cannot provide one: code that
+// runs where no allocator is available or allowed (a runtime with a fixed memory plan, a
+// plugin that must not call cudaMalloc, a host language binding without a device allocator).
+// sdpa_varlen_splitk_static serves them: it runs the scheduler, the split-K kernel and the
+// combine pass (every segment on the split-K route) with their scratch in a file-scope
+// device array of kStaticScratchBytes, and allocates nothing.
+//
+// The array is a host-side stand-in symbol in host code, not a device address: its device
+// address is fetched with cudaGetSymbolAddress once per device (with that device current)
+// on the first call there, and passed to the kernels.  That first call should come before
+// any stream capture.  Every call on a device shares the one array, which keeps the last
+// call's contents; nothing in it needs to start at zero (the scheduler kernel writes every
+// field the later kernels read), but two calls that overlap on the GPU (different streams,
+// or graphs replayed concurrently) race on it.
+#include <cmath>
+#include <cstdio>
+#include <mutex>
+
+#include "common.cuh"
+
+namespace sdpa {
+
+constexpr size_t kStaticScratchBytes = (size_t)SDPA_STATIC_SCRATCH_BYTES;
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
+namespace {
+
+struct StaticDev {
+  bool ready = false;
+  void* scratch = nullptr;  // device address of g_static_scratch on this device
+  int sms = 0;
+  int per_sm[3] = {0, 0, 0};  // split-K CTAs per SM for D = 64, 128, 256
+};
+std::mutex g_static_mu;
+StaticDev g_static_dev[64];
+sdpa_status static_fail(sdpa_status code, const char* msg) {
+  set_last_error(msg);
+  return code;
+}
+
+int dix(int D) { return D == 64 ? 0 : D == 128 ? 1 : 2; }
+
+// Once per device, with that device current: the scratch address and the launch facts.
+sdpa_status static_setup(StaticDev* out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+    return static_fail(SDPA_ERR_CUDA, "no current CUDA device");
+  std::lock_guard<std::mutex> lk(g_static_mu);
+  StaticDev& sd = g_static_dev[dev];
+  if (!sd.ready) {
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
+    if (e != cudaSuccess || p == nullptr) {
+      cudaGetLastError();
+      return static_fail(SDPA_ERR_CUDA, "cudaGetSymbolAddress of the static scratch failed");
+    }
+    if (cudaDeviceGetAttribute(&sd.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return static_fail(SDPA_ERR_CUDA, "SM count query failed");
+    const int Ds[3] = {64, 128, 256};
+    for (int k = 0; k < 3; ++k) {
+      const void* f = splitk_kernel_ptr(Ds[k]);
+      const int smem = splitk_smem_bytes(Ds[k]);
+      int nb = 0;
+      if (cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
+          cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, f, 128, smem) != cudaSuccess)
+        return static_fail(SDPA_ERR_CUDA, "split-K kernel setup failed");
+      sd.per_sm[k] = nb > 0 ? nb : 1;
+    }
+    sd.scratch = p;
+    sd.ready = true;
+  }
+  *out = sd;
+  return SDPA_OK;
+}
+
+// Workspace layout with the split-K route only (no prefill tables); same records as the
+// general layout.  Returns the bytes it needs.
+size_t layout_splitk_only(char* base, int64_t T, int Hq, int Hkv, int D, int S, int64_t grid,
+                          Workspace* ws) {
+  int64_t off = 0;
+  auto take = [&](int64_t bytes) {
+    const int64_t o = off;
+    off = align_up(off + bytes, 256);
+    return base ? base + o : nullptr;
+  };
+  Workspace w{};
+  w.hdr = (SchedHdr*)take(sizeof(SchedHdr));
+  w.segs = (SegRec*)take((int64_t)sizeof(SegRec) * (S > 0 ? S : 1));
+  w.row_seg = (int32_t*)take(4 * (T > 0 ? T : 1));
+  w.seg_flag = (int32_t*)take(4 * (S > 0 ? S : 1));
+  w.unit_cap[kRouteSplitk] = unit_cap(T, Hq, Hkv, S, kSplitkRows);
+  w.part_cap[kRouteSplitk] = part_cap(w.unit_cap[kRouteSplitk], grid, kSplitkRows);
+  w.units[kRouteSplitk] = (UnitRec*)take((int64_t)sizeof(UnitRec) * w.unit_cap[kRouteSplitk]);
+  w.part_ml[kRouteSplitk] = (float2*)take(8 * w.part_cap[kRouteSplitk]);
+  w.part_o[kRouteSplitk] = (float*)take(4 * w.part_cap[kRouteSplitk] * D);
+  if (ws) *ws = w;
+  return (size_t)off;
+}
+
+}  // namespace
+}  // namespace sdpa
+
+using namespace sdpa;
+
+extern "C" sdpa_status sdpa_varlen_splitk_static(
+    const void* q, int64_t T, int Hq, int D, int64_t q_row_stride, int64_t q_head_stride,
+    const void* k_store, const void* v_store, int64_t rows, int cols, int Hkv, const int32_t* seq_info,
+    int S, int causal, int window, float scale, void* out, int64_t o_row_stride, int64_t o_head_stride,
+    int32_t* status_dev, void* stream) {
+  set_last_error("");
+  if (T < 0 || S < 0 || Hq <= 0 || Hkv <= 0 || rows <= 0 || cols <= 0 || T > INT32_MAX || rows > INT32_MAX)
+    return static_fail(SDPA_ERR_SHAPE, "bad sizes");
+  if (D != 64 && D != 128 && D != 256) return static_fail(SDPA_ERR_HEAD_DIM, "head dim not in {64,128,256}");
+  if (Hq % Hkv != 0 || Hq / Hkv > 128) return static_fail(SDPA_ERR_GQA, "Hq must be a multiple of Hkv (group <= 128)");
+  if (window < 0 || !std::isfinite(scale)) return static_fail(SDPA_ERR_ARG, "window < 0 or scale not finite");
+  if (!q || !k_store || !v_store || !out || (!seq_info && S > 0))
+    return static_fail(SDPA_ERR_NULL, "a required pointer is NULL");
+  if (((uintptr_t)q | (uintptr_t)k_store | (uintptr_t)v_store | (uintptr_t)out | (uintptr_t)seq_info) & 15u)
+    return static_fail(SDPA_ERR_ALIGN, "tensor pointers must be 16-byte aligned");
+  if (q_row_stride % 8 || q_head_stride % 8 || o_row_stride % 8 || o_head_stride % 8 || q_row_stride < 0 ||
+      q_head_stride < 0 || o_row_stride < 0 || o_head_stride < 0)
+    return static_fail(SDPA_ERR_STRIDE, "row/head strides must be non-negative multiples of 8 elements");
+
+  StaticDev sd;
+  sdpa_status st = static_setup(&sd);
+  if (st) return st;
+  // The general grid if its scratch fits; otherwise fewer CTAs, down to one per SM.
+  int64_t grid = (int64_t)sd.sms * sd.per_sm[dix(D)];
+  size_t need = layout_splitk_only(nullptr, T, Hq, Hkv, D, S, grid, nullptr);
+  if (need > kStaticScratchBytes) {
+    grid = sd.sms;
+    need = layout_splitk_only(nullptr, T, Hq, Hkv, D, S, grid, nullptr);
+  }
+  if (need > kStaticScratchBytes) {
+    char msg[256];
+    snprintf(msg, sizeof(msg),
+             "these sizes need %zu bytes of scratch; the static scratch holds %zu bytes "
+             "(use sdpa_varlen with a caller-provided workspace)",
+             need, kStaticScratchBytes);
+    return static_fail(SDPA_ERR_WORKSPACE, msg);
+  }
+  Workspace W;
+  layout_splitk_only((char*)sd.scratch, T, Hq, Hkv, D, S, grid, &W);
+
+  SchedArgs sa{};
+  sa.seq_info = seq_info;
+  sa.S = S;
+  sa.use_inline = 0;
+  sa.T = T;
+  sa.rows = rows;
+  sa.cols = cols;
+  sa.Hkv = Hkv;
+  sa.group = Hq / Hkv;
+  sa.causal = causal ? 1 : 0;
+  sa.window = window;
+  sa.policy = SDPA_ROUTE_SPLITK;
+  sa.prefill_ok = 0;
+  sa.tile_pf = kPrefillTile;
+  sa.grid[0] = 0;
+  sa.grid[1] = grid;
+  sa.grid[2] = 0;
+  sa.ws = W;
+  sa.status_dev = status_dev;
+
+  AttnArgs aa{};
+  aa.q = (const __nv_bfloat16*)q;
+  aa.q_rs = q_row_stride;
+  aa.q_hs = q_head_stride;
+  aa.k = (const __nv_bfloat16*)k_store;
+  aa.v = (const __nv_bfloat16*)v_store;
+  aa.rows = rows;
+  aa.cols = cols;
+  aa.Hkv = Hkv;
+  aa.Hq = Hq;
+  aa.group = Hq / Hkv;
+  aa.D = D;
+  aa.causal = sa.causal;
+  aa.window = window;
+  aa.scale_log2 = scale * 1.4426950408889634f;
+  aa.out = (__nv_bfloat16*)out;
+  aa.o_rs = o_row_stride;
+  aa.o_hs = o_head_stride;
+  aa.T = T;
+  aa.ws = W;
+  aa.status_dev = status_dev;
+
+  cudaStream_t s = (cudaStream_t)stream;
+  cudaError_t e;
+  {
+    void* args[] = {(void*)&sa};
+    e = cudaLaunchKernel(sched_kernel_ptr(), dim3(1), dim3(kSchedThreads), args, 0, s);
+  }
+  if (e == cudaSuccess) {
+    void* args[] = {(void*)&aa};
+    e = cudaLaunchKernel(splitk_kernel_ptr(D), dim3((unsigned)grid), dim3(128), args, splitk_smem_bytes(D), s);
+  }
+  if (e == cudaSuccess && T > 0) {
+    void* args[] = {(void*)&aa};
+    const int64_t blocks = (T * Hq * 32 + 255) / 256;
+    e = cudaLaunchKernel(combine_kernel_ptr(D), dim3((unsigned)blocks), dim3(256), args, 0, s);
+  }
+  if (e != cudaSuccess) {
+    char msg[256];
+    snprintf(msg, sizeof(msg), "launch failed: %s", cudaGetErrorString(e));
+    return static_fail(SDPA_ERR_CUDA, msg);
+  }
+  return SDPA_OK;
+}
+

@@ -237,7 +237,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // 2^x on the SFU (PTX ex2.approx; -inf gives +0).
 __device__ __forceinline__ float exp2_approx(float x) {
   float y;
-  asm volatile("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
   return y;
 }
 

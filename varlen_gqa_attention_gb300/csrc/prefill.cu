@@ -327,22 +327,30 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_fence_after();
-        float s[C::BN];
-#pragma unroll
-        for (int c = 0; c < C::BN / 32; ++c) tmem_ld32(tmem + lane_off + C::S_COL0 + b * C::BN + 32 * c, s + 32 * c);
-        tc_fence_before();
-        mbar_arrive(bar(PfBars::S_FREE + b));
-
+        // Pass 1: row max of the visible scores, 32 columns of S at a time.  The visible
+        // keys of this tile are columns [vlo, vhi) (tile-relative, clamped to the tile).
         const int64_t j0 = pos_lo + (int64_t)j * C::BN;
-        const bool full = j0 >= rlo && j0 + C::BN <= rhi;
-        float mx = -INFINITY;
+        const int vlo = (int)min(max(rlo - j0, (int64_t)0), (int64_t)C::BN);
+        const int vhi = (int)min(max(rhi - j0, (int64_t)0), (int64_t)C::BN);
+        const uint32_t s_addr = tmem + lane_off + C::S_COL0 + b * C::BN;
+        float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll 1
+        for (int c = 0; c < C::BN / 32; ++c) {
+          float x[32];
+          tmem_ld32(s_addr + 32 * c, x);
+          if (vlo <= 32 * c && 32 * c + 32 <= vhi) {
 #pragma unroll
-        for (int k = 0; k < C::BN; ++k) {
-          float x = s[k] * sl2;
-          if (!full) x = (j0 + k >= rlo && j0 + k < rhi) ? x : -INFINITY;
-          s[k] = x;
-          mx = fmaxf(mx, x);
+            for (int k = 0; k < 32; ++k) mx4[k & 3] = fmaxf(mx4[k & 3], x[k]);
+          } else {
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+              const bool vis = (32 * c + k >= vlo) && (32 * c + k < vhi);
+              mx4[k & 3] = fmaxf(mx4[k & 3], vis ? x[k] : -INFINITY);
+            }
+          }
         }
+        // scale is positive, so max(scale * s) = scale * max(s)
+        const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * sl2;
         const float m_new = fmaxf(m_use, mx);
         const bool resc = m_new > m_use + 8.f;  // false while nothing is visible
         const float alpha = resc ? exp2_approx(m_use - m_new) : 1.f;
@@ -367,26 +375,36 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           m_use = m_new;
           l *= alpha;
         }
-        const float mu = m_use == -INFINITY ? 0.f : m_use;
-        float sum = 0.f;
-#pragma unroll
-        for (int k = 0; k < C::BN; ++k) {
-          const float p = exp2_approx(s[k] - mu);
-          s[k] = p;
-          sum += p;
-        }
-        l += sum;
-        // P row (bf16) into the swizzled K-major tile of buffer b
+        const float nmu = m_use == -INFINITY ? 0.f : -m_use;
+        // Pass 2: p = 2^(scale*s - m), row sum, bf16 P row into the swizzled K-major tile.
         uint8_t* prow = smem + C::OFF_P + b * C::P_BYTES + row * 128;
+        float sum4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+        for (int c = 0; c < C::BN / 32; ++c) {
+          float x[32];
+          tmem_ld32(s_addr + 32 * c, x);
+          const bool all = vlo <= 32 * c && 32 * c + 32 <= vhi;
 #pragma unroll
-        for (int c = 0; c < C::BN / 8; ++c) {
-          uint4 v;
-          v.x = pack_bf16x2(s[8 * c + 0], s[8 * c + 1]);
-          v.y = pack_bf16x2(s[8 * c + 2], s[8 * c + 3]);
-          v.z = pack_bf16x2(s[8 * c + 4], s[8 * c + 5]);
-          v.w = pack_bf16x2(s[8 * c + 6], s[8 * c + 7]);
-          *reinterpret_cast<uint4*>(prow + (c >> 3) * (C::BM * 128) + (((c & 7) ^ (row & 7)) << 4)) = v;
+          for (int k = 0; k < 32; ++k) {
+            float p = exp2_approx(fmaf(x[k], sl2, nmu));
+            if (!all) p = (32 * c + k >= vlo && 32 * c + k < vhi) ? p : 0.f;
+            x[k] = p;
+            sum4[k & 3] += p;
+          }
+#pragma unroll
+          for (int q8 = 0; q8 < 4; ++q8) {
+            const int cc = 4 * c + q8;  // 16-byte chunk index within the row
+            uint4 v;
+            v.x = pack_bf16x2(x[8 * q8 + 0], x[8 * q8 + 1]);
+            v.y = pack_bf16x2(x[8 * q8 + 2], x[8 * q8 + 3]);
+            v.z = pack_bf16x2(x[8 * q8 + 4], x[8 * q8 + 5]);
+            v.w = pack_bf16x2(x[8 * q8 + 6], x[8 * q8 + 7]);
+            *reinterpret_cast<uint4*>(prow + (cc >> 3) * (C::BM * 128) + (((cc & 7) ^ (row & 7)) << 4)) = v;
+          }
         }
+        tc_fence_before();
+        mbar_arrive(bar(PfBars::S_FREE + b));  // S buffer b is read for the last time
+        l += (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
         fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(bar(PfBars::P_FULL + b));

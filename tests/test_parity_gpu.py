@@ -226,3 +226,19 @@ def test_empty_step_and_zero_segments(dev):
     out = run_call(call, dev)
     torch.cuda.synchronize()
     assert bool((out.view(torch.int16) == 0).all())
+
+
+@pytest.mark.parametrize("D", [64, 128, 256])
+def test_short_pieces_are_deterministic_and_exact(dev, route, D):
+    # one 16-query segment per KV head: every CTA gets one or two short pieces of different
+    # units, the case where an epilogue could read O before its last PV landed
+    call = synth.random_call(np.random.default_rng(D), D=D, Hq=32, Hkv=8, T=64, S=1, rows=8192, cols=2,
+                             causal=False, window=0, max_q=1, max_kv=1, gen_seed=D, allow_gaps=False)
+    call.seq_info = np.array([[0, 16, 1, 5186]], dtype=np.int32)
+    outs = [run_call(call, dev).clone() for _ in range(4)]
+    torch.cuda.synchronize()
+    for o in outs[1:]:
+        assert torch.equal(outs[0].view(torch.int16), o.view(torch.int16))
+    ref, seg_id, _ = oracle(call)
+    _, lo, hi, _ = O.visible_interval(call.seq_info, call.T, False, 0, call.rows, call.cols)
+    assert_matches(outs[0], ref, seg_id, lo, hi, tag=f"short pieces D{D}")

@@ -70,6 +70,10 @@ struct PfBars {
   static constexpr int Q_FULL = 19;
   static constexpr int Q_EMPTY = 20;
   static constexpr int DRAIN = 21;
+  // completes once per piece, after the piece's last PV: the epilogue waits on it with the
+  // piece parity.  (O_DONE completes once per PV; when the softmax runs ahead it can be two
+  // phases behind at the end of a piece, which a parity wait cannot tell from done.)
+  static constexpr int O_FINAL = 22;
 };
 
 struct PfPiece {
@@ -139,6 +143,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     mbar_init(bar(PfBars::Q_FULL), 1);
     mbar_init(bar(PfBars::Q_EMPTY), 1);
     mbar_init(bar(PfBars::DRAIN), 1);
+    mbar_init(bar(PfBars::O_FINAL), 1);
     s_abort = 0;
     mbar_fence_init();
   }
@@ -284,6 +289,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             tc_mma_ss(tmem + C::O_COL, a, bd, IDESC_PV, (j > 0 || k > 0) ? 1u : 0u);
           }
           tc_commit(bar(PfBars::O_DONE));
+          if (j + 1 == n) tc_commit(bar(PfBars::O_FINAL));
           tc_commit(bar(PfBars::KV_EMPTY + s));
         }
         gt += n;
@@ -302,7 +308,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     const float sl2 = A.scale_log2;
     int64_t t0 = t_begin, u = u0;
     PfPiece pc;
-    uint32_t gt = 0;
+    uint32_t gt = 0, pi = 0;
     bool ok = true;
     while (ok && pf_next(A.ws, t0, t_end, u, U, pc)) {
       const UnitRec& ur = pc.ur;
@@ -327,30 +333,30 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         ok = __all_sync(0xffffffffu, ok);
         if (!ok) break;
         tc_fence_after();
-        // Pass 1: row max of the visible scores, 32 columns of S at a time.  The visible
-        // keys of this tile are columns [vlo, vhi) (tile-relative, clamped to the tile).
+        // The whole S row in one batch of tensor-memory loads; the buffer is free at once.
         const int64_t j0 = pos_lo + (int64_t)j * C::BN;
         const int vlo = (int)min(max(rlo - j0, (int64_t)0), (int64_t)C::BN);
         const int vhi = (int)min(max(rhi - j0, (int64_t)0), (int64_t)C::BN);
-        const uint32_t s_addr = tmem + lane_off + C::S_COL0 + b * C::BN;
-        float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll 1
-        for (int c = 0; c < C::BN / 32; ++c) {
-          float x[32];
-          tmem_ld32(s_addr + 32 * c, x);
-          if (vlo <= 32 * c && 32 * c + 32 <= vhi) {
+        float x[C::BN];
+        if constexpr (C::BN == 128)
+          tmem_ld128(tmem + lane_off + C::S_COL0 + b * C::BN, x);
+        else
+          tmem_ld64(tmem + lane_off + C::S_COL0 + b * C::BN, x);
+        tc_fence_before();
+        mbar_arrive(bar(PfBars::S_FREE + b));
+        // columns outside [vlo, vhi) (masked keys, stale cells past the last key) -> -inf
+        if (vlo > 0 || vhi < C::BN) {
 #pragma unroll
-            for (int k = 0; k < 32; ++k) mx4[k & 3] = fmaxf(mx4[k & 3], x[k]);
-          } else {
-#pragma unroll
-            for (int k = 0; k < 32; ++k) {
-              const bool vis = (32 * c + k >= vlo) && (32 * c + k < vhi);
-              mx4[k & 3] = fmaxf(mx4[k & 3], vis ? x[k] : -INFINITY);
-            }
-          }
+          for (int k = 0; k < C::BN; ++k) x[k] = (k >= vlo && k < vhi) ? x[k] : -INFINITY;
         }
+        float mx8[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mx8[k] = x[k];
+#pragma unroll
+        for (int k = 8; k < C::BN; ++k) mx8[k & 7] = fmaxf(mx8[k & 7], x[k]);
         // scale is positive, so max(scale * s) = scale * max(s)
-        const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * sl2;
+        const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) * sl2;
         const float m_new = fmaxf(m_use, mx);
         const bool resc = m_new > m_use + 8.f;  // false while nothing is visible
         const float alpha = resc ? exp2_approx(m_use - m_new) : 1.f;
@@ -376,35 +382,25 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           l *= alpha;
         }
         const float nmu = m_use == -INFINITY ? 0.f : -m_use;
-        // Pass 2: p = 2^(scale*s - m), row sum, bf16 P row into the swizzled K-major tile.
-        uint8_t* prow = smem + C::OFF_P + b * C::P_BYTES + row * 128;
-        float sum4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 1
-        for (int c = 0; c < C::BN / 32; ++c) {
-          float x[32];
-          tmem_ld32(s_addr + 32 * c, x);
-          const bool all = vlo <= 32 * c && 32 * c + 32 <= vhi;
+        // p = 2^(scale*s - m) (masked columns give 0), row sum, bf16 P into the swizzled
+        // K-major tile of buffer b
+        float sum8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-          for (int k = 0; k < 32; ++k) {
-            float p = exp2_approx(fmaf(x[k], sl2, nmu));
-            if (!all) p = (32 * c + k >= vlo && 32 * c + k < vhi) ? p : 0.f;
-            x[k] = p;
-            sum4[k & 3] += p;
-          }
-#pragma unroll
-          for (int q8 = 0; q8 < 4; ++q8) {
-            const int cc = 4 * c + q8;  // 16-byte chunk index within the row
-            uint4 v;
-            v.x = pack_bf16x2(x[8 * q8 + 0], x[8 * q8 + 1]);
-            v.y = pack_bf16x2(x[8 * q8 + 2], x[8 * q8 + 3]);
-            v.z = pack_bf16x2(x[8 * q8 + 4], x[8 * q8 + 5]);
-            v.w = pack_bf16x2(x[8 * q8 + 6], x[8 * q8 + 7]);
-            *reinterpret_cast<uint4*>(prow + (cc >> 3) * (C::BM * 128) + (((cc & 7) ^ (row & 7)) << 4)) = v;
-          }
+        for (int k = 0; k < C::BN; ++k) {
+          x[k] = exp2_approx(fmaf(x[k], sl2, nmu));
+          sum8[k & 7] += x[k];
         }
-        tc_fence_before();
-        mbar_arrive(bar(PfBars::S_FREE + b));  // S buffer b is read for the last time
-        l += (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
+        l += ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
+        uint8_t* prow = smem + C::OFF_P + b * C::P_BYTES + row * 128;
+#pragma unroll
+        for (int cc = 0; cc < C::BN / 8; ++cc) {
+          uint4 v;
+          v.x = pack_bf16x2(x[8 * cc + 0], x[8 * cc + 1]);
+          v.y = pack_bf16x2(x[8 * cc + 2], x[8 * cc + 3]);
+          v.z = pack_bf16x2(x[8 * cc + 4], x[8 * cc + 5]);
+          v.w = pack_bf16x2(x[8 * cc + 6], x[8 * cc + 7]);
+          *reinterpret_cast<uint4*>(prow + (cc >> 3) * (C::BM * 128) + (((cc & 7) ^ (row & 7)) << 4)) = v;
+        }
         fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(bar(PfBars::P_FULL + b));
@@ -412,7 +408,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       if (!ok) break;
       gt += n;
       // epilogue: wait for the last PV, then normalise (direct) or write a partial
-      ok = mbar_wait(bar(PfBars::O_DONE), (gt - 1) & 1, abort);
+      ok = mbar_wait(bar(PfBars::O_FINAL), pi & 1, abort);
+      ++pi;
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();

@@ -172,7 +172,7 @@ static sdpa_status launch_all(const SchedArgs& sa, const AttnArgs& aa, int D, co
   if (e == cudaSuccess) e = mark(1, st);
   if (e == cudaSuccess && sa.prefill_ok) {
     void* args[] = {(void*)&aa, (void*)&tm.q, (void*)&tm.k, (void*)&tm.v};
-    e = cudaLaunchKernel(prefill_kernel_ptr(D), dim3((unsigned)g.prefill), dim3(192), args,
+    e = cudaLaunchKernel(prefill_kernel_ptr(D), dim3((unsigned)g.prefill), dim3(prefill_block_threads(D)), args,
                          prefill_smem_bytes(D), st);
     if (e != cudaSuccess) return fail(SDPA_ERR_CUDA, "prefill launch: %s", cudaGetErrorString(e));
   }

@@ -152,6 +152,7 @@ const void* combine_kernel_ptr(int D);
 const void* prefill_kernel_ptr(int D);
 int prefill_smem_bytes(int D);
 int prefill_tile_keys(int D);
+int prefill_block_threads(int D);
 // Sets the message sdpa_last_error() returns on this thread.
 void set_last_error(const char* msg);
 

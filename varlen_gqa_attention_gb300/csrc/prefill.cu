@@ -11,17 +11,20 @@
 //     (same scheduler output as the split-K kernel): every CTA gets the same number of key
 //     tiles, units being (segment, KV head, 128 packed rows r = i * group + g) - the query
 //     heads sharing a KV head fill the MMA's M dimension together (GQA packing);
-//   * warp 4 (producer) moves Q and K/V tiles with TMA (128-byte swizzle) into a ring of
+//   * the producer warp moves Q and K/V tiles with TMA (128-byte swizzle) into a ring of
 //     shared-memory stages; the store is a 4-d tensor [rows, cols, Hkv, D], so a tile of one
 //     column and KV head is one box;
-//   * warp 5 (one thread) issues tcgen05.mma: S = Q K^T into one of two tensor-memory
+//   * one thread of the MMA warp issues tcgen05.mma: S = Q K^T into one of two tensor-memory
 //     buffers (fp32, 128 lanes x BN columns), then O += P V into a tensor-memory accumulator;
 //     completion is signalled with tcgen05.commit on mbarriers;
-//   * warps 0-3 (softmax): one thread per row reads its S row from tensor memory, masks by
+//   * softmax warpgroups: one thread per row reads its S row from tensor memory, masks by
 //     select (causal, window, piece bounds), keeps a base-2 running max with lazy rescaling
-//     (O is only rescaled when the max grows by more than 2^8), writes P as bf16 into a
-//     swizzled shared-memory tile for the PV MMA, and at the end of a piece normalises O and
-//     writes `out` (the unit's only CTA) or a log-sum-exp partial for the combine pass;
+//     (O is only rescaled when the max grows by more than 2^8) and writes P as bf16 into a
+//     swizzled shared-memory tile for the PV MMA.  For D <= 128 two warpgroups take
+//     alternate key tiles, each with its own running max, sum and O accumulator in tensor
+//     memory (S0, S1, O0, O1 fill the 512 columns), so two softmax streams overlap the MMAs;
+//     at the end of a piece warpgroup 0 merges the two by log-sum-exp and writes `out` (the
+//     unit's only CTA) or a partial for the combine pass.  D = 256 uses one warpgroup;
 //   * V rows past the last visible key of a unit are zeroed in shared memory before the PV
 //     MMA, so stale or NaN store cells never meet a zero probability (0 * NaN).
 // Every mbarrier wait is bounded; a wait that gives up sets SDPA_DEV_TIMEOUT and the CTA
@@ -42,27 +45,35 @@ struct PfCfg {
   static constexpr int KV_BYTES = BN * D * 2;             // K (or V) of one stage
   static constexpr int P_BYTES = BM * BN * 2;
   static constexpr int S_COL0 = 0;                        // S buffers: columns [b*BN, (b+1)*BN)
-  static constexpr int O_COL = 2 * BN;                    // O: columns [2*BN, 2*BN + D)
-  static constexpr int TMEM_COLS = (2 * BN + D) <= 256 ? 256 : 512;
+  // Two softmax warpgroups take alternate key tiles (tile g goes to warpgroup g & 1), each
+  // with its own O accumulator, when S0, S1, O0 and O1 fit in tensor memory.
+  static constexpr bool DUAL = 2 * BN + 2 * D <= 512;
+  static constexpr int SOFT_WARPS = DUAL ? 8 : 4;
+  static constexpr int THREADS = 32 * (SOFT_WARPS + 2);  // + TMA producer + MMA issuer
+  static constexpr int O_COL = 2 * BN;                    // O_b: columns [2*BN + b*D, +D)
+  static constexpr int TMEM_COLS = DUAL ? 512 : ((2 * BN + D) <= 256 ? 256 : 512);
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + Q_BYTES;
   static constexpr int OFF_V = OFF_K + STAGES * KV_BYTES;
   static constexpr int OFF_P = OFF_V + STAGES * KV_BYTES;
   static constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
-  static constexpr int BAR_BYTES = 256;
+  static constexpr int BAR_BYTES = 512 + (DUAL ? 1024 : 0);  // + (m, l) exchange of 128 rows
   static constexpr int SMEM = OFF_BAR + BAR_BYTES + 1024;  // + alignment slack
 };
 static_assert(PfCfg<128>::SMEM <= 232448, "prefill D=128 shared memory");
 static_assert(PfCfg<64>::SMEM <= 232448, "prefill D=64 shared memory");
 static_assert(PfCfg<256>::SMEM <= 232448, "prefill D=256 shared memory");
 
-constexpr int kPfThreads = 192;
 
 // barrier slots (8 bytes each) inside the barrier block
 struct PfBars {
-  static constexpr int KV_FULL = 0;    // [4]
-  static constexpr int KV_EMPTY = 4;   // [4]
-  static constexpr int V_READY = 8;    // [4]
+  // K and V stages are filled and released separately: K(g) is free once S(g) is done,
+  // V(g) once PV(g) is done, so the next K tile streams in while the softmax runs.
+  static constexpr int K_FULL = 0;     // [4]
+  static constexpr int K_EMPTY = 4;    // [4]
+  static constexpr int V_READY = 8;    // [4] V landed and, on a boundary tile, zeroed
+  static constexpr int V_FULL = 25;    // [4]
+  static constexpr int V_EMPTY = 29;   // [4]
   static constexpr int S_FULL = 12;    // [2]
   static constexpr int S_FREE = 14;    // [2]
   static constexpr int P_FULL = 16;    // [2]
@@ -74,6 +85,11 @@ struct PfBars {
   // piece parity.  (O_DONE completes once per PV; when the softmax runs ahead it can be two
   // phases behind at the end of a piece, which a parity wait cannot tell from done.)
   static constexpr int O_FINAL = 22;
+  // warpgroup 1 -> warpgroup 0: its row max and sum are in the exchange block (X_FULL), and
+  // warpgroup 0 has finished the piece's epilogue, so O1 and the block are free (X_FREE)
+  static constexpr int X_FULL = 23;
+  static constexpr int X_FREE = 24;
+  static constexpr int X_OFF = 512;  // byte offset of the exchange block (float2 per row)
 };
 
 struct PfPiece {
@@ -104,7 +120,7 @@ __device__ __forceinline__ bool pf_next(const Workspace& W, int64_t& t0, int64_t
 }
 
 template <int D>
-__global__ void __launch_bounds__(kPfThreads, 1)
+__global__ void __launch_bounds__(PfCfg<D>::THREADS, 1)
     sdpa_prefill_kernel(const AttnArgs A, const __grid_constant__ CUtensorMap tmQ,
                         const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV) {
   using C = PfCfg<D>;
@@ -126,12 +142,15 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                  sP = sbase + C::OFF_P, sBar = sbase + C::OFF_BAR;
   auto bar = [&](int i) { return sBar + 8u * (uint32_t)i; };
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int W_PROD = C::SOFT_WARPS, W_MMA = C::SOFT_WARPS + 1;
   volatile int* abort = &s_abort;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
-      mbar_init(bar(PfBars::KV_FULL + s), 1);
-      mbar_init(bar(PfBars::KV_EMPTY + s), 1);
+      mbar_init(bar(PfBars::K_FULL + s), 1);
+      mbar_init(bar(PfBars::K_EMPTY + s), 1);
+      mbar_init(bar(PfBars::V_FULL + s), 1);
+      mbar_init(bar(PfBars::V_EMPTY + s), 1);
       mbar_init(bar(PfBars::V_READY + s), 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -144,10 +163,12 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     mbar_init(bar(PfBars::Q_EMPTY), 1);
     mbar_init(bar(PfBars::DRAIN), 1);
     mbar_init(bar(PfBars::O_FINAL), 1);
+    mbar_init(bar(PfBars::X_FULL), 128);
+    mbar_init(bar(PfBars::X_FREE), 128);
     s_abort = 0;
     mbar_fence_init();
   }
-  if (warp == 5) {
+  if (warp == W_MMA) {
     tmem_alloc(smem_u32(&s_tmem), C::TMEM_COLS);
     tmem_relinquish();
   }
@@ -167,7 +188,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     }
   }
 
-  if (warp == 4) {
+  if (warp == W_PROD) {
     // ------------------------------------------------------------ TMA producer
     int64_t t0 = t_begin, u = u0;
     PfPiece pc;
@@ -195,24 +216,29 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         const int64_t j0 = pos_lo + (int64_t)j * C::BN;
         const int valid = (int)min((int64_t)C::BN, pos_hi - j0);
         if (lane == 0) {
-          ok = mbar_wait(bar(PfBars::KV_EMPTY + s), (use & 1) ^ 1, abort);
+          const int row0 = (int)(j0 % A.rows);
+          ok = mbar_wait(bar(PfBars::K_EMPTY + s), (use & 1) ^ 1, abort);
           if (ok) {
-            mbar_expect_tx(bar(PfBars::KV_FULL + s), 2 * C::KV_BYTES);
-            const int row0 = (int)(j0 % A.rows);
+            mbar_expect_tx(bar(PfBars::K_FULL + s), C::KV_BYTES);
 #pragma unroll
-            for (int c = 0; c < C::NREG; ++c) {
-              tma_load_4d(sK + s * C::KV_BYTES + c * (C::BN * 128), &tmK, bar(PfBars::KV_FULL + s),
+            for (int c = 0; c < C::NREG; ++c)
+              tma_load_4d(sK + s * C::KV_BYTES + c * (C::BN * 128), &tmK, bar(PfBars::K_FULL + s),
                           64 * c, hk, pc.sg.col, row0);
-              tma_load_4d(sV + s * C::KV_BYTES + c * (C::BN * 128), &tmV, bar(PfBars::KV_FULL + s),
+            ok = mbar_wait(bar(PfBars::V_EMPTY + s), (use & 1) ^ 1, abort);
+          }
+          if (ok) {
+            mbar_expect_tx(bar(PfBars::V_FULL + s), C::KV_BYTES);
+#pragma unroll
+            for (int c = 0; c < C::NREG; ++c)
+              tma_load_4d(sV + s * C::KV_BYTES + c * (C::BN * 128), &tmV, bar(PfBars::V_FULL + s),
                           64 * c, hk, pc.sg.col, row0);
-            }
           }
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
         if (valid < C::BN) {
           // V rows past the last visible key: wait for the tile, then zero them
-          ok = mbar_wait(bar(PfBars::KV_FULL + s), use & 1, abort);
+          ok = mbar_wait(bar(PfBars::V_FULL + s), use & 1, abort);
           ok = __all_sync(0xffffffffu, ok);
           if (!ok) break;
           const int bytes = (C::BN - valid) * 128;
@@ -234,12 +260,14 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     if (lane == 0) {
       int dummy = 0;
       const uint32_t first = gt > (uint32_t)C::STAGES ? gt - C::STAGES : 0u;
-      for (uint32_t g = first; g < gt; ++g)
-        mbar_wait(bar(PfBars::KV_FULL + g % C::STAGES), (g / C::STAGES) & 1, &dummy);
+      for (uint32_t g = first; g < gt; ++g) {
+        mbar_wait(bar(PfBars::K_FULL + g % C::STAGES), (g / C::STAGES) & 1, &dummy);
+        mbar_wait(bar(PfBars::V_FULL + g % C::STAGES), (g / C::STAGES) & 1, &dummy);
+      }
       if (pi > 0) mbar_wait(bar(PfBars::Q_FULL), (pi - 1) & 1, &dummy);
     }
     __syncwarp();
-  } else if (warp == 5) {
+  } else if (warp == W_MMA) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t IDESC_QK = idesc_bf16_f32(128, C::BN, false, false);
@@ -250,7 +278,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       bool ok = true;
       auto issue_s = [&](uint32_t g) -> bool {
         const int s = g % C::STAGES, b = g & 1;
-        if (!mbar_wait(bar(PfBars::KV_FULL + s), (g / C::STAGES) & 1, abort)) return false;
+        if (!mbar_wait(bar(PfBars::K_FULL + s), (g / C::STAGES) & 1, abort)) return false;
         if (!mbar_wait(bar(PfBars::S_FREE + b), ((g >> 1) & 1) ^ 1, abort)) return false;
         tc_fence_after();
 #pragma unroll
@@ -261,6 +289,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           tc_mma_ss(tmem + C::S_COL0 + b * C::BN, a, bd, IDESC_QK, k > 0 ? 1u : 0u);
         }
         tc_commit(bar(PfBars::S_FULL + b));
+        tc_commit(bar(PfBars::K_EMPTY + s));  // K(g) is free once S(g) is done
         return true;
       };
       while (ok && pf_next(A.ws, t0, t_end, u, U, pc)) {
@@ -279,18 +308,22 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           }
           const int b = g & 1, s = g % C::STAGES;
           ok = mbar_wait(bar(PfBars::P_FULL + b), (g >> 1) & 1, abort) &&
+               mbar_wait(bar(PfBars::V_FULL + s), (g / C::STAGES) & 1, abort) &&
                mbar_wait(bar(PfBars::V_READY + s), (g / C::STAGES) & 1, abort);
           if (!ok) break;
           tc_fence_after();
+          // O_b of warpgroup b (one O when single): its first PV of the piece overwrites
+          const uint32_t o_col = C::O_COL + (C::DUAL ? b * D : 0);
+          const int first_j = C::DUAL ? 2 : 1;
 #pragma unroll
           for (int k = 0; k < C::BN / 16; ++k) {
             const uint64_t a = sdesc_sw128(sP + b * C::P_BYTES + (k >> 2) * (C::BM * 128) + (k & 3) * 32, 16, 1024);
             const uint64_t bd = sdesc_sw128(sV + s * C::KV_BYTES + k * 16 * 128, C::BN * 128, 1024);
-            tc_mma_ss(tmem + C::O_COL, a, bd, IDESC_PV, (j > 0 || k > 0) ? 1u : 0u);
+            tc_mma_ss(tmem + o_col, a, bd, IDESC_PV, (j >= first_j || k > 0) ? 1u : 0u);
           }
-          tc_commit(bar(PfBars::O_DONE));
+          if (!C::DUAL) tc_commit(bar(PfBars::O_DONE));
           if (j + 1 == n) tc_commit(bar(PfBars::O_FINAL));
-          tc_commit(bar(PfBars::KV_EMPTY + s));
+          tc_commit(bar(PfBars::V_EMPTY + s));  // V(g) is free once PV(g) is done
         }
         gt += n;
         ++pi;
@@ -303,8 +336,14 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax + epilogue
-    const int row = threadIdx.x;  // 0..127 = tensor-memory lane
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    // Warpgroup wg (warps 4*wg .. 4*wg+3) handles the key tiles g with g & 1 == wg (all tiles
+    // when single); thread = row = tensor-memory lane.  Each warpgroup keeps its own running
+    // max / sum and O accumulator; warpgroup 0 merges both at the end of a piece.
+    const int wg = C::DUAL ? (warp >> 2) : 0;
+    const int row = (warp & 3) * 32 + lane;
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t o_mine = tmem + lane_off + C::O_COL + (C::DUAL ? wg * D : 0);
+    float2* xchg = reinterpret_cast<float2*>(smem + C::OFF_BAR + PfBars::X_OFF);
     const float sl2 = A.scale_log2;
     int64_t t0 = t_begin, u = u0;
     PfPiece pc;
@@ -325,9 +364,16 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         rhi = min((int64_t)w.hi, pos_hi);
       }
       const int n = (int)(pc.tb - pc.ta);
+      if (C::DUAL && wg == 1) {
+        // O1 and the exchange block are free once warpgroup 0 has finished the last piece
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(PfBars::X_FREE), (pi & 1) ^ 1, abort));
+        if (!ok) break;
+      }
       float m_use = -INFINITY, l = 0.f;
+      bool first = true;  // no PV of this warpgroup in this piece yet
       for (int j = 0; j < n; ++j) {
         const uint32_t g = gt + j;
+        if (C::DUAL && (int)(g & 1) != wg) continue;
         const int b = g & 1;
         ok = mbar_wait(bar(PfBars::S_FULL + b), (g >> 1) & 1, abort);
         ok = __all_sync(0xffffffffu, ok);
@@ -360,23 +406,27 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         const float m_new = fmaxf(m_use, mx);
         const bool resc = m_new > m_use + 8.f;  // false while nothing is visible
         const float alpha = resc ? exp2_approx(m_use - m_new) : 1.f;
-        const bool need_o = resc && j > 0 && m_use != -INFINITY;
+        const bool need_o = resc && !first && m_use != -INFINITY;
         if (__any_sync(0xffffffffu, need_o)) {
-          // O holds P V of earlier tiles: wait for the last PV, then rescale in place
-          ok = mbar_wait(bar(PfBars::O_DONE), (g - 1) & 1, abort);
-          ok = __all_sync(0xffffffffu, ok);
-          if (!ok) break;
-          tc_fence_after();
+          // Rescale this warpgroup's O in place.  Dual: its last PV (tile g-2) was issued
+          // before S(g), whose completion this thread has seen, so O_wg is settled.
+          // Single: wait for the PV of tile g-1.
+          if (!C::DUAL) {
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(PfBars::O_DONE), (g - 1) & 1, abort));
+            if (!ok) break;
+            tc_fence_after();
+          }
           const float f = need_o ? alpha : 1.f;
 #pragma unroll 1
           for (int c = 0; c < D / 32; ++c) {
             float o[32];
-            tmem_ld32(tmem + lane_off + C::O_COL + 32 * c, o);
+            tmem_ld32(o_mine + 32 * c, o);
 #pragma unroll
             for (int k = 0; k < 32; ++k) o[k] *= f;
-            tmem_st32(tmem + lane_off + C::O_COL + 32 * c, o);
+            tmem_st32(o_mine + 32 * c, o);
           }
         }
+        first = false;
         if (resc) {
           m_use = m_new;
           l *= alpha;
@@ -385,53 +435,87 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         // p = 2^(scale*s - m) (masked columns give 0), row sum, bf16 P into the swizzled
         // K-major tile of buffer b
         float sum8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int k = 0; k < C::BN; ++k) {
-          x[k] = exp2_approx(fmaf(x[k], sl2, nmu));
-          sum8[k & 7] += x[k];
-        }
-        l += ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
         uint8_t* prow = smem + C::OFF_P + b * C::P_BYTES + row * 128;
 #pragma unroll
-        for (int cc = 0; cc < C::BN / 8; ++cc) {
+        for (int cc = 0; cc < C::BN / 8; ++cc) {  // 8 probabilities = one 16-byte chunk
+          float p8[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            p8[k] = exp2_approx(fmaf(x[8 * cc + k], sl2, nmu));
+            sum8[k] += p8[k];
+          }
           uint4 v;
-          v.x = pack_bf16x2(x[8 * cc + 0], x[8 * cc + 1]);
-          v.y = pack_bf16x2(x[8 * cc + 2], x[8 * cc + 3]);
-          v.z = pack_bf16x2(x[8 * cc + 4], x[8 * cc + 5]);
-          v.w = pack_bf16x2(x[8 * cc + 6], x[8 * cc + 7]);
+          v.x = pack_bf16x2(p8[0], p8[1]);
+          v.y = pack_bf16x2(p8[2], p8[3]);
+          v.z = pack_bf16x2(p8[4], p8[5]);
+          v.w = pack_bf16x2(p8[6], p8[7]);
           *reinterpret_cast<uint4*>(prow + (cc >> 3) * (C::BM * 128) + (((cc & 7) ^ (row & 7)) << 4)) = v;
         }
+        l += ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
         fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(bar(PfBars::P_FULL + b));
       }
       if (!ok) break;
       gt += n;
-      // epilogue: wait for the last PV, then normalise (direct) or write a partial
+      if (C::DUAL && wg == 1) {
+        // hand this warpgroup's row max and sum to warpgroup 0, which merges and writes
+        xchg[row] = make_float2(m_use, l);
+        mbar_arrive(bar(PfBars::X_FULL));
+        ++pi;
+        continue;
+      }
+      // epilogue: wait for the piece's last PV (and warpgroup 1's half), then normalise
+      // (direct) or write a partial
       ok = mbar_wait(bar(PfBars::O_FINAL), pi & 1, abort);
+      if (C::DUAL) ok = ok && mbar_wait(bar(PfBars::X_FULL), pi & 1, abort);
       ++pi;
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
+      // merge the two halves: M = max m_b, weights 2^(m_b - M) (0 for a half with no keys,
+      // whose O_b is stale), L = sum l_b * weight
+      float m1 = -INFINITY, l1 = 0.f;
+      if (C::DUAL) {
+        const float2 h1 = xchg[row];
+        m1 = h1.x;
+        l1 = h1.y;
+      }
+      const float M = fmaxf(m_use, m1);
+      const float Mu = M == -INFINITY ? 0.f : M;
+      const float f0 = l > 0.f ? exp2_approx(m_use - Mu) : 0.f;
+      const float f1 = l1 > 0.f ? exp2_approx(m1 - Mu) : 0.f;
+      const float L = l * f0 + l1 * f1;
       const bool direct = ur.nslots == 1;
       const int h = ur.hk * A.group + (int)(r % A.group);
       __nv_bfloat16* orow = A.out + ((int64_t)sg.q_start + qi) * A.o_rs + (int64_t)h * A.o_hs;
       const int64_t pidx = ur.slot_base + (int64_t)pc.slot * ur.rows + row;
       float* prow = A.ws.part_o[kRoutePrefill] + pidx * D;
-      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const float inv = L > 0.f ? 1.f / L : 0.f;
+      const float w0 = direct ? f0 * inv : f0, w1 = direct ? f1 * inv : f1;
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         float o[32];
         tmem_ld32(tmem + lane_off + C::O_COL + 32 * c, o);
+        if (C::DUAL) {
+          float o1[32];
+          tmem_ld32(tmem + lane_off + C::O_COL + D + 32 * c, o1);
+#pragma unroll
+          for (int k = 0; k < 32; ++k)
+            o[k] = (f0 != 0.f ? o[k] * w0 : 0.f) + (f1 != 0.f ? o1[k] * w1 : 0.f);
+        } else {
+#pragma unroll
+          for (int k = 0; k < 32; ++k) o[k] = f0 != 0.f ? o[k] * w0 : 0.f;
+        }
         if (!live) continue;
         if (direct) {
 #pragma unroll
           for (int k = 0; k < 32; k += 8) {
             uint4 v;
-            v.x = pack_bf16x2(o[k] * inv, o[k + 1] * inv);
-            v.y = pack_bf16x2(o[k + 2] * inv, o[k + 3] * inv);
-            v.z = pack_bf16x2(o[k + 4] * inv, o[k + 5] * inv);
-            v.w = pack_bf16x2(o[k + 6] * inv, o[k + 7] * inv);
+            v.x = pack_bf16x2(o[k], o[k + 1]);
+            v.y = pack_bf16x2(o[k + 2], o[k + 3]);
+            v.z = pack_bf16x2(o[k + 4], o[k + 5]);
+            v.w = pack_bf16x2(o[k + 6], o[k + 7]);
             *reinterpret_cast<uint4*>(orow + 32 * c + k) = v;
           }
         } else {
@@ -440,8 +524,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             *reinterpret_cast<float4*>(prow + 32 * c + k) = make_float4(o[k], o[k + 1], o[k + 2], o[k + 3]);
         }
       }
-      if (live && !direct) A.ws.part_ml[kRoutePrefill][pidx] = make_float2(m_use, l);
+      if (live && !direct) A.ws.part_ml[kRoutePrefill][pidx] = make_float2(M, L);
       tc_fence_before();
+      if (C::DUAL) mbar_arrive(bar(PfBars::X_FREE));  // O1 and the exchange block are free
     }
   }
 
@@ -452,7 +537,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     atomicOr((int*)&A.ws.hdr->status, SDPA_DEV_TIMEOUT);
     if (A.status_dev) atomicOr(A.status_dev, SDPA_DEV_TIMEOUT);
   }
-  if (warp == 5) tmem_dealloc(tmem, C::TMEM_COLS);
+  if (warp == W_MMA) tmem_dealloc(tmem, C::TMEM_COLS);
 }
 
 template __global__ void sdpa_prefill_kernel<64>(const AttnArgs, const __grid_constant__ CUtensorMap,
@@ -477,6 +562,13 @@ int prefill_smem_bytes(int D) {
     case 64: return PfCfg<64>::SMEM;
     case 128: return PfCfg<128>::SMEM;
     default: return PfCfg<256>::SMEM;
+  }
+}
+int prefill_block_threads(int D) {
+  switch (D) {
+    case 64: return PfCfg<64>::THREADS;
+    case 128: return PfCfg<128>::THREADS;
+    default: return PfCfg<256>::THREADS;
   }
 }
 int prefill_tile_keys(int D) { return D == 256 ? PfCfg<256>::BN : PfCfg<128>::BN; }

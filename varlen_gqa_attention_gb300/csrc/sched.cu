@@ -87,13 +87,23 @@ __device__ __forceinline__ int route_of(const SchedArgs& A, const SegRec& r) {
   return R >= kPrefillRows ? kRoutePrefill : kRouteSplitk;
 }
 
+// Segment tables up to this size are staged in shared memory, so the walk below is a few
+// block-wide steps instead of chains of dependent global loads; larger tables are read from
+// the workspace copy.
+constexpr int kSegCache = 1024;
+
 __global__ void __launch_bounds__(kSchedThreads) sdpa_sched_kernel(SchedArgs A) {
   __shared__ int64_t sh[33];
   __shared__ int32_t s_status;
   __shared__ int64_t s_tot[3];
+  __shared__ int4 c_seg[kSegCache];  // (q_start, q_len, col, kv_end)
+  __shared__ int32_t c_bits[kSegCache];
+  __shared__ int2 c_rn[kSegCache];   // (route, nrb)
+  __shared__ int2 c_ub[kSegCache];   // unit bases of routes 1 and 2
   const Workspace& W = A.ws;
   const int S = A.S;
   const int64_t T = A.T;
+  const bool cached = S <= kSegCache;
   if (threadIdx.x == 0) s_status = 0;
   __syncthreads();
 
@@ -101,27 +111,44 @@ __global__ void __launch_bounds__(kSchedThreads) sdpa_sched_kernel(SchedArgs A) 
   for (int s = threadIdx.x; s < S; s += blockDim.x) {
     int32_t g[4];
     load_seg(A, s, g);
-    int32_t bits = segment_bits(g[0], g[1], g[2], g[3], T, A.rows, A.cols, A.window);
+    const int32_t bits = segment_bits(g[0], g[1], g[2], g[3], T, A.rows, A.cols, A.window);
     SegRec r;
     r.q_start = g[0]; r.q_len = g[1]; r.col = g[2]; r.kv_end = g[3];
     r.route = kRouteNone; r.nrb = 0; r.bits = bits; r.pad = 0;
     r.ubase[0] = r.ubase[1] = r.ubase[2] = r.ubase[3] = 0;
     W.segs[s] = r;
     W.seg_flag[s] = 0;
+    if (cached) {
+      c_seg[s] = make_int4(g[0], g[1], g[2], g[3]);
+      c_bits[s] = bits;
+    }
     if (bits) atomicOr(&s_status, bits);
   }
   for (int64_t t = threadIdx.x; t < T; t += blockDim.x) W.row_seg[t] = -1;
   __syncthreads();
+  auto seg_of = [&](int s) -> int4 {
+    if (cached) return c_seg[s];
+    const SegRec r = W.segs[s];
+    return make_int4(r.q_start, r.q_len, r.col, r.kv_end);
+  };
+  auto bits_of = [&](int s) -> int32_t { return cached ? c_bits[s] : W.segs[s].bits; };
 
-  // 2. claim rows; a segment that meets another one marks both
-  for (int s = 0; s < S; ++s) {
-    SegRec r = W.segs[s];
-    if (r.bits) continue;
-    for (int i = threadIdx.x; i < r.q_len; i += blockDim.x) {
-      int old = atomicCAS(&W.row_seg[r.q_start + i], -1, s);
-      if (old != -1) {
-        atomicExch(&W.seg_flag[s], 1);
-        atomicExch(&W.seg_flag[old], 1);
+  // 2. claim rows; a segment that meets another one marks both.  Teams of threads take
+  // segments round-robin: the whole block per segment when segments are few, one warp per
+  // segment when there are at least as many segments as warps.
+  {
+    int team = blockDim.x;
+    while (team > 32 && team * S > (int)blockDim.x * 2) team >>= 1;
+    const int nteam = blockDim.x / team, tm = threadIdx.x / team, ti = threadIdx.x % team;
+    for (int s = tm; s < S; s += nteam) {
+      if (bits_of(s)) continue;
+      const int4 g = seg_of(s);
+      for (int i = ti; i < g.y; i += team) {
+        const int old = atomicCAS(&W.row_seg[g.x + i], -1, s);
+        if (old != -1) {
+          atomicExch(&W.seg_flag[s], 1);
+          atomicExch(&W.seg_flag[old], 1);
+        }
       }
     }
   }
@@ -132,16 +159,23 @@ __global__ void __launch_bounds__(kSchedThreads) sdpa_sched_kernel(SchedArgs A) 
   my_range(S, &sa, &sb);
   int64_t cnt[3] = {0, 0, 0};
   for (int64_t s = sa; s < sb; ++s) {
-    SegRec r = W.segs[s];
-    if (r.bits == 0 && W.seg_flag[s]) atomicOr(&s_status, SDPA_SEG_OVERLAP);
-    if (r.bits || W.seg_flag[s] || r.q_len == 0) continue;
-    const int64_t R = (int64_t)r.q_len * A.group;
-    const int route = route_of(A, r);
-    const int rpu = rows_per_unit(route);
-    const int nrb = (int)((R + rpu - 1) / rpu);
+    const int32_t bits = bits_of((int)s);
+    const int flag = W.seg_flag[s];
+    if (bits == 0 && flag) atomicOr(&s_status, SDPA_SEG_OVERLAP);
+    const int4 g = seg_of((int)s);
+    int route = kRouteNone, nrb = 0;
+    if (bits == 0 && !flag && g.y > 0) {
+      SegRec r;
+      r.q_start = g.x; r.q_len = g.y; r.col = g.z; r.kv_end = g.w;
+      const int64_t R = (int64_t)g.y * A.group;
+      route = route_of(A, r);
+      const int rpu = rows_per_unit(route);
+      nrb = (int)((R + rpu - 1) / rpu);
+      cnt[route] += (int64_t)A.Hkv * nrb;
+    }
     W.segs[s].route = route;
     W.segs[s].nrb = nrb;
-    cnt[route] += (int64_t)A.Hkv * nrb;
+    if (cached) c_rn[s] = make_int2(route, nrb);
   }
   int64_t ubase[3];
   for (int q = 1; q < 3; ++q) {
@@ -152,9 +186,11 @@ __global__ void __launch_bounds__(kSchedThreads) sdpa_sched_kernel(SchedArgs A) 
     if (threadIdx.x == 0) s_tot[q] = min(tot, W.unit_cap[q]);
   }
   for (int64_t s = sa; s < sb; ++s) {
-    SegRec r = W.segs[s];
-    for (int q = 1; q < 3; ++q) W.segs[s].ubase[q] = (int32_t)ubase[q];
-    if (r.route != kRouteNone) ubase[r.route] += (int64_t)A.Hkv * r.nrb;
+    W.segs[s].ubase[1] = (int32_t)ubase[1];
+    W.segs[s].ubase[2] = (int32_t)ubase[2];
+    if (cached) c_ub[s] = make_int2((int32_t)ubase[1], (int32_t)ubase[2]);
+    const int2 rn = cached ? c_rn[s] : make_int2(W.segs[s].route, W.segs[s].nrb);
+    if (rn.x != kRouteNone) ubase[rn.x] += (int64_t)A.Hkv * rn.y;
   }
   __syncthreads();
 
@@ -170,10 +206,19 @@ __global__ void __launch_bounds__(kSchedThreads) sdpa_sched_kernel(SchedArgs A) 
       // owning segment: the last one whose route-q unit base is <= u
       int lo = 0, hi = S - 1, s = 0;
       while (lo <= hi) {
-        int mid = (lo + hi) >> 1;
-        if (W.segs[mid].ubase[q] <= u) { s = mid; lo = mid + 1; } else { hi = mid - 1; }
+        const int mid = (lo + hi) >> 1;
+        const int32_t ubm = cached ? (q == 1 ? c_ub[mid].x : c_ub[mid].y) : W.segs[mid].ubase[q];
+        if (ubm <= u) { s = mid; lo = mid + 1; } else { hi = mid - 1; }
       }
-      SegRec g = W.segs[s];
+      SegRec g;
+      if (cached) {
+        const int4 c = c_seg[s];
+        g.q_start = c.x; g.q_len = c.y; g.col = c.z; g.kv_end = c.w;
+        g.nrb = c_rn[s].y;
+        g.ubase[q] = q == 1 ? c_ub[s].x : c_ub[s].y;
+      } else {
+        g = W.segs[s];
+      }
       UnitRec ur;
       int64_t j = u - g.ubase[q];
       ur.seg = s;

@@ -23,37 +23,61 @@
 namespace sdpa {
 
 constexpr int kSplitkThreads = 128;
-constexpr int kStages = 2;
 
 template <int D>
 struct SplitkSmem {
+  // key tiles in flight: 3 stages keep two tiles loading while one is used (two CTAs per
+  // SM at D <= 128); D = 256 tiles are twice as large, so two stages
+  static constexpr int kStages = D == 256 ? 2 : 3;
   static constexpr int kRowBytes = D * 2;
   static constexpr int kQBytes = kSplitkRows * kRowBytes;
   static constexpr int kTileBytes = kSplitkTile * kRowBytes;
   static constexpr int kBytes = kQBytes + 2 * kStages * kTileBytes;
 };
 
+// Per-thread cursor over the key tiles of one unit: each thread always copies the same
+// 16-byte chunk column of rows n0, n0 + kRowStep, ... of a tile, so only the tile's first
+// store row (kept modulo `rows` incrementally) changes from tile to tile.
 template <int D>
-__device__ __forceinline__ void load_kv_tile(const AttnArgs& A, const SegRec& sg, int hk,
-                                             int64_t tile_start, int64_t pos_hi, char* sK,
-                                             char* sV) {
-  constexpr int CH = D / 8;  // 16-byte chunks per store row
-  constexpr int RB = D * 2;
-  const int64_t row_stride = (int64_t)A.cols * A.Hkv * D;
-  const int64_t col_off = ((int64_t)sg.col * A.Hkv + hk) * D;
-  const int64_t base_row = tile_start % A.rows;
-#pragma unroll 4
-  for (int idx = threadIdx.x; idx < kSplitkTile * CH; idx += kSplitkThreads) {
-    const int n = idx / CH, c = idx % CH;
-    const bool ok = tile_start + n < pos_hi;
-    int64_t phys = base_row + n;
-    if (phys >= A.rows) phys -= A.rows;  // valid positions span at most `rows` rows
-    const int64_t off = ok ? phys * row_stride + col_off + c * 8 : 0;
-    const uint32_t so = swz(n, c, RB);
-    cp_async_16(smem_u32(sK + so), A.k + off, ok);
-    cp_async_16(smem_u32(sV + so), A.v + off, ok);
+struct KvCursor {
+  static constexpr int CH = D / 8;                      // 16-byte chunks per store row
+  static constexpr int kRowStep = kSplitkThreads / CH;  // rows one pass of the CTA covers
+  static constexpr int kPasses = kSplitkTile / kRowStep;
+  const __nv_bfloat16* kb;  // this thread's chunk column of (column, KV head), store row 0
+  const __nv_bfloat16* vb;
+  int64_t rstride;          // elements between store rows
+  int rows;
+  int row0;                 // store row of the next tile's first key
+  int n0, c;
+
+  __device__ __forceinline__ void init(const AttnArgs& A, const SegRec& sg, int hk, int64_t first_pos) {
+    c = threadIdx.x % CH;
+    n0 = threadIdx.x / CH;
+    rstride = (int64_t)A.cols * A.Hkv * D;
+    const int64_t off = ((int64_t)sg.col * A.Hkv + hk) * D + c * 8;
+    kb = A.k + off;
+    vb = A.v + off;
+    rows = (int)A.rows;
+    row0 = (int)(first_pos % A.rows);
   }
-}
+  // Issues the copies of the next tile (keys [0, valid) of it; the rest are zero-filled),
+  // then advances to the following tile.
+  __device__ __forceinline__ void load(int valid, char* sK, char* sV) {
+#pragma unroll
+    for (int i = 0; i < kPasses; ++i) {
+      const int n = n0 + i * kRowStep;
+      const bool ok = n < valid;
+      int phys = row0 + n;
+      if (phys >= rows) phys -= rows;  // valid keys span at most `rows` store rows
+      const int64_t off = ok ? (int64_t)phys * rstride : 0;
+      const uint32_t so = swz(n, c, D * 2);
+      cp_async_16(smem_u32(sK + so), kb + off, ok);
+      cp_async_16(smem_u32(sV + so), vb + off, ok);
+    }
+    row0 += kSplitkTile;
+    if (row0 >= rows) row0 %= rows;
+  }
+};
 
 // One warp's share of a unit: 16 packed rows x a slice of each key tile.
 template <int D, int NCS>
@@ -67,6 +91,7 @@ __device__ __forceinline__ void splitk_unit(const AttnArgs& A, const UnitRec& ur
   constexpr int ND = D / 8;              // n8 blocks of the output
   char* sQ = smem;
   char* sK = smem + S::kQBytes;
+  constexpr int kStages = S::kStages;
   char* sV = sK + kStages * S::kTileBytes;
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -96,8 +121,15 @@ __device__ __forceinline__ void splitk_unit(const AttnArgs& A, const UnitRec& ur
       cp_async_16(smem_u32(sQ + swz(rl, c, RB)), A.q + off, ok);
     }
   }
-  load_kv_tile<D>(A, sg, ur.hk, pos_lo, pos_hi, sK, sV);
-  cp_async_commit();
+  // prologue: Q and the first kStages-1 tiles, one commit group per tile (empty past the end)
+  KvCursor<D> cur;
+  cur.init(A, sg, ur.hk, pos_lo);
+  for (int st = 0; st < kStages - 1; ++st) {
+    if (st < ntiles)
+      cur.load((int)min((int64_t)kSplitkTile, pos_hi - pos_lo - (int64_t)st * kSplitkTile),
+               sK + st * S::kTileBytes, sV + st * S::kTileBytes);
+    cp_async_commit();
+  }
 
   // this thread's two rows: local rows mt*16 + gq and +8
   int32_t rlo[2], rhi[2];
@@ -125,15 +157,15 @@ __device__ __forceinline__ void splitk_unit(const AttnArgs& A, const UnitRec& ur
   const float sl2 = A.scale_log2;
 
   for (int kt = 0; kt < ntiles; ++kt) {
-    if (kt + 1 < ntiles) {
-      const int st = (kt + 1) % kStages;
-      load_kv_tile<D>(A, sg, ur.hk, pos_lo + (int64_t)(kt + 1) * kSplitkTile, pos_hi,
-                      sK + st * S::kTileBytes, sV + st * S::kTileBytes);
-      cp_async_commit();
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
+    // tile kt + kStages - 1 goes into the stage tile kt - 1 used (freed by the barrier that
+    // ended the previous iteration); then wait until tile kt has landed
+    if (kt + kStages - 1 < ntiles) {
+      const int st = (kt + kStages - 1) % kStages;
+      cur.load((int)min((int64_t)kSplitkTile, pos_hi - pos_lo - (int64_t)(kt + kStages - 1) * kSplitkTile),
+               sK + st * S::kTileBytes, sV + st * S::kTileBytes);
     }
+    cp_async_commit();
+    cp_async_wait<kStages - 1>();
     __syncthreads();
     const char* cK = sK + (kt % kStages) * S::kTileBytes;
     const char* cV = sV + (kt % kStages) * S::kTileBytes;
@@ -158,7 +190,8 @@ __device__ __forceinline__ void splitk_unit(const AttnArgs& A, const UnitRec& ur
       }
     }
 
-    // mask (select), scale to base 2, online softmax
+    // mask (select, on the raw scores), online softmax in base 2 with a lazily updated max:
+    // O and l are only rescaled when a row's max grows by more than 2^8
     const bool full = tile0 >= lo_max && tile0 + SW <= hi_min;
     float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
@@ -166,7 +199,7 @@ __device__ __forceinline__ void splitk_unit(const AttnArgs& A, const UnitRec& ur
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int rr = e >> 1;
-        float x = s[nb][e] * sl2;
+        float x = s[nb][e];
         if (!full) {
           const int64_t j = tile0 + nb * 8 + 2 * tq + (e & 1);
           const bool vis = !live[rr] || (j >= rlo[rr] && j < rhi[rr]);
@@ -177,34 +210,39 @@ __device__ __forceinline__ void splitk_unit(const AttnArgs& A, const UnitRec& ur
         mx[rr] = fmaxf(mx[rr], x);
       }
     }
-    float alpha[2], muse[2];
+    float alpha[2], nmu[2];
+    bool resc = false;
 #pragma unroll
     for (int rr = 0; rr < 2; ++rr) {
       mx[rr] = fmaxf(mx[rr], __shfl_xor_sync(0xffffffffu, mx[rr], 1));
       mx[rr] = fmaxf(mx[rr], __shfl_xor_sync(0xffffffffu, mx[rr], 2));
-      const float mn = fmaxf(m[rr], mx[rr]);
-      muse[rr] = mn == -INFINITY ? 0.f : mn;
-      alpha[rr] = exp2_approx(m[rr] - muse[rr]);
-      m[rr] = mn;
+      const float mn = fmaxf(m[rr], mx[rr] * sl2);  // scale > 0: max(scale*s) = scale*max(s)
+      const bool up = mn > m[rr] + 8.f;            // false while nothing is visible
+      alpha[rr] = up ? exp2_approx(m[rr] - mn) : 1.f;
+      if (up) m[rr] = mn;
+      resc |= up;
+      nmu[rr] = m[rr] == -INFINITY ? 0.f : -m[rr];
     }
     float ls[2] = {0.f, 0.f};
 #pragma unroll
     for (int nb = 0; nb < NB; ++nb) {
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const float p = exp2_approx(s[nb][e] - muse[e >> 1]);
+        const float p = exp2_approx(fmaf(s[nb][e], sl2, nmu[e >> 1]));
         s[nb][e] = p;
         ls[e >> 1] += p;
       }
     }
 #pragma unroll
     for (int rr = 0; rr < 2; ++rr) l[rr] = l[rr] * alpha[rr] + ls[rr];
+    if (__any_sync(0xffffffffu, resc)) {
 #pragma unroll
-    for (int nd = 0; nd < ND; ++nd) {
-      o[nd][0] *= alpha[0];
-      o[nd][1] *= alpha[0];
-      o[nd][2] *= alpha[1];
-      o[nd][3] *= alpha[1];
+      for (int nd = 0; nd < ND; ++nd) {
+        o[nd][0] *= alpha[0];
+        o[nd][1] *= alpha[0];
+        o[nd][2] *= alpha[1];
+        o[nd][3] *= alpha[1];
+      }
     }
 
     // O += P V

@@ -235,6 +235,7 @@ static sdpa_status run(const void* q, int64_t T, int Hq, int D, int64_t q_rs, in
   sa.group = Hq / Hkv;
   sa.causal = causal ? 1 : 0;
   sa.window = window;
+  sa.D = D;
   sa.policy = g_policy.load();
   TensorMaps tm;
   const int group = Hq / Hkv;

@@ -39,19 +39,27 @@ struct UnitRec {
   int32_t nslots;             // CTAs that work on the unit (0: no keys; 1: written directly)
   int32_t g_first;            // first such CTA
   int32_t ntiles;             // key tiles of the unit
-  int32_t pad;
+  int32_t phase;              // scheduling phase of the unit (see SchedHdr)
   int64_t tile_base;          // first tile of the unit in the flattened tile space
   int64_t slot_base;          // first partial row of the unit's slots
 };
 
 
+// Phases: a route's tile line is cut at (segment, KV head) boundaries into phases whose
+// re-read K/V (units sharing a group's keys) fits a budget below the L2 size; every CTA
+// takes its stream-K share of phase 0, then of phase 1, ... so the K/V tiles the whole
+// grid touches at one time stay cached.
+constexpr int kMaxPhases = 16;
+constexpr int64_t kPhaseBytes = 48ll << 20;
+
 // Scheduler header (int64 words).
 struct SchedHdr {
   int64_t tiles[3];   // total tiles per route (index = route)
   int64_t units[3];   // units per route
-  int64_t grid[3];    // working CTAs per route: min(launched grid, tiles)
+  int64_t grid[3];    // CTAs per route as launched
   int64_t status;     // OR of the status bits of this call
-  int64_t pad[4];
+  int64_t nphase[3];  // phases per route
+  int64_t phase_base[3][kMaxPhases + 1];  // first tile of each phase; [nphase] = tiles
 };
 
 struct Workspace {
@@ -134,6 +142,7 @@ struct SchedArgs {
   int32_t inl[4];
   int64_t T, rows;
   int cols, Hkv, group, causal, window;
+  int D;           // head dim (bytes of the K/V each phase holds)
   int policy;      // SDPA_ROUTE_*
   int prefill_ok;  // prefill kernel usable for this call (group divides 128, tensor maps made)
   int tile_pf;     // keys per prefill tile
@@ -184,11 +193,79 @@ __device__ __forceinline__ RowWin row_window(int i, int q_len, int kv_end, int c
   return w;
 }
 
+// Work of one CTA on one route: for each phase, its stream-K share of the phase's tiles,
+// cut into pieces (one unit's consecutive tiles each).  All roles of a CTA walk the same
+// sequence.
+struct PieceWalk {
+  const Workspace* W;
+  int route;
+  int64_t G;        // launched grid
+  int64_t nphase;
+  int64_t p;        // current phase
+  int64_t t0, t1;   // remaining tiles of this CTA in phase p
+  int64_t u;        // next unit to look at
+};
+
 // Stream-K partition: CTA g of G owns flattened tiles [g*W/G, (g+1)*W/G).
 __host__ __device__ inline int64_t sk_start(int64_t g, int64_t W, int64_t G) { return g * W / G; }
 // CTA whose range holds tile x.
 __host__ __device__ inline int64_t sk_owner(int64_t x, int64_t W, int64_t G) {
   return ((x + 1) * G - 1) / W;
+}
+
+__device__ inline void walk_begin(PieceWalk& w, const Workspace& W, int route) {
+  w.W = &W;
+  w.route = route;
+  w.G = W.hdr->grid[route];
+  w.nphase = W.hdr->nphase[route];
+  w.p = -1;
+  w.t0 = w.t1 = 0;
+  w.u = 0;
+}
+
+// Moves to the next phase in which this CTA owns tiles; false when there is none.
+__device__ inline bool walk_phase(PieceWalk& w) {
+  const SchedHdr* h = w.W->hdr;
+  while (++w.p < w.nphase) {
+    const int64_t b0 = h->phase_base[w.route][w.p], Wp = h->phase_base[w.route][w.p + 1] - b0;
+    if (Wp <= 0) continue;
+    const int64_t Gp = min(w.G, Wp);  // at most one CTA per tile: nslots stays exact
+    if ((int64_t)blockIdx.x >= Gp) continue;
+    w.t0 = b0 + sk_start(blockIdx.x, Wp, Gp);
+    w.t1 = b0 + sk_start(blockIdx.x + 1, Wp, Gp);
+    if (w.t0 >= w.t1) continue;
+    // first unit holding tile t0: the last unit whose tile_base <= t0
+    const UnitRec* units = w.W->units[w.route];
+    int64_t lo = 0, hi = h->units[w.route] - 1, uu = 0;
+    while (lo <= hi) {
+      const int64_t mid = (lo + hi) >> 1;
+      if (units[mid].tile_base <= w.t0) { uu = mid; lo = mid + 1; } else { hi = mid - 1; }
+    }
+    w.u = uu;
+    return true;
+  }
+  return false;
+}
+
+// Next piece of this CTA: a unit and its tiles [ta, tb) that this CTA processes.
+__device__ inline bool walk_next(PieceWalk& w, UnitRec& ur, int64_t& ta, int64_t& tb) {
+  for (;;) {
+    const int64_t U = w.W->hdr->units[w.route];
+    while (w.t0 < w.t1 && w.u < U) {
+      const UnitRec r = w.W->units[w.route][w.u];
+      if (r.ntiles == 0 || w.t0 >= r.tile_base + r.ntiles) {
+        ++w.u;
+        continue;
+      }
+      ur = r;
+      ta = w.t0 - r.tile_base;
+      tb = min(w.t1, r.tile_base + r.ntiles) - r.tile_base;
+      w.t0 = r.tile_base + tb;
+      ++w.u;
+      return true;
+    }
+    if (!walk_phase(w)) return false;
+  }
 }
 
 // ------------------------------------------------------------------------------------

@@ -99,24 +99,11 @@ struct PfPiece {
   int slot;
 };
 
-__device__ __forceinline__ bool pf_next(const Workspace& W, int64_t& t0, int64_t t1, int64_t& u,
-                                        int64_t U, PfPiece& pc) {
-  while (t0 < t1 && u < U) {
-    const UnitRec ur = W.units[kRoutePrefill][u];
-    if (ur.ntiles == 0 || t0 >= ur.tile_base + ur.ntiles) {
-      ++u;
-      continue;
-    }
-    pc.ur = ur;
-    pc.sg = W.segs[ur.seg];
-    pc.ta = t0 - ur.tile_base;
-    pc.tb = min(t1, ur.tile_base + ur.ntiles) - ur.tile_base;
-    pc.slot = (int)(blockIdx.x - ur.g_first);
-    t0 = ur.tile_base + pc.tb;
-    ++u;
-    return true;
-  }
-  return false;
+__device__ __forceinline__ bool pf_next(PieceWalk& w, PfPiece& pc) {
+  if (!walk_next(w, pc.ur, pc.ta, pc.tb)) return false;
+  pc.sg = w.W->segs[pc.ur.seg];
+  pc.slot = (int)(blockIdx.x - pc.ur.g_first);
+  return true;
 }
 
 template <int D>
@@ -128,13 +115,12 @@ __global__ void __launch_bounds__(PfCfg<D>::THREADS, 1)
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
 
-  const SchedHdr* hdr = A.ws.hdr;
-  const int64_t Wt = hdr->tiles[kRoutePrefill];
-  const int64_t U = hdr->units[kRoutePrefill];
-  const int64_t G = hdr->grid[kRoutePrefill];
-  if (Wt == 0 || (int64_t)blockIdx.x >= G) return;  // whole CTA leaves before any setup
-  const int64_t t_begin = sk_start(blockIdx.x, Wt, G), t_end = sk_start(blockIdx.x + 1, Wt, G);
-  if (t_begin >= t_end) return;
+  if (A.ws.hdr->tiles[kRoutePrefill] == 0) return;  // whole CTA leaves before any setup
+  {
+    PieceWalk probe;
+    walk_begin(probe, A.ws, kRoutePrefill);
+    if (!walk_phase(probe)) return;  // no tiles for this CTA in any phase
+  }
 
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   const uint32_t sbase = smem_u32(smem);
@@ -177,24 +163,14 @@ __global__ void __launch_bounds__(PfCfg<D>::THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = s_tmem;
 
-  // first unit holding tile t_begin
-  const UnitRec* units = A.ws.units[kRoutePrefill];
-  int64_t u0 = 0;
-  {
-    int64_t lo = 0, hi = U - 1;
-    while (lo <= hi) {
-      const int64_t mid = (lo + hi) >> 1;
-      if (units[mid].tile_base <= t_begin) { u0 = mid; lo = mid + 1; } else { hi = mid - 1; }
-    }
-  }
-
   if (warp == W_PROD) {
     // ------------------------------------------------------------ TMA producer
-    int64_t t0 = t_begin, u = u0;
+    PieceWalk wk;
+    walk_begin(wk, A.ws, kRoutePrefill);
     PfPiece pc;
     uint32_t gt = 0, pi = 0;
     bool ok = true;
-    while (ok && pf_next(A.ws, t0, t_end, u, U, pc)) {
+    while (ok && pf_next(wk, pc)) {
       const int hk = pc.ur.hk;
       if (lane == 0) {
         ok = mbar_wait(bar(PfBars::Q_EMPTY), (pi & 1) ^ 1, abort);
@@ -272,7 +248,8 @@ __global__ void __launch_bounds__(PfCfg<D>::THREADS, 1)
     if (lane == 0) {
       constexpr uint32_t IDESC_QK = idesc_bf16_f32(128, C::BN, false, false);
       constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, D, false, true);
-      int64_t t0 = t_begin, u = u0;
+      PieceWalk wk;
+      walk_begin(wk, A.ws, kRoutePrefill);
       PfPiece pc;
       uint32_t gt = 0, pi = 0;
       bool ok = true;
@@ -292,7 +269,7 @@ __global__ void __launch_bounds__(PfCfg<D>::THREADS, 1)
         tc_commit(bar(PfBars::K_EMPTY + s));  // K(g) is free once S(g) is done
         return true;
       };
-      while (ok && pf_next(A.ws, t0, t_end, u, U, pc)) {
+      while (ok && pf_next(wk, pc)) {
         ok = mbar_wait(bar(PfBars::Q_FULL), pi & 1, abort);
         if (!ok) break;
         tc_fence_after();
@@ -345,11 +322,12 @@ __global__ void __launch_bounds__(PfCfg<D>::THREADS, 1)
     const uint32_t o_mine = tmem + lane_off + C::O_COL + (C::DUAL ? wg * D : 0);
     float2* xchg = reinterpret_cast<float2*>(smem + C::OFF_BAR + PfBars::X_OFF);
     const float sl2 = A.scale_log2;
-    int64_t t0 = t_begin, u = u0;
+    PieceWalk wk;
+    walk_begin(wk, A.ws, kRoutePrefill);
     PfPiece pc;
     uint32_t gt = 0, pi = 0;
     bool ok = true;
-    while (ok && pf_next(A.ws, t0, t_end, u, U, pc)) {
+    while (ok && pf_next(wk, pc)) {
       const UnitRec& ur = pc.ur;
       const SegRec& sg = pc.sg;
       const bool live = row < ur.rows;

@@ -201,7 +201,7 @@ __global__ void __launch_bounds__(kSchedThreads) sdpa_sched_kernel(SchedArgs A) 
     UnitRec* units = W.units[q];
     int64_t ua, ub;
     my_range(U, &ua, &ub);
-    int64_t my_tiles = 0;
+    int64_t my_tiles = 0, my_bytes = 0;
     for (int64_t u = ua; u < ub; ++u) {
       // owning segment: the last one whose route-q unit base is <= u
       int lo = 0, hi = S - 1, s = 0;
@@ -236,29 +236,64 @@ __global__ void __launch_bounds__(kSchedThreads) sdpa_sched_kernel(SchedArgs A) 
       ur.nslots = 0;
       ur.g_first = 0;
       ur.ntiles = (int32_t)nt;
-      ur.pad = 0;
+      ur.phase = 0;
       ur.tile_base = nt;  // the count, until the scan below
-      ur.slot_base = 0;
+      // K/V bytes the group's units read again (counted once, on the group's last unit;
+      // only groups of several units re-read them): phases are cut on these
+      int64_t reuse = 0;
+      if (g.nrb >= 2 && ur.rb == g.nrb - 1) {
+        int64_t span = g.kv_end;
+        if (A.window > 0) span = min(span, (int64_t)g.q_len + A.window - 1);
+        reuse = span * (int64_t)A.D * 4;
+      }
+      ur.slot_base = reuse;  // kept here until the phase pass below
       units[u] = ur;
       my_tiles += nt;
+      my_bytes += reuse;
     }
-    int64_t Wt;
+    int64_t Wt, Bt;
     int64_t tb = block_excl_scan(my_tiles, &Wt, sh);
-    // Effective grid: at most one CTA per tile, so every working CTA owns at least one tile
-    // and the CTAs between a unit's first and last owner all work on it (nslots is exact).
-    const int64_t G = min(A.grid[q], max(Wt, (int64_t)1));
+    int64_t bb = block_excl_scan(my_bytes, &Bt, sh);
+    for (int64_t u = ua; u < ub; ++u) {
+      UnitRec ur = units[u];
+      const int64_t nt = ur.tile_base, reuse = ur.slot_base;
+      ur.tile_base = tb;
+      ur.phase = (int32_t)min(bb / kPhaseBytes, (int64_t)kMaxPhases - 1);
+      tb += nt;
+      bb += reuse;
+      units[u] = ur;
+    }
+    __syncthreads();
+    // phase bases: phase k starts at the first unit whose phase is >= k
+    for (int64_t u = ua; u < ub; ++u) {
+      const int cp = units[u].phase, pp = u > 0 ? units[u - 1].phase : -1;
+      for (int k = pp + 1; k <= cp; ++k) W.hdr->phase_base[q][k] = units[u].tile_base;
+    }
+    if (threadIdx.x == 0) {
+      const int64_t np = U > 0 ? units[U - 1].phase + 1 : 0;
+      W.hdr->nphase[q] = np;
+      W.hdr->phase_base[q][0] = 0;
+      W.hdr->phase_base[q][np] = Wt;
+    }
+    __syncthreads();
+    // stream-K within each phase: CTA g of G_p = min(G, W_p) owns [g W_p / G_p, (g+1) W_p / G_p);
+    // G_p <= W_p makes every working CTA own a tile, so the owners of a unit's tiles are
+    // consecutive CTAs that all work on it (nslots is exact)
+    const int64_t G = A.grid[q];
     int64_t my_rows = 0;
     for (int64_t u = ua; u < ub; ++u) {
       UnitRec ur = units[u];
-      const int64_t nt = ur.tile_base;
-      ur.tile_base = tb;
+      const int64_t nt = ur.ntiles;
       if (nt > 0) {
-        const int64_t g0 = sk_owner(tb, Wt, G), g1 = sk_owner(tb + nt - 1, Wt, G);
+        const int64_t b0 = W.hdr->phase_base[q][ur.phase];
+        const int64_t Wp = W.hdr->phase_base[q][ur.phase + 1] - b0;
+        const int64_t Gp = min(G, Wp);
+        const int64_t g0 = sk_owner(ur.tile_base - b0, Wp, Gp);
+        const int64_t g1 = sk_owner(ur.tile_base + nt - 1 - b0, Wp, Gp);
         ur.g_first = (int32_t)g0;
         ur.nslots = (int32_t)(g1 - g0 + 1);
         if (ur.nslots > 1) my_rows += (int64_t)ur.nslots * ur.rows;
       }
-      tb += nt;
       units[u] = ur;
     }
     int64_t Pt;

@@ -338,27 +338,12 @@ template <int D>
 __global__ void __launch_bounds__(kSplitkThreads) sdpa_splitk_kernel(AttnArgs A) {
   extern __shared__ __align__(128) char smem[];
   __shared__ float2 s_ml[4 * 16];
-  const SchedHdr* hdr = A.ws.hdr;
-  const int64_t Wt = hdr->tiles[kRouteSplitk];
-  const int64_t U = hdr->units[kRouteSplitk];
-  const int64_t G = hdr->grid[kRouteSplitk];  // effective grid chosen by the scheduler
-  if (Wt == 0 || (int64_t)blockIdx.x >= G) return;
-  int64_t t0 = sk_start(blockIdx.x, Wt, G);
-  const int64_t t1 = sk_start(blockIdx.x + 1, Wt, G);
-  if (t0 >= t1) return;
-  const UnitRec* units = A.ws.units[kRouteSplitk];
-  // first unit holding tile t0: the last unit whose tile_base <= t0
-  int64_t lo = 0, hi = U - 1, u = 0;
-  while (lo <= hi) {
-    const int64_t mid = (lo + hi) >> 1;
-    if (units[mid].tile_base <= t0) { u = mid; lo = mid + 1; } else { hi = mid - 1; }
-  }
-  for (; u < U && t0 < t1; ++u) {
-    const UnitRec ur = units[u];
-    if (ur.ntiles == 0) continue;
-    const int64_t ta = t0 - ur.tile_base;
-    const int64_t tb = min(t1, ur.tile_base + ur.ntiles) - ur.tile_base;
-    if (ta >= tb) continue;
+  if (A.ws.hdr->tiles[kRouteSplitk] == 0) return;
+  PieceWalk wk;
+  walk_begin(wk, A.ws, kRouteSplitk);
+  UnitRec ur;
+  int64_t ta, tb;
+  while (walk_next(wk, ur, ta, tb)) {
     const SegRec sg = A.ws.segs[ur.seg];
     const int slot = (int)(blockIdx.x - ur.g_first);
     if (ur.rows <= 16)
@@ -367,7 +352,6 @@ __global__ void __launch_bounds__(kSplitkThreads) sdpa_splitk_kernel(AttnArgs A)
       splitk_unit<D, 2>(A, ur, sg, ta, tb, slot, smem, s_ml);
     else
       splitk_unit<D, 1>(A, ur, sg, ta, tb, slot, smem, s_ml);
-    t0 = ur.tile_base + tb;
   }
 }
 

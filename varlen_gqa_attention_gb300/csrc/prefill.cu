@@ -39,11 +39,10 @@ template <int D>
 struct PfCfg {
   static constexpr int BM = kPrefillRows;                 // 128 packed rows
   static constexpr int BN = D == 256 ? 64 : kPrefillTile;  // keys per tile
-  static constexpr int STAGES = D == 64 ? 4 : 2;
+  static constexpr int STAGES = D == 64 ? 6 : (D == 128 ? 3 : 2);  // K/V ring depth
   static constexpr int NREG = D / 64;                     // 64-element (128-byte) column regions
   static constexpr int Q_BYTES = BM * D * 2;
   static constexpr int KV_BYTES = BN * D * 2;             // K (or V) of one stage
-  static constexpr int P_BYTES = BM * BN * 2;
   static constexpr int S_COL0 = 0;                        // S buffers: columns [b*BN, (b+1)*BN)
   // Two softmax warpgroups take alternate key tiles (tile g goes to warpgroup g & 1), each
   // with its own O accumulator, when S0, S1, O0 and O1 fit in tensor memory.
@@ -55,11 +54,12 @@ struct PfCfg {
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + Q_BYTES;
   static constexpr int OFF_V = OFF_K + STAGES * KV_BYTES;
-  static constexpr int OFF_P = OFF_V + STAGES * KV_BYTES;
-  static constexpr int OFF_BAR = OFF_P + 2 * P_BYTES;
+  static constexpr int OFF_BAR = OFF_V + STAGES * KV_BYTES;
   static constexpr int BAR_BYTES = 512 + (DUAL ? 1024 : 0);  // + (m, l) exchange of 128 rows
   static constexpr int SMEM = OFF_BAR + BAR_BYTES + 1024;  // + alignment slack
 };
+static_assert(PfCfg<64>::STAGES <= 6 && PfCfg<128>::STAGES <= 6 && PfCfg<256>::STAGES <= 6,
+              "K/V ring deeper than the barrier arrays");
 static_assert(PfCfg<128>::SMEM <= 232448, "prefill D=128 shared memory");
 static_assert(PfCfg<64>::SMEM <= 232448, "prefill D=64 shared memory");
 static_assert(PfCfg<256>::SMEM <= 232448, "prefill D=256 shared memory");
@@ -69,11 +69,12 @@ static_assert(PfCfg<256>::SMEM <= 232448, "prefill D=256 shared memory");
 struct PfBars {
   // K and V stages are filled and released separately: K(g) is free once S(g) is done,
   // V(g) once PV(g) is done, so the next K tile streams in while the softmax runs.
-  static constexpr int K_FULL = 0;     // [4]
-  static constexpr int K_EMPTY = 4;    // [4]
-  static constexpr int V_READY = 8;    // [4] V landed and, on a boundary tile, zeroed
-  static constexpr int V_FULL = 25;    // [4]
-  static constexpr int V_EMPTY = 29;   // [4]
+  static constexpr int K_FULL = 26;    // [6]
+  static constexpr int K_EMPTY = 32;   // [6]
+  static constexpr int V_READY = 38;   // [6] V landed and, on a boundary tile, zeroed
+  static constexpr int V_FULL = 44;    // [6]
+  static constexpr int V_EMPTY = 50;   // [6]
+  static constexpr int kMaxStages = 6; // slots 0..55 fit the 512-byte block
   static constexpr int S_FULL = 12;    // [2]
   static constexpr int S_FREE = 14;    // [2]
   static constexpr int P_FULL = 16;    // [2]
@@ -125,7 +126,7 @@ __global__ void __launch_bounds__(PfCfg<D>::THREADS, 1)
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   const uint32_t sbase = smem_u32(smem);
   const uint32_t sQ = sbase + C::OFF_Q, sK = sbase + C::OFF_K, sV = sbase + C::OFF_V,
-                 sP = sbase + C::OFF_P, sBar = sbase + C::OFF_BAR;
+                 sBar = sbase + C::OFF_BAR;
   auto bar = [&](int i) { return sBar + 8u * (uint32_t)i; };
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   constexpr int W_PROD = C::SOFT_WARPS, W_MMA = C::SOFT_WARPS + 1;
@@ -292,11 +293,14 @@ __global__ void __launch_bounds__(PfCfg<D>::THREADS, 1)
           // O_b of warpgroup b (one O when single): its first PV of the piece overwrites
           const uint32_t o_col = C::O_COL + (C::DUAL ? b * D : 0);
           const int first_j = C::DUAL ? 2 : 1;
+          // A = P(g) in tensor memory (bf16 pairs in S_b's first BN/2 columns); it is read
+          // before S(g+2) overwrites S_b, since this thread issues that MMA later and a
+          // thread's MMAs run in issue order
 #pragma unroll
           for (int k = 0; k < C::BN / 16; ++k) {
-            const uint64_t a = sdesc_sw128(sP + b * C::P_BYTES + (k >> 2) * (C::BM * 128) + (k & 3) * 32, 16, 1024);
+            const uint32_t a = tmem + C::S_COL0 + b * C::BN + 8 * k;
             const uint64_t bd = sdesc_sw128(sV + s * C::KV_BYTES + k * 16 * 128, C::BN * 128, 1024);
-            tc_mma_ss(tmem + o_col, a, bd, IDESC_PV, (j >= first_j || k > 0) ? 1u : 0u);
+            tc_mma_ts(tmem + o_col, a, bd, IDESC_PV, (j >= first_j || k > 0) ? 1u : 0u);
           }
           if (!C::DUAL) tc_commit(bar(PfBars::O_DONE));
           if (j + 1 == n) tc_commit(bar(PfBars::O_FINAL));
@@ -410,27 +414,23 @@ __global__ void __launch_bounds__(PfCfg<D>::THREADS, 1)
           l *= alpha;
         }
         const float nmu = m_use == -INFINITY ? 0.f : -m_use;
-        // p = 2^(scale*s - m) (masked columns give 0), row sum, bf16 P into the swizzled
-        // K-major tile of buffer b
+        // p = 2^(scale*s - m) (masked columns give 0), row sum; P as bf16 pairs into the
+        // first BN/2 columns of S_b (this row's S is in registers already)
         float sum8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        uint8_t* prow = smem + C::OFF_P + b * C::P_BYTES + row * 128;
 #pragma unroll
-        for (int cc = 0; cc < C::BN / 8; ++cc) {  // 8 probabilities = one 16-byte chunk
-          float p8[8];
+        for (int c = 0; c < C::BN / 64; ++c) {
+          uint32_t pw[32];
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            p8[k] = exp2_approx(fmaf(x[8 * cc + k], sl2, nmu));
-            sum8[k] += p8[k];
+          for (int k = 0; k < 32; ++k) {
+            const float p0 = exp2_approx(fmaf(x[64 * c + 2 * k], sl2, nmu));
+            const float p1 = exp2_approx(fmaf(x[64 * c + 2 * k + 1], sl2, nmu));
+            sum8[(2 * k) & 7] += p0;
+            sum8[(2 * k + 1) & 7] += p1;
+            pw[k] = pack_bf16x2(p0, p1);
           }
-          uint4 v;
-          v.x = pack_bf16x2(p8[0], p8[1]);
-          v.y = pack_bf16x2(p8[2], p8[3]);
-          v.z = pack_bf16x2(p8[4], p8[5]);
-          v.w = pack_bf16x2(p8[6], p8[7]);
-          *reinterpret_cast<uint4*>(prow + (cc >> 3) * (C::BM * 128) + (((cc & 7) ^ (row & 7)) << 4)) = v;
+          tmem_st32u(tmem + lane_off + C::S_COL0 + b * C::BN + 32 * c, pw);
         }
         l += ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
-        fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(bar(PfBars::P_FULL + b));
       }

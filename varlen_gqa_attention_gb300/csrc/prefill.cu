@@ -254,17 +254,23 @@ __global__ void __launch_bounds__(PfCfg<D>::THREADS, 1)
       PfPiece pc;
       uint32_t gt = 0, pi = 0;
       bool ok = true;
+      // Descriptors differ only in their start-address field (bits 0-13, address / 16), so
+      // each MMA's operands are a base descriptor plus a byte offset / 16.
+      const uint64_t q_desc = sdesc_sw128(sQ, 16, 1024);
+      const uint64_t k_desc = sdesc_sw128(sK, 16, 1024);
+      const uint64_t v_desc = sdesc_sw128(sV, C::BN * 128, 1024);
       auto issue_s = [&](uint32_t g) -> bool {
         const int s = g % C::STAGES, b = g & 1;
         if (!mbar_wait(bar(PfBars::K_FULL + s), (g / C::STAGES) & 1, abort)) return false;
         if (!mbar_wait(bar(PfBars::S_FREE + b), ((g >> 1) & 1) ^ 1, abort)) return false;
         tc_fence_after();
+        const uint64_t kd = k_desc + (uint64_t)((s * C::KV_BYTES) >> 4);
+        const uint32_t d = tmem + C::S_COL0 + b * C::BN;
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
-          const uint64_t a = sdesc_sw128(sQ + (k >> 2) * (C::BM * 128) + (k & 3) * 32, 16, 1024);
-          const uint64_t bd =
-              sdesc_sw128(sK + s * C::KV_BYTES + (k >> 2) * (C::BN * 128) + (k & 3) * 32, 16, 1024);
-          tc_mma_ss(tmem + C::S_COL0 + b * C::BN, a, bd, IDESC_QK, k > 0 ? 1u : 0u);
+          const uint32_t off = ((k >> 2) * (C::BM * 128) + (k & 3) * 32) >> 4;
+          const uint32_t offk = ((k >> 2) * (C::BN * 128) + (k & 3) * 32) >> 4;
+          tc_mma_ss(d, q_desc + off, kd + offk, IDESC_QK, k > 0 ? 1u : 0u);
         }
         tc_commit(bar(PfBars::S_FULL + b));
         tc_commit(bar(PfBars::K_EMPTY + s));  // K(g) is free once S(g) is done
@@ -296,12 +302,12 @@ __global__ void __launch_bounds__(PfCfg<D>::THREADS, 1)
           // A = P(g) in tensor memory (bf16 pairs in S_b's first BN/2 columns); it is read
           // before S(g+2) overwrites S_b, since this thread issues that MMA later and a
           // thread's MMAs run in issue order
+          const uint64_t vd = v_desc + (uint64_t)((s * C::KV_BYTES) >> 4);
+          const uint32_t pa = tmem + C::S_COL0 + b * C::BN, od = tmem + o_col;
+          const uint32_t acc0 = j >= first_j ? 1u : 0u;
 #pragma unroll
-          for (int k = 0; k < C::BN / 16; ++k) {
-            const uint32_t a = tmem + C::S_COL0 + b * C::BN + 8 * k;
-            const uint64_t bd = sdesc_sw128(sV + s * C::KV_BYTES + k * 16 * 128, C::BN * 128, 1024);
-            tc_mma_ts(tmem + o_col, a, bd, IDESC_PV, (j >= first_j || k > 0) ? 1u : 0u);
-          }
+          for (int k = 0; k < C::BN / 16; ++k)
+            tc_mma_ts(od, pa + 8 * k, vd + (uint64_t)((k * 16 * 128) >> 4), IDESC_PV, k > 0 ? 1u : acc0);
           if (!C::DUAL) tc_commit(bar(PfBars::O_DONE));
           if (j + 1 == n) tc_commit(bar(PfBars::O_FINAL));
           tc_commit(bar(PfBars::V_EMPTY + s));  // V(g) is free once PV(g) is done

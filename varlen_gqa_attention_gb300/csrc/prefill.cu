@@ -11,8 +11,8 @@
 //     (same scheduler output as the split-K kernel): every CTA gets the same number of key
 //     tiles, units being (segment, KV head, 128 packed rows r = i * group + g) - the query
 //     heads sharing a KV head fill the MMA's M dimension together (GQA packing);
-//   * the producer warp moves Q and K/V tiles with TMA (128-byte swizzle) into a ring of
-//     shared-memory stages; the store is a 4-d tensor [rows, cols, Hkv, D], so a tile of one
+//   * two producer warps move Q and K tiles, and V tiles, with TMA (128-byte swizzle) into
+//     rings of shared-memory stages; the store is a 4-d tensor [rows, cols, Hkv, D], so a tile of one
 //     column and KV head is one box;
 //   * one thread of the MMA warp issues tcgen05.mma: S = Q K^T into one of two tensor-memory
 //     buffers (fp32, 128 lanes x BN columns), then O += P V into a tensor-memory accumulator;
@@ -48,7 +48,7 @@ struct PfCfg {
   // with its own O accumulator, when S0, S1, O0 and O1 fit in tensor memory.
   static constexpr bool DUAL = 2 * BN + 2 * D <= 512;
   static constexpr int SOFT_WARPS = DUAL ? 8 : 4;
-  static constexpr int THREADS = 32 * (SOFT_WARPS + 2);  // + TMA producer + MMA issuer
+  static constexpr int THREADS = 32 * (SOFT_WARPS + 3);  // + K and V producers + MMA issuer
   static constexpr int O_COL = 2 * BN;                    // O_b: columns [2*BN + b*D, +D)
   static constexpr int TMEM_COLS = DUAL ? 512 : ((2 * BN + D) <= 256 ? 256 : 512);
   static constexpr int OFF_Q = 0;
@@ -68,7 +68,9 @@ static_assert(PfCfg<256>::SMEM <= 232448, "prefill D=256 shared memory");
 // barrier slots (8 bytes each) inside the barrier block
 struct PfBars {
   // K and V stages are filled and released separately: K(g) is free once S(g) is done,
-  // V(g) once PV(g) is done, so the next K tile streams in while the softmax runs.
+  // V(g) once PV(g) is done, so the next K tile streams in while the softmax runs.  Both
+  // releases are signalled by the softmax warpgroup that sees S complete (S(g+2) completes
+  // after PV(g), which was issued before it), keeping commits off the MMA thread.
   static constexpr int K_FULL = 26;    // [6]
   static constexpr int K_EMPTY = 32;   // [6]
   static constexpr int V_READY = 38;   // [6] V landed and, on a boundary tile, zeroed
@@ -76,7 +78,6 @@ struct PfBars {
   static constexpr int V_EMPTY = 50;   // [6]
   static constexpr int kMaxStages = 6; // slots 0..55 fit the 512-byte block
   static constexpr int S_FULL = 12;    // [2]
-  static constexpr int S_FREE = 14;    // [2]
   static constexpr int P_FULL = 16;    // [2]
   static constexpr int O_DONE = 18;
   static constexpr int Q_FULL = 19;
@@ -129,7 +130,7 @@ __global__ void __launch_bounds__(PfCfg<D>::THREADS, 1)
                  sBar = sbase + C::OFF_BAR;
   auto bar = [&](int i) { return sBar + 8u * (uint32_t)i; };
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  constexpr int W_PROD = C::SOFT_WARPS, W_MMA = C::SOFT_WARPS + 1;
+  constexpr int W_PROD_K = C::SOFT_WARPS, W_PROD_V = C::SOFT_WARPS + 1, W_MMA = C::SOFT_WARPS + 2;
   volatile int* abort = &s_abort;
 
   if (threadIdx.x == 0) {
@@ -142,7 +143,6 @@ __global__ void __launch_bounds__(PfCfg<D>::THREADS, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar(PfBars::S_FULL + b), 1);
-      mbar_init(bar(PfBars::S_FREE + b), 128);
       mbar_init(bar(PfBars::P_FULL + b), 128);
     }
     mbar_init(bar(PfBars::O_DONE), 1);
@@ -164,8 +164,11 @@ __global__ void __launch_bounds__(PfCfg<D>::THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = s_tmem;
 
-  if (warp == W_PROD) {
-    // ------------------------------------------------------------ TMA producer
+  if (warp == W_PROD_K || warp == W_PROD_V) {
+    // ------------------------------------------------------------ TMA producers
+    // One warp streams Q and K tiles, the other V tiles: K(g) is released as soon as S(g)
+    // completes, so the K warp can run ahead while the V warp waits for PV to free V slots.
+    const bool is_k = warp == W_PROD_K;
     PieceWalk wk;
     walk_begin(wk, A.ws, kRoutePrefill);
     PfPiece pc;
@@ -173,7 +176,7 @@ __global__ void __launch_bounds__(PfCfg<D>::THREADS, 1)
     bool ok = true;
     while (ok && pf_next(wk, pc)) {
       const int hk = pc.ur.hk;
-      if (lane == 0) {
+      if (is_k && lane == 0) {
         ok = mbar_wait(bar(PfBars::Q_EMPTY), (pi & 1) ^ 1, abort);
         if (ok) {
           mbar_expect_tx(bar(PfBars::Q_FULL), C::Q_BYTES);
@@ -192,18 +195,27 @@ __global__ void __launch_bounds__(PfCfg<D>::THREADS, 1)
         const uint32_t use = gt / C::STAGES;
         const int64_t j0 = pos_lo + (int64_t)j * C::BN;
         const int valid = (int)min((int64_t)C::BN, pos_hi - j0);
-        if (lane == 0) {
-          const int row0 = (int)(j0 % A.rows);
-          ok = mbar_wait(bar(PfBars::K_EMPTY + s), (use & 1) ^ 1, abort);
-          if (ok) {
-            mbar_expect_tx(bar(PfBars::K_FULL + s), C::KV_BYTES);
+        const int row0 = (int)(j0 % A.rows);
+        if (is_k) {
+          if (lane == 0) {
+            ok = mbar_wait(bar(PfBars::K_EMPTY + s), (use & 1) ^ 1, abort);
+            if (ok) {
+              mbar_expect_tx(bar(PfBars::K_FULL + s), C::KV_BYTES);
 #pragma unroll
-            for (int c = 0; c < C::NREG; ++c)
-              tma_load_4d(sK + s * C::KV_BYTES + c * (C::BN * 128), &tmK, bar(PfBars::K_FULL + s),
-                          64 * c, hk, pc.sg.col, row0);
-            ok = mbar_wait(bar(PfBars::V_EMPTY + s), (use & 1) ^ 1, abort);
+              for (int c = 0; c < C::NREG; ++c)
+                tma_load_4d(sK + s * C::KV_BYTES + c * (C::BN * 128), &tmK, bar(PfBars::K_FULL + s),
+                            64 * c, hk, pc.sg.col, row0);
+            }
           }
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          continue;
+        }
+        if (lane == 0) {
+          ok = mbar_wait(bar(PfBars::V_EMPTY + s), (use & 1) ^ 1, abort);
           if (ok) {
+            // a full tile needs no zeroing: V_READY goes ahead of the copy, so it is complete
+            // whenever V_FULL is
+            if (valid == C::BN) mbar_arrive(bar(PfBars::V_READY + s));
             mbar_expect_tx(bar(PfBars::V_FULL + s), C::KV_BYTES);
 #pragma unroll
             for (int c = 0; c < C::NREG; ++c)
@@ -227,8 +239,8 @@ __global__ void __launch_bounds__(PfCfg<D>::THREADS, 1)
           }
           fence_proxy_async_smem();
           __syncwarp();
+          if (lane == 0) mbar_arrive(bar(PfBars::V_READY + s));
         }
-        if (lane == 0) mbar_arrive(bar(PfBars::V_READY + s));
       }
       ++pi;
     }
@@ -237,11 +249,9 @@ __global__ void __launch_bounds__(PfCfg<D>::THREADS, 1)
     if (lane == 0) {
       int dummy = 0;
       const uint32_t first = gt > (uint32_t)C::STAGES ? gt - C::STAGES : 0u;
-      for (uint32_t g = first; g < gt; ++g) {
-        mbar_wait(bar(PfBars::K_FULL + g % C::STAGES), (g / C::STAGES) & 1, &dummy);
-        mbar_wait(bar(PfBars::V_FULL + g % C::STAGES), (g / C::STAGES) & 1, &dummy);
-      }
-      if (pi > 0) mbar_wait(bar(PfBars::Q_FULL), (pi - 1) & 1, &dummy);
+      for (uint32_t g = first; g < gt; ++g)
+        mbar_wait(bar((is_k ? PfBars::K_FULL : PfBars::V_FULL) + g % C::STAGES), (g / C::STAGES) & 1, &dummy);
+      if (is_k && pi > 0) mbar_wait(bar(PfBars::Q_FULL), (pi - 1) & 1, &dummy);
     }
     __syncwarp();
   } else if (warp == W_MMA) {
@@ -259,11 +269,18 @@ __global__ void __launch_bounds__(PfCfg<D>::THREADS, 1)
       const uint64_t q_desc = sdesc_sw128(sQ, 16, 1024);
       const uint64_t k_desc = sdesc_sw128(sK, 16, 1024);
       const uint64_t v_desc = sdesc_sw128(sV, C::BN * 128, 1024);
-      auto issue_s = [&](uint32_t g) -> bool {
+      // Issue order S(0) S(1) | PV(0) S(2) | PV(1) S(3) | ...: S(g+2) reuses buffer
+      // b = g & 1, whose last reader is PV(g) (P(g) sits in S_b's columns; a thread's MMAs
+      // run in issue order), so the two go out back to back as soon as P(g) is ready, with
+      // every wait of the pair done before the first MMA.  P_FULL(g) also says that the
+      // softmax has read S(g) out, so S_b needs no separate release.  Each wait or commit
+      // here costs the tensor pipe its duration (the MMA queue is shallow), so this thread
+      // does only those that carry information.
+      auto s_ready = [&](uint32_t g) -> bool {
+        return mbar_wait(bar(PfBars::K_FULL + g % C::STAGES), (g / C::STAGES) & 1, abort);
+      };
+      auto issue_s = [&](uint32_t g) {
         const int s = g % C::STAGES, b = g & 1;
-        if (!mbar_wait(bar(PfBars::K_FULL + s), (g / C::STAGES) & 1, abort)) return false;
-        if (!mbar_wait(bar(PfBars::S_FREE + b), ((g >> 1) & 1) ^ 1, abort)) return false;
-        tc_fence_after();
         const uint64_t kd = k_desc + (uint64_t)((s * C::KV_BYTES) >> 4);
         const uint32_t d = tmem + C::S_COL0 + b * C::BN;
 #pragma unroll
@@ -273,35 +290,36 @@ __global__ void __launch_bounds__(PfCfg<D>::THREADS, 1)
           tc_mma_ss(d, q_desc + off, kd + offk, IDESC_QK, k > 0 ? 1u : 0u);
         }
         tc_commit(bar(PfBars::S_FULL + b));
-        tc_commit(bar(PfBars::K_EMPTY + s));  // K(g) is free once S(g) is done
-        return true;
       };
       while (ok && pf_next(wk, pc)) {
-        ok = mbar_wait(bar(PfBars::Q_FULL), pi & 1, abort);
+        const int n = (int)(pc.tb - pc.ta);
+        // keys of the piece's last tile (the V producer zeroes the rest of that tile)
+        const int64_t span = min((int64_t)pc.ur.lo + pc.tb * C::BN, (int64_t)pc.ur.hi) -
+                             ((int64_t)pc.ur.lo + pc.ta * C::BN);
+        const bool ragged = span < (int64_t)n * C::BN;
+        ok = mbar_wait(bar(PfBars::Q_FULL), pi & 1, abort) && s_ready(gt) && (n < 2 || s_ready(gt + 1));
         if (!ok) break;
         tc_fence_after();
-        const int n = (int)(pc.tb - pc.ta);
-        ok = issue_s(gt);
-        for (int j = 0; ok && j < n; ++j) {
+        issue_s(gt);
+        if (n > 1) issue_s(gt + 1);
+        if (n <= 2) tc_commit(bar(PfBars::Q_EMPTY));  // every S of this piece has been issued
+        for (int j = 0; j < n; ++j) {
           const uint32_t g = gt + j;
-          if (j + 1 < n) {
-            ok = issue_s(g + 1);
-            if (!ok) break;
-          } else {
-            tc_commit(bar(PfBars::Q_EMPTY));  // every S of this piece has been issued
-          }
           const int b = g & 1, s = g % C::STAGES;
+          const bool more = j + 2 < n;
+          // V_READY is awaited on the ragged tile only: the producer arrives on it for every
+          // tile (before the copy, or after zeroing the rows past the last key), so at this
+          // wait the barrier has completed exactly the phases of earlier uses and this one.
+          const bool tail = ragged && j + 1 == n;
           ok = mbar_wait(bar(PfBars::P_FULL + b), (g >> 1) & 1, abort) &&
                mbar_wait(bar(PfBars::V_FULL + s), (g / C::STAGES) & 1, abort) &&
-               mbar_wait(bar(PfBars::V_READY + s), (g / C::STAGES) & 1, abort);
+               (!tail || mbar_wait(bar(PfBars::V_READY + s), (g / C::STAGES) & 1, abort)) &&
+               (!more || s_ready(g + 2));
           if (!ok) break;
           tc_fence_after();
           // O_b of warpgroup b (one O when single): its first PV of the piece overwrites
           const uint32_t o_col = C::O_COL + (C::DUAL ? b * D : 0);
           const int first_j = C::DUAL ? 2 : 1;
-          // A = P(g) in tensor memory (bf16 pairs in S_b's first BN/2 columns); it is read
-          // before S(g+2) overwrites S_b, since this thread issues that MMA later and a
-          // thread's MMAs run in issue order
           const uint64_t vd = v_desc + (uint64_t)((s * C::KV_BYTES) >> 4);
           const uint32_t pa = tmem + C::S_COL0 + b * C::BN, od = tmem + o_col;
           const uint32_t acc0 = j >= first_j ? 1u : 0u;
@@ -310,7 +328,11 @@ __global__ void __launch_bounds__(PfCfg<D>::THREADS, 1)
             tc_mma_ts(od, pa + 8 * k, vd + (uint64_t)((k * 16 * 128) >> 4), IDESC_PV, k > 0 ? 1u : acc0);
           if (!C::DUAL) tc_commit(bar(PfBars::O_DONE));
           if (j + 1 == n) tc_commit(bar(PfBars::O_FINAL));
-          tc_commit(bar(PfBars::V_EMPTY + s));  // V(g) is free once PV(g) is done
+          if (!more) tc_commit(bar(PfBars::V_EMPTY + s));  // else released when S(g+2) completes
+          if (more) {
+            issue_s(g + 2);
+            if (j + 3 == n) tc_commit(bar(PfBars::Q_EMPTY));
+          }
         }
         gt += n;
         ++pi;
@@ -376,8 +398,12 @@ __global__ void __launch_bounds__(PfCfg<D>::THREADS, 1)
           tmem_ld128(tmem + lane_off + C::S_COL0 + b * C::BN, x);
         else
           tmem_ld64(tmem + lane_off + C::S_COL0 + b * C::BN, x);
-        tc_fence_before();
-        mbar_arrive(bar(PfBars::S_FREE + b));
+        if ((threadIdx.x & 127) == 0) {
+          // S(g) done: K(g) is free, and so is V(g-2) of this piece (PV(g-2) was issued
+          // before S(g))
+          mbar_arrive(bar(PfBars::K_EMPTY + g % C::STAGES));
+          if (j >= 2) mbar_arrive(bar(PfBars::V_EMPTY + (g - 2) % C::STAGES));
+        }
         // columns outside [vlo, vhi) (masked keys, stale cells past the last key) -> -inf
         if (vlo > 0 || vhi < C::BN) {
 #pragma unroll

@@ -39,23 +39,24 @@ template <int D>
 struct PfCfg {
   static constexpr int BM = kPrefillRows;                 // 128 packed rows
   static constexpr int BN = D == 256 ? 64 : kPrefillTile;  // keys per tile
+  static constexpr int HALF = BN / 2;                     // key columns per softmax warpgroup
   static constexpr int STAGES = D == 64 ? 6 : (D == 128 ? 3 : 2);  // K/V ring depth
   static constexpr int NREG = D / 64;                     // 64-element (128-byte) column regions
   static constexpr int Q_BYTES = BM * D * 2;
   static constexpr int KV_BYTES = BN * D * 2;             // K (or V) of one stage
-  static constexpr int S_COL0 = 0;                        // S buffers: columns [b*BN, (b+1)*BN)
-  // Two softmax warpgroups take alternate key tiles (tile g goes to warpgroup g & 1), each
-  // with its own O accumulator, when S0, S1, O0 and O1 fit in tensor memory.
-  static constexpr bool DUAL = 2 * BN + 2 * D <= 512;
-  static constexpr int SOFT_WARPS = DUAL ? 8 : 4;
+  // Tensor memory: S_b fp32 [b*BN, (b+1)*BN); P_b as bf16 pairs [P_COL + b*BN/2, +BN/2);
+  // one O accumulator of D columns.  Two softmax warpgroups split every tile's key columns.
+  static constexpr int S_COL0 = 0;
+  static constexpr int P_COL = 2 * BN;
+  static constexpr int O_COL = D == 256 ? 256 : 3 * BN;
+  static constexpr int TMEM_COLS = 512;
+  static constexpr int SOFT_WARPS = 8;
   static constexpr int THREADS = 32 * (SOFT_WARPS + 3);  // + K and V producers + MMA issuer
-  static constexpr int O_COL = 2 * BN;                    // O_b: columns [2*BN + b*D, +D)
-  static constexpr int TMEM_COLS = DUAL ? 512 : ((2 * BN + D) <= 256 ? 256 : 512);
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + Q_BYTES;
   static constexpr int OFF_V = OFF_K + STAGES * KV_BYTES;
   static constexpr int OFF_BAR = OFF_V + STAGES * KV_BYTES;
-  static constexpr int BAR_BYTES = 512 + (DUAL ? 1024 : 0);  // + (m, l) exchange of 128 rows
+  static constexpr int BAR_BYTES = 512;
   static constexpr int SMEM = OFF_BAR + BAR_BYTES + 1024;  // + alignment slack
 };
 static_assert(PfCfg<64>::STAGES <= 6 && PfCfg<128>::STAGES <= 6 && PfCfg<256>::STAGES <= 6,
@@ -63,36 +64,30 @@ static_assert(PfCfg<64>::STAGES <= 6 && PfCfg<128>::STAGES <= 6 && PfCfg<256>::S
 static_assert(PfCfg<128>::SMEM <= 232448, "prefill D=128 shared memory");
 static_assert(PfCfg<64>::SMEM <= 232448, "prefill D=64 shared memory");
 static_assert(PfCfg<256>::SMEM <= 232448, "prefill D=256 shared memory");
-
+static_assert(PfCfg<64>::O_COL + 64 <= 512 && PfCfg<128>::O_COL + 128 <= 512 &&
+                  PfCfg<256>::O_COL + 256 <= 512 && PfCfg<256>::P_COL + 64 <= PfCfg<256>::O_COL,
+              "prefill tensor-memory layout");
 
 // barrier slots (8 bytes each) inside the barrier block
 struct PfBars {
-  // K and V stages are filled and released separately: K(g) is free once S(g) is done,
-  // V(g) once PV(g) is done, so the next K tile streams in while the softmax runs.  Both
-  // releases are signalled by the softmax warpgroup that sees S complete (S(g+2) completes
-  // after PV(g), which was issued before it), keeping commits off the MMA thread.
+  // K and V stages are filled and released separately.  K(g) is free once S(g) is done:
+  // the softmax thread that sees S_FULL(g) releases it.  V(g) is released by a commit after
+  // PV(g); the softmax also waits on that phase to know that PV(g) no longer reads P_b or O.
   static constexpr int K_FULL = 26;    // [6]
   static constexpr int K_EMPTY = 32;   // [6]
   static constexpr int V_READY = 38;   // [6] V landed and, on a boundary tile, zeroed
   static constexpr int V_FULL = 44;    // [6]
-  static constexpr int V_EMPTY = 50;   // [6]
+  static constexpr int V_EMPTY = 50;   // [6] PV of this stage's tile done
   static constexpr int kMaxStages = 6; // slots 0..55 fit the 512-byte block
   static constexpr int S_FULL = 12;    // [2]
-  static constexpr int P_FULL = 16;    // [2]
-  static constexpr int O_DONE = 18;
+  static constexpr int S_FREE = 14;    // [2] both warpgroups have read S_b out
+  static constexpr int P_FULL = 16;    // [2] both warpgroups have written P_b
   static constexpr int Q_FULL = 19;
   static constexpr int Q_EMPTY = 20;
   static constexpr int DRAIN = 21;
-  // completes once per piece, after the piece's last PV: the epilogue waits on it with the
-  // piece parity.  (O_DONE completes once per PV; when the softmax runs ahead it can be two
-  // phases behind at the end of a piece, which a parity wait cannot tell from done.)
-  static constexpr int O_FINAL = 22;
-  // warpgroup 1 -> warpgroup 0: its row max and sum are in the exchange block (X_FULL), and
-  // warpgroup 0 has finished the piece's epilogue, so O1 and the block are free (X_FREE)
-  static constexpr int X_FULL = 23;
-  static constexpr int X_FREE = 24;
-  static constexpr int X_OFF = 512;  // byte offset of the exchange block (float2 per row)
 };
+// named barrier of the two softmax warpgroups (id 0 is __syncthreads)
+constexpr int kSoftBar = 1;
 
 struct PfPiece {
   UnitRec ur;
@@ -143,15 +138,12 @@ __global__ void __launch_bounds__(PfCfg<D>::THREADS, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar(PfBars::S_FULL + b), 1);
-      mbar_init(bar(PfBars::P_FULL + b), 128);
+      mbar_init(bar(PfBars::S_FREE + b), 32 * C::SOFT_WARPS);
+      mbar_init(bar(PfBars::P_FULL + b), 32 * C::SOFT_WARPS);
     }
-    mbar_init(bar(PfBars::O_DONE), 1);
     mbar_init(bar(PfBars::Q_FULL), 1);
     mbar_init(bar(PfBars::Q_EMPTY), 1);
     mbar_init(bar(PfBars::DRAIN), 1);
-    mbar_init(bar(PfBars::O_FINAL), 1);
-    mbar_init(bar(PfBars::X_FULL), 128);
-    mbar_init(bar(PfBars::X_FREE), 128);
     s_abort = 0;
     mbar_fence_init();
   }
@@ -256,7 +248,9 @@ __global__ void __launch_bounds__(PfCfg<D>::THREADS, 1)
     __syncwarp();
   } else if (warp == W_MMA) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // The whole warp runs this loop with warp-uniform values; one elected lane issues
+    // each MMA and commit.
+    {
       constexpr uint32_t IDESC_QK = idesc_bf16_f32(128, C::BN, false, false);
       constexpr uint32_t IDESC_PV = idesc_bf16_f32(128, D, false, true);
       PieceWalk wk;
@@ -269,27 +263,57 @@ __global__ void __launch_bounds__(PfCfg<D>::THREADS, 1)
       const uint64_t q_desc = sdesc_sw128(sQ, 16, 1024);
       const uint64_t k_desc = sdesc_sw128(sK, 16, 1024);
       const uint64_t v_desc = sdesc_sw128(sV, C::BN * 128, 1024);
-      // Issue order S(0) S(1) | PV(0) S(2) | PV(1) S(3) | ...: S(g+2) reuses buffer
-      // b = g & 1, whose last reader is PV(g) (P(g) sits in S_b's columns; a thread's MMAs
-      // run in issue order), so the two go out back to back as soon as P(g) is ready, with
-      // every wait of the pair done before the first MMA.  P_FULL(g) also says that the
-      // softmax has read S(g) out, so S_b needs no separate release.  Each wait or commit
-      // here costs the tensor pipe its duration (the MMA queue is shallow), so this thread
-      // does only those that carry information.
-      auto s_ready = [&](uint32_t g) -> bool {
-        return mbar_wait(bar(PfBars::K_FULL + g % C::STAGES), (g / C::STAGES) & 1, abort);
+      // Issue order S(0) S(1) | S(2) PV(0) | S(3) PV(1) | ...: S(g+2) goes out as soon as
+      // the softmax has read S(g) out of S_b (S_FREE), PV(g) once P(g) is in P_b (P_FULL),
+      // so the tensor pipe computes the next scores while the softmax works on this tile.
+      // The MMA queue is shallow: a blocking wait here leaves the pipe idle for its
+      // latency.  So the next waits are tested (non-blocking) between the last MMAs of a
+      // block, where the test's latency hides behind MMA issue, and the blocking waits run
+      // only when a test came back negative.
+      constexpr int KS = D / 16, KP = C::BN / 16;  // k-steps of S and of PV
+      auto s_deps = [&](uint32_t g) -> bool {
+        return __all_sync(0xffffffffu,
+                          mbar_wait(bar(PfBars::K_FULL + g % C::STAGES), (g / C::STAGES) & 1, abort) &&
+                              mbar_wait(bar(PfBars::S_FREE + (g & 1)), ((g >> 1) & 1) ^ 1, abort));
       };
-      auto issue_s = [&](uint32_t g) {
+      // (the tests' results are voted on only after the block, so no MMA waits for them)
+      auto s_test = [&](uint32_t g) -> bool {
+        return mbar_test_wait(bar(PfBars::K_FULL + g % C::STAGES), (g / C::STAGES) & 1) &
+               mbar_test_wait(bar(PfBars::S_FREE + (g & 1)), ((g >> 1) & 1) ^ 1);
+      };
+      auto pv_test = [&](uint32_t g) -> bool {
+        return mbar_test_wait(bar(PfBars::P_FULL + (g & 1)), (g >> 1) & 1) &
+               mbar_test_wait(bar(PfBars::V_FULL + g % C::STAGES), (g / C::STAGES) & 1);
+      };
+      // S(g) = Q K(g)^T into S_b; tests PV(tg)'s barriers on the way when `test`
+      auto issue_s = [&](uint32_t g, bool test, uint32_t tg) -> bool {
         const int s = g % C::STAGES, b = g & 1;
         const uint64_t kd = k_desc + (uint64_t)((s * C::KV_BYTES) >> 4);
         const uint32_t d = tmem + C::S_COL0 + b * C::BN;
+        bool pre = false;
 #pragma unroll
-        for (int k = 0; k < D / 16; ++k) {
+        for (int k = 0; k < KS; ++k) {
+          if (k == KS - 2 && test) pre = pv_test(tg);
           const uint32_t off = ((k >> 2) * (C::BM * 128) + (k & 3) * 32) >> 4;
           const uint32_t offk = ((k >> 2) * (C::BN * 128) + (k & 3) * 32) >> 4;
-          tc_mma_ss(d, q_desc + off, kd + offk, IDESC_QK, k > 0 ? 1u : 0u);
+          tc_mma_ss_w(d, q_desc + off, kd + offk, IDESC_QK, k > 0 ? 1u : 0u);
         }
-        tc_commit(bar(PfBars::S_FULL + b));
+        tc_commit_w(bar(PfBars::S_FULL + b));
+        return test && __all_sync(0xffffffffu, pre);
+      };
+      // O (+)= P(g) V(g), A = P_b from tensor memory; tests S(tg)'s barriers when `test`
+      auto issue_pv = [&](uint32_t g, uint32_t acc0, bool test, uint32_t tg) -> bool {
+        const int s = g % C::STAGES, b = g & 1;
+        const uint64_t vd = v_desc + (uint64_t)((s * C::KV_BYTES) >> 4);
+        const uint32_t pa = tmem + C::P_COL + b * (C::BN / 2), od = tmem + C::O_COL;
+        bool pre = false;
+#pragma unroll
+        for (int k = 0; k < KP; ++k) {
+          if (k == KP - 2 && test) pre = s_test(tg);
+          tc_mma_ts_w(od, pa + 8 * k, vd + (uint64_t)((k * 16 * 128) >> 4), IDESC_PV, k > 0 ? 1u : acc0);
+        }
+        tc_commit_w(bar(PfBars::V_EMPTY + s));  // V(g) free, and PV(g) done with P_b and O
+        return test && __all_sync(0xffffffffu, pre);
       };
       while (ok && pf_next(wk, pc)) {
         const int n = (int)(pc.tb - pc.ta);
@@ -297,67 +321,79 @@ __global__ void __launch_bounds__(PfCfg<D>::THREADS, 1)
         const int64_t span = min((int64_t)pc.ur.lo + pc.tb * C::BN, (int64_t)pc.ur.hi) -
                              ((int64_t)pc.ur.lo + pc.ta * C::BN);
         const bool ragged = span < (int64_t)n * C::BN;
-        ok = mbar_wait(bar(PfBars::Q_FULL), pi & 1, abort) && s_ready(gt) && (n < 2 || s_ready(gt + 1));
+        ok = __all_sync(0xffffffffu, mbar_wait(bar(PfBars::Q_FULL), pi & 1, abort)) && s_deps(gt) &&
+             (n < 2 || s_deps(gt + 1));
         if (!ok) break;
         tc_fence_after();
-        issue_s(gt);
-        if (n > 1) issue_s(gt + 1);
-        if (n <= 2) tc_commit(bar(PfBars::Q_EMPTY));  // every S of this piece has been issued
+        issue_s(gt, false, 0);
+        if (n > 1) issue_s(gt + 1, false, 0);
+        if (n <= 2) tc_commit_w(bar(PfBars::Q_EMPTY));  // every S of this piece has been issued
+        bool pre_s = false;  // S(g+2)'s barriers were seen complete by the tests
         for (int j = 0; j < n; ++j) {
           const uint32_t g = gt + j;
           const int b = g & 1, s = g % C::STAGES;
-          const bool more = j + 2 < n;
           // V_READY is awaited on the ragged tile only: the producer arrives on it for every
           // tile (before the copy, or after zeroing the rows past the last key), so at this
           // wait the barrier has completed exactly the phases of earlier uses and this one.
           const bool tail = ragged && j + 1 == n;
-          ok = mbar_wait(bar(PfBars::P_FULL + b), (g >> 1) & 1, abort) &&
-               mbar_wait(bar(PfBars::V_FULL + s), (g / C::STAGES) & 1, abort) &&
-               (!tail || mbar_wait(bar(PfBars::V_READY + s), (g / C::STAGES) & 1, abort)) &&
-               (!more || s_ready(g + 2));
-          if (!ok) break;
-          tc_fence_after();
-          // O_b of warpgroup b (one O when single): its first PV of the piece overwrites
-          const uint32_t o_col = C::O_COL + (C::DUAL ? b * D : 0);
-          const int first_j = C::DUAL ? 2 : 1;
-          const uint64_t vd = v_desc + (uint64_t)((s * C::KV_BYTES) >> 4);
-          const uint32_t pa = tmem + C::S_COL0 + b * C::BN, od = tmem + o_col;
-          const uint32_t acc0 = j >= first_j ? 1u : 0u;
-#pragma unroll
-          for (int k = 0; k < C::BN / 16; ++k)
-            tc_mma_ts(od, pa + 8 * k, vd + (uint64_t)((k * 16 * 128) >> 4), IDESC_PV, k > 0 ? 1u : acc0);
-          if (!C::DUAL) tc_commit(bar(PfBars::O_DONE));
-          if (j + 1 == n) tc_commit(bar(PfBars::O_FINAL));
-          if (!more) tc_commit(bar(PfBars::V_EMPTY + s));  // else released when S(g+2) completes
-          if (more) {
-            issue_s(g + 2);
-            if (j + 3 == n) tc_commit(bar(PfBars::Q_EMPTY));
+          bool pre_pv = false;
+          if (j + 2 < n) {
+            if (!pre_s) {
+              ok = s_deps(g + 2);
+              if (!ok) break;
+            }
+            tc_fence_after();
+            pre_pv = issue_s(g + 2, !tail, g);
+            if (j + 3 == n) tc_commit_w(bar(PfBars::Q_EMPTY));
           }
+          if (!pre_pv) {
+            ok = __all_sync(0xffffffffu,
+                            mbar_wait(bar(PfBars::P_FULL + b), (g >> 1) & 1, abort) &&
+                                mbar_wait(bar(PfBars::V_FULL + s), (g / C::STAGES) & 1, abort) &&
+                                (!tail || mbar_wait(bar(PfBars::V_READY + s), (g / C::STAGES) & 1, abort)));
+            if (!ok) break;
+          }
+          tc_fence_after();
+          pre_s = issue_pv(g, j > 0 ? 1u : 0u, j + 3 < n, g + 3);
         }
         gt += n;
         ++pi;
       }
       // drain: wait (bounded) until every MMA this thread issued has finished
-      tc_commit(bar(PfBars::DRAIN));
+      tc_commit_w(bar(PfBars::DRAIN));
       int dummy = 0;
       mbar_wait(bar(PfBars::DRAIN), 0, &dummy);
     }
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax + epilogue
-    // Warpgroup wg (warps 4*wg .. 4*wg+3) handles the key tiles g with g & 1 == wg (all tiles
-    // when single); thread = row = tensor-memory lane.  Each warpgroup keeps its own running
-    // max / sum and O accumulator; warpgroup 0 merges both at the end of a piece.
-    const int wg = C::DUAL ? (warp >> 2) : 0;
+    // Both warpgroups work on every tile: warpgroup wg takes key columns
+    // [wg*HALF, (wg+1)*HALF) of S_b, thread = row = tensor-memory lane.  They share one
+    // running max per row, keep their own partial row sums, and rescale / finalise their
+    // own half of O's columns.  Values are swapped through tensor memory (same lane = same
+    // row): each warpgroup writes into a column of the OTHER's half of P_b, which only that
+    // other warpgroup reads and later overwrites with its P, so no slot is overwritten
+    // before its reader is done.  The named barrier that
+    // carries the max exchange also ANDs the CTA's abort state, so the two warpgroups
+    // always leave together; waits between two such barriers record a failure instead of
+    // leaving at once.
+    const int wg = warp >> 2;
     const int row = (warp & 3) * 32 + lane;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-    const uint32_t o_mine = tmem + lane_off + C::O_COL + (C::DUAL ? wg * D : 0);
-    float2* xchg = reinterpret_cast<float2*>(smem + C::OFF_BAR + PfBars::X_OFF);
+    const uint32_t t_s = tmem + lane_off + C::S_COL0 + wg * C::HALF;
+    const uint32_t t_p = tmem + lane_off + C::P_COL + wg * (C::HALF / 2);
+    const uint32_t t_o = tmem + lane_off + C::O_COL + wg * (D / 2);
+    const uint32_t t_xw = tmem + lane_off + C::P_COL + (wg == 0 ? C::HALF / 2 : 0);
+    const uint32_t t_xr = tmem + lane_off + C::P_COL + (wg == 0 ? 0 : C::HALF / 2);
     const float sl2 = A.scale_log2;
+    // PV(g) finished (its commit completes stage g % STAGES's V_EMPTY phase)
+    auto pv_done = [&](uint32_t g) -> bool {
+      return mbar_wait(bar(PfBars::V_EMPTY + g % C::STAGES), (g / C::STAGES) & 1, abort);
+    };
     PieceWalk wk;
     walk_begin(wk, A.ws, kRoutePrefill);
     PfPiece pc;
-    uint32_t gt = 0, pi = 0;
+    uint32_t gt = 0;
     bool ok = true;
     while (ok && pf_next(wk, pc)) {
       const UnitRec& ur = pc.ur;
@@ -374,93 +410,92 @@ __global__ void __launch_bounds__(PfCfg<D>::THREADS, 1)
         rhi = min((int64_t)w.hi, pos_hi);
       }
       const int n = (int)(pc.tb - pc.ta);
-      if (C::DUAL && wg == 1) {
-        // O1 and the exchange block are free once warpgroup 0 has finished the last piece
-        ok = __all_sync(0xffffffffu, mbar_wait(bar(PfBars::X_FREE), (pi & 1) ^ 1, abort));
-        if (!ok) break;
-      }
       float m_use = -INFINITY, l = 0.f;
-      bool first = true;  // no PV of this warpgroup in this piece yet
+      bool okp = true;  // no wait failed since the last barrier
       for (int j = 0; j < n; ++j) {
         const uint32_t g = gt + j;
-        if (C::DUAL && (int)(g & 1) != wg) continue;
         const int b = g & 1;
-        ok = mbar_wait(bar(PfBars::S_FULL + b), (g >> 1) & 1, abort);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) break;
-        tc_fence_after();
-        // The whole S row in one batch of tensor-memory loads; the buffer is free at once.
-        const int64_t j0 = pos_lo + (int64_t)j * C::BN;
-        const int vlo = (int)min(max(rlo - j0, (int64_t)0), (int64_t)C::BN);
-        const int vhi = (int)min(max(rhi - j0, (int64_t)0), (int64_t)C::BN);
-        float x[C::BN];
-        if constexpr (C::BN == 128)
-          tmem_ld128(tmem + lane_off + C::S_COL0 + b * C::BN, x);
-        else
-          tmem_ld64(tmem + lane_off + C::S_COL0 + b * C::BN, x);
-        if ((threadIdx.x & 127) == 0) {
-          // S(g) done: K(g) is free, and so is V(g-2) of this piece (PV(g-2) was issued
-          // before S(g))
-          mbar_arrive(bar(PfBars::K_EMPTY + g % C::STAGES));
-          if (j >= 2) mbar_arrive(bar(PfBars::V_EMPTY + (g - 2) % C::STAGES));
+        const bool okw = mbar_wait(bar(PfBars::S_FULL + b), (g >> 1) & 1, abort);
+        // this half's visible columns of the tile
+        const int64_t j0 = pos_lo + (int64_t)j * C::BN + wg * C::HALF;
+        const int vlo = okw ? (int)min(max(rlo - j0, (int64_t)0), (int64_t)C::HALF) : 0;
+        const int vhi = okw ? (int)min(max(rhi - j0, (int64_t)0), (int64_t)C::HALF) : 0;
+        float x[C::HALF];
+        if (okw) {
+          tc_fence_after();
+          if constexpr (C::HALF == 64)
+            tmem_ld64(t_s + b * C::BN, x);
+          else
+            tmem_ld32(t_s + b * C::BN, x);
         }
+        tc_fence_before();
+        mbar_arrive(bar(PfBars::S_FREE + b));
+        if (threadIdx.x == 0 && okw) mbar_arrive(bar(PfBars::K_EMPTY + g % C::STAGES));  // S(g) done
         // columns outside [vlo, vhi) (masked keys, stale cells past the last key) -> -inf
-        if (vlo > 0 || vhi < C::BN) {
+        if (vlo > 0 || vhi < C::HALF) {
 #pragma unroll
-          for (int k = 0; k < C::BN; ++k) x[k] = (k >= vlo && k < vhi) ? x[k] : -INFINITY;
+          for (int k = 0; k < C::HALF; ++k) x[k] = (k >= vlo && k < vhi) ? x[k] : -INFINITY;
         }
         float mx8[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) mx8[k] = x[k];
 #pragma unroll
-        for (int k = 8; k < C::BN; ++k) mx8[k & 7] = fmaxf(mx8[k & 7], x[k]);
+        for (int k = 8; k < C::HALF; ++k) mx8[k & 7] = fmaxf(mx8[k & 7], x[k]);
         // scale is positive, so max(scale * s) = scale * max(s)
         const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
                                fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) * sl2;
-        const float m_new = fmaxf(m_use, mx);
+        // P_b (and its exchange slots) was last read by PV(g-2)
+        if (g >= 2) okp = okp && __all_sync(0xffffffffu, pv_done(g - 2));
+        if (okp) {
+          tc_fence_after();
+          tmem_st1(t_xw + b * (C::BN / 2), mx);
+        }
+        tc_fence_before();
+        ok = bar_and(kSoftBar, 32 * C::SOFT_WARPS, ok && okp && okw);
+        if (!ok) break;
+        tc_fence_after();
+        const float m_tile = fmaxf(mx, tmem_ld1(t_xr + b * (C::BN / 2)));
+        const float m_new = fmaxf(m_use, m_tile);
         const bool resc = m_new > m_use + 8.f;  // false while nothing is visible
         const float alpha = resc ? exp2_approx(m_use - m_new) : 1.f;
-        const bool need_o = resc && !first && m_use != -INFINITY;
+        const bool need_o = resc && j > 0 && m_use != -INFINITY;
         if (__any_sync(0xffffffffu, need_o)) {
-          // Rescale this warpgroup's O in place.  Dual: its last PV (tile g-2) was issued
-          // before S(g), whose completion this thread has seen, so O_wg is settled.
-          // Single: wait for the PV of tile g-1.
-          if (!C::DUAL) {
-            ok = __all_sync(0xffffffffu, mbar_wait(bar(PfBars::O_DONE), (g - 1) & 1, abort));
-            if (!ok) break;
+          // rescale this half of O once PV(g-1) has landed in it
+          okp = okp && __all_sync(0xffffffffu, pv_done(g - 1));
+          if (okp) {
             tc_fence_after();
-          }
-          const float f = need_o ? alpha : 1.f;
+            const float f = need_o ? alpha : 1.f;
 #pragma unroll 1
-          for (int c = 0; c < D / 32; ++c) {
-            float o[32];
-            tmem_ld32(o_mine + 32 * c, o);
+            for (int c = 0; c < D / 64; ++c) {
+              float o[32];
+              tmem_ld32(t_o + 32 * c, o);
 #pragma unroll
-            for (int k = 0; k < 32; ++k) o[k] *= f;
-            tmem_st32(o_mine + 32 * c, o);
+              for (int k = 0; k < 32; ++k) o[k] *= f;
+              tmem_st32(t_o + 32 * c, o);
+            }
           }
         }
-        first = false;
         if (resc) {
           m_use = m_new;
           l *= alpha;
         }
         const float nmu = m_use == -INFINITY ? 0.f : -m_use;
-        // p = 2^(scale*s - m) (masked columns give 0), row sum; P as bf16 pairs into the
-        // first BN/2 columns of S_b (this row's S is in registers already)
+        // p = 2^(scale*s - m) (masked columns give 0), row sum; P as bf16 pairs into P_b
         float sum8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        uint32_t pw[C::HALF / 2];
 #pragma unroll
-        for (int c = 0; c < C::BN / 64; ++c) {
-          uint32_t pw[32];
-#pragma unroll
-          for (int k = 0; k < 32; ++k) {
-            const float p0 = exp2_approx(fmaf(x[64 * c + 2 * k], sl2, nmu));
-            const float p1 = exp2_approx(fmaf(x[64 * c + 2 * k + 1], sl2, nmu));
-            sum8[(2 * k) & 7] += p0;
-            sum8[(2 * k + 1) & 7] += p1;
-            pw[k] = pack_bf16x2(p0, p1);
-          }
-          tmem_st32u(tmem + lane_off + C::S_COL0 + b * C::BN + 32 * c, pw);
+        for (int k = 0; k < C::HALF / 2; ++k) {
+          const float p0 = exp2_approx(fmaf(x[2 * k], sl2, nmu));
+          const float p1 = exp2_approx(fmaf(x[2 * k + 1], sl2, nmu));
+          sum8[(2 * k) & 7] += p0;
+          sum8[(2 * k + 1) & 7] += p1;
+          pw[k] = pack_bf16x2(p0, p1);
+        }
+        if (okp) {
+          if constexpr (C::HALF == 64)
+            tmem_st32u(t_p + b * (C::BN / 2), pw);
+          else
+            tmem_st16u(t_p + b * (C::BN / 2), pw);
         }
         l += ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
         tc_fence_before();
@@ -468,56 +503,35 @@ __global__ void __launch_bounds__(PfCfg<D>::THREADS, 1)
       }
       if (!ok) break;
       gt += n;
-      if (C::DUAL && wg == 1) {
-        // hand this warpgroup's row max and sum to warpgroup 0, which merges and writes
-        xchg[row] = make_float2(m_use, l);
-        mbar_arrive(bar(PfBars::X_FULL));
-        ++pi;
-        continue;
+      // epilogue: once the piece's last PV is done, swap the partial row sums through the
+      // exchange slots of that PV's (now idle) P buffer - the one the next piece writes
+      // second, behind a barrier - then normalise (direct) or write a partial
+      const bool okw = pv_done(gt - 1);
+      const uint32_t xb = ((gt - 1) & 1) * (C::BN / 2);
+      if (okw) {
+        tc_fence_after();
+        tmem_st1(t_xw + xb, l);
       }
-      // epilogue: wait for the piece's last PV (and warpgroup 1's half), then normalise
-      // (direct) or write a partial
-      ok = mbar_wait(bar(PfBars::O_FINAL), pi & 1, abort);
-      if (C::DUAL) ok = ok && mbar_wait(bar(PfBars::X_FULL), pi & 1, abort);
-      ++pi;
-      ok = __all_sync(0xffffffffu, ok);
+      tc_fence_before();
+      ok = bar_and(kSoftBar, 32 * C::SOFT_WARPS, ok && okp && okw);
       if (!ok) break;
       tc_fence_after();
-      // merge the two halves: M = max m_b, weights 2^(m_b - M) (0 for a half with no keys,
-      // whose O_b is stale), L = sum l_b * weight
-      float m1 = -INFINITY, l1 = 0.f;
-      if (C::DUAL) {
-        const float2 h1 = xchg[row];
-        m1 = h1.x;
-        l1 = h1.y;
-      }
-      const float M = fmaxf(m_use, m1);
-      const float Mu = M == -INFINITY ? 0.f : M;
-      const float f0 = l > 0.f ? exp2_approx(m_use - Mu) : 0.f;
-      const float f1 = l1 > 0.f ? exp2_approx(m1 - Mu) : 0.f;
-      const float L = l * f0 + l1 * f1;
+      const float L = l + tmem_ld1(t_xr + xb);
       const bool direct = ur.nslots == 1;
       const int h = ur.hk * A.group + (int)(r % A.group);
-      __nv_bfloat16* orow = A.out + ((int64_t)sg.q_start + qi) * A.o_rs + (int64_t)h * A.o_hs;
+      __nv_bfloat16* orow = A.out + ((int64_t)sg.q_start + qi) * A.o_rs + (int64_t)h * A.o_hs + wg * (D / 2);
       const int64_t pidx = ur.slot_base + (int64_t)pc.slot * ur.rows + row;
-      float* prow = A.ws.part_o[kRoutePrefill] + pidx * D;
-      const float inv = L > 0.f ? 1.f / L : 0.f;
-      const float w0 = direct ? f0 * inv : f0, w1 = direct ? f1 * inv : f1;
+      float* prow = A.ws.part_o[kRoutePrefill] + pidx * D + wg * (D / 2);
+      // a row with no visible key has L = 0 and writes zeros (never 0 * O)
+      const bool empty = !(L > 0.f);
+      const float w = direct ? 1.f / L : 1.f;
 #pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = 0; c < D / 64; ++c) {
         float o[32];
-        tmem_ld32(tmem + lane_off + C::O_COL + 32 * c, o);
-        if (C::DUAL) {
-          float o1[32];
-          tmem_ld32(tmem + lane_off + C::O_COL + D + 32 * c, o1);
-#pragma unroll
-          for (int k = 0; k < 32; ++k)
-            o[k] = (f0 != 0.f ? o[k] * w0 : 0.f) + (f1 != 0.f ? o1[k] * w1 : 0.f);
-        } else {
-#pragma unroll
-          for (int k = 0; k < 32; ++k) o[k] = f0 != 0.f ? o[k] * w0 : 0.f;
-        }
+        tmem_ld32(t_o + 32 * c, o);
         if (!live) continue;
+#pragma unroll
+        for (int k = 0; k < 32; ++k) o[k] = empty ? 0.f : o[k] * w;
         if (direct) {
 #pragma unroll
           for (int k = 0; k < 32; k += 8) {
@@ -534,9 +548,8 @@ __global__ void __launch_bounds__(PfCfg<D>::THREADS, 1)
             *reinterpret_cast<float4*>(prow + 32 * c + k) = make_float4(o[k], o[k + 1], o[k + 2], o[k + 3]);
         }
       }
-      if (live && !direct) A.ws.part_ml[kRoutePrefill][pidx] = make_float2(M, L);
+      if (live && !direct && wg == 0) A.ws.part_ml[kRoutePrefill][pidx] = make_float2(m_use, L);
       tc_fence_before();
-      if (C::DUAL) mbar_arrive(bar(PfBars::X_FREE));  // O1 and the exchange block are free
     }
   }
 

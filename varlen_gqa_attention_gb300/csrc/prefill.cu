@@ -416,6 +416,9 @@ __global__ void __launch_bounds__(PfCfg<D>::THREADS, 1)
         const uint32_t g = gt + j;
         const int b = g & 1;
         const bool okw = mbar_wait(bar(PfBars::S_FULL + b), (g >> 1) & 1, abort);
+        // P_b was last read by PV(g-2): tested here, its answer used after the max
+        const uint32_t g2 = g - 2;
+        const bool pv2 = g < 2 || mbar_test_wait(bar(PfBars::V_EMPTY + g2 % C::STAGES), (g2 / C::STAGES) & 1);
         // this half's visible columns of the tile
         const int64_t j0 = pos_lo + (int64_t)j * C::BN + wg * C::HALF;
         const int vlo = okw ? (int)min(max(rlo - j0, (int64_t)0), (int64_t)C::HALF) : 0;
@@ -444,41 +447,50 @@ __global__ void __launch_bounds__(PfCfg<D>::THREADS, 1)
         // scale is positive, so max(scale * s) = scale * max(s)
         const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
                                fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) * sl2;
-        // P_b (and its exchange slots) was last read by PV(g-2)
-        if (g >= 2) okp = okp && __all_sync(0xffffffffu, pv_done(g - 2));
-        if (okp) {
-          tc_fence_after();
-          tmem_st1(t_xw + b * (C::BN / 2), mx);
-        }
-        tc_fence_before();
-        ok = bar_and(kSoftBar, 32 * C::SOFT_WARPS, ok && okp && okw);
-        if (!ok) break;
-        tc_fence_after();
-        const float m_tile = fmaxf(mx, tmem_ld1(t_xr + b * (C::BN / 2)));
-        const float m_new = fmaxf(m_use, m_tile);
-        const bool resc = m_new > m_use + 8.f;  // false while nothing is visible
-        const float alpha = resc ? exp2_approx(m_use - m_new) : 1.f;
-        const bool need_o = resc && j > 0 && m_use != -INFINITY;
-        if (__any_sync(0xffffffffu, need_o)) {
-          // rescale this half of O once PV(g-1) has landed in it
-          okp = okp && __all_sync(0xffffffffu, pv_done(g - 1));
-          if (okp) {
+        // Fast path: no row of either half has a tile max above m_use + 2^8, so every running
+        // max stays as it is and nothing needs exchanging.  The barrier's AND also carries
+        // the wait results; a false AND takes the slow path, whose barrier tells them apart.
+        const bool calm = mx <= m_use + 8.f;
+        const bool fast = bar_and(kSoftBar, 32 * C::SOFT_WARPS, ok && okp && okw && calm);
+        if (!fast) {
+          if (!__all_sync(0xffffffffu, pv2)) okp = okp && __all_sync(0xffffffffu, pv_done(g2));
+          if (okp && okw) {
             tc_fence_after();
-            const float f = need_o ? alpha : 1.f;
+            tmem_st1(t_xw + b * (C::BN / 2), mx);
+          }
+          tc_fence_before();
+          ok = bar_and(kSoftBar, 32 * C::SOFT_WARPS, ok && okp && okw);
+          if (!ok) break;
+          tc_fence_after();
+          const float m_tile = fmaxf(mx, tmem_ld1(t_xr + b * (C::BN / 2)));
+          const float m_new = fmaxf(m_use, m_tile);
+          const bool resc = m_new > m_use + 8.f;  // false while nothing is visible
+          const float alpha = resc ? exp2_approx(m_use - m_new) : 1.f;
+          const bool need_o = resc && j > 0 && m_use != -INFINITY;
+          if (__any_sync(0xffffffffu, need_o)) {
+            // rescale this half of O once PV(g-1) has landed in it
+            okp = okp && __all_sync(0xffffffffu, pv_done(g - 1));
+            if (okp) {
+              tc_fence_after();
+              const float f = need_o ? alpha : 1.f;
 #pragma unroll 1
-            for (int c = 0; c < D / 64; ++c) {
-              float o[32];
-              tmem_ld32(t_o + 32 * c, o);
+              for (int c = 0; c < D / 64; ++c) {
+                float o[32];
+                tmem_ld32(t_o + 32 * c, o);
 #pragma unroll
-              for (int k = 0; k < 32; ++k) o[k] *= f;
-              tmem_st32(t_o + 32 * c, o);
+                for (int k = 0; k < 32; ++k) o[k] *= f;
+                tmem_st32(t_o + 32 * c, o);
+              }
             }
           }
+          if (resc) {
+            m_use = m_new;
+            l *= alpha;
+          }
+        } else if (!__all_sync(0xffffffffu, pv2)) {
+          okp = okp && __all_sync(0xffffffffu, pv_done(g2));
         }
-        if (resc) {
-          m_use = m_new;
-          l *= alpha;
-        }
+        tc_fence_after();
         const float nmu = m_use == -INFINITY ? 0.f : -m_use;
         // p = 2^(scale*s - m) (masked columns give 0), row sum; P as bf16 pairs into P_b
         float sum8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};

@@ -89,6 +89,29 @@ struct PfBars {
 // named barrier of the two softmax warpgroups (id 0 is __syncthreads)
 constexpr int kSoftBar = 1;
 
+// Packed two-lane fp32 arithmetic and three-input max: the softmax warps share their
+// schedulers with the MMA-issuing warp, so every instruction they save is issue time the
+// tensor pipe's feeder gets back.
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float m;
+  asm("max.f32 %0, %1, %2, %3;\n" : "=f"(m) : "f"(a), "f"(b), "f"(c));
+  return m;
+}
+// (y0, y1) = (x0, x1) * a + c
+__device__ __forceinline__ void fma2f(float& y0, float& y1, float x0, float x1, float a, float c) {
+  asm("{\n .reg .b64 x, a, c, y;\n mov.b64 x, {%2, %3};\n mov.b64 a, {%4, %4};\n"
+      " mov.b64 c, {%5, %5};\n fma.rn.f32x2 y, x, a, c;\n mov.b64 {%0, %1}, y;\n}\n"
+      : "=f"(y0), "=f"(y1)
+      : "f"(x0), "f"(x1), "f"(a), "f"(c));
+}
+// (s0, s1) += (x0, x1)
+__device__ __forceinline__ void add2f(float& s0, float& s1, float x0, float x1) {
+  asm("{\n .reg .b64 s, x;\n mov.b64 s, {%0, %1};\n mov.b64 x, {%2, %3};\n"
+      " add.rn.f32x2 s, s, x;\n mov.b64 {%0, %1}, s;\n}\n"
+      : "+f"(s0), "+f"(s1)
+      : "f"(x0), "f"(x1));
+}
+
 struct PfPiece {
   UnitRec ur;
   SegRec sg;
@@ -439,14 +462,11 @@ __global__ void __launch_bounds__(PfCfg<D>::THREADS, 1)
 #pragma unroll
           for (int k = 0; k < C::HALF; ++k) x[k] = (k >= vlo && k < vhi) ? x[k] : -INFINITY;
         }
-        float mx8[8];
+        float mx4[4] = {x[0], x[1], x[2], x[3]};
 #pragma unroll
-        for (int k = 0; k < 8; ++k) mx8[k] = x[k];
-#pragma unroll
-        for (int k = 8; k < C::HALF; ++k) mx8[k & 7] = fmaxf(mx8[k & 7], x[k]);
+        for (int k = 4; k < C::HALF; k += 2) mx4[(k >> 1) & 3] = max3f(mx4[(k >> 1) & 3], x[k], x[k + 1]);
         // scale is positive, so max(scale * s) = scale * max(s)
-        const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]))) * sl2;
+        const float mx = fmaxf(max3f(mx4[0], mx4[1], mx4[2]), mx4[3]) * sl2;
         // Fast path: no row of either half has a tile max above m_use + 2^8, so every running
         // max stays as it is and nothing needs exchanging.  The barrier's AND also carries
         // the wait results; a false AND takes the slow path, whose barrier tells them apart.
@@ -497,10 +517,10 @@ __global__ void __launch_bounds__(PfCfg<D>::THREADS, 1)
         uint32_t pw[C::HALF / 2];
 #pragma unroll
         for (int k = 0; k < C::HALF / 2; ++k) {
-          const float p0 = exp2_approx(fmaf(x[2 * k], sl2, nmu));
-          const float p1 = exp2_approx(fmaf(x[2 * k + 1], sl2, nmu));
-          sum8[(2 * k) & 7] += p0;
-          sum8[(2 * k + 1) & 7] += p1;
+          float a0, a1;
+          fma2f(a0, a1, x[2 * k], x[2 * k + 1], sl2, nmu);
+          const float p0 = exp2_approx(a0), p1 = exp2_approx(a1);
+          add2f(sum8[(2 * k) & 7], sum8[(2 * k + 1) & 7], p0, p1);
           pw[k] = pack_bf16x2(p0, p1);
         }
         if (okp) {

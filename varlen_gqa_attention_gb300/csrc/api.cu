@@ -72,8 +72,11 @@ static sdpa_status device_info(DevInfo* out) {
       const int smem = splitk_smem_bytes(Ds[k]);
       e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
       if (e != cudaSuccess) return fail(SDPA_ERR_CUDA, "smem attribute: %s", cudaGetErrorString(e));
+      // two split-K CTAs per SM need the whole shared-memory carveout
+      e = cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+      if (e != cudaSuccess) return fail(SDPA_ERR_CUDA, "carveout attribute: %s", cudaGetErrorString(e));
       int nb = 0;
-      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, f, 128, smem);
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, f, kSplitkThreads, smem);
       if (e != cudaSuccess) return fail(SDPA_ERR_CUDA, "occupancy: %s", cudaGetErrorString(e));
       di.splitk_per_sm[k] = nb > 0 ? nb : 1;
       const void* pf = prefill_kernel_ptr(Ds[k]);
@@ -179,7 +182,7 @@ static sdpa_status launch_all(const SchedArgs& sa, const AttnArgs& aa, int D, co
   if (e == cudaSuccess) e = mark(2, st);
   if (e == cudaSuccess) {
     void* args[] = {(void*)&aa};
-    e = cudaLaunchKernel(splitk_kernel_ptr(D), dim3((unsigned)g.splitk), dim3(128), args,
+    e = cudaLaunchKernel(splitk_kernel_ptr(D), dim3((unsigned)g.splitk), dim3(kSplitkThreads), args,
                          splitk_smem_bytes(D), st);
     if (e != cudaSuccess) return fail(SDPA_ERR_CUDA, "split-K launch: %s", cudaGetErrorString(e));
   }

@@ -14,6 +14,7 @@ namespace sdpa {
 // heads that share a KV head sit side by side in one tile (GQA packing).
 constexpr int kSplitkRows = 64;    // split-K kernel: 4 warps x 16 rows
 constexpr int kSplitkTile = 64;    // split-K kernel: key positions per tile
+constexpr int kSplitkThreads = 128;  // split-K kernel: four warps
 constexpr int kPrefillRows = 128;  // tensor-memory prefill kernel: one 128-lane accumulator
 constexpr int kPrefillTile = 128;  // prefill kernel: key positions per tile
 
@@ -40,9 +41,14 @@ struct UnitRec {
   int32_t g_first;            // first such CTA
   int32_t ntiles;             // key tiles of the unit
   int32_t phase;              // scheduling phase of the unit (see SchedHdr)
-  int64_t tile_base;          // first tile of the unit in the flattened tile space
+  int32_t q_start, q_len, col, kv_end;  // the segment's entry, copied so that one record
+                                        // (80 bytes, 16-byte multiple) describes a piece
+  int32_t pad[2];
+  int64_t tile_base;          // start of the unit's span in the flattened tile line: `lead`
+                              // placeholder tiles, then its ntiles key tiles
   int64_t slot_base;          // first partial row of the unit's slots
 };
+static_assert(sizeof(UnitRec) == 80, "unit record layout");
 
 
 // Phases: a route's tile line is cut at (segment, KV head) boundaries into phases whose
@@ -60,6 +66,10 @@ struct SchedHdr {
   int64_t status;     // OR of the status bits of this call
   int64_t nphase[3];  // phases per route
   int64_t phase_base[3][kMaxPhases + 1];  // first tile of each phase; [nphase] = tiles
+  // Placeholder tiles ahead of each unit's key tiles on the line: they stand for the cost of
+  // starting a piece (operand loads, pipeline fill, the epilogue), so a CTA whose share
+  // starts a unit gets that many fewer key tiles.
+  int64_t lead[3];
 };
 
 struct Workspace {
@@ -68,6 +78,7 @@ struct Workspace {
   int32_t* row_seg;     // [T] owning segment or -1
   int32_t* seg_flag;    // [S] overlap flags
   UnitRec* units[3];    // [route][U_cap]
+  int32_t* first_unit[3];  // [route][phase * grid + CTA]: unit whose span holds the CTA's first tile
   float2* part_ml[3];   // [route][P_cap] (running max in log2 units, sum)
   float* part_o[3];     // [route][P_cap * D] unnormalised output
   int64_t unit_cap[3];
@@ -110,6 +121,7 @@ __host__ inline size_t layout_workspace(char* base, int64_t T, int Hq, int Hkv, 
     w.unit_cap[r] = unit_cap(T, Hq, Hkv, S, rpu[r]);
     w.part_cap[r] = part_cap(w.unit_cap[r], grid[r], rpu[r]);
     w.units[r] = (UnitRec*)take((int64_t)sizeof(UnitRec) * w.unit_cap[r]);
+    w.first_unit[r] = (int32_t*)take(4 * (int64_t)kMaxPhases * (grid[r] > 0 ? grid[r] : 1));
     w.part_ml[r] = (float2*)take(8 * w.part_cap[r]);
     w.part_o[r] = (float*)take(4 * w.part_cap[r] * D);
   }
@@ -204,6 +216,7 @@ struct PieceWalk {
   int64_t p;        // current phase
   int64_t t0, t1;   // remaining tiles of this CTA in phase p
   int64_t u;        // next unit to look at
+  int64_t lead;     // placeholder tiles ahead of each unit's key tiles
 };
 
 // Stream-K partition: CTA g of G owns flattened tiles [g*W/G, (g+1)*W/G).
@@ -218,6 +231,7 @@ __device__ inline void walk_begin(PieceWalk& w, const Workspace& W, int route) {
   w.route = route;
   w.G = W.hdr->grid[route];
   w.nphase = W.hdr->nphase[route];
+  w.lead = W.hdr->lead[route];
   w.p = -1;
   w.t0 = w.t1 = 0;
   w.u = 0;
@@ -234,14 +248,8 @@ __device__ inline bool walk_phase(PieceWalk& w) {
     w.t0 = b0 + sk_start(blockIdx.x, Wp, Gp);
     w.t1 = b0 + sk_start(blockIdx.x + 1, Wp, Gp);
     if (w.t0 >= w.t1) continue;
-    // first unit holding tile t0: the last unit whose tile_base <= t0
-    const UnitRec* units = w.W->units[w.route];
-    int64_t lo = 0, hi = h->units[w.route] - 1, uu = 0;
-    while (lo <= hi) {
-      const int64_t mid = (lo + hi) >> 1;
-      if (units[mid].tile_base <= w.t0) { uu = mid; lo = mid + 1; } else { hi = mid - 1; }
-    }
-    w.u = uu;
+    // the unit whose span holds tile t0, recorded by the scheduler
+    w.u = w.W->first_unit[w.route][w.p * w.G + blockIdx.x];
     return true;
   }
   return false;
@@ -253,14 +261,19 @@ __device__ inline bool walk_next(PieceWalk& w, UnitRec& ur, int64_t& ta, int64_t
     const int64_t U = w.W->hdr->units[w.route];
     while (w.t0 < w.t1 && w.u < U) {
       const UnitRec r = w.W->units[w.route][w.u];
-      if (r.ntiles == 0 || w.t0 >= r.tile_base + r.ntiles) {
+      const int64_t k0 = r.tile_base + w.lead, k1 = k0 + r.ntiles;  // the unit's key tiles
+      if (r.ntiles == 0 || w.t0 >= k1) {
         ++w.u;
         continue;
       }
+      if (w.t1 <= k0) {  // the share ends among the unit's placeholders
+        w.t0 = w.t1;
+        break;
+      }
       ur = r;
-      ta = w.t0 - r.tile_base;
-      tb = min(w.t1, r.tile_base + r.ntiles) - r.tile_base;
-      w.t0 = r.tile_base + tb;
+      ta = max(w.t0, k0) - k0;
+      tb = min(w.t1, k1) - k0;
+      w.t0 = k0 + tb;
       ++w.u;
       return true;
     }

@@ -64,7 +64,8 @@ sdpa_status static_setup(StaticDev* out) {
       const int smem = splitk_smem_bytes(Ds[k]);
       int nb = 0;
       if (cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
-          cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, f, 128, smem) != cudaSuccess)
+          cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess ||
+          cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, f, kSplitkThreads, smem) != cudaSuccess)
         return static_fail(SDPA_ERR_CUDA, "split-K kernel setup failed");
       sd.per_sm[k] = nb > 0 ? nb : 1;
     }
@@ -93,6 +94,7 @@ size_t layout_splitk_only(char* base, int64_t T, int Hq, int Hkv, int D, int S, 
   w.unit_cap[kRouteSplitk] = unit_cap(T, Hq, Hkv, S, kSplitkRows);
   w.part_cap[kRouteSplitk] = part_cap(w.unit_cap[kRouteSplitk], grid, kSplitkRows);
   w.units[kRouteSplitk] = (UnitRec*)take((int64_t)sizeof(UnitRec) * w.unit_cap[kRouteSplitk]);
+  w.first_unit[kRouteSplitk] = (int32_t*)take(4 * (int64_t)kMaxPhases * grid);
   w.part_ml[kRouteSplitk] = (float2*)take(8 * w.part_cap[kRouteSplitk]);
   w.part_o[kRouteSplitk] = (float*)take(4 * w.part_cap[kRouteSplitk] * D);
   if (ws) *ws = w;
@@ -155,6 +157,7 @@ extern "C" sdpa_status sdpa_varlen_splitk_static(
   sa.group = Hq / Hkv;
   sa.causal = causal ? 1 : 0;
   sa.window = window;
+  sa.D = D;
   sa.policy = SDPA_ROUTE_SPLITK;
   sa.prefill_ok = 0;
   sa.tile_pf = kPrefillTile;
@@ -194,7 +197,8 @@ extern "C" sdpa_status sdpa_varlen_splitk_static(
   }
   if (e == cudaSuccess) {
     void* args[] = {(void*)&aa};
-    e = cudaLaunchKernel(splitk_kernel_ptr(D), dim3((unsigned)grid), dim3(128), args, splitk_smem_bytes(D), s);
+    e = cudaLaunchKernel(splitk_kernel_ptr(D), dim3((unsigned)grid), dim3(kSplitkThreads), args,
+                         splitk_smem_bytes(D), s);
   }
   if (e == cudaSuccess && T > 0) {
     void* args[] = {(void*)&aa};

@@ -69,6 +69,10 @@ __device__ __forceinline__ int rows_per_unit(int route) {
 __device__ __forceinline__ int tile_len(const SchedArgs& A, int route) {
   return route == kRoutePrefill ? A.tile_pf : kSplitkTile;
 }
+// Start-up cost of a piece in key tiles of its route (operand loads, pipeline fill, the
+// epilogue): about 4 us per prefill piece of 128-key tiles that take about 0.7 us, about
+// 4 us per split-K piece of 64-key tiles that stream at about 1.6 us.
+__device__ __forceinline__ int64_t lead_tiles(int route) { return route == kRoutePrefill ? 6 : 3; }
 
 // Route of a live segment.  The prefill kernel takes segments that fill at least one
 // 128-row tile and whose visible keys do not wrap around a ring store (a TMA box cannot
@@ -198,6 +202,7 @@ __global__ void __launch_bounds__(kSchedThreads) sdpa_sched_kernel(SchedArgs A) 
   for (int q = 1; q < 3; ++q) {
     const int64_t U = s_tot[q];
     const int rpu = rows_per_unit(q), tl = tile_len(A, q);
+    const int64_t lead = lead_tiles(q);
     UnitRec* units = W.units[q];
     int64_t ua, ub;
     my_range(U, &ua, &ub);
@@ -222,6 +227,11 @@ __global__ void __launch_bounds__(kSchedThreads) sdpa_sched_kernel(SchedArgs A) 
       UnitRec ur;
       int64_t j = u - g.ubase[q];
       ur.seg = s;
+      ur.q_start = g.q_start;
+      ur.q_len = g.q_len;
+      ur.col = g.col;
+      ur.kv_end = g.kv_end;
+      ur.pad[0] = ur.pad[1] = 0;
       ur.hk = (int32_t)(j / g.nrb);
       ur.rb = (int32_t)(j % g.nrb);
       int64_t R = (int64_t)g.q_len * A.group;
@@ -237,7 +247,8 @@ __global__ void __launch_bounds__(kSchedThreads) sdpa_sched_kernel(SchedArgs A) 
       ur.g_first = 0;
       ur.ntiles = (int32_t)nt;
       ur.phase = 0;
-      ur.tile_base = nt;  // the count, until the scan below
+      const int64_t span_tiles = nt > 0 ? nt + lead : 0;
+      ur.tile_base = span_tiles;  // the span, until the scan below
       // K/V bytes the group's units read again (counted once, on the group's last unit;
       // only groups of several units re-read them): phases are cut on these
       int64_t reuse = 0;
@@ -248,7 +259,7 @@ __global__ void __launch_bounds__(kSchedThreads) sdpa_sched_kernel(SchedArgs A) 
       }
       ur.slot_base = reuse;  // kept here until the phase pass below
       units[u] = ur;
-      my_tiles += nt;
+      my_tiles += span_tiles;
       my_bytes += reuse;
     }
     int64_t Wt, Bt;
@@ -256,7 +267,7 @@ __global__ void __launch_bounds__(kSchedThreads) sdpa_sched_kernel(SchedArgs A) 
     int64_t bb = block_excl_scan(my_bytes, &Bt, sh);
     for (int64_t u = ua; u < ub; ++u) {
       UnitRec ur = units[u];
-      const int64_t nt = ur.tile_base, reuse = ur.slot_base;
+      const int64_t nt = ur.tile_base, reuse = ur.slot_base;  // span and re-read bytes
       ur.tile_base = tb;
       ur.phase = (int32_t)min(bb / kPhaseBytes, (int64_t)kMaxPhases - 1);
       tb += nt;
@@ -288,11 +299,16 @@ __global__ void __launch_bounds__(kSchedThreads) sdpa_sched_kernel(SchedArgs A) 
         const int64_t b0 = W.hdr->phase_base[q][ur.phase];
         const int64_t Wp = W.hdr->phase_base[q][ur.phase + 1] - b0;
         const int64_t Gp = min(G, Wp);
-        const int64_t g0 = sk_owner(ur.tile_base - b0, Wp, Gp);
-        const int64_t g1 = sk_owner(ur.tile_base + nt - 1 - b0, Wp, Gp);
+        const int64_t k0 = ur.tile_base + lead - b0;  // the key tiles, phase-relative
+        const int64_t g0 = sk_owner(k0, Wp, Gp);
+        const int64_t g1 = sk_owner(k0 + nt - 1, Wp, Gp);
         ur.g_first = (int32_t)g0;
         ur.nslots = (int32_t)(g1 - g0 + 1);
         if (ur.nslots > 1) my_rows += (int64_t)ur.nslots * ur.rows;
+        // CTAs whose share starts inside this unit's span begin their walk here
+        const int64_t s0 = ur.tile_base - b0, s1 = k0 + nt;
+        for (int64_t g = sk_owner(s0, Wp, Gp); g <= sk_owner(s1 - 1, Wp, Gp); ++g)
+          if (sk_start(g, Wp, Gp) >= s0) W.first_unit[q][ur.phase * G + g] = (int32_t)u;
       }
       units[u] = ur;
     }
@@ -307,6 +323,7 @@ __global__ void __launch_bounds__(kSchedThreads) sdpa_sched_kernel(SchedArgs A) 
       W.hdr->tiles[q] = Wt;
       W.hdr->units[q] = U;
       W.hdr->grid[q] = G;
+      W.hdr->lead[q] = lead;
     }
     __syncthreads();
   }

@@ -22,8 +22,6 @@
 
 namespace sdpa {
 
-constexpr int kSplitkThreads = 128;
-
 template <int D>
 struct SplitkSmem {
   // key tiles in flight: 3 stages keep two tiles loading while one is used (two CTAs per
@@ -344,7 +342,11 @@ __global__ void __launch_bounds__(kSplitkThreads) sdpa_splitk_kernel(AttnArgs A)
   UnitRec ur;
   int64_t ta, tb;
   while (walk_next(wk, ur, ta, tb)) {
-    const SegRec sg = A.ws.segs[ur.seg];
+    SegRec sg;  // the unit record carries its segment's entry: no second dependent load
+    sg.q_start = ur.q_start;
+    sg.q_len = ur.q_len;
+    sg.col = ur.col;
+    sg.kv_end = ur.kv_end;
     const int slot = (int)(blockIdx.x - ur.g_first);
     if (ur.rows <= 16)
       splitk_unit<D, 4>(A, ur, sg, ta, tb, slot, smem, s_ml);

@@ -1,0 +1,87 @@
+"""Host-side logic of bench.py, on the CPU: the replica ranks' barrier and max-over-ranks timing
+(world size 2 over gloo, as torchrun would launch it), and the useful-work counts that turn a
+timing into TFLOP/s and GB/s, checked against the oracle's own counts."""
+import os
+import socket
+import sys
+
+import numpy as np
+import pytest
+
+sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+
+import bench  # noqa: E402
+from oracle import sdpa_varlen_oracle as O  # noqa: E402
+from workloads import synth  # noqa: E402
+
+
+def _free_port() -> int:
+    with socket.socket(socket.AF_INET, socket.SOCK_STREAM) as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank: int, world: int, port: int, out):
+    os.environ.update({"WORLD_SIZE": str(world), "RANK": str(rank), "LOCAL_RANK": str(rank),
+                       "MASTER_ADDR": "127.0.0.1", "MASTER_PORT": str(port)})
+    w, r, local = bench.dist_setup()
+    bench.barrier(w)
+    # each rank's "elapsed time": the job's time is the slowest rank's
+    t = bench.max_over_ranks(1.5 + rank, w)
+    bench.barrier(w)
+    out.put((r, local, w, t))
+    import torch.distributed as dist
+
+    dist.destroy_process_group()
+
+
+def test_replica_ranks_agree_on_the_slowest_time():
+    import torch.multiprocessing as mp
+
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+    assert all(p.exitcode == 0 for p in procs), [p.exitcode for p in procs]
+    got = sorted(q.get(timeout=5) for _ in range(2))
+    assert [g[0] for g in got] == [0, 1]
+    assert [g[1] for g in got] == [0, 1]
+    assert all(g[2] == 2 for g in got)
+    assert all(g[3] == 2.5 for g in got)  # max over the two ranks, on both
+
+
+def test_single_rank_needs_no_process_group(monkeypatch):
+    for k in ("WORLD_SIZE", "RANK", "LOCAL_RANK"):
+        monkeypatch.delenv(k, raising=False)
+    w, r, local = bench.dist_setup()
+    assert (w, r, local) == (1, 0, 0)
+    assert bench.max_over_ranks(3.25, w) == 3.25
+
+
+@pytest.mark.parametrize("index", [0, 1, 3, 4])
+def test_useful_work_matches_the_oracle_counts(index):
+    wl = synth.workload(index)
+    for c in wl.calls:
+        flops, kv, _ = bench.useful_work(c)
+        assert flops == O.useful_flops(c.seq_info, c.T, c.Hq, c.D, c.causal, c.window, c.rows, c.cols)
+        assert kv == O.useful_kv_bytes(c.seq_info, c.T, c.Hkv, c.D, c.window, c.rows, c.cols)
+
+
+def test_useful_work_skips_invalid_and_overlapping_segments():
+    rng = np.random.default_rng(5)
+    c = synth.random_call(rng, D=64, Hq=4, Hkv=2, T=64, S=6, rows=256, cols=3, causal=True,
+                          window=0, max_q=12, max_kv=200, gen_seed=2)
+    seq = np.array(c.seq_info, copy=True)
+    seq[0] = (0, 8, 0, 50)
+    seq[1] = (4, 8, 1, 60)    # overlaps segment 0: both dropped
+    seq[2] = (20, 4, 7, 30)   # column out of range: skipped
+    c.seq_info = seq
+    flops, kv, _ = bench.useful_work(c)
+    assert flops == O.useful_flops(seq, c.T, c.Hq, c.D, c.causal, c.window, c.rows, c.cols)
+    assert kv == O.useful_kv_bytes(seq, c.T, c.Hkv, c.D, c.window, c.rows, c.cols) - \
+        sum(O.needed_span(int(s[1]), int(s[3]), c.window) * c.Hkv * c.D * 4 for s in seq[:2]
+            if not O.segment_status(s, c.T, c.rows, c.cols, c.window))

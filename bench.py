@@ -285,43 +285,57 @@ def main():
         step()
     torch.cuda.synchronize()
 
-    # The step is captured once as a CUDA graph (events at the kernel boundaries recorded by
-    # the library inside it) and replayed: no host submission gaps inside the timed step.
+    # The step is captured as CUDA graphs and replayed: no host submission gaps inside a step.
+    # graph_s is the step as a caller runs it (the library chains its kernels with programmatic
+    # dependent launch) and gives the timed value; graph_k has the library's timing events at
+    # every kernel boundary (each kernel then runs alone) and gives the per-kernel times that
+    # the roofline uses.
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in calls]
     for e in (e for b in ev for e in b):
         e.record(stream)  # torch creates the CUDA event on its first record
     torch.cuda.synchronize()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph):
+    graph_k = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph_k):
         step(ev)
+    graph_s = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph_s):
+        step()
     for _ in range(args.warmup):
-        graph.replay()
+        graph_s.replay()
+        graph_k.replay()
     torch.cuda.synchronize()
+    e_beg = torch.cuda.Event(enable_timing=True)
+    e_end = torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
     clocks.start()
     barrier(world)
     torch.cuda.synchronize()
-    times = []
+    step_ms = []
     for k in range(args.steps):
         flush.fill_(k & 0xFF)  # L2 flush outside the step's events
-        graph.replay()
+        e_beg.record(stream)
+        graph_s.replay()
+        e_end.record(stream)
         torch.cuda.synchronize()
-        times.append([[ev[i][a].elapsed_time(ev[i][a + 1]) for a in range(4)] for i in range(len(calls))])
+        step_ms.append(e_beg.elapsed_time(e_end))
     barrier(world)
     clk = clocks.stop()
 
-    step_ms = []
+    # per-kernel breakdown, same L2 flush, outside the timed steps
+    times = []
+    for k in range(args.steps):
+        flush.fill_(k & 0xFF)
+        graph_k.replay()
+        torch.cuda.synchronize()
+        times.append([[ev[i][a].elapsed_time(ev[i][a + 1]) for a in range(4)] for i in range(len(calls))])
     kern_ms = {"sched": [], "prefill": [], "splitk": [], "combine": []}
     for k in range(args.steps):
-        tot = 0.0
         for i in range(len(calls)):
             e = times[k][i]
-            tot += sum(e)
             kern_ms["sched"].append(e[0])
             kern_ms["prefill"].append(e[1])
             kern_ms["splitk"].append(e[2])
             kern_ms["combine"].append(e[3])
-        step_ms.append(tot)
     ms = statistics.mean(step_ms)
     ms_all = max_over_ranks(ms, world)
     if prefill_like:

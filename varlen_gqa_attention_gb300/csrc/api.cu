@@ -164,6 +164,26 @@ struct TensorMaps {
   CUtensorMap q, k, v;
 };
 
+// Launch with programmatic stream serialisation (the kernel waits in-kernel for its
+// predecessor), except while the timing hook records events between the kernels: an event
+// between two kernels would only serialise them again, and each kernel is then timed alone.
+static cudaError_t launch_k(const void* f, unsigned grid, unsigned block, void** args, size_t smem,
+                            cudaStream_t st, bool pdl) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  if (pdl && !g_ev_on) {
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+  }
+  return cudaLaunchKernelExC(&cfg, f, args);
+}
+
 static sdpa_status launch_all(const SchedArgs& sa, const AttnArgs& aa, int D, const Grids& g,
                               const TensorMaps& tm, cudaStream_t st) {
   cudaError_t e = mark(0, st);
@@ -175,15 +195,14 @@ static sdpa_status launch_all(const SchedArgs& sa, const AttnArgs& aa, int D, co
   if (e == cudaSuccess) e = mark(1, st);
   if (e == cudaSuccess && sa.prefill_ok) {
     void* args[] = {(void*)&aa, (void*)&tm.q, (void*)&tm.k, (void*)&tm.v};
-    e = cudaLaunchKernel(prefill_kernel_ptr(D), dim3((unsigned)g.prefill), dim3(prefill_block_threads(D)), args,
-                         prefill_smem_bytes(D), st);
+    e = launch_k(prefill_kernel_ptr(D), (unsigned)g.prefill, prefill_block_threads(D), args,
+                 prefill_smem_bytes(D), st, true);
     if (e != cudaSuccess) return fail(SDPA_ERR_CUDA, "prefill launch: %s", cudaGetErrorString(e));
   }
   if (e == cudaSuccess) e = mark(2, st);
   if (e == cudaSuccess) {
     void* args[] = {(void*)&aa};
-    e = cudaLaunchKernel(splitk_kernel_ptr(D), dim3((unsigned)g.splitk), dim3(kSplitkThreads), args,
-                         splitk_smem_bytes(D), st);
+    e = launch_k(splitk_kernel_ptr(D), (unsigned)g.splitk, kSplitkThreads, args, splitk_smem_bytes(D), st, true);
     if (e != cudaSuccess) return fail(SDPA_ERR_CUDA, "split-K launch: %s", cudaGetErrorString(e));
   }
   if (e == cudaSuccess) e = mark(3, st);
@@ -191,7 +210,7 @@ static sdpa_status launch_all(const SchedArgs& sa, const AttnArgs& aa, int D, co
     void* args[] = {(void*)&aa};
     const int64_t warps = aa.T * aa.Hq;
     const int64_t blocks = (warps * 32 + 255) / 256;
-    e = cudaLaunchKernel(combine_kernel_ptr(D), dim3((unsigned)blocks), dim3(256), args, 0, st);
+    e = launch_k(combine_kernel_ptr(D), (unsigned)blocks, 256, args, 0, st, true);
     if (e != cudaSuccess) return fail(SDPA_ERR_CUDA, "combine launch: %s", cudaGetErrorString(e));
   }
   if (e == cudaSuccess) e = mark(4, st);

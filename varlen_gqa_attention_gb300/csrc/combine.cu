@@ -20,6 +20,7 @@ __global__ void __launch_bounds__(kCombineThreads) sdpa_combine_kernel(AttnArgs 
   constexpr int PER = D / 32;  // elements per lane
   const int64_t gw = ((int64_t)blockIdx.x * kCombineThreads + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
+  griddep_wait();  // the attention kernels' slots and direct writes
   if (gw >= A.T * A.Hq) return;
   const int64_t t = gw / A.Hq;
   const int h = (int)(gw % A.Hq);

@@ -284,6 +284,13 @@ __device__ inline bool walk_next(PieceWalk& w, UnitRec& ur, int64_t& ta, int64_t
 // ------------------------------------------------------------------------------------
 // inline PTX helpers
 // ------------------------------------------------------------------------------------
+// Programmatic dependent launch: a kernel launched with programmatic stream serialisation
+// may start while the previous kernel of the stream drains; it must wait here before reading
+// anything that kernel (or an earlier one) wrote.  Without that launch attribute the wait
+// returns at once.  launch_dependents lets the next such kernel start launching.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;\n" :::); }
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
 }

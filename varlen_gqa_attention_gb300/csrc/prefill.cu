@@ -135,6 +135,8 @@ __global__ void __launch_bounds__(PfCfg<D>::THREADS, 1)
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
 
+  griddep_wait();    // the scheduler's output
+  griddep_launch();
   if (A.ws.hdr->tiles[kRoutePrefill] == 0) return;  // whole CTA leaves before any setup
   {
     PieceWalk probe;

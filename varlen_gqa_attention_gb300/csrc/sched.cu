@@ -108,6 +108,7 @@ __global__ void __launch_bounds__(kSchedThreads) sdpa_sched_kernel(SchedArgs A) 
   const int S = A.S;
   const int64_t T = A.T;
   const bool cached = S <= kSegCache;
+  griddep_launch();  // the attention kernels may start launching; they wait for this grid
   if (threadIdx.x == 0) s_status = 0;
   __syncthreads();
 

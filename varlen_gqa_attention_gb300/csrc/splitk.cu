@@ -336,6 +336,8 @@ template <int D>
 __global__ void __launch_bounds__(kSplitkThreads) sdpa_splitk_kernel(AttnArgs A) {
   extern __shared__ __align__(128) char smem[];
   __shared__ float2 s_ml[4 * 16];
+  griddep_wait();    // the scheduler's output (and the prefill kernel's end)
+  griddep_launch();
   if (A.ws.hdr->tiles[kRouteSplitk] == 0) return;
   PieceWalk wk;
   walk_begin(wk, A.ws, kRouteSplitk);

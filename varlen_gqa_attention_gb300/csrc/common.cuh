@@ -299,6 +299,12 @@ __device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, bool 
   int sz = pred ? 16 : 0;  // src-size 0 fills the 16 bytes with zeros
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(sz));
 }
+// The same, hinting the L2 to fetch the whole 256-byte block around `src` from DRAM: the
+// CTA's other threads read the rest of that store row in the same instruction.
+__device__ __forceinline__ void cp_async_16_row(uint32_t dst, const void* src, bool pred) {
+  int sz = pred ? 16 : 0;
+  asm volatile("cp.async.cg.shared.global.L2::256B [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(sz));
+}
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {

@@ -69,8 +69,8 @@ struct KvCursor {
       if (phys >= rows) phys -= rows;  // valid keys span at most `rows` store rows
       const int64_t off = ok ? (int64_t)phys * rstride : 0;
       const uint32_t so = swz(n, c, D * 2);
-      cp_async_16(smem_u32(sK + so), kb + off, ok);
-      cp_async_16(smem_u32(sV + so), vb + off, ok);
+      cp_async_16_row(smem_u32(sK + so), kb + off, ok);
+      cp_async_16_row(smem_u32(sV + so), vb + off, ok);
     }
     row0 += kSplitkTile;
     if (row0 >= rows) row0 %= rows;

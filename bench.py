@@ -37,6 +37,16 @@ WORKLOADS = {
 PREFILL_LIKE = {"tiny", "prefill_d64", "prefill_d128"}
 METRIC = "varlen GQA attention TFLOP/s (prefill) & KV GB/s (decode), % of roofline"
 L2_FLUSH_BYTES = 512 << 20
+# DRAM bytes (read + write) of the dominant kernel per step, from one ncu capture of the same
+# bench line on a GB300 (dram__bytes_read.sum + dram__bytes_write.sum; the file under profiles/
+# named for the kernel and workload gives the command).  They describe the kernel source they
+# were taken on: a kernel change makes them stale until the capture is repeated.
+NCU_TRAFFIC_BYTES = {
+    "prefill_d128": 2137420288 + 38294272,  # sdpa_prefill_kernel<128>, one launch
+    "prefill_d64": 9514496 + 0,             # sdpa_prefill_kernel<64>, one launch
+    "decode": 141747200 + 2986752,          # sdpa_splitk_kernel<128>, one launch
+    "mixed": 135023616 + 3034368 + 150764800 + 613376,  # sdpa_splitk_kernel<128>, both calls
+}
 
 
 def useful_work(call):
@@ -353,13 +363,13 @@ def main():
     if prefill_like:
         achieved = flops / (dom_ms * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": bf16, "unit": "TFLOP/s",
-                "frac": achieved / bf16, "traffic": None, "kernel": dom,
+                "frac": achieved / bf16, "traffic": NCU_TRAFFIC_BYTES.get(args.workload), "kernel": dom,
                 "peak_source": f"{peak_src} bf16 dense (burst)"}
     else:
         alg = kv_bytes + qo_bytes
         achieved = alg / (dom_ms * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                "frac": achieved / hbm, "traffic": None, "kernel": dom,
+                "frac": achieved / hbm, "traffic": NCU_TRAFFIC_BYTES.get(args.workload), "kernel": dom,
                 "peak_source": f"{peak_src} HBM copy"}
 
     # end to end through the C interface from pinned host buffers

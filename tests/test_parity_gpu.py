@@ -242,3 +242,22 @@ def test_short_pieces_are_deterministic_and_exact(dev, route, D):
     ref, seg_id, _ = oracle(call)
     _, lo, hi, _ = O.visible_interval(call.seq_info, call.T, False, 0, call.rows, call.cols)
     assert_matches(outs[0], ref, seg_id, lo, hi, tag=f"short pieces D{D}")
+
+
+def test_segment_table_larger_than_the_scheduler_cache(dev, route):
+    # 1500 segments: more than the scheduler stages in shared memory, so it walks the
+    # workspace copy of the table instead
+    rng = np.random.default_rng(1500)
+    call = synth.random_call(rng, D=64, Hq=4, Hkv=2, T=3000, S=1500, rows=64, cols=8, causal=True,
+                             window=0, max_q=2, max_kv=48, gen_seed=77)
+    check_call(call, dev, tag="S=1500")
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(32, 1), (128, 1), (24, 8)])
+def test_large_and_odd_head_groups(dev, route, Hq, Hkv):
+    # group 32 and 128 fill a 128-row prefill tile with 4 and 1 query rows; group 3 does not
+    # divide 128 and always takes the split-K kernel
+    rng = np.random.default_rng(Hq * 7 + Hkv)
+    call = synth.random_call(rng, D=64, Hq=Hq, Hkv=Hkv, T=40, S=4, rows=300, cols=2, causal=True,
+                             window=0, max_q=12, max_kv=300, gen_seed=Hq + Hkv)
+    check_call(call, dev, tag=f"Hq{Hq}/Hkv{Hkv}")

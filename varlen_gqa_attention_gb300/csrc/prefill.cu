@@ -14,17 +14,18 @@
 //   * two producer warps move Q and K tiles, and V tiles, with TMA (128-byte swizzle) into
 //     rings of shared-memory stages; the store is a 4-d tensor [rows, cols, Hkv, D], so a tile of one
 //     column and KV head is one box;
-//   * one thread of the MMA warp issues tcgen05.mma: S = Q K^T into one of two tensor-memory
-//     buffers (fp32, 128 lanes x BN columns), then O += P V into a tensor-memory accumulator;
-//     completion is signalled with tcgen05.commit on mbarriers;
-//   * softmax warpgroups: one thread per row reads its S row from tensor memory, masks by
-//     select (causal, window, piece bounds), keeps a base-2 running max with lazy rescaling
-//     (O is only rescaled when the max grows by more than 2^8) and writes P as bf16 into a
-//     swizzled shared-memory tile for the PV MMA.  For D <= 128 two warpgroups take
-//     alternate key tiles, each with its own running max, sum and O accumulator in tensor
-//     memory (S0, S1, O0, O1 fill the 512 columns), so two softmax streams overlap the MMAs;
-//     at the end of a piece warpgroup 0 merges the two by log-sum-exp and writes `out` (the
-//     unit's only CTA) or a partial for the combine pass.  D = 256 uses one warpgroup;
+//   * the MMA warp issues tcgen05.mma (the whole warp runs the loop, one elected lane
+//     issues): S = Q K^T into one of two tensor-memory buffers (fp32, 128 lanes x BN
+//     columns) and O += P V with P read from tensor memory; S(g+2) goes out as soon as the
+//     softmax has read S(g) out, PV(g) once P(g) is written; completion is signalled with
+//     tcgen05.commit on mbarriers;
+//   * two softmax warpgroups each take half of every tile's key columns, one thread per row
+//     (= tensor-memory lane): the thread reads its S half-row, masks by select (causal,
+//     window, piece bounds), keeps a base-2 running max shared by the two halves with lazy
+//     rescaling (one barrier per tile checks that no row's tile max left the 2^8 window; only
+//     then are maxima swapped and O rescaled) and writes P as bf16 pairs into tensor memory;
+//     at the end of a piece the two row-sum halves are added and each warpgroup writes its
+//     half of O's columns to `out` (the unit's only CTA) or to a partial for the combine pass;
 //   * V rows past the last visible key of a unit are zeroed in shared memory before the PV
 //     MMA, so stale or NaN store cells never meet a zero probability (0 * NaN).
 // Every mbarrier wait is bounded; a wait that gives up sets SDPA_DEV_TIMEOUT and the CTA

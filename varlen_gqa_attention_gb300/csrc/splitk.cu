@@ -8,8 +8,9 @@
 // built: each CTA owns an equal share of key tiles across all units, a unit being
 // (segment, KV head, 64 packed rows r = i * group + g).  Per unit and CTA:
 //   * Q rows and 64-position K/V tiles are staged in shared memory with 16-byte cp.async
-//     (coalesced: a store row of one KV head is D*2 contiguous bytes; ring rows wrap per row),
-//     double buffered so the next tile streams in while this one is used;
+//     (coalesced: a store row of one KV head is D*2 contiguous bytes, fetched from DRAM as
+//     one 256-byte block; ring rows wrap per row) through a three-stage ring (two at
+//     D = 256), so two tiles stream in while one is used; two CTAs share an SM at D <= 128;
 //   * each warp takes 16 packed rows and a slice of the tile: S = Q K^T and O += P V with
 //     bf16 m16n8k16 tensor-core MMAs and fp32 accumulation; with few rows (decode: q_len=1,
 //     group 8) the four warps split the tile's keys instead of the rows;

@@ -227,6 +227,38 @@ def sdpa_causal_prefill(q, k, v, scale: float, rows_subset: Optional[Iterable[in
     return out
 
 
+def kv_append(k_store, v_store, k_new, v_new, seq_info, window: int):
+    """The step's keys and values written into the column store before attention [B].
+
+    k_store, v_store: [rows, cols, Hkv, D]; k_new, v_new: [T, Hkv, D] (packed rows).
+    Row q_start + i of a live segment (valid and not overlapping, reading 7) holds
+    position p = kv_end - q_len + i (reading 1) and is written to store row p % rows
+    (reading 3) of the segment's column, every KV head.  Rows with p < 0, rows of
+    invalid or overlapping segments and rows no segment covers write nothing.  Returns
+    new copies of the stores (same dtype); the inputs are not modified.
+    """
+    import torch
+
+    T = k_new.shape[0]
+    rows, cols = k_store.shape[0], k_store.shape[1]
+    seg_id, _, _, _ = visible_interval(seq_info, T, True, window, rows, cols)
+    k_out = k_store.clone()
+    v_out = v_store.clone()
+    seq_info = np.asarray(seq_info, dtype=np.int64).reshape(-1, 4)
+    for s, (q_start, q_len, col, kv_end) in enumerate(seq_info):
+        for i in range(max(int(q_len), 0)):
+            t = int(q_start) + i
+            if not (0 <= t < T) or seg_id[t] != s:
+                continue
+            p = int(kv_end) - int(q_len) + i
+            if p < 0:
+                continue
+            k_out[store_row(p, rows), int(col)] = k_new[t]
+            v_out[store_row(p, rows), int(col)] = v_new[t]
+    assert isinstance(k_out, torch.Tensor)
+    return k_out, v_out
+
+
 def useful_flops(seq_info, T: int, Hq: int, D: int, causal: bool, window: int, rows: int, cols: int) -> int:
     """4 * D * Hq * sum over covered rows of |visible set| (QK^T and PV multiply-adds)."""
     _, lo, hi, _ = visible_interval(seq_info, T, causal, window, rows, cols)

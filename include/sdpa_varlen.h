@@ -105,6 +105,35 @@ sdpa_status sdpa_varlen(const void* q, int64_t T, int Hq, int D, int64_t q_row_s
                         int32_t* status_dev, void* stream);
 
 /*
+ * Write the step's keys and values, then attend: the in-graph slot write followed by the
+ * attention of "[executorch][cuda] Add a length-aware Triton SDPA over per-sequence KV
+ * columns" (#24074 commit message in its stack: slot (position % rows) * columns + col).
+ *
+ *  k_new, v_new    device bf16, [T, Hkv, D] packed like q: row t holds the new key / value
+ *                  of packed query row t, every KV head; element (t, h, d) at
+ *                  t*new_row_stride + h*new_head_stride + d; 16-byte aligned; strides
+ *                  non-negative multiples of 8 elements; read only.
+ *  k_store, v_store  as for sdpa_varlen, but written: for every live segment (valid and
+ *                  not sharing a packed row with another valid segment), packed row
+ *                  q_start + i, at position p = kv_end - q_len + i >= 0, is copied to store
+ *                  row p % rows of column col, all KV heads.  Rows of invalid or
+ *                  overlapping segments, uncovered rows and rows with p < 0 write nothing.
+ *                  Two live segments that write the same (row, column) cell leave it
+ *                  holding one of the two rows.
+ * Every other argument, the attention that follows (it reads the written rows) and the
+ * status bits are those of sdpa_varlen; the write runs on the device between its
+ * scheduler and its attention kernels, in the same stream (so a captured graph holds both).
+ * Errors as sdpa_varlen, plus SDPA_ERR_NULL / _ALIGN / _STRIDE for k_new and v_new.
+ */
+sdpa_status sdpa_varlen_append(const void* q, int64_t T, int Hq, int D, int64_t q_row_stride,
+                               int64_t q_head_stride, const void* k_new, const void* v_new,
+                               int64_t new_row_stride, int64_t new_head_stride, void* k_store,
+                               void* v_store, int64_t rows, int cols, int Hkv, const int32_t* seq_info,
+                               int S, int causal, int window, float scale, void* out,
+                               int64_t o_row_stride, int64_t o_head_stride, void* workspace,
+                               size_t ws_bytes, int32_t* status_dev, void* stream);
+
+/*
  * Dense causal GQA prefill ("[CUDA] Use Triton TMA for long-context causal prefill",
  * Operator-level performance table: B = 1, global causal, queries being the last Lq of
  * Lkv positions).  q [Lq, Hq, D], k and v [Lkv, Hkv, D] contiguous bf16; out [Lq, Hq, D]

@@ -38,6 +38,7 @@ STATUS_NAMES = {
 EXPORTS = [
     "sdpa_varlen_workspace_bytes", "sdpa_varlen", "sdpa_causal_prefill", "sdpa_set_route_policy",
     "sdpa_set_timing_events", "sdpa_last_error", "sdpa_version", "sdpa_varlen_splitk_static",
+    "sdpa_varlen_append",
 ]
 
 
@@ -68,6 +69,10 @@ def library(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.sdpa_varlen.argtypes = [c_vp, c_i64, c_int, c_int, c_i64, c_i64, c_vp, c_vp, c_i64, c_int,
                                 c_int, c_vp, c_int, c_int, c_int, c_f, c_vp, c_i64, c_i64, c_vp,
                                 ctypes.c_size_t, c_vp, c_vp]
+    lib.sdpa_varlen_append.restype = c_int
+    lib.sdpa_varlen_append.argtypes = [c_vp, c_i64, c_int, c_int, c_i64, c_i64, c_vp, c_vp, c_i64, c_i64,
+                                       c_vp, c_vp, c_i64, c_int, c_int, c_vp, c_int, c_int, c_int, c_f,
+                                       c_vp, c_i64, c_i64, c_vp, ctypes.c_size_t, c_vp, c_vp]
     lib.sdpa_causal_prefill.restype = c_int
     lib.sdpa_causal_prefill.argtypes = [c_vp, c_vp, c_vp, c_i64, c_i64, c_int, c_int, c_int, c_f,
                                         c_vp, c_vp, ctypes.c_size_t, c_vp]
@@ -158,6 +163,55 @@ def sdpa_varlen(q: torch.Tensor, k_store: torch.Tensor, v_store: torch.Tensor, s
                            S, int(bool(causal)), int(window), float(scale), out.data_ptr(),
                            out.stride(0), out.stride(1), workspace.data_ptr(), workspace.numel(),
                            st_ptr, _stream_ptr(stream))
+    _check(code)
+    return out
+
+
+def sdpa_varlen_append(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor, k_store: torch.Tensor,
+                       v_store: torch.Tensor, seq_info: torch.Tensor, *, causal: bool, window: int = 0,
+                       scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
+                       workspace: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
+                       stream=None) -> torch.Tensor:
+    """Write the step's keys and values into the stores, then attend (one enqueued call).
+
+    k_new, v_new: bf16 [T, Hkv, D] (inner stride 1), row t the new key / value of packed
+    query row t; they go to store row (kv_end - q_len + i) % rows of each live segment's
+    column.  The stores are modified in place; everything else is as ``sdpa_varlen``.
+    """
+    lib = library()
+    if q.dim() != 3 or k_store.dim() != 4 or tuple(v_store.shape) != tuple(k_store.shape):
+        raise ValueError("q must be [T, Hq, D] and the stores [rows, cols, Hkv, D]")
+    T, Hq, D = q.shape
+    rows, cols, Hkv, Dk = k_store.shape
+    for name, t in (("q", q), ("k_new", k_new), ("v_new", v_new), ("k_store", k_store), ("v_store", v_store)):
+        if t.dtype != torch.bfloat16 or not t.is_cuda:
+            raise ValueError(f"{name} must be a bf16 CUDA tensor")
+    if tuple(k_new.shape) != (T, Hkv, D) or tuple(v_new.shape) != (T, Hkv, D):
+        raise ValueError("k_new and v_new must be [T, Hkv, D]")
+    if k_new.stride() != v_new.stride() or k_new.stride(2) != 1:
+        raise ValueError("k_new and v_new must share strides, with unit inner stride")
+    if not (k_store.is_contiguous() and v_store.is_contiguous()):
+        raise ValueError("k_store and v_store must be contiguous")
+    if seq_info.dtype != torch.int32 or not seq_info.is_cuda or not seq_info.is_contiguous():
+        raise ValueError("seq_info must be a contiguous int32 CUDA tensor")
+    if Dk != D or q.stride(2) != 1:
+        raise ValueError("head dims differ, or q has a non-unit inner stride")
+    S = seq_info.shape[0] if seq_info.numel() else 0
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty((T, Hq, D), dtype=torch.bfloat16, device=q.device)
+    elif out.dtype != torch.bfloat16 or tuple(out.shape) != (T, Hq, D) or out.stride(2) != 1:
+        raise ValueError("out must be bf16 [T, Hq, D] with unit inner stride")
+    if workspace is None:
+        workspace = _workspace(workspace_bytes(T, Hq, Hkv, D, S), q.device)
+    st_ptr = status.data_ptr() if status is not None else None
+    code = lib.sdpa_varlen_append(q.data_ptr(), T, Hq, D, q.stride(0), q.stride(1), k_new.data_ptr(),
+                                  v_new.data_ptr(), k_new.stride(0), k_new.stride(1), k_store.data_ptr(),
+                                  v_store.data_ptr(), rows, cols, Hkv, seq_info.data_ptr() if S else None,
+                                  S, int(bool(causal)), int(window), float(scale), out.data_ptr(),
+                                  out.stride(0), out.stride(1), workspace.data_ptr(), workspace.numel(),
+                                  st_ptr, _stream_ptr(stream))
     _check(code)
     return out
 

@@ -3,6 +3,7 @@
 // Every check runs before any CUDA call, so a bad argument never touches the device.  The
 // launches are asynchronous and allocation-free, so a call can be captured in a CUDA graph;
 // the device scheduler reads the segment table when the graph replays.
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdarg>
@@ -185,12 +186,33 @@ static cudaError_t launch_k(const void* f, unsigned grid, unsigned block, void**
 }
 
 static sdpa_status launch_all(const SchedArgs& sa, const AttnArgs& aa, int D, const Grids& g,
-                              const TensorMaps& tm, cudaStream_t st) {
+                              const TensorMaps& tm, const AppendArgs* ap, cudaStream_t st) {
   cudaError_t e = mark(0, st);
   if (e == cudaSuccess) {
     void* args[] = {(void*)&sa};
     e = cudaLaunchKernel(sched_kernel_ptr(), dim3(1), dim3(kSchedThreads), args, 0, st);
     if (e != cudaSuccess) return fail(SDPA_ERR_CUDA, "scheduler launch: %s", cudaGetErrorString(e));
+  }
+  if (e == cudaSuccess && ap && sa.S > 0) {
+    // the step's new keys and values, between the scheduler (whose segment records say
+    // which segments are live) and the attention kernels that read them
+    void* args[] = {(void*)ap};
+    const int64_t per_seg = (aa.T + sa.S - 1) / sa.S;
+    const int64_t chunks = per_seg * ap->Hkv * (ap->D / 8);
+    const unsigned gy = (unsigned)std::min<int64_t>(256, std::max<int64_t>(1, chunks / (4 * kAppendThreads)));
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)sa.S, gy);
+    cfg.blockDim = dim3(kAppendThreads);
+    cfg.stream = st;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    if (!g_ev_on) {
+      cfg.attrs = at;
+      cfg.numAttrs = 1;
+    }
+    e = cudaLaunchKernelExC(&cfg, append_kernel_ptr(), args);
+    if (e != cudaSuccess) return fail(SDPA_ERR_CUDA, "append launch: %s", cudaGetErrorString(e));
   }
   if (e == cudaSuccess) e = mark(1, st);
   if (e == cudaSuccess && sa.prefill_ok) {
@@ -222,7 +244,7 @@ static sdpa_status run(const void* q, int64_t T, int Hq, int D, int64_t q_rs, in
                        const void* k, const void* v, int64_t rows, int cols, int Hkv,
                        const int32_t* seq_info, int S, const int32_t* inl, int causal, int window,
                        float scale, void* out, int64_t o_rs, int64_t o_hs, void* ws, size_t ws_bytes,
-                       int32_t* status_dev, void* stream) {
+                       int32_t* status_dev, void* stream, const AppendArgs* ap = nullptr) {
   g_err[0] = 0;
   sdpa_status st = check_common(T, Hq, Hkv, D, S, rows, cols, window, scale);
   if (st) return st;
@@ -293,7 +315,12 @@ static sdpa_status run(const void* q, int64_t T, int Hq, int D, int64_t q_rs, in
   aa.T = T;
   aa.ws = W;
   aa.status_dev = status_dev;
-  return launch_all(sa, aa, D, g, tm, (cudaStream_t)stream);
+  AppendArgs apw;
+  if (ap) {
+    apw = *ap;
+    apw.segs = W.segs;
+  }
+  return launch_all(sa, aa, D, g, tm, ap ? &apw : nullptr, (cudaStream_t)stream);
 }
 
 }  // namespace sdpa
@@ -326,6 +353,34 @@ sdpa_status sdpa_varlen(const void* q, int64_t T, int Hq, int D, int64_t q_row_s
   return run(q, T, Hq, D, q_row_stride, q_head_stride, k_store, v_store, rows, cols, Hkv, seq_info,
              S, nullptr, causal, window, scale, out, o_row_stride, o_head_stride, workspace,
              ws_bytes, status_dev, stream);
+}
+
+sdpa_status sdpa_varlen_append(const void* q, int64_t T, int Hq, int D, int64_t q_row_stride,
+                               int64_t q_head_stride, const void* k_new, const void* v_new,
+                               int64_t new_row_stride, int64_t new_head_stride, void* k_store,
+                               void* v_store, int64_t rows, int cols, int Hkv, const int32_t* seq_info,
+                               int S, int causal, int window, float scale, void* out,
+                               int64_t o_row_stride, int64_t o_head_stride, void* workspace,
+                               size_t ws_bytes, int32_t* status_dev, void* stream) {
+  g_err[0] = 0;
+  if (!k_new || !v_new) return fail(SDPA_ERR_NULL, "k_new or v_new is NULL");
+  if (!aligned16(k_new) || !aligned16(v_new)) return fail(SDPA_ERR_ALIGN, "k_new and v_new must be 16-byte aligned");
+  if (new_row_stride < 0 || new_head_stride < 0 || (new_row_stride % 8) || (new_head_stride % 8))
+    return fail(SDPA_ERR_STRIDE, "new-row strides must be non-negative multiples of 8 elements");
+  AppendArgs ap{};
+  ap.k_new = (const __nv_bfloat16*)k_new;
+  ap.v_new = (const __nv_bfloat16*)v_new;
+  ap.new_rs = new_row_stride;
+  ap.new_hs = new_head_stride;
+  ap.k_store = (__nv_bfloat16*)k_store;
+  ap.v_store = (__nv_bfloat16*)v_store;
+  ap.rows = rows;
+  ap.cols = cols;
+  ap.Hkv = Hkv;
+  ap.D = D;
+  return run(q, T, Hq, D, q_row_stride, q_head_stride, k_store, v_store, rows, cols, Hkv, seq_info,
+             S, nullptr, causal, window, scale, out, o_row_stride, o_head_stride, workspace,
+             ws_bytes, status_dev, stream, &ap);
 }
 
 sdpa_status sdpa_causal_prefill(const void* q, const void* k, const void* v, int64_t Lq,

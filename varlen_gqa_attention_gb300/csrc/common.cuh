@@ -146,6 +146,19 @@ struct AttnArgs {
   int32_t* status_dev;
 };
 
+// Arguments of the KV append kernel (the step's new rows into the column store).
+struct AppendArgs {
+  const __nv_bfloat16* k_new;
+  const __nv_bfloat16* v_new;
+  int64_t new_rs, new_hs;  // element strides of the new rows and heads
+  __nv_bfloat16* k_store;
+  __nv_bfloat16* v_store;
+  int64_t rows;
+  int cols, Hkv, D;
+  const SegRec* segs;      // the scheduler's segment records (route none: not live)
+};
+constexpr int kAppendThreads = 128;
+
 // Arguments of the scheduler kernel.
 struct SchedArgs {
   const int32_t* seq_info;
@@ -167,6 +180,7 @@ constexpr int kSchedThreads = 1024;
 
 // Kernel entry points (defined in their own translation units).
 const void* sched_kernel_ptr();
+const void* append_kernel_ptr();
 const void* splitk_kernel_ptr(int D);
 int splitk_smem_bytes(int D);
 const void* combine_kernel_ptr(int D);

@@ -32,8 +32,10 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 WORKLOADS = {
-    "tiny": 0, "prefill_d64": 1, "prefill_d128": 2, "decode": 3, "mixed": 4,
+    "tiny": 0, "prefill_d64": 1, "prefill_d128": 2, "decode": 3, "mixed": 4, "decode_append": 3,
 }
+# workloads whose step first writes its new keys and values into the stores (sdpa_varlen_append)
+APPEND = {"decode_append"}
 PREFILL_LIKE = {"tiny", "prefill_d64", "prefill_d128"}
 METRIC = "varlen GQA attention TFLOP/s (prefill) & KV GB/s (decode), % of roofline"
 L2_FLUSH_BYTES = 512 << 20
@@ -274,10 +276,29 @@ def main():
                  ws=torch.empty(pkg.workspace_bytes(c.T, c.Hq, c.Hkv, c.D, len(c.seq_info)),
                                 dtype=torch.uint8, device=dev))
         d["out"] = out[c.row_begin:(c.row_end or c.T)]
+        if args.workload in APPEND:
+            g = torch.Generator().manual_seed(1000 + args.seed)
+            shape = (c.T, c.Hkv, c.D)
+            d["kn_host"] = torch.randn(shape, generator=g).to(torch.bfloat16)
+            d["vn_host"] = torch.randn(shape, generator=g).to(torch.bfloat16)
+            d["kn"], d["vn"] = d["kn_host"].to(dev), d["vn_host"].to(dev)
         calls.append(d)
+
+    def attend(d):
+        c = d["call"]
+        if "kn" in d:
+            pkg.sdpa_varlen_append(d["q"], d["kn"], d["vn"], d["k"], d["v"], d["seq"], causal=c.causal,
+                                   window=c.window, scale=c.scale, out=d["out"], workspace=d["ws"])
+        else:
+            pkg.sdpa_varlen(d["q"], d["k"], d["v"], d["seq"], causal=c.causal, window=c.window,
+                            scale=c.scale, out=d["out"], workspace=d["ws"])
     flops = sum(useful_work(c)[0] for c in wl.calls)
     kv_bytes = sum(useful_work(c)[1] for c in wl.calls)
     qo_bytes = sum(useful_work(c)[2] for c in wl.calls)
+    if args.workload in APPEND:
+        # the step's new K and V rows, read once and written once (every covered row writes:
+        # kv_end >= q_len in these workloads)
+        kv_bytes += sum(useful_work(c)[2] // (4 * c.Hq * c.D) * c.Hkv * c.D * 2 * 2 * 2 for c in wl.calls)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
@@ -285,9 +306,7 @@ def main():
         for i, d in enumerate(calls):
             if evs is not None:
                 pkg.set_timing_events(evs[i])
-            c = d["call"]
-            pkg.sdpa_varlen(d["q"], d["k"], d["v"], d["seq"], causal=c.causal, window=c.window,
-                            scale=c.scale, out=d["out"], workspace=d["ws"])
+            attend(d)
         if evs is not None:
             pkg.set_timing_events(None)
 
@@ -381,6 +400,9 @@ def main():
         hs = torch.from_numpy(c.seq_info.copy()).pin_memory()
         host.append((hq, hk, hv, hs))
         h2d += hq.numel() * 2 + hk.numel() * 2 + hv.numel() * 2 + hs.numel() * 4
+        if "kn" in d:
+            d["kn_pin"], d["vn_pin"] = d["kn_host"].pin_memory(), d["vn_host"].pin_memory()
+            h2d += (d["kn_pin"].numel() + d["vn_pin"].numel()) * 2
     hout = torch.empty(out.shape, dtype=torch.bfloat16).pin_memory()
     d2h = hout.numel() * 2
 
@@ -390,9 +412,10 @@ def main():
             d["k"].copy_(hk, non_blocking=True)
             d["v"].copy_(hv, non_blocking=True)
             d["seq"].copy_(hs, non_blocking=True)
-            c = d["call"]
-            pkg.sdpa_varlen(d["q"], d["k"], d["v"], d["seq"], causal=c.causal, window=c.window,
-                            scale=c.scale, out=d["out"], workspace=d["ws"])
+            if "kn" in d:
+                d["kn"].copy_(d["kn_pin"], non_blocking=True)
+                d["vn"].copy_(d["vn_pin"], non_blocking=True)
+            attend(d)
         hout.copy_(out, non_blocking=True)
 
     for _ in range(2):
@@ -426,7 +449,8 @@ def main():
         "metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_all, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": vs, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": wl.name, "description": wl.description, "seed": args.seed,
+        "config": {"workload": wl.name + ("+kv_append" if args.workload in APPEND else ""),
+                   "description": wl.description, "seed": args.seed,
                    "l2": "flushed between steps (512 MiB write outside the step's events)",
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "useful_tflop_per_step": flops / 1e12, "kv_gb_per_step": kv_bytes / 1e9},

@@ -259,6 +259,25 @@ def kv_append(k_store, v_store, k_new, v_new, seq_info, window: int):
     return k_out, v_out
 
 
+def seq_clone(k_store, v_store, src_col: int, dst_col: int, n: int):
+    """Column dst_col takes over the first n positions of column src_col (the #24073 commit
+    message in the stack of [A]: seq_clone, a device copy of the source prefix).
+
+    Position j lives in store row j % rows (reading 3), so a ring only holds the last
+    `rows` of them: positions [max(0, n - rows), n) are copied, each from its row of the
+    source column to the same row of the destination, every KV head, K and V.  Rows the
+    prefix does not reach keep their contents.  Returns new copies of the stores.
+    """
+    rows = k_store.shape[0]
+    k_out = k_store.clone()
+    v_out = v_store.clone()
+    for j in range(max(0, n - rows), n):
+        r = store_row(j, rows)
+        k_out[r, dst_col] = k_store[r, src_col]
+        v_out[r, dst_col] = v_store[r, src_col]
+    return k_out, v_out
+
+
 def useful_flops(seq_info, T: int, Hq: int, D: int, causal: bool, window: int, rows: int, cols: int) -> int:
     """4 * D * Hq * sum over covered rows of |visible set| (QK^T and PV multiply-adds)."""
     _, lo, hi, _ = visible_interval(seq_info, T, causal, window, rows, cols)

@@ -107,3 +107,37 @@ def test_append_is_idempotent_and_leaves_inputs_alone():
     k2, v2 = O.kv_append(k1, v1, kn, vn, seq, 0)
     assert torch.equal(k1, k2) and torch.equal(v1, v2)
     assert torch.equal(k0, torch.full_like(k0, 0.5)) and torch.equal(v0, torch.full_like(v0, -0.5))
+
+
+# seq_clone: column dst takes over the first n positions of column src (#24073 commit message)
+
+def test_clone_of_a_short_prefix_copies_that_many_rows():
+    g = torch.Generator().manual_seed(21)
+    k0 = torch.randn(16, 4, 2, 8, generator=g).to(torch.bfloat16)
+    v0 = torch.randn(16, 4, 2, 8, generator=g).to(torch.bfloat16)
+    k, v = O.seq_clone(k0, v0, 1, 3, 5)
+    assert torch.equal(k[:5, 3], k0[:5, 1]) and torch.equal(v[:5, 3], v0[:5, 1])
+    assert torch.equal(k[5:, 3], k0[5:, 3]) and torch.equal(k[:, :3], k0[:, :3])
+
+
+def test_clone_of_a_wrapped_ring_copies_the_whole_column():
+    # n > rows: every row holds a position of the prefix, so the whole column moves
+    g = torch.Generator().manual_seed(22)
+    k0 = torch.randn(7, 3, 1, 4, generator=g).to(torch.bfloat16)
+    v0 = torch.randn(7, 3, 1, 4, generator=g).to(torch.bfloat16)
+    k, v = O.seq_clone(k0, v0, 0, 2, 30)
+    assert torch.equal(k[:, 2], k0[:, 0]) and torch.equal(v[:, 2], v0[:, 0])
+    assert torch.equal(k[:, :2], k0[:, :2])
+
+
+def test_clone_then_attend_matches_the_source_sequence():
+    # a sequence cloned into a new column attends exactly like the original one
+    g = torch.Generator().manual_seed(23)
+    rows, Hkv, D = 20, 2, 8
+    k0 = torch.randn(rows, 3, Hkv, D, generator=g).to(torch.bfloat16)
+    v0 = torch.randn(rows, 3, Hkv, D, generator=g).to(torch.bfloat16)
+    q = torch.randn(3, 4, D, generator=g).to(torch.bfloat16)
+    k, v = O.seq_clone(k0, v0, 0, 2, 26)
+    a, _, _ = O.sdpa_varlen(q, k, v, [[0, 3, 0, 26]], True, 10, 0.3)
+    b, _, _ = O.sdpa_varlen(q, k, v, [[0, 3, 2, 26]], True, 10, 0.3)
+    np.testing.assert_array_equal(a, b)

@@ -33,7 +33,10 @@ sys.path.insert(0, ROOT)
 
 WORKLOADS = {
     "tiny": 0, "prefill_d64": 1, "prefill_d128": 2, "decode": 3, "mixed": 4, "decode_append": 3,
+    "seq_clone": -1,
 }
+# seq_clone workload: one column of a [rows, cols, Hkv, D] store pair copied whole into another
+CLONE_SHAPE = (32768, 9, 8, 128)
 # workloads whose step first writes its new keys and values into the stores (sdpa_varlen_append)
 APPEND = {"decode_append"}
 PREFILL_LIKE = {"tiny", "prefill_d64", "prefill_d128"}
@@ -238,6 +241,104 @@ def run_reference(args, wl, world, rank):
     print(json.dumps(line), flush=True)
 
 
+def run_clone(args, world, rank, local):
+    """The column clone: K and V of one whole column (rows x Hkv x D) read once and written
+    once per step, against the HBM copy roofline; the oracle's copy times the CPU leg."""
+    import torch
+
+    import varlen_gqa_attention_gb300 as pkg
+    from oracle import sdpa_varlen_oracle as O
+
+    rows, cols, Hkv, D = CLONE_SHAPE
+    name = f"seq_clone_store{rows}x{cols}x{Hkv}x{D}_full_column"
+    moved = 2 * 2 * rows * Hkv * D * 2  # K and V, read and written
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        n_cpu = 4096
+        k0 = torch.zeros((n_cpu, 2, Hkv, D), dtype=torch.bfloat16)
+        t0 = time.perf_counter()
+        for _ in range(args.warmup + args.steps):
+            O.seq_clone(k0, k0, 0, 1, n_cpu)
+        el = (time.perf_counter() - t0) / (args.warmup + args.steps)
+        v = 2 * 2 * n_cpu * Hkv * D * 2 / el / 1e9
+        cores = len(os.sched_getaffinity(0))
+        print(json.dumps({"impl": "reference", "metric": "seq_clone GB/s moved", "value": v, "unit": "GB/s",
+                          "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": el * 1e3,
+                          "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+                          "data": "synthetic", "config": {"workload": name},
+                          "cpu_baseline": {"value": v, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                                           "sample": f"{n_cpu} rows of one column"},
+                          "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}),
+              flush=True)
+        return
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    g = torch.Generator().manual_seed(args.seed)
+    k = torch.randn((rows, cols, Hkv, D), generator=g).to(torch.bfloat16).to(dev)
+    v = torch.randn((rows, cols, Hkv, D), generator=g).to(torch.bfloat16).to(dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    for _ in range(args.warmup):
+        pkg.sdpa_seq_clone(k, v, 0, cols - 1, rows)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    ms = []
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        e0.record()
+        pkg.sdpa_seq_clone(k, v, i % (cols - 1), cols - 1, rows)
+        e1.record()
+        torch.cuda.synchronize()
+        ms.append(e0.elapsed_time(e1))
+    barrier(world)
+    clk = clocks.stop()
+    mean = max_over_ranks(statistics.mean(ms), world)
+    value = world * moved / (mean * 1e-3) / 1e9
+    hbm, _, _, src = read_peaks()
+    # end to end: the column pair goes up from pinned host memory, the clone runs, and the
+    # destination column comes back
+    hk, hv = k.cpu().pin_memory(), v.cpu().pin_memory()
+    hcol = torch.empty((rows, Hkv, D), dtype=torch.bfloat16).pin_memory()
+    e2e = []
+    for i in range(max(2, args.steps // 2)):
+        e0.record()
+        k.copy_(hk, non_blocking=True)
+        v.copy_(hv, non_blocking=True)
+        pkg.sdpa_seq_clone(k, v, 0, cols - 1, rows)
+        hcol.copy_(k[:, cols - 1], non_blocking=True)
+        e1.record()
+        torch.cuda.synchronize()
+        e2e.append(e0.elapsed_time(e1))
+    e2e_ms = statistics.mean(e2e)
+    if rank != 0:
+        return
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        n_cpu = 4096
+        kc = torch.zeros((n_cpu, 2, Hkv, D), dtype=torch.bfloat16)
+        t0 = time.perf_counter()
+        O.seq_clone(kc, kc, 0, 1, n_cpu)
+        el = time.perf_counter() - t0
+        cpu = {"value": 2 * 2 * n_cpu * Hkv * D * 2 / el / 1e9, "unit": "GB/s", "cores": len(os.sched_getaffinity(0)),
+               "kind": "oracle", "sample": f"{n_cpu} rows of one column ({el:.2f} s)"}
+    print(json.dumps({
+        "metric": "seq_clone GB/s moved", "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": mean, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": name, "l2": "flushed between steps"},
+        "roofline": {"bound": "hbm", "achieved": moved / (mean * 1e-3) / 1e9, "peak": hbm, "unit": "GB/s",
+                     "frac": moved / (mean * 1e-3) / 1e9 / hbm, "traffic": None, "kernel": "clone",
+                     "peak_source": f"{src} HBM copy"},
+        "e2e": {"value": moved / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": 2 * hk.numel() * 2,
+                "d2h_bytes_per_step": hcol.numel() * 2, "ms_per_step": e2e_ms},
+        "gpu_launches": args.steps, "clocks": clk, "cpu_baseline": cpu,
+    }), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -253,6 +354,9 @@ def main():
     world, rank, local = dist_setup()
     from workloads import synth
 
+    if args.workload == "seq_clone":
+        run_clone(args, world, rank, local)
+        return
     wl = synth.workload(WORKLOADS[args.workload], seed=args.seed)
     if args.impl == "reference":
         run_reference(args, wl, world, rank)

@@ -134,6 +134,21 @@ sdpa_status sdpa_varlen_append(const void* q, int64_t T, int Hq, int D, int64_t 
                                size_t ws_bytes, int32_t* status_dev, void* stream);
 
 /*
+ * seq_clone: column dst_col takes over the first n positions of column src_col ("[executorch]
+ * [cuda] Add a length-aware Triton SDPA over per-sequence KV columns", #24073 commit message
+ * in its stack: seq_clone, a device copy of the source prefix).  Position j lives in store
+ * row j % rows, so positions [max(0, n - rows), n) are copied: store rows [0, min(n, rows))
+ * of the source column, every KV head, K and V, to the same rows of the destination column.
+ * Other rows of the destination keep their contents; src_col == dst_col or n == 0 does
+ * nothing.  k_store, v_store: [rows, cols, Hkv, D] contiguous bf16 device stores, 16-byte
+ * aligned.  Enqueued on `stream` (cudaStream_t), no host synchronisation.
+ * Errors: SDPA_ERR_NULL, _ALIGN, _SHAPE (rows, cols, Hkv < 1 or n < 0), _HEAD_DIM, _ARG
+ * (a column outside [0, cols)), _CUDA.
+ */
+sdpa_status sdpa_seq_clone(void* k_store, void* v_store, int64_t rows, int cols, int Hkv, int D,
+                           int src_col, int dst_col, int64_t n, void* stream);
+
+/*
  * Dense causal GQA prefill ("[CUDA] Use Triton TMA for long-context causal prefill",
  * Operator-level performance table: B = 1, global causal, queries being the last Lq of
  * Lkv positions).  q [Lq, Hq, D], k and v [Lkv, Hkv, D] contiguous bf16; out [Lq, Hq, D]

@@ -127,3 +127,36 @@ def test_append_in_a_captured_graph(dev):
         ref, seg_id, _ = O.sdpa_varlen(call.q, k_ref, v_ref, call.seq_info, True, 0, call.scale)
         _, lo, hi, _ = O.visible_interval(call.seq_info, call.T, True, 0, call.rows, call.cols)
         assert_matches(out, ref, seg_id, lo, hi, tag=f"graph step {step}")
+
+
+@pytest.mark.parametrize("rows,n,src,dst", [(64, 40, 1, 3), (64, 64, 0, 2), (64, 200, 2, 0), (512, 0, 1, 2),
+                                             (300, 123, 3, 3)])
+def test_seq_clone_matches_the_oracle_bit_for_bit(dev, rows, n, src, dst):
+    g = torch.Generator().manual_seed(rows + n)
+    k0 = torch.randn(rows, 4, 2, 128, generator=g).to(torch.bfloat16)
+    v0 = torch.randn(rows, 4, 2, 128, generator=g).to(torch.bfloat16)
+    k, v = k0.to(dev), v0.to(dev)
+    pkg.sdpa_seq_clone(k, v, src, dst, n)
+    torch.cuda.synchronize()
+    k_ref, v_ref = O.seq_clone(k0, v0, src, dst, n)
+    assert torch.equal(k.cpu().view(torch.int16), k_ref.view(torch.int16))
+    assert torch.equal(v.cpu().view(torch.int16), v_ref.view(torch.int16))
+
+
+def test_cloned_sequence_attends_bit_identically(dev, route):
+    # the mixed step's ring segments, each cloned into a fresh column: same outputs, bit for bit
+    call = synth.mixed_step(seed=3).calls[0]
+    k, v = call.k_store.to(dev), call.v_store.to(dev)
+    seq = np.array(call.seq_info, copy=True)
+    free = call.cols - 1  # the scratch column
+    for s in range(len(seq)):
+        q_start, q_len, col, kv_end = (int(x) for x in seq[s])
+        one = np.array([[q_start, q_len, col, kv_end]], dtype=np.int32)
+        a = pkg.sdpa_varlen(call.q.to(dev), k, v, torch.from_numpy(one).to(dev), causal=True,
+                            window=call.window, scale=call.scale)
+        pkg.sdpa_seq_clone(k, v, col, free, kv_end)
+        one[0, 2] = free
+        b = pkg.sdpa_varlen(call.q.to(dev), k, v, torch.from_numpy(one).to(dev), causal=True,
+                            window=call.window, scale=call.scale)
+        torch.cuda.synchronize()
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16)), s

@@ -103,3 +103,18 @@ def test_product_path_does_not_import_the_oracle():
             if f.endswith((".py", ".cu", ".cuh", ".h")):
                 text = open(os.path.join(dirpath, f)).read()
                 assert "oracle" not in text.lower().replace("oracles", ""), f
+
+
+def test_seq_clone_rejects_bad_arguments_before_touching_the_device():
+    import varlen_gqa_attention_gb300 as pkg
+    lib = pkg.library()
+    NULL, SHAPE, HEAD_DIM, ALIGN, ARG = 1, 2, 3, 6, 8  # sdpa_status codes of the header
+    p = 1 << 20  # a 16-byte aligned address that is never dereferenced
+    assert lib.sdpa_seq_clone(None, p, 8, 2, 1, 128, 0, 1, 4, None) == NULL
+    assert lib.sdpa_seq_clone(p + 2, p, 8, 2, 1, 128, 0, 1, 4, None) == ALIGN
+    assert lib.sdpa_seq_clone(p, p, 0, 2, 1, 128, 0, 1, 4, None) == SHAPE
+    assert lib.sdpa_seq_clone(p, p, 8, 2, 1, 128, 0, 1, -1, None) == SHAPE
+    assert lib.sdpa_seq_clone(p, p, 8, 2, 1, 96, 0, 1, 4, None) == HEAD_DIM
+    assert lib.sdpa_seq_clone(p, p, 8, 2, 1, 128, 0, 2, 4, None) == ARG
+    assert lib.sdpa_seq_clone(p, p, 8, 2, 1, 128, 1, 1, 4, None) == pkg.SDPA_OK  # same column
+    assert lib.sdpa_seq_clone(p, p, 8, 2, 1, 128, 0, 1, 0, None) == pkg.SDPA_OK  # empty prefix

@@ -38,7 +38,7 @@ STATUS_NAMES = {
 EXPORTS = [
     "sdpa_varlen_workspace_bytes", "sdpa_varlen", "sdpa_causal_prefill", "sdpa_set_route_policy",
     "sdpa_set_timing_events", "sdpa_last_error", "sdpa_version", "sdpa_varlen_splitk_static",
-    "sdpa_varlen_append",
+    "sdpa_varlen_append", "sdpa_seq_clone",
 ]
 
 
@@ -73,6 +73,8 @@ def library(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.sdpa_varlen_append.argtypes = [c_vp, c_i64, c_int, c_int, c_i64, c_i64, c_vp, c_vp, c_i64, c_i64,
                                        c_vp, c_vp, c_i64, c_int, c_int, c_vp, c_int, c_int, c_int, c_f,
                                        c_vp, c_i64, c_i64, c_vp, ctypes.c_size_t, c_vp, c_vp]
+    lib.sdpa_seq_clone.restype = c_int
+    lib.sdpa_seq_clone.argtypes = [c_vp, c_vp, c_i64, c_int, c_int, c_int, c_int, c_int, c_i64, c_vp]
     lib.sdpa_causal_prefill.restype = c_int
     lib.sdpa_causal_prefill.argtypes = [c_vp, c_vp, c_vp, c_i64, c_i64, c_int, c_int, c_int, c_f,
                                         c_vp, c_vp, ctypes.c_size_t, c_vp]
@@ -214,6 +216,21 @@ def sdpa_varlen_append(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor
                                   st_ptr, _stream_ptr(stream))
     _check(code)
     return out
+
+
+def sdpa_seq_clone(k_store: torch.Tensor, v_store: torch.Tensor, src_col: int, dst_col: int, n: int,
+                   stream=None) -> None:
+    """Column dst_col of both stores takes over the first n positions of column src_col
+    (ring-aware: store rows [0, min(n, rows)) are copied).  In place, on the device."""
+    lib = library()
+    if k_store.dim() != 4 or tuple(v_store.shape) != tuple(k_store.shape):
+        raise ValueError("the stores must both be [rows, cols, Hkv, D]")
+    for name, t in (("k_store", k_store), ("v_store", v_store)):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous bf16 CUDA tensor")
+    rows, cols, Hkv, D = k_store.shape
+    _check(lib.sdpa_seq_clone(k_store.data_ptr(), v_store.data_ptr(), rows, cols, Hkv, D, int(src_col),
+                              int(dst_col), int(n), _stream_ptr(stream)))
 
 
 def sdpa_causal_prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale: Optional[float] = None,

@@ -383,6 +383,40 @@ sdpa_status sdpa_varlen_append(const void* q, int64_t T, int Hq, int D, int64_t 
              ws_bytes, status_dev, stream, &ap);
 }
 
+sdpa_status sdpa_seq_clone(void* k_store, void* v_store, int64_t rows, int cols, int Hkv, int D,
+                           int src_col, int dst_col, int64_t n, void* stream) {
+  g_err[0] = 0;
+  if (!k_store || !v_store) return fail(SDPA_ERR_NULL, "a store pointer is NULL");
+  if (!aligned16(k_store) || !aligned16(v_store)) return fail(SDPA_ERR_ALIGN, "stores must be 16-byte aligned");
+  if (rows <= 0 || cols <= 0 || Hkv <= 0 || n < 0)
+    return fail(SDPA_ERR_SHAPE, "bad sizes: rows=%lld cols=%d Hkv=%d n=%lld", (long long)rows, cols, Hkv,
+                (long long)n);
+  if (D != 64 && D != 128 && D != 256) return fail(SDPA_ERR_HEAD_DIM, "head dim %d not in {64,128,256}", D);
+  if (src_col < 0 || src_col >= cols || dst_col < 0 || dst_col >= cols)
+    return fail(SDPA_ERR_ARG, "columns %d -> %d outside [0, %d)", src_col, dst_col, cols);
+  const int64_t m = std::min(n, rows);
+  if (m == 0 || src_col == dst_col) return SDPA_OK;
+  DevInfo di;
+  sdpa_status st = device_info(&di);
+  if (st) return st;
+  CloneArgs ca{};
+  ca.k_store = (__nv_bfloat16*)k_store;
+  ca.v_store = (__nv_bfloat16*)v_store;
+  ca.m = m;
+  ca.cols = cols;
+  ca.Hkv = Hkv;
+  ca.D = D;
+  ca.src_col = src_col;
+  ca.dst_col = dst_col;
+  const int64_t total = m * Hkv * (D / 8);
+  const int64_t blocks = std::max<int64_t>(1, std::min<int64_t>((int64_t)di.sms * 8, (total + 4 * kCloneThreads - 1) / (4 * kCloneThreads)));
+  void* args[] = {(void*)&ca};
+  cudaError_t e = cudaLaunchKernel(clone_kernel_ptr(), dim3((unsigned)blocks), dim3(kCloneThreads), args, 0,
+                                   (cudaStream_t)stream);
+  if (e != cudaSuccess) return fail(SDPA_ERR_CUDA, "clone launch: %s", cudaGetErrorString(e));
+  return SDPA_OK;
+}
+
 sdpa_status sdpa_causal_prefill(const void* q, const void* k, const void* v, int64_t Lq,
                                 int64_t Lkv, int Hq, int Hkv, int D, float scale, void* out,
                                 void* workspace, size_t ws_bytes, void* stream) {

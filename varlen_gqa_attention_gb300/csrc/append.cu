@@ -38,3 +38,45 @@ __global__ void __launch_bounds__(kAppendThreads) sdpa_append_kernel(AppendArgs 
 const void* append_kernel_ptr() { return (const void*)sdpa_append_kernel; }
 
 }  // namespace sdpa
+
+namespace sdpa {
+
+// seq_clone ("[executorch][cuda] Add a length-aware Triton SDPA over per-sequence KV columns",
+// the #24073 commit message in its stack: seq_clone, a device copy of the source prefix).
+// Positions [max(0, n - rows), n) of the source column live in store rows [0, min(n, rows)),
+// each at row j % rows; they are copied row for row into the destination column, every KV
+// head, K and V.  A column's cell of one row is Hkv * D contiguous elements; the grid walks
+// 16-byte chunks, four per thread per step so each thread keeps four loads in flight.
+__global__ void __launch_bounds__(kCloneThreads) sdpa_clone_kernel(CloneArgs A) {
+  const int cpr = A.Hkv * (A.D / 8);  // chunks per (row, column) cell
+  const int64_t total = A.m * cpr;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t base = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; base < total; base += 4 * stride) {
+    uint4 kk[4], vv[4];
+    int64_t dst[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int64_t idx = base + u * stride;
+      dst[u] = -1;
+      if (idx < total) {
+        const int64_t r = idx / cpr;
+        const int c = (int)(idx - r * cpr);
+        const int64_t cell = r * A.cols;
+        const int64_t src = (cell + A.src_col) * A.Hkv * A.D + (int64_t)c * 8;
+        dst[u] = (cell + A.dst_col) * A.Hkv * A.D + (int64_t)c * 8;
+        kk[u] = *reinterpret_cast<const uint4*>(A.k_store + src);
+        vv[u] = *reinterpret_cast<const uint4*>(A.v_store + src);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      if (dst[u] < 0) continue;
+      *reinterpret_cast<uint4*>(A.k_store + dst[u]) = kk[u];
+      *reinterpret_cast<uint4*>(A.v_store + dst[u]) = vv[u];
+    }
+  }
+}
+
+const void* clone_kernel_ptr() { return (const void*)sdpa_clone_kernel; }
+
+}  // namespace sdpa

@@ -159,6 +159,15 @@ struct AppendArgs {
 };
 constexpr int kAppendThreads = 128;
 
+// Arguments of the column clone kernel: store rows [0, m) of column src_col copied to dst_col.
+struct CloneArgs {
+  __nv_bfloat16* k_store;
+  __nv_bfloat16* v_store;
+  int64_t m;
+  int cols, Hkv, D, src_col, dst_col;
+};
+constexpr int kCloneThreads = 256;
+
 // Arguments of the scheduler kernel.
 struct SchedArgs {
   const int32_t* seq_info;
@@ -181,6 +190,7 @@ constexpr int kSchedThreads = 1024;
 // Kernel entry points (defined in their own translation units).
 const void* sched_kernel_ptr();
 const void* append_kernel_ptr();
+const void* clone_kernel_ptr();
 const void* splitk_kernel_ptr(int D);
 int splitk_smem_bytes(int D);
 const void* combine_kernel_ptr(int D);

@@ -124,7 +124,19 @@ def segment_status(seg, T: int, rows: int, cols: int, window: int) -> int:
     return bits
 
 
-def visible_interval(seq_info, T: int, causal: bool, window: int, rows: int, cols: int):
+def segment_modes(seq_info, causal: bool, window: int, seg_mode=None):
+    """Per segment (causal, window): the call's pair for every segment, or the rows of
+    ``seg_mode`` [S, 2] when given (a per-segment mask mode, so that causal target segments
+    and non-causal draft blocks can share one call)."""
+    n = len(np.asarray(seq_info, dtype=np.int64).reshape(-1, 4))
+    if seg_mode is None:
+        return [(bool(causal), int(window))] * n
+    m = np.asarray(seg_mode, dtype=np.int64).reshape(-1, 2)
+    assert len(m) == n
+    return [(bool(c), int(w)) for c, w in m]
+
+
+def visible_interval(seq_info, T: int, causal: bool, window: int, rows: int, cols: int, seg_mode=None):
     """Per packed row: (segment id, lo, hi, status).
 
     seg_id[t] is the index of the valid segment covering row t, UNCOVERED when none
@@ -133,6 +145,7 @@ def visible_interval(seq_info, T: int, causal: bool, window: int, rows: int, col
     empty); both are 0 for uncovered and overlapped rows.  status is the OR of every
     segment's bits plus SEG_OVERLAP.
     """
+    modes = segment_modes(seq_info, causal, window, seg_mode)
     seq_info = np.asarray(seq_info, dtype=np.int64).reshape(-1, 4)
     seg_id = np.full(T, UNCOVERED, dtype=np.int64)
     lo = np.zeros(T, dtype=np.int64)
@@ -141,7 +154,7 @@ def visible_interval(seq_info, T: int, causal: bool, window: int, rows: int, col
     owners = [[] for _ in range(T)]
     valid = []
     for s, seg in enumerate(seq_info):
-        bits = segment_status(seg, T, rows, cols, window)
+        bits = segment_status(seg, T, rows, cols, modes[s][1])
         status |= bits
         if bits:
             continue
@@ -164,17 +177,18 @@ def visible_interval(seq_info, T: int, causal: bool, window: int, rows: int, col
                 lo[t] = hi[t] = 0
                 continue
             seg_id[t] = s
-            lo[t], hi[t] = row_interval(i, q_len, kv_end, causal, window)
+            lo[t], hi[t] = row_interval(i, q_len, kv_end, modes[s][0], modes[s][1])
     return seg_id, lo, hi, status
 
 
 def sdpa_varlen(q, k_store, v_store, seq_info, causal: bool, window: int, scale: float,
-                rows_subset: Optional[Iterable[int]] = None):
+                rows_subset: Optional[Iterable[int]] = None, seg_mode=None):
     """Length-aware GQA attention over a column store, in fp64.
 
     q: [T, Hq, D]; k_store, v_store: [rows, cols, Hkv, D]; seq_info: [S, 4].
     Returns (out [T, Hq, D] float64, seg_id [T], status).  Rows outside
-    ``rows_subset`` (when given) are left at 0 and not computed.
+    ``rows_subset`` (when given) are left at 0 and not computed.  ``seg_mode`` [S, 2]
+    (optional) gives each segment its own (causal, window) in place of the call's.
     """
     qf = _as_f64(q)
     T, Hq, D = qf.shape
@@ -183,7 +197,8 @@ def sdpa_varlen(q, k_store, v_store, seq_info, causal: bool, window: int, scale:
     assert Hq % Hkv == 0
     group = Hq // Hkv
     seq_info = np.asarray(seq_info, dtype=np.int64).reshape(-1, 4)
-    seg_id, lo, hi, status = visible_interval(seq_info, T, causal, window, rows, cols)
+    modes = segment_modes(seq_info, causal, window, seg_mode)
+    seg_id, lo, hi, status = visible_interval(seq_info, T, causal, window, rows, cols, seg_mode)
     out = np.zeros((T, Hq, D), dtype=np.float64)
     wanted = None if rows_subset is None else set(int(t) for t in rows_subset)
 
@@ -193,7 +208,7 @@ def sdpa_varlen(q, k_store, v_store, seq_info, causal: bool, window: int, scale:
         if not rows_of_s:
             continue
         # Upcast the keys/values this segment can see once: positions [u_lo, kv_end).
-        u_lo = kv_end - needed_span(q_len, kv_end, window)
+        u_lo = kv_end - needed_span(q_len, kv_end, modes[s][1])
         pos = np.arange(u_lo, kv_end)
         phys = store_row(pos, rows)
         Kc = _as_f64(k_store[phys, col])                     # [n, Hkv, D]

@@ -33,7 +33,7 @@ sys.path.insert(0, ROOT)
 
 WORKLOADS = {
     "tiny": 0, "prefill_d64": 1, "prefill_d128": 2, "decode": 3, "mixed": 4, "decode_append": 3,
-    "seq_clone": -1,
+    "seq_clone": -1, "mixed_modes": 5,
 }
 # seq_clone workload: one column of a [rows, cols, Hkv, D] store pair copied whole into another
 CLONE_SHAPE = (32768, 9, 8, 128)
@@ -46,26 +46,25 @@ L2_FLUSH_BYTES = 512 << 20
 # bench line on a GB300 (dram__bytes_read.sum + dram__bytes_write.sum; the file under profiles/
 # named for the kernel and workload gives the command).  They describe the kernel source they
 # were taken on: a kernel change makes them stale until the capture is repeated.
-NCU_TRAFFIC_BYTES = {
-    "prefill_d128": 2137420288 + 38294272,  # sdpa_prefill_kernel<128>, one launch
-    "prefill_d64": 9514496 + 0,             # sdpa_prefill_kernel<64>, one launch
-    "decode": 141747200 + 2986752,          # sdpa_splitk_kernel<128>, one launch
-    "mixed": 135023616 + 3034368 + 150764800 + 613376,  # sdpa_splitk_kernel<128>, both calls
-}
+NCU_TRAFFIC_BYTES = {}  # kernels changed since the last capture
 
 
 def useful_work(call):
     """(flops, kv_bytes, q_out_bytes) the call must do: 4*D*Hq per (row, visible key) pair,
     K and V bytes of the union of each valid segment's visible positions, and q/out bytes of
     the rows valid segments cover."""
-    T, rows, cols, W = call.T, call.rows, call.cols, call.window
+    T, rows, cols = call.T, call.rows, call.cols
+    segs = np.asarray(call.seq_info, dtype=np.int64)
+    if call.seg_mode is None:
+        modes = [(bool(call.causal), int(call.window))] * len(segs)
+    else:
+        modes = [(bool(c), int(w)) for c, w in np.asarray(call.seg_mode, dtype=np.int64)]
     pairs = 0
     kv = 0
     covered = 0
     owners = np.zeros(T, dtype=np.int64)
-    segs = np.asarray(call.seq_info, dtype=np.int64)
     ok = []
-    for (qs, ql, col, ke) in segs:
+    for (qs, ql, col, ke), (_, W) in zip(segs, modes):
         bad = ql < 0 or qs < 0 or qs + ql > T or col < 0 or col >= cols or ke < 0
         if not bad and ql > 0 and ke > 0:
             span = min(ke, ql + W - 1) if W > 0 else ke
@@ -73,11 +72,11 @@ def useful_work(call):
         ok.append(not bad)
         if not bad and ql > 0:
             owners[qs:qs + ql] += 1
-    for (qs, ql, col, ke), good in zip(segs, ok):
+    for (qs, ql, col, ke), good, (causal, W) in zip(segs, ok, modes):
         if not good or ql <= 0 or (owners[qs:qs + ql] > 1).any():
             continue
         p = ke - ql + np.arange(ql)
-        hi = np.minimum(p + 1, ke) if call.causal else np.full(ql, ke)
+        hi = np.minimum(p + 1, ke) if causal else np.full(ql, ke)
         lo = np.maximum(0, p - W + 1) if W > 0 else np.zeros(ql, dtype=np.int64)
         pairs += int(np.maximum(hi - lo, 0).sum())
         if ke > 0:
@@ -190,24 +189,27 @@ def cpu_baseline(wl, prefill_like: bool, budget_s: float = 12.0):
     n_rows = 0
     per_call = budget_s / len(wl.calls)
     for c in wl.calls:
-        seg_id, lo, hi, _ = O.visible_interval(c.seq_info, c.T, c.causal, c.window, c.rows, c.cols)
+        seg_id, lo, hi, _ = O.visible_interval(c.seq_info, c.T, c.causal, c.window, c.rows, c.cols,
+                                               seg_mode=c.seg_mode)
         live = [t for t in range(c.T) if seg_id[t] >= 0]
         if not live:
             continue
         t0 = time.perf_counter()
         O.sdpa_varlen(c.q, c.k_store, c.v_store, c.seq_info, c.causal, c.window, c.scale,
-                      rows_subset=live[-8:])
+                      rows_subset=live[-8:], seg_mode=c.seg_mode)
         cal = max(time.perf_counter() - t0, 1e-3)
         n = int(min(len(live), max(8, 8 * per_call / cal)))
         rows = live[-n:]
         t0 = time.perf_counter()
-        O.sdpa_varlen(c.q, c.k_store, c.v_store, c.seq_info, c.causal, c.window, c.scale, rows_subset=rows)
+        O.sdpa_varlen(c.q, c.k_store, c.v_store, c.seq_info, c.causal, c.window, c.scale, rows_subset=rows,
+                      seg_mode=c.seg_mode)
         el += time.perf_counter() - t0
         n_rows += len(rows)
         done_flops += 4 * c.D * c.Hq * int(np.maximum(hi[rows] - lo[rows], 0).sum())
         for s in sorted(set(int(seg_id[t]) for t in rows)):
             qs, ql, col, ke = (int(x) for x in c.seq_info[s])
-            done_bytes += O.needed_span(ql, ke, c.window) * c.Hkv * c.D * 2 * 2
+            w = c.window if c.seg_mode is None else int(c.seg_mode[s][1])
+            done_bytes += O.needed_span(ql, ke, w) * c.Hkv * c.D * 2 * 2
     cores = len(os.sched_getaffinity(0))
     el = max(el, 1e-9)
     value = done_flops / el / 1e12 if prefill_like else done_bytes / el / 1e9
@@ -380,6 +382,8 @@ def main():
                  ws=torch.empty(pkg.workspace_bytes(c.T, c.Hq, c.Hkv, c.D, len(c.seq_info)),
                                 dtype=torch.uint8, device=dev))
         d["out"] = out[c.row_begin:(c.row_end or c.T)]
+        if c.seg_mode is not None:
+            d["md"] = torch.from_numpy(np.ascontiguousarray(c.seg_mode, dtype=np.int32)).to(dev)
         if args.workload in APPEND:
             g = torch.Generator().manual_seed(1000 + args.seed)
             shape = (c.T, c.Hkv, c.D)
@@ -393,6 +397,9 @@ def main():
         if "kn" in d:
             pkg.sdpa_varlen_append(d["q"], d["kn"], d["vn"], d["k"], d["v"], d["seq"], causal=c.causal,
                                    window=c.window, scale=c.scale, out=d["out"], workspace=d["ws"])
+        elif "md" in d:
+            pkg.sdpa_varlen_modes(d["q"], d["k"], d["v"], d["seq"], d["md"], scale=c.scale, out=d["out"],
+                                  workspace=d["ws"])
         else:
             pkg.sdpa_varlen(d["q"], d["k"], d["v"], d["seq"], causal=c.causal, window=c.window,
                             scale=c.scale, out=d["out"], workspace=d["ws"])
@@ -507,6 +514,9 @@ def main():
         if "kn" in d:
             d["kn_pin"], d["vn_pin"] = d["kn_host"].pin_memory(), d["vn_host"].pin_memory()
             h2d += (d["kn_pin"].numel() + d["vn_pin"].numel()) * 2
+        if "md" in d:
+            d["md_pin"] = d["md"].cpu().pin_memory()
+            h2d += d["md_pin"].numel() * 4
     hout = torch.empty(out.shape, dtype=torch.bfloat16).pin_memory()
     d2h = hout.numel() * 2
 
@@ -519,6 +529,8 @@ def main():
             if "kn" in d:
                 d["kn"].copy_(d["kn_pin"], non_blocking=True)
                 d["vn"].copy_(d["vn_pin"], non_blocking=True)
+            if "md" in d:
+                d["md"].copy_(d["md_pin"], non_blocking=True)
             attend(d)
         hout.copy_(out, non_blocking=True)
 

@@ -134,6 +134,27 @@ sdpa_status sdpa_varlen_append(const void* q, int64_t T, int Hq, int D, int64_t 
                                size_t ws_bytes, int32_t* status_dev, void* stream);
 
 /*
+ * Attention with a mask mode per segment, so that causal target segments and non-causal
+ * draft blocks of one step share one launch (the #24074 manifest of "[executorch][cuda] Add a
+ * length-aware Triton SDPA over per-sequence KV columns" carries `causal` per model, false for
+ * DFlash drafts; here the choice moves into the segment table).
+ *
+ *  seg_mode  device int32 [S, 2], 16-byte aligned: row s = (causal, window) of segment s,
+ *            with the meanings of sdpa_varlen's causal (non-zero: causal) and window (W > 0
+ *            keys counting the query's own; <= 0: no window).  Read on the device, so one
+ *            captured graph serves any mix; a segment's validity (needed span <= rows) uses
+ *            its own window.
+ * Every other argument and the result are those of sdpa_varlen, whose causal / window
+ * arguments this call replaces.  Errors as sdpa_varlen, plus SDPA_ERR_NULL for seg_mode.
+ */
+sdpa_status sdpa_varlen_modes(const void* q, int64_t T, int Hq, int D, int64_t q_row_stride,
+                              int64_t q_head_stride, const void* k_store, const void* v_store,
+                              int64_t rows, int cols, int Hkv, const int32_t* seq_info,
+                              const int32_t* seg_mode, int S, float scale, void* out,
+                              int64_t o_row_stride, int64_t o_head_stride, void* workspace,
+                              size_t ws_bytes, int32_t* status_dev, void* stream);
+
+/*
  * seq_clone: column dst_col takes over the first n positions of column src_col ("[executorch]
  * [cuda] Add a length-aware Triton SDPA over per-sequence KV columns", #24073 commit message
  * in its stack: seq_clone, a device copy of the source prefix).  Position j lives in store

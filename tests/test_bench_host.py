@@ -85,3 +85,18 @@ def test_useful_work_skips_invalid_and_overlapping_segments():
     assert kv == O.useful_kv_bytes(seq, c.T, c.Hkv, c.D, c.window, c.rows, c.cols) - \
         sum(O.needed_span(int(s[1]), int(s[3]), c.window) * c.Hkv * c.D * 4 for s in seq[:2]
             if not O.segment_status(s, c.T, c.rows, c.cols, c.window))
+
+
+def test_useful_work_of_the_one_store_mixed_step_uses_each_segments_mode():
+    c = synth.workload(5).calls[0]
+    flops, kv, _ = bench.useful_work(c)
+    _, lo, hi, st = O.visible_interval(c.seq_info, c.T, True, 0, c.rows, c.cols, seg_mode=c.seg_mode)
+    assert st == 0
+    assert flops == 4 * c.D * c.Hq * int(np.maximum(hi - lo, 0).sum())
+    assert kv == sum(O.needed_span(int(s[1]), int(s[3]), int(m[1])) * c.Hkv * c.D * 4
+                     for s, m in zip(c.seq_info, c.seg_mode))
+    # the same segments as two call-level calls (targets causal W=4096, drafts non-causal)
+    t, d = c.seg_mode[:, 0] == 1, c.seg_mode[:, 0] == 0
+    f_t = O.useful_flops(c.seq_info[t], c.T, c.Hq, c.D, True, 4096, c.rows, c.cols)
+    f_d = O.useful_flops(c.seq_info[d], c.T, c.Hq, c.D, False, 0, c.rows, c.cols)
+    assert flops == f_t + f_d

@@ -38,7 +38,7 @@ STATUS_NAMES = {
 EXPORTS = [
     "sdpa_varlen_workspace_bytes", "sdpa_varlen", "sdpa_causal_prefill", "sdpa_set_route_policy",
     "sdpa_set_timing_events", "sdpa_last_error", "sdpa_version", "sdpa_varlen_splitk_static",
-    "sdpa_varlen_append", "sdpa_seq_clone",
+    "sdpa_varlen_append", "sdpa_seq_clone", "sdpa_varlen_modes",
 ]
 
 
@@ -73,6 +73,10 @@ def library(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.sdpa_varlen_append.argtypes = [c_vp, c_i64, c_int, c_int, c_i64, c_i64, c_vp, c_vp, c_i64, c_i64,
                                        c_vp, c_vp, c_i64, c_int, c_int, c_vp, c_int, c_int, c_int, c_f,
                                        c_vp, c_i64, c_i64, c_vp, ctypes.c_size_t, c_vp, c_vp]
+    lib.sdpa_varlen_modes.restype = c_int
+    lib.sdpa_varlen_modes.argtypes = [c_vp, c_i64, c_int, c_int, c_i64, c_i64, c_vp, c_vp, c_i64, c_int,
+                                      c_int, c_vp, c_vp, c_int, c_f, c_vp, c_i64, c_i64, c_vp,
+                                      ctypes.c_size_t, c_vp, c_vp]
     lib.sdpa_seq_clone.restype = c_int
     lib.sdpa_seq_clone.argtypes = [c_vp, c_vp, c_i64, c_int, c_int, c_int, c_int, c_int, c_i64, c_vp]
     lib.sdpa_causal_prefill.restype = c_int
@@ -214,6 +218,48 @@ def sdpa_varlen_append(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor
                                   S, int(bool(causal)), int(window), float(scale), out.data_ptr(),
                                   out.stride(0), out.stride(1), workspace.data_ptr(), workspace.numel(),
                                   st_ptr, _stream_ptr(stream))
+    _check(code)
+    return out
+
+
+def sdpa_varlen_modes(q: torch.Tensor, k_store: torch.Tensor, v_store: torch.Tensor, seq_info: torch.Tensor,
+                      seg_mode: torch.Tensor, *, scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
+                      workspace: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
+                      stream=None) -> torch.Tensor:
+    """``sdpa_varlen`` with a mask mode per segment: seg_mode int32 [S, 2] = (causal, window)
+    on the device, in place of the call's causal / window."""
+    lib = library()
+    if q.dim() != 3 or k_store.dim() != 4 or tuple(v_store.shape) != tuple(k_store.shape):
+        raise ValueError("q must be [T, Hq, D] and the stores [rows, cols, Hkv, D]")
+    for name, t in (("q", q), ("k_store", k_store), ("v_store", v_store)):
+        if t.dtype != torch.bfloat16 or not t.is_cuda:
+            raise ValueError(f"{name} must be a bf16 CUDA tensor")
+    if not (k_store.is_contiguous() and v_store.is_contiguous()):
+        raise ValueError("k_store and v_store must be contiguous")
+    for name, t in (("seq_info", seq_info), ("seg_mode", seg_mode)):
+        if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous int32 CUDA tensor")
+    T, Hq, D = q.shape
+    rows, cols, Hkv, Dk = k_store.shape
+    S = seq_info.shape[0] if seq_info.numel() else 0
+    if tuple(seg_mode.shape) != (S, 2) and S:
+        raise ValueError("seg_mode must be [S, 2]")
+    if Dk != D or q.stride(2) != 1:
+        raise ValueError("head dims differ, or q has a non-unit inner stride")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty((T, Hq, D), dtype=torch.bfloat16, device=q.device)
+    elif out.dtype != torch.bfloat16 or tuple(out.shape) != (T, Hq, D) or out.stride(2) != 1:
+        raise ValueError("out must be bf16 [T, Hq, D] with unit inner stride")
+    if workspace is None:
+        workspace = _workspace(workspace_bytes(T, Hq, Hkv, D, S), q.device)
+    st_ptr = status.data_ptr() if status is not None else None
+    code = lib.sdpa_varlen_modes(q.data_ptr(), T, Hq, D, q.stride(0), q.stride(1), k_store.data_ptr(),
+                                 v_store.data_ptr(), rows, cols, Hkv, seq_info.data_ptr() if S else None,
+                                 seg_mode.data_ptr() if S else None, S, float(scale), out.data_ptr(),
+                                 out.stride(0), out.stride(1), workspace.data_ptr(), workspace.numel(),
+                                 st_ptr, _stream_ptr(stream))
     _check(code)
     return out
 

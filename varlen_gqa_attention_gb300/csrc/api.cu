@@ -244,7 +244,8 @@ static sdpa_status run(const void* q, int64_t T, int Hq, int D, int64_t q_rs, in
                        const void* k, const void* v, int64_t rows, int cols, int Hkv,
                        const int32_t* seq_info, int S, const int32_t* inl, int causal, int window,
                        float scale, void* out, int64_t o_rs, int64_t o_hs, void* ws, size_t ws_bytes,
-                       int32_t* status_dev, void* stream, const AppendArgs* ap = nullptr) {
+                       int32_t* status_dev, void* stream, const AppendArgs* ap = nullptr,
+                       const int32_t* seg_mode = nullptr) {
   g_err[0] = 0;
   sdpa_status st = check_common(T, Hq, Hkv, D, S, rows, cols, window, scale);
   if (st) return st;
@@ -266,8 +267,10 @@ static sdpa_status run(const void* q, int64_t T, int Hq, int D, int64_t q_rs, in
   if (ws_bytes < need)
     return fail(SDPA_ERR_WORKSPACE, "workspace of %zu bytes, %zu needed", ws_bytes, need);
 
+  if (seg_mode && !aligned16(seg_mode)) return fail(SDPA_ERR_ALIGN, "seg_mode must be 16-byte aligned");
   SchedArgs sa{};
   sa.seq_info = seq_info;
+  sa.seg_mode = S > 0 ? seg_mode : nullptr;
   sa.S = S;
   sa.use_inline = inl != nullptr;
   if (inl)
@@ -381,6 +384,19 @@ sdpa_status sdpa_varlen_append(const void* q, int64_t T, int Hq, int D, int64_t 
   return run(q, T, Hq, D, q_row_stride, q_head_stride, k_store, v_store, rows, cols, Hkv, seq_info,
              S, nullptr, causal, window, scale, out, o_row_stride, o_head_stride, workspace,
              ws_bytes, status_dev, stream, &ap);
+}
+
+sdpa_status sdpa_varlen_modes(const void* q, int64_t T, int Hq, int D, int64_t q_row_stride,
+                              int64_t q_head_stride, const void* k_store, const void* v_store,
+                              int64_t rows, int cols, int Hkv, const int32_t* seq_info,
+                              const int32_t* seg_mode, int S, float scale, void* out,
+                              int64_t o_row_stride, int64_t o_head_stride, void* workspace,
+                              size_t ws_bytes, int32_t* status_dev, void* stream) {
+  g_err[0] = 0;
+  if (!seg_mode && S > 0) return fail(SDPA_ERR_NULL, "seg_mode is NULL");
+  return run(q, T, Hq, D, q_row_stride, q_head_stride, k_store, v_store, rows, cols, Hkv, seq_info,
+             S, nullptr, 1, 0, scale, out, o_row_stride, o_head_stride, workspace, ws_bytes,
+             status_dev, stream, nullptr, seg_mode);
 }
 
 sdpa_status sdpa_seq_clone(void* k_store, void* v_store, int64_t rows, int cols, int Hkv, int D,

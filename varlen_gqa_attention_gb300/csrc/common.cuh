@@ -31,6 +31,8 @@ struct SegRec {
   int32_t pad;
   int32_t ubase[4];  // per route: units of all earlier segments on that route (monotone in
                      // the segment index, so a binary search maps a unit to its segment)
+  int32_t causal, window;  // the segment's mask mode (the call's, or its row of seg_mode)
+  int32_t pad2[2];
 };
 
 // Per-unit record: (segment, KV head, row block) and its stream-K split.
@@ -41,9 +43,8 @@ struct UnitRec {
   int32_t g_first;            // first such CTA
   int32_t ntiles;             // key tiles of the unit
   int32_t phase;              // scheduling phase of the unit (see SchedHdr)
-  int32_t q_start, q_len, col, kv_end;  // the segment's entry, copied so that one record
-                                        // (80 bytes, 16-byte multiple) describes a piece
-  int32_t pad[2];
+  int32_t q_start, q_len, col, kv_end;  // the segment's entry and mask mode, copied so
+  int32_t causal, window;               // that one record (80 bytes) describes a piece
   int64_t tile_base;          // start of the unit's span in the flattened tile line: `lead`
                               // placeholder tiles, then its ntiles key tiles
   int64_t slot_base;          // first partial row of the unit's slots
@@ -171,6 +172,7 @@ constexpr int kCloneThreads = 256;
 // Arguments of the scheduler kernel.
 struct SchedArgs {
   const int32_t* seq_info;
+  const int32_t* seg_mode;  // NULL, or [S, 2] (causal, window) per segment
   int S;
   int use_inline;  // dense entry: one segment passed by value
   int32_t inl[4];

@@ -431,7 +431,7 @@ __global__ void __launch_bounds__(PfCfg<D>::THREADS, 1)
       const int64_t pos_hi = min((int64_t)ur.lo + pc.tb * C::BN, (int64_t)ur.hi);
       int64_t rlo = 1, rhi = 0;  // padding rows see nothing
       if (live) {
-        const RowWin w = row_window(qi, sg.q_len, sg.kv_end, A.causal, A.window);
+        const RowWin w = row_window(qi, sg.q_len, sg.kv_end, sg.causal, sg.window);
         rlo = max((int64_t)w.lo, pos_lo);
         rhi = min((int64_t)w.hi, pos_hi);
       }

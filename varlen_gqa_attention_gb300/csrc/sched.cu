@@ -83,7 +83,7 @@ __device__ __forceinline__ int route_of(const SchedArgs& A, const SegRec& r) {
   if (A.policy == SDPA_ROUTE_SPLITK || !A.prefill_ok) return kRouteSplitk;
   if (r.kv_end > 0) {
     int64_t span = r.kv_end;
-    if (A.window > 0) span = min(span, (int64_t)r.q_len + A.window - 1);
+    if (r.window > 0) span = min(span, (int64_t)r.q_len + r.window - 1);
     const int64_t first = r.kv_end - span;
     if (first / A.rows != (r.kv_end - 1) / A.rows) return kRouteSplitk;
   }
@@ -104,6 +104,7 @@ __global__ void __launch_bounds__(kSchedThreads) sdpa_sched_kernel(SchedArgs A) 
   __shared__ int32_t c_bits[kSegCache];
   __shared__ int2 c_rn[kSegCache];   // (route, nrb)
   __shared__ int2 c_ub[kSegCache];   // unit bases of routes 1 and 2
+  __shared__ int2 c_mode[kSegCache]; // (causal, window)
   const Workspace& W = A.ws;
   const int S = A.S;
   const int64_t T = A.T;
@@ -116,16 +117,25 @@ __global__ void __launch_bounds__(kSchedThreads) sdpa_sched_kernel(SchedArgs A) 
   for (int s = threadIdx.x; s < S; s += blockDim.x) {
     int32_t g[4];
     load_seg(A, s, g);
-    const int32_t bits = segment_bits(g[0], g[1], g[2], g[3], T, A.rows, A.cols, A.window);
+    int2 md = make_int2(A.causal, A.window);
+    if (A.seg_mode) {
+      md = reinterpret_cast<const int2*>(A.seg_mode)[s];
+      md.x = md.x != 0;
+    }
+    const int32_t bits = segment_bits(g[0], g[1], g[2], g[3], T, A.rows, A.cols, md.y);
     SegRec r;
     r.q_start = g[0]; r.q_len = g[1]; r.col = g[2]; r.kv_end = g[3];
     r.route = kRouteNone; r.nrb = 0; r.bits = bits; r.pad = 0;
     r.ubase[0] = r.ubase[1] = r.ubase[2] = r.ubase[3] = 0;
+    r.causal = md.x;
+    r.window = md.y;
+    r.pad2[0] = r.pad2[1] = 0;
     W.segs[s] = r;
     W.seg_flag[s] = 0;
     if (cached) {
       c_seg[s] = make_int4(g[0], g[1], g[2], g[3]);
       c_bits[s] = bits;
+      c_mode[s] = md;
     }
     if (bits) atomicOr(&s_status, bits);
   }
@@ -172,6 +182,7 @@ __global__ void __launch_bounds__(kSchedThreads) sdpa_sched_kernel(SchedArgs A) 
     if (bits == 0 && !flag && g.y > 0) {
       SegRec r;
       r.q_start = g.x; r.q_len = g.y; r.col = g.z; r.kv_end = g.w;
+      r.window = cached ? c_mode[s].y : W.segs[s].window;
       const int64_t R = (int64_t)g.y * A.group;
       route = route_of(A, r);
       const int rpu = rows_per_unit(route);
@@ -222,6 +233,8 @@ __global__ void __launch_bounds__(kSchedThreads) sdpa_sched_kernel(SchedArgs A) 
         g.q_start = c.x; g.q_len = c.y; g.col = c.z; g.kv_end = c.w;
         g.nrb = c_rn[s].y;
         g.ubase[q] = q == 1 ? c_ub[s].x : c_ub[s].y;
+        g.causal = c_mode[s].x;
+        g.window = c_mode[s].y;
       } else {
         g = W.segs[s];
       }
@@ -232,15 +245,16 @@ __global__ void __launch_bounds__(kSchedThreads) sdpa_sched_kernel(SchedArgs A) 
       ur.q_len = g.q_len;
       ur.col = g.col;
       ur.kv_end = g.kv_end;
-      ur.pad[0] = ur.pad[1] = 0;
+      ur.causal = g.causal;
+      ur.window = g.window;
       ur.hk = (int32_t)(j / g.nrb);
       ur.rb = (int32_t)(j % g.nrb);
       int64_t R = (int64_t)g.q_len * A.group;
       int64_t r0 = (int64_t)ur.rb * rpu;
       ur.rows = (int32_t)min((int64_t)rpu, R - r0);
       int i0 = (int)(r0 / A.group), i1 = (int)((r0 + ur.rows - 1) / A.group);
-      RowWin w0 = row_window(i0, g.q_len, g.kv_end, A.causal, A.window);
-      RowWin w1 = row_window(i1, g.q_len, g.kv_end, A.causal, A.window);
+      RowWin w0 = row_window(i0, g.q_len, g.kv_end, g.causal, g.window);
+      RowWin w1 = row_window(i1, g.q_len, g.kv_end, g.causal, g.window);
       ur.lo = w0.lo;  // lo and hi grow with the query row
       ur.hi = max(w1.hi, w0.lo);
       int64_t nt = ur.hi > ur.lo ? ((int64_t)(ur.hi - ur.lo) + tl - 1) / tl : 0;
@@ -255,7 +269,7 @@ __global__ void __launch_bounds__(kSchedThreads) sdpa_sched_kernel(SchedArgs A) 
       int64_t reuse = 0;
       if (g.nrb >= 2 && ur.rb == g.nrb - 1) {
         int64_t span = g.kv_end;
-        if (A.window > 0) span = min(span, (int64_t)g.q_len + A.window - 1);
+        if (g.window > 0) span = min(span, (int64_t)g.q_len + g.window - 1);
         reuse = span * (int64_t)A.D * 4;
       }
       ur.slot_base = reuse;  // kept here until the phase pass below

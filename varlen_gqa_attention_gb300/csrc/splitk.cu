@@ -139,7 +139,7 @@ __device__ __forceinline__ void splitk_unit(const AttnArgs& A, const UnitRec& ur
     live[e] = rl < R;
     if (live[e]) {
       const int i = (int)((r0 + rl) / A.group);
-      RowWin w = row_window(i, sg.q_len, sg.kv_end, A.causal, A.window);
+      RowWin w = row_window(i, sg.q_len, sg.kv_end, sg.causal, sg.window);
       rlo[e] = (int32_t)max((int64_t)w.lo, pos_lo);
       rhi[e] = (int32_t)min((int64_t)w.hi, pos_hi);
     } else {
@@ -350,6 +350,8 @@ __global__ void __launch_bounds__(kSplitkThreads) sdpa_splitk_kernel(AttnArgs A)
     sg.q_len = ur.q_len;
     sg.col = ur.col;
     sg.kv_end = ur.kv_end;
+    sg.causal = ur.causal;
+    sg.window = ur.window;
     const int slot = (int)(blockIdx.x - ur.g_first);
     if (ur.rows <= 16)
       splitk_unit<D, 4>(A, ur, sg, ta, tb, slot, smem, s_ml);

@@ -54,6 +54,8 @@ class Call:
     # call per store); q and seq_info are relative to row_begin.
     row_begin: int = 0
     row_end: Optional[int] = None
+    # int32 [S, 2] = (causal, window) per segment, replacing causal / window when given
+    seg_mode: Optional[np.ndarray] = None
 
 
 @dataclasses.dataclass
@@ -152,8 +154,46 @@ def mixed_step(seed: int = 0, n_target: int = 8, n_draft: int = 8, Hq: int = 32,
                     f"(rows {ring_rows}) + {n_draft} non-causal {max_write}-row draft blocks")
 
 
+def mixed_step_one_store(seed: int = 0, n_target: int = 8, n_draft: int = 8, Hq: int = 32, Hkv: int = 8,
+                         D: int = 128, window: int = 4096, max_write: int = 16, kv_lo: int = 2000,
+                         kv_hi: int = 60000, T: int = 256) -> Workload:
+    """The mixed step of ``mixed_step`` as one call over one ring store: the targets (causal,
+    window W, kv_end far past the ring) and the draft blocks (non-causal, no window, kv_end
+    within the ring) each carry their own mode in ``seg_mode``.
+
+    Rows [0, T/2) hold the targets, packed from row 0; draft block k holds rows
+    T/2 + max_write * k onwards.  Column k holds target k, column n_target + k draft k.
+    """
+    rng = np.random.default_rng(seed)
+    q_len_t = rng.integers(1, max_write + 1, size=n_target)
+    kv_end_t = rng.integers(kv_lo, kv_hi + 1, size=n_target)
+    rows = window + max_write - 1
+    kv_end_d = rng.integers(max_write, rows + 1, size=n_draft)
+    cols = n_target + n_draft + 1
+    half = T // 2
+    gen = torch.Generator().manual_seed(seed)
+    q = _randn_bf16(gen, (T, Hq, D))
+    k = _randn_bf16(gen, (rows, cols, Hkv, D))
+    v = _randn_bf16(gen, (rows, cols, Hkv, D))
+    segs, modes, start = [], [], 0
+    for i in range(n_target):
+        segs.append((start, int(q_len_t[i]), i, int(kv_end_t[i])))
+        modes.append((1, window))
+        start += int(q_len_t[i])
+    for i in range(n_draft):
+        segs.append((half + max_write * i, max_write, n_target + i, int(kv_end_d[i])))
+        modes.append((0, 0))
+    c = Call(T, Hq, Hkv, D, rows, cols, _seq_info(segs), True, 0, 1.0 / math.sqrt(D), q, k, v,
+             seg_mode=np.array(modes, dtype=np.int32))
+    return Workload("mixed_swa_ring_draft_step_one_store", [c],
+                    f"T={T} Hq={Hq} Hkv={Hkv} D={D}: {n_target} causal W={window} segments + {n_draft} "
+                    f"non-causal {max_write}-row draft blocks on one {rows}-row ring store, one launch "
+                    f"(per-segment modes)")
+
+
 def workload(index: int, seed: int = 0) -> Workload:
-    """The five measured shapes, in order: tiny, D=64 prefill, D=128 prefill, decode, mixed."""
+    """The measured shapes, in order: tiny, D=64 prefill, D=128 prefill, decode, mixed, and the
+    mixed step as one call with per-segment modes."""
     if index == 0:
         return tiny_causal_prefill(seed)
     if index == 1:
@@ -164,6 +204,8 @@ def workload(index: int, seed: int = 0) -> Workload:
         return batched_decode(seed)
     if index == 4:
         return mixed_step(seed)
+    if index == 5:
+        return mixed_step_one_store(seed)
     raise ValueError(f"no workload {index}")
 
 

@@ -261,3 +261,25 @@ def test_large_and_odd_head_groups(dev, route, Hq, Hkv):
     call = synth.random_call(rng, D=64, Hq=Hq, Hkv=Hkv, T=40, S=4, rows=300, cols=2, causal=True,
                              window=0, max_q=12, max_kv=300, gen_seed=Hq + Hkv)
     check_call(call, dev, tag=f"Hq{Hq}/Hkv{Hkv}")
+
+
+@pytest.mark.parametrize("T,Hq,Hkv,segs", [
+    # more packed rows than the scheduler's shared-memory owner map, and more units
+    (9000, 16, 2, [(0, 4000, 0, 4000), (4000, 3000, 1, 7000), (7000, 2000, 2, 9500)]),
+    # rows within the owner map, units beyond the shared-memory unit table
+    (8000, 32, 4, [(0, 5000, 0, 5000), (5000, 2990, 2, 8000)]),
+])
+def test_more_rows_and_units_than_the_scheduler_stages(dev, route, T, Hq, Hkv, segs):
+    D, rows, cols = 64, 10000, 3
+    g = torch.Generator().manual_seed(T + Hq)
+    q = torch.randn(T, Hq, D, generator=g).to(torch.bfloat16)
+    k = torch.randn(rows, cols, Hkv, D, generator=g).to(torch.bfloat16)
+    v = torch.randn(rows, cols, Hkv, D, generator=g).to(torch.bfloat16)
+    call = synth.Call(T, Hq, Hkv, D, rows, cols, np.array(segs, dtype=np.int32), True, 0,
+                      1.0 / np.sqrt(D), q, k, v)
+    rng = np.random.default_rng(T)
+    sample = set(rng.choice(T, size=120, replace=False).tolist())
+    for (qs, ql, _, _) in segs:  # segment edges and the uncovered tail
+        sample.update([qs, qs + ql - 1])
+    sample.update(range(T - 12, T))
+    check_call(call, dev, rows_subset=sorted(sample), tag=f"T={T}")

@@ -67,6 +67,16 @@ static sdpa_status device_info(DevInfo* out) {
   if (!di.ready) {
     e = cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return fail(SDPA_ERR_CUDA, "SM count: %s", cudaGetErrorString(e));
+    e = cudaFuncSetAttribute(sched_kernel_ptr(), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)sched_smem_bytes());
+    if (e != cudaSuccess) return fail(SDPA_ERR_CUDA, "scheduler smem attribute: %s", cudaGetErrorString(e));
+    // every kernel of a call asks for the whole shared-memory carveout, so that the SMs keep
+    // one L1 / shared split from kernel to kernel
+    const void* others[3] = {sched_kernel_ptr(), append_kernel_ptr(), clone_kernel_ptr()};
+    for (const void* f : others) {
+      e = cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+      if (e != cudaSuccess) return fail(SDPA_ERR_CUDA, "carveout attribute: %s", cudaGetErrorString(e));
+    }
     const int Ds[3] = {64, 128, 256};
     for (int k = 0; k < 3; ++k) {
       const void* f = splitk_kernel_ptr(Ds[k]);
@@ -80,8 +90,11 @@ static sdpa_status device_info(DevInfo* out) {
       e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, f, kSplitkThreads, smem);
       if (e != cudaSuccess) return fail(SDPA_ERR_CUDA, "occupancy: %s", cudaGetErrorString(e));
       di.splitk_per_sm[k] = nb > 0 ? nb : 1;
+      e = cudaFuncSetAttribute(combine_kernel_ptr(Ds[k]), cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+      if (e != cudaSuccess) return fail(SDPA_ERR_CUDA, "carveout attribute: %s", cudaGetErrorString(e));
       const void* pf = prefill_kernel_ptr(Ds[k]);
       e = cudaFuncSetAttribute(pf, cudaFuncAttributeMaxDynamicSharedMemorySize, prefill_smem_bytes(Ds[k]));
+      if (e == cudaSuccess) e = cudaFuncSetAttribute(pf, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
       di.prefill_ok[k] = e == cudaSuccess;
       if (e != cudaSuccess) cudaGetLastError();  // leave no sticky error; split-K covers it
     }
@@ -190,7 +203,7 @@ static sdpa_status launch_all(const SchedArgs& sa, const AttnArgs& aa, int D, co
   cudaError_t e = mark(0, st);
   if (e == cudaSuccess) {
     void* args[] = {(void*)&sa};
-    e = cudaLaunchKernel(sched_kernel_ptr(), dim3(1), dim3(kSchedThreads), args, 0, st);
+    e = cudaLaunchKernel(sched_kernel_ptr(), dim3(1), dim3(kSchedThreads), args, sched_smem_bytes(), st);
     if (e != cudaSuccess) return fail(SDPA_ERR_CUDA, "scheduler launch: %s", cudaGetErrorString(e));
   }
   if (e == cudaSuccess && ap && sa.S > 0) {

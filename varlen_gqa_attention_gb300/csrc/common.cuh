@@ -187,10 +187,11 @@ struct SchedArgs {
   int32_t* status_dev;
 };
 
-constexpr int kSchedThreads = 1024;
+constexpr int kSchedThreads = 512;
 
 // Kernel entry points (defined in their own translation units).
 const void* sched_kernel_ptr();
+size_t sched_smem_bytes();  // dynamic shared memory of the scheduler kernel
 const void* append_kernel_ptr();
 const void* clone_kernel_ptr();
 const void* splitk_kernel_ptr(int D);

@@ -58,6 +58,9 @@ sdpa_status static_setup(StaticDev* out) {
     }
     if (cudaDeviceGetAttribute(&sd.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
       return static_fail(SDPA_ERR_CUDA, "SM count query failed");
+    if (cudaFuncSetAttribute(sched_kernel_ptr(), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)sched_smem_bytes()) != cudaSuccess)
+      return static_fail(SDPA_ERR_CUDA, "scheduler kernel setup failed");
     const int Ds[3] = {64, 128, 256};
     for (int k = 0; k < 3; ++k) {
       const void* f = splitk_kernel_ptr(Ds[k]);
@@ -193,7 +196,7 @@ extern "C" sdpa_status sdpa_varlen_splitk_static(
   cudaError_t e;
   {
     void* args[] = {(void*)&sa};
-    e = cudaLaunchKernel(sched_kernel_ptr(), dim3(1), dim3(kSchedThreads), args, 0, s);
+    e = cudaLaunchKernel(sched_kernel_ptr(), dim3(1), dim3(kSchedThreads), args, sched_smem_bytes(), s);
   }
   if (e == cudaSuccess) {
     void* args[] = {(void*)&aa};

@@ -14,37 +14,47 @@
 //      of key tiles whatever the length mix; G is capped at W so that no CTA is idle inside
 //      a unit's range), and each (unit, CTA) pair gets a slot of
 //      partial results unless the unit has a single CTA, which then writes `out` itself.
-// One CTA of 1024 threads does all of it; block-wide scans give the prefix sums.
+// One CTA of 512 threads does all of it; block-wide scans give the prefix sums.
 #include "common.cuh"
 
 namespace sdpa {
 
 
-// Exclusive block scan of one int64 per thread; returns the prefix, writes the total.
-__device__ int64_t block_excl_scan(int64_t v, int64_t* total, int64_t* sh /*[33]*/) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int64_t x = v;
+// Exclusive block scan of N int64 values per thread (N <= warps): v becomes this thread's
+// prefix, tot the block totals.  Warp k scans the warp totals of value k, so the N scans
+// cost the barriers of one.
+template <int N>
+__device__ void block_scan(int64_t (&v)[N], int64_t (&tot)[N], int64_t* sh /*[N * 32]*/) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  int64_t x[N];
 #pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    int64_t y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
-  }
-  if (lane == 31) sh[warp] = x;
-  __syncthreads();
-  if (warp == 0) {
-    int64_t w = lane < (int)(blockDim.x >> 5) ? sh[lane] : 0;
+  for (int k = 0; k < N; ++k) {
+    x[k] = v[k];
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      int64_t y = __shfl_up_sync(0xffffffffu, w, o);
-      if (lane >= o) w += y;
+      const int64_t y = __shfl_up_sync(0xffffffffu, x[k], o);
+      if (lane >= o) x[k] += y;
     }
-    sh[lane] = w;  // inclusive warp totals
+    if (lane == 31) sh[k * 32 + warp] = x[k];
   }
   __syncthreads();
-  int64_t base = warp > 0 ? sh[warp - 1] : 0;
-  if (total) *total = sh[(blockDim.x >> 5) - 1];
+  if (warp < N) {
+    int64_t w = lane < nw ? sh[warp * 32 + lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int64_t y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    if (lane < nw) sh[warp * 32 + lane] = w;  // inclusive warp totals
+  }
   __syncthreads();
-  return base + x - v;
+#pragma unroll
+  for (int k = 0; k < N; ++k) {
+    const int64_t base = warp > 0 ? sh[k * 32 + warp - 1] : 0;
+    tot[k] = sh[k * 32 + nw - 1];
+    v[k] = base + x[k] - v[k];
+  }
+  __syncthreads();
 }
 
 // Contiguous range of n items owned by this thread.
@@ -91,24 +101,39 @@ __device__ __forceinline__ int route_of(const SchedArgs& A, const SegRec& r) {
   return R >= kPrefillRows ? kRoutePrefill : kRouteSplitk;
 }
 
-// Segment tables up to this size are staged in shared memory, so the walk below is a few
-// block-wide steps instead of chains of dependent global loads; larger tables are read from
-// the workspace copy.
+// Shared-memory staging: segment tables of up to kSegCache rows, the row-owner map of up
+// to kRowCache packed rows and up to kUnitCache units (both routes) are built in shared
+// memory, so the walk is a chain of block-wide steps with no global round trips, and the
+// records are written out once at the end.  Larger calls keep the same steps on the
+// workspace copies in global memory.
 constexpr int kSegCache = 1024;
+constexpr int kRowCache = 8192;
+constexpr int kUnitCache = 1024;
+constexpr size_t kSchedSmem = (size_t)kSegCache * (16 + 8 + 8 + 8 + 4 + 4) + (size_t)kRowCache * 4 +
+                              (size_t)kUnitCache * sizeof(UnitRec);
 
 __global__ void __launch_bounds__(kSchedThreads) sdpa_sched_kernel(SchedArgs A) {
-  __shared__ int64_t sh[33];
+  extern __shared__ __align__(16) unsigned char smem[];
+  __shared__ int64_t sh[4 * 32];
+  __shared__ int64_t s_pb[3][kMaxPhases + 1];
+  __shared__ int64_t s_U[3], s_np[3];
   __shared__ int32_t s_status;
-  __shared__ int64_t s_tot[3];
-  __shared__ int4 c_seg[kSegCache];  // (q_start, q_len, col, kv_end)
-  __shared__ int32_t c_bits[kSegCache];
-  __shared__ int2 c_rn[kSegCache];   // (route, nrb)
-  __shared__ int2 c_ub[kSegCache];   // unit bases of routes 1 and 2
-  __shared__ int2 c_mode[kSegCache]; // (causal, window)
+  int4* c_seg = reinterpret_cast<int4*>(smem);      // (q_start, q_len, col, kv_end)
+  int2* c_mode = reinterpret_cast<int2*>(c_seg + kSegCache);  // (causal, window)
+  int2* c_rn = c_mode + kSegCache;                  // (route, nrb)
+  int2* c_ub = c_rn + kSegCache;                    // unit bases on routes 1 and 2
+  int32_t* c_bits = reinterpret_cast<int32_t*>(c_ub + kSegCache);
+  int32_t* c_flag = c_bits + kSegCache;             // overlap flags
+  int32_t* c_row = c_flag + kSegCache;              // packed row -> owning segment
+  UnitRec* c_unit = reinterpret_cast<UnitRec*>(c_row + kRowCache);
+
   const Workspace& W = A.ws;
   const int S = A.S;
   const int64_t T = A.T;
   const bool cached = S <= kSegCache;
+  const bool rows_cached = cached && T <= kRowCache;
+  int32_t* row_map = rows_cached ? c_row : W.row_seg;
+  int32_t* flag = cached ? c_flag : W.seg_flag;
   griddep_launch();  // the attention kernels may start launching; they wait for this grid
   if (threadIdx.x == 0) s_status = 0;
   __syncthreads();
@@ -123,23 +148,23 @@ __global__ void __launch_bounds__(kSchedThreads) sdpa_sched_kernel(SchedArgs A) 
       md.x = md.x != 0;
     }
     const int32_t bits = segment_bits(g[0], g[1], g[2], g[3], T, A.rows, A.cols, md.y);
-    SegRec r;
-    r.q_start = g[0]; r.q_len = g[1]; r.col = g[2]; r.kv_end = g[3];
-    r.route = kRouteNone; r.nrb = 0; r.bits = bits; r.pad = 0;
-    r.ubase[0] = r.ubase[1] = r.ubase[2] = r.ubase[3] = 0;
-    r.causal = md.x;
-    r.window = md.y;
-    r.pad2[0] = r.pad2[1] = 0;
-    W.segs[s] = r;
-    W.seg_flag[s] = 0;
     if (cached) {
       c_seg[s] = make_int4(g[0], g[1], g[2], g[3]);
       c_bits[s] = bits;
       c_mode[s] = md;
+    } else {
+      SegRec r;
+      r.q_start = g[0]; r.q_len = g[1]; r.col = g[2]; r.kv_end = g[3];
+      r.route = kRouteNone; r.nrb = 0; r.bits = bits; r.pad = 0;
+      r.ubase[0] = r.ubase[1] = r.ubase[2] = r.ubase[3] = 0;
+      r.causal = md.x; r.window = md.y;
+      r.pad2[0] = r.pad2[1] = 0;
+      W.segs[s] = r;
     }
+    flag[s] = 0;
     if (bits) atomicOr(&s_status, bits);
   }
-  for (int64_t t = threadIdx.x; t < T; t += blockDim.x) W.row_seg[t] = -1;
+  for (int64_t t = threadIdx.x; t < T; t += blockDim.x) row_map[t] = -1;
   __syncthreads();
   auto seg_of = [&](int s) -> int4 {
     if (cached) return c_seg[s];
@@ -159,27 +184,28 @@ __global__ void __launch_bounds__(kSchedThreads) sdpa_sched_kernel(SchedArgs A) 
       if (bits_of(s)) continue;
       const int4 g = seg_of(s);
       for (int i = ti; i < g.y; i += team) {
-        const int old = atomicCAS(&W.row_seg[g.x + i], -1, s);
+        const int old = atomicCAS(&row_map[g.x + i], -1, s);
         if (old != -1) {
-          atomicExch(&W.seg_flag[s], 1);
-          atomicExch(&W.seg_flag[old], 1);
+          atomicExch(&flag[s], 1);
+          atomicExch(&flag[old], 1);
         }
       }
     }
   }
   __syncthreads();
 
-  // 3. route each live segment and count its units (contiguous segment ranges per thread)
+  // 3. route each live segment and count its units (contiguous segment ranges per thread);
+  // the finished owner map goes out for the combine pass
   int64_t sa, sb;
   my_range(S, &sa, &sb);
-  int64_t cnt[3] = {0, 0, 0};
+  int64_t cnt[2] = {0, 0};  // units on routes 1 and 2
   for (int64_t s = sa; s < sb; ++s) {
     const int32_t bits = bits_of((int)s);
-    const int flag = W.seg_flag[s];
-    if (bits == 0 && flag) atomicOr(&s_status, SDPA_SEG_OVERLAP);
+    const int fl = flag[s];
+    if (bits == 0 && fl) atomicOr(&s_status, SDPA_SEG_OVERLAP);
     const int4 g = seg_of((int)s);
     int route = kRouteNone, nrb = 0;
-    if (bits == 0 && !flag && g.y > 0) {
+    if (bits == 0 && !fl && g.y > 0) {
       SegRec r;
       r.q_start = g.x; r.q_len = g.y; r.col = g.z; r.kv_end = g.w;
       r.window = cached ? c_mode[s].y : W.segs[s].window;
@@ -187,160 +213,215 @@ __global__ void __launch_bounds__(kSchedThreads) sdpa_sched_kernel(SchedArgs A) 
       route = route_of(A, r);
       const int rpu = rows_per_unit(route);
       nrb = (int)((R + rpu - 1) / rpu);
-      cnt[route] += (int64_t)A.Hkv * nrb;
+      cnt[route - 1] += (int64_t)A.Hkv * nrb;
     }
-    W.segs[s].route = route;
-    W.segs[s].nrb = nrb;
-    if (cached) c_rn[s] = make_int2(route, nrb);
+    if (cached) {
+      c_rn[s] = make_int2(route, nrb);
+    } else {
+      W.segs[s].route = route;
+      W.segs[s].nrb = nrb;
+    }
   }
-  int64_t ubase[3];
-  for (int q = 1; q < 3; ++q) {
-    int64_t tot;
-    ubase[q] = block_excl_scan(cnt[q], &tot, sh);
+  if (rows_cached)
+    for (int64_t t = threadIdx.x; t < T; t += blockDim.x) W.row_seg[t] = c_row[t];
+  {
+    int64_t tot[2];
+    block_scan<2>(cnt, tot, sh);
     // Live segments cover disjoint rows, so tot <= unit_cap; units past the cap (none)
     // would simply not be generated.
-    if (threadIdx.x == 0) s_tot[q] = min(tot, W.unit_cap[q]);
+    if (threadIdx.x == 0) {
+      s_U[1] = min(tot[0], W.unit_cap[1]);
+      s_U[2] = min(tot[1], W.unit_cap[2]);
+    }
   }
   for (int64_t s = sa; s < sb; ++s) {
-    W.segs[s].ubase[1] = (int32_t)ubase[1];
-    W.segs[s].ubase[2] = (int32_t)ubase[2];
-    if (cached) c_ub[s] = make_int2((int32_t)ubase[1], (int32_t)ubase[2]);
-    const int2 rn = cached ? c_rn[s] : make_int2(W.segs[s].route, W.segs[s].nrb);
-    if (rn.x != kRouteNone) ubase[rn.x] += (int64_t)A.Hkv * rn.y;
+    int2 rn;
+    if (cached) {
+      c_ub[s] = make_int2((int32_t)cnt[0], (int32_t)cnt[1]);
+      rn = c_rn[s];
+    } else {
+      W.segs[s].ubase[1] = (int32_t)cnt[0];
+      W.segs[s].ubase[2] = (int32_t)cnt[1];
+      rn = make_int2(W.segs[s].route, W.segs[s].nrb);
+    }
+    if (rn.x != kRouteNone) cnt[rn.x - 1] += (int64_t)A.Hkv * rn.y;
   }
   __syncthreads();
 
-  // 4. per route: units, their tiles, the stream-K split and partial slots
-  for (int q = 1; q < 3; ++q) {
-    const int64_t U = s_tot[q];
+  // 4. the units of both routes in one index space, [0, U1) on route 1 and [U1, U1 + U2) on
+  // route 2, each thread a contiguous range: records, key tiles and re-read bytes, then
+  // each unit's place on its route's tile line and its phase
+  const int64_t U1 = s_U[1], U2 = s_U[2], U = U1 + U2;
+  const bool units_cached = U <= kUnitCache;
+  UnitRec* ubuf1 = units_cached ? c_unit : W.units[1];
+  UnitRec* ubuf2 = units_cached ? c_unit + U1 : W.units[2];
+  auto unit_at = [&](int64_t u) -> UnitRec& { return u < U1 ? ubuf1[u] : ubuf2[u - U1]; };
+  int64_t ua, ub;
+  my_range(U, &ua, &ub);
+  int64_t acc[4] = {0, 0, 0, 0};  // key-line tiles on routes 1, 2; re-read bytes on routes 1, 2
+  for (int64_t u = ua; u < ub; ++u) {
+    const int q = u < U1 ? 1 : 2;
+    const int64_t uq = q == 1 ? u : u - U1;
     const int rpu = rows_per_unit(q), tl = tile_len(A, q);
-    const int64_t lead = lead_tiles(q);
-    UnitRec* units = W.units[q];
-    int64_t ua, ub;
-    my_range(U, &ua, &ub);
-    int64_t my_tiles = 0, my_bytes = 0;
-    for (int64_t u = ua; u < ub; ++u) {
-      // owning segment: the last one whose route-q unit base is <= u
-      int lo = 0, hi = S - 1, s = 0;
-      while (lo <= hi) {
-        const int mid = (lo + hi) >> 1;
-        const int32_t ubm = cached ? (q == 1 ? c_ub[mid].x : c_ub[mid].y) : W.segs[mid].ubase[q];
-        if (ubm <= u) { s = mid; lo = mid + 1; } else { hi = mid - 1; }
-      }
-      SegRec g;
-      if (cached) {
-        const int4 c = c_seg[s];
-        g.q_start = c.x; g.q_len = c.y; g.col = c.z; g.kv_end = c.w;
-        g.nrb = c_rn[s].y;
-        g.ubase[q] = q == 1 ? c_ub[s].x : c_ub[s].y;
-        g.causal = c_mode[s].x;
-        g.window = c_mode[s].y;
-      } else {
-        g = W.segs[s];
-      }
-      UnitRec ur;
-      int64_t j = u - g.ubase[q];
-      ur.seg = s;
-      ur.q_start = g.q_start;
-      ur.q_len = g.q_len;
-      ur.col = g.col;
-      ur.kv_end = g.kv_end;
-      ur.causal = g.causal;
-      ur.window = g.window;
-      ur.hk = (int32_t)(j / g.nrb);
-      ur.rb = (int32_t)(j % g.nrb);
-      int64_t R = (int64_t)g.q_len * A.group;
-      int64_t r0 = (int64_t)ur.rb * rpu;
-      ur.rows = (int32_t)min((int64_t)rpu, R - r0);
-      int i0 = (int)(r0 / A.group), i1 = (int)((r0 + ur.rows - 1) / A.group);
-      RowWin w0 = row_window(i0, g.q_len, g.kv_end, g.causal, g.window);
-      RowWin w1 = row_window(i1, g.q_len, g.kv_end, g.causal, g.window);
-      ur.lo = w0.lo;  // lo and hi grow with the query row
-      ur.hi = max(w1.hi, w0.lo);
-      int64_t nt = ur.hi > ur.lo ? ((int64_t)(ur.hi - ur.lo) + tl - 1) / tl : 0;
-      ur.nslots = 0;
-      ur.g_first = 0;
-      ur.ntiles = (int32_t)nt;
-      ur.phase = 0;
-      const int64_t span_tiles = nt > 0 ? nt + lead : 0;
-      ur.tile_base = span_tiles;  // the span, until the scan below
-      // K/V bytes the group's units read again (counted once, on the group's last unit;
-      // only groups of several units re-read them): phases are cut on these
-      int64_t reuse = 0;
-      if (g.nrb >= 2 && ur.rb == g.nrb - 1) {
-        int64_t span = g.kv_end;
-        if (g.window > 0) span = min(span, (int64_t)g.q_len + g.window - 1);
-        reuse = span * (int64_t)A.D * 4;
-      }
-      ur.slot_base = reuse;  // kept here until the phase pass below
-      units[u] = ur;
-      my_tiles += span_tiles;
-      my_bytes += reuse;
+    // owning segment: the last one whose route-q unit base is <= uq
+    int lo = 0, hi = S - 1, s = 0;
+    while (lo <= hi) {
+      const int mid = (lo + hi) >> 1;
+      const int32_t ubm = cached ? (q == 1 ? c_ub[mid].x : c_ub[mid].y) : W.segs[mid].ubase[q];
+      if (ubm <= uq) { s = mid; lo = mid + 1; } else { hi = mid - 1; }
     }
-    int64_t Wt, Bt;
-    int64_t tb = block_excl_scan(my_tiles, &Wt, sh);
-    int64_t bb = block_excl_scan(my_bytes, &Bt, sh);
-    for (int64_t u = ua; u < ub; ++u) {
-      UnitRec ur = units[u];
-      const int64_t nt = ur.tile_base, reuse = ur.slot_base;  // span and re-read bytes
-      ur.tile_base = tb;
-      ur.phase = (int32_t)min(bb / kPhaseBytes, (int64_t)kMaxPhases - 1);
-      tb += nt;
-      bb += reuse;
-      units[u] = ur;
+    SegRec g;
+    if (cached) {
+      const int4 c = c_seg[s];
+      g.q_start = c.x; g.q_len = c.y; g.col = c.z; g.kv_end = c.w;
+      g.nrb = c_rn[s].y;
+      g.ubase[q] = q == 1 ? c_ub[s].x : c_ub[s].y;
+      g.causal = c_mode[s].x;
+      g.window = c_mode[s].y;
+    } else {
+      g = W.segs[s];
     }
-    __syncthreads();
-    // phase bases: phase k starts at the first unit whose phase is >= k
-    for (int64_t u = ua; u < ub; ++u) {
-      const int cp = units[u].phase, pp = u > 0 ? units[u - 1].phase : -1;
-      for (int k = pp + 1; k <= cp; ++k) W.hdr->phase_base[q][k] = units[u].tile_base;
+    UnitRec ur;
+    const int64_t j = uq - g.ubase[q];
+    ur.seg = s;
+    ur.q_start = g.q_start;
+    ur.q_len = g.q_len;
+    ur.col = g.col;
+    ur.kv_end = g.kv_end;
+    ur.causal = g.causal;
+    ur.window = g.window;
+    ur.hk = (int32_t)(j / g.nrb);
+    ur.rb = (int32_t)(j % g.nrb);
+    const int64_t R = (int64_t)g.q_len * A.group;
+    const int64_t r0 = (int64_t)ur.rb * rpu;
+    ur.rows = (int32_t)min((int64_t)rpu, R - r0);
+    const int i0 = (int)(r0 / A.group), i1 = (int)((r0 + ur.rows - 1) / A.group);
+    const RowWin w0 = row_window(i0, g.q_len, g.kv_end, g.causal, g.window);
+    const RowWin w1 = row_window(i1, g.q_len, g.kv_end, g.causal, g.window);
+    ur.lo = w0.lo;  // lo and hi grow with the query row
+    ur.hi = max(w1.hi, w0.lo);
+    const int64_t nt = ur.hi > ur.lo ? ((int64_t)(ur.hi - ur.lo) + tl - 1) / tl : 0;
+    ur.nslots = 0;
+    ur.g_first = 0;
+    ur.ntiles = (int32_t)nt;
+    ur.phase = 0;
+    const int64_t span_tiles = nt > 0 ? nt + lead_tiles(q) : 0;
+    ur.tile_base = span_tiles;  // the span, until the scan below
+    // K/V bytes the group's units read again (counted once, on the group's last unit;
+    // only groups of several units re-read them): phases are cut on these
+    int64_t reuse = 0;
+    if (g.nrb >= 2 && ur.rb == g.nrb - 1) {
+      int64_t span = g.kv_end;
+      if (g.window > 0) span = min(span, (int64_t)g.q_len + g.window - 1);
+      reuse = span * (int64_t)A.D * 4;
     }
-    if (threadIdx.x == 0) {
-      const int64_t np = U > 0 ? units[U - 1].phase + 1 : 0;
-      W.hdr->nphase[q] = np;
-      W.hdr->phase_base[q][0] = 0;
-      W.hdr->phase_base[q][np] = Wt;
+    ur.slot_base = reuse;  // kept here until the phase pass below
+    unit_at(u) = ur;
+    acc[q - 1] += span_tiles;
+    acc[q + 1] += reuse;
+  }
+  int64_t tot4[4];
+  block_scan<4>(acc, tot4, sh);
+  for (int64_t u = ua; u < ub; ++u) {
+    const int q = u < U1 ? 1 : 2;
+    UnitRec& ur = unit_at(u);
+    const int64_t span = ur.tile_base, reuse = ur.slot_base;
+    ur.tile_base = acc[q - 1];
+    ur.phase = (int32_t)min(acc[q + 1] / kPhaseBytes, (int64_t)kMaxPhases - 1);
+    acc[q - 1] += span;
+    acc[q + 1] += reuse;
+  }
+  __syncthreads();
+
+  // 5. phase bases: phase k of a route starts at the first unit whose phase is >= k
+  for (int64_t u = ua; u < ub; ++u) {
+    const int q = u < U1 ? 1 : 2;
+    const int64_t uq = q == 1 ? u : u - U1;
+    const int cp = unit_at(u).phase, pp = uq > 0 ? unit_at(u - 1).phase : -1;
+    for (int k = pp + 1; k <= cp; ++k) s_pb[q][k] = unit_at(u).tile_base;
+  }
+  if (threadIdx.x < 2) {
+    const int q = 1 + threadIdx.x;
+    const int64_t Uq = s_U[q];
+    const int64_t np = Uq > 0 ? unit_at(q == 1 ? Uq - 1 : U1 + Uq - 1).phase + 1 : 0;
+    s_np[q] = np;
+    s_pb[q][0] = 0;
+    s_pb[q][np] = tot4[q - 1];
+  }
+  __syncthreads();
+
+  // 6. stream-K within each phase: CTA g of G_p = min(G, W_p) owns [g W_p / G_p, (g+1) W_p / G_p);
+  // G_p <= W_p makes every working CTA own a tile, so the owners of a unit's tiles are
+  // consecutive CTAs that all work on it (nslots is exact)
+  int64_t prow[2] = {0, 0};  // partial rows on routes 1, 2
+  for (int64_t u = ua; u < ub; ++u) {
+    const int q = u < U1 ? 1 : 2;
+    const int64_t uq = q == 1 ? u : u - U1;
+    UnitRec& ur = unit_at(u);
+    const int64_t nt = ur.ntiles;
+    if (nt > 0) {
+      const int64_t G = A.grid[q];
+      const int64_t lead = lead_tiles(q);
+      const int64_t b0 = s_pb[q][ur.phase];
+      const int64_t Wp = s_pb[q][ur.phase + 1] - b0;
+      const int64_t Gp = min(G, Wp);
+      const int64_t k0 = ur.tile_base + lead - b0;  // the key tiles, phase-relative
+      const int64_t g0 = sk_owner(k0, Wp, Gp);
+      const int64_t g1 = sk_owner(k0 + nt - 1, Wp, Gp);
+      ur.g_first = (int32_t)g0;
+      ur.nslots = (int32_t)(g1 - g0 + 1);
+      if (ur.nslots > 1) prow[q - 1] += (int64_t)ur.nslots * ur.rows;
+      // CTAs whose share starts inside this unit's span begin their walk here
+      const int64_t s0 = ur.tile_base - b0, s1 = k0 + nt;
+      for (int64_t c = sk_owner(s0, Wp, Gp); c <= sk_owner(s1 - 1, Wp, Gp); ++c)
+        if (sk_start(c, Wp, Gp) >= s0) W.first_unit[q][ur.phase * G + c] = (int32_t)uq;
     }
-    __syncthreads();
-    // stream-K within each phase: CTA g of G_p = min(G, W_p) owns [g W_p / G_p, (g+1) W_p / G_p);
-    // G_p <= W_p makes every working CTA own a tile, so the owners of a unit's tiles are
-    // consecutive CTAs that all work on it (nslots is exact)
-    const int64_t G = A.grid[q];
-    int64_t my_rows = 0;
-    for (int64_t u = ua; u < ub; ++u) {
-      UnitRec ur = units[u];
-      const int64_t nt = ur.ntiles;
-      if (nt > 0) {
-        const int64_t b0 = W.hdr->phase_base[q][ur.phase];
-        const int64_t Wp = W.hdr->phase_base[q][ur.phase + 1] - b0;
-        const int64_t Gp = min(G, Wp);
-        const int64_t k0 = ur.tile_base + lead - b0;  // the key tiles, phase-relative
-        const int64_t g0 = sk_owner(k0, Wp, Gp);
-        const int64_t g1 = sk_owner(k0 + nt - 1, Wp, Gp);
-        ur.g_first = (int32_t)g0;
-        ur.nslots = (int32_t)(g1 - g0 + 1);
-        if (ur.nslots > 1) my_rows += (int64_t)ur.nslots * ur.rows;
-        // CTAs whose share starts inside this unit's span begin their walk here
-        const int64_t s0 = ur.tile_base - b0, s1 = k0 + nt;
-        for (int64_t g = sk_owner(s0, Wp, Gp); g <= sk_owner(s1 - 1, Wp, Gp); ++g)
-          if (sk_start(g, Wp, Gp) >= s0) W.first_unit[q][ur.phase * G + g] = (int32_t)u;
-      }
-      units[u] = ur;
+  }
+  {
+    int64_t tot[2];
+    block_scan<2>(prow, tot, sh);
+  }
+  for (int64_t u = ua; u < ub; ++u) {
+    const int q = u < U1 ? 1 : 2;
+    UnitRec& ur = unit_at(u);
+    ur.slot_base = prow[q - 1];
+    if (ur.nslots > 1) prow[q - 1] += (int64_t)ur.nslots * ur.rows;
+  }
+  __syncthreads();
+
+  // 7. write the shared-memory records out, then the header
+  if (units_cached) {
+    const int4* src = reinterpret_cast<const int4*>(c_unit);
+    constexpr int kWords = (int)(sizeof(UnitRec) / 16);
+    for (int64_t i = threadIdx.x; i < U * kWords; i += blockDim.x) {
+      int4* dst = i < U1 * kWords ? reinterpret_cast<int4*>(W.units[1]) + i
+                                  : reinterpret_cast<int4*>(W.units[2]) + (i - U1 * kWords);
+      *dst = src[i];
     }
-    int64_t Pt;
-    int64_t pb = block_excl_scan(my_rows, &Pt, sh);
-    for (int64_t u = ua; u < ub; ++u) {
-      units[u].slot_base = pb;
-      UnitRec ur = units[u];
-      if (ur.nslots > 1) pb += (int64_t)ur.nslots * ur.rows;
+  }
+  if (cached) {
+    for (int s = threadIdx.x; s < S; s += blockDim.x) {
+      const int4 c = c_seg[s];
+      SegRec r;
+      r.q_start = c.x; r.q_len = c.y; r.col = c.z; r.kv_end = c.w;
+      r.route = c_rn[s].x; r.nrb = c_rn[s].y; r.bits = c_bits[s]; r.pad = 0;
+      r.ubase[0] = 0; r.ubase[1] = c_ub[s].x; r.ubase[2] = c_ub[s].y; r.ubase[3] = 0;
+      r.causal = c_mode[s].x; r.window = c_mode[s].y;
+      r.pad2[0] = r.pad2[1] = 0;
+      W.segs[s] = r;
     }
-    if (threadIdx.x == 0) {
-      W.hdr->tiles[q] = Wt;
-      W.hdr->units[q] = U;
-      W.hdr->grid[q] = G;
-      W.hdr->lead[q] = lead;
-    }
-    __syncthreads();
+  }
+  for (int i = threadIdx.x; i < 2 * (kMaxPhases + 1); i += blockDim.x) {
+    const int q = 1 + i / (kMaxPhases + 1), k = i % (kMaxPhases + 1);
+    if (k <= s_np[q]) W.hdr->phase_base[q][k] = s_pb[q][k];
+  }
+  if (threadIdx.x < 2) {
+    const int q = 1 + threadIdx.x;
+    W.hdr->tiles[q] = s_pb[q][s_np[q]];
+    W.hdr->units[q] = s_U[q];
+    W.hdr->grid[q] = A.grid[q];
+    W.hdr->lead[q] = lead_tiles(q);
+    W.hdr->nphase[q] = s_np[q];
   }
   if (threadIdx.x == 0) {
     W.hdr->status = s_status;
@@ -349,5 +430,6 @@ __global__ void __launch_bounds__(kSchedThreads) sdpa_sched_kernel(SchedArgs A) 
 }
 
 const void* sched_kernel_ptr() { return (const void*)sdpa_sched_kernel; }
+size_t sched_smem_bytes() { return kSchedSmem; }
 
 }  // namespace sdpa

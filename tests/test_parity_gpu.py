@@ -283,3 +283,38 @@ def test_more_rows_and_units_than_the_scheduler_stages(dev, route, T, Hq, Hkv, s
         sample.update([qs, qs + ql - 1])
     sample.update(range(T - 12, T))
     check_call(call, dev, rows_subset=sorted(sample), tag=f"T={T}")
+
+
+def _multi_phase_prefill_call():
+    # 8 prefill segments of 512 rows over 16384 keys each: 16 (segment, KV head) groups whose
+    # units re-read 8 MB of K/V each, so the tile line is cut into several phases
+    S, ql, kv, Hq, Hkv, D = 8, 512, 16384, 16, 2, 128
+    g = torch.Generator().manual_seed(88)
+    q = torch.randn(S * ql, Hq, D, generator=g).to(torch.bfloat16)
+    k = torch.randn(kv, S, Hkv, D, generator=g).to(torch.bfloat16)
+    v = torch.randn(kv, S, Hkv, D, generator=g).to(torch.bfloat16)
+    si = np.array([(s * ql, ql, s, kv) for s in range(S)], dtype=np.int32)
+    return synth.Call(S * ql, Hq, Hkv, D, kv, S, si, True, 0, 1.0 / np.sqrt(D), q, k, v)
+
+
+@pytest.mark.parametrize("which", ["draft_blocks", "prefill_groups"])
+def test_multi_phase_calls_stay_inside_the_workspace(dev, route, which):
+    # several phases add (unit, CTA) pairs; the partial slots must hold them all and no byte
+    # past the workspace may change
+    call = synth.mixed_step(seed=2).calls[1] if which == "draft_blocks" else _multi_phase_prefill_call()
+    n = pkg.workspace_bytes(call.T, call.Hq, call.Hkv, call.D, len(call.seq_info))
+    big = torch.full((n + (1 << 20),), 0xA5, dtype=torch.uint8, device=dev)
+    ws = big[:n]
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    got = pkg.sdpa_varlen(call.q.to(dev), call.k_store.to(dev), call.v_store.to(dev),
+                          torch.from_numpy(call.seq_info).to(dev), causal=call.causal, window=call.window,
+                          scale=call.scale, workspace=ws, status=status)
+    torch.cuda.synchronize()
+    assert bool((big[n:] == 0xA5).all()), "bytes past the workspace changed"
+    rng = np.random.default_rng(3)
+    rows = np.unique(np.concatenate([rng.choice(call.T, size=96, replace=False),
+                                     call.seq_info[:, 0], call.seq_info[:, 0] + call.seq_info[:, 1] - 1]))
+    ref, seg_id, st = oracle(call, rows_subset=rows)
+    _, lo, hi, _ = O.visible_interval(call.seq_info, call.T, call.causal, call.window, call.rows, call.cols)
+    assert int(status.item()) == st
+    assert_matches(got, ref, seg_id, lo, hi, rows=rows, tag=which)

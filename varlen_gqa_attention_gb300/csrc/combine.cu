@@ -1,10 +1,12 @@
 // combine.cu - log-sum-exp merge of split partials, and zero rows.
 //
-// One warp per (packed row t, query head h):
+// Runs only when the scheduler found work for it (combine_work); then one warp per
+// (packed row t, query head h):
 //   * t owned by no live segment (uncovered, or an overlapping segment) -> 0
 //     ("[executorch][cuda] Add a length-aware Triton SDPA over per-sequence KV columns",
 //     PR description: rows no segment covers are zeroed);
-//   * the unit holding (t, h) had a single CTA -> that CTA already wrote the row; skip;
+//   * the unit holding (t, h) had a single CTA, or is a split-K unit of at most kMergeRows
+//     rows (its last CTA merged the slots) -> already written; skip;
 //   * no keys at all -> 0 (finite output for fully masked rows, "[CUDA] Use Triton TMA for
 //     long-context causal prefill", Summary);
 //   * otherwise merge the unit's slots: M = max m_c, L = sum l_c 2^(m_c - M),
@@ -21,7 +23,7 @@ __global__ void __launch_bounds__(kCombineThreads) sdpa_combine_kernel(AttnArgs 
   const int64_t gw = ((int64_t)blockIdx.x * kCombineThreads + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   griddep_wait();  // the attention kernels' slots and direct writes
-  if (gw >= A.T * A.Hq) return;
+  if (!A.ws.hdr->combine_work || gw >= A.T * A.Hq) return;
   const int64_t t = gw / A.Hq;
   const int h = (int)(gw % A.Hq);
   __nv_bfloat16* dst = A.out + t * A.o_rs + (int64_t)h * A.o_hs + lane * PER;
@@ -41,7 +43,8 @@ __global__ void __launch_bounds__(kCombineThreads) sdpa_combine_kernel(AttnArgs 
       const int64_t u = (int64_t)sg.ubase[q] + (int64_t)hk * sg.nrb + rb;
       if (u < W.hdr->units[q]) {
         const UnitRec ur = W.units[q][u];
-        if (ur.nslots == 1) return;  // written by the unit's only CTA
+        // written by the unit's only CTA, or merged by the last of a split-K unit's CTAs
+        if (ur.nslots == 1 || (q == kRouteSplitk && ur.nslots > 1 && ur.rows <= kMergeRows)) return;
         if (ur.nslots > 1) {
           zero = false;
           const int64_t rl = r - rb * rpu;

@@ -12,8 +12,13 @@ namespace sdpa {
 
 // Rows of one work unit: query rows (t, g) packed as r = i * group + g, so the query
 // heads that share a KV head sit side by side in one tile (GQA packing).
-constexpr int kSplitkRows = 64;    // split-K kernel: 4 warps x 16 rows
+// split-K kernel: up to two 16-row groups, the four warps splitting each key tile among
+// them; more rows per unit would leave each warp a whole tile of legacy tensor-core work
+constexpr int kSplitkRows = 32;
 constexpr int kSplitkTile = 64;    // split-K kernel: key positions per tile
+// split-K units of up to this many rows are merged by their last CTA (a few KB of slots);
+// larger split units leave it to the combine pass, which spreads it over the whole GPU
+constexpr int kMergeRows = 16;
 constexpr int kSplitkThreads = 128;  // split-K kernel: four warps
 constexpr int kPrefillRows = 128;  // tensor-memory prefill kernel: one 128-lane accumulator
 constexpr int kPrefillTile = 128;  // prefill kernel: key positions per tile
@@ -71,6 +76,10 @@ struct SchedHdr {
   // starting a piece (operand loads, pipeline fill, the epilogue), so a CTA whose share
   // starts a unit gets that many fewer key tiles.
   int64_t lead[3];
+  // Non-zero when the combine pass has rows to write: rows no live segment covers, units
+  // with no keys, or units split over several CTAs other than split-K units of at most
+  // kMergeRows rows (those merge their own partial results).
+  int64_t combine_work;
 };
 
 struct Workspace {
@@ -82,6 +91,7 @@ struct Workspace {
   int32_t* first_unit[3];  // [route][phase * grid + CTA]: unit whose span holds the CTA's first tile
   float2* part_ml[3];   // [route][P_cap] (running max in log2 units, sum)
   float* part_o[3];     // [route][P_cap * D] unnormalised output
+  int32_t* arrive;       // [split-K unit_cap]: CTAs of the unit that finished (zeroed by the scheduler)
   int64_t unit_cap[3];
   int64_t part_cap[3];
 };
@@ -96,9 +106,13 @@ __host__ __device__ inline int64_t unit_cap(int64_t T, int Hq, int Hkv, int S, i
 }
 
 // Partial rows: each (unit, CTA) pair that is not the only CTA of its unit writes one slot
-// of `unit rows` rows; there are at most units + CTAs such pairs.
+// of `unit rows` rows.  Within one phase the CTAs' shares cut the units at most grid - 1
+// times, so there are at most units + phases * grid pairs; the slots are sized for
+// kPartPhases phases and the scheduler lowers a route's phase count below that whenever
+// its units leave less room.
+constexpr int kPartPhases = 4;
 __host__ __device__ inline int64_t part_cap(int64_t ucap, int64_t grid, int rows_per_unit) {
-  return (ucap + grid + 1) * rows_per_unit;
+  return (ucap + kPartPhases * grid + 1) * rows_per_unit;
 }
 
 // Lays the workspace out from `base` (base may be null to only measure). Returns bytes.
@@ -126,6 +140,7 @@ __host__ inline size_t layout_workspace(char* base, int64_t T, int Hq, int Hkv, 
     w.part_ml[r] = (float2*)take(8 * w.part_cap[r]);
     w.part_o[r] = (float*)take(4 * w.part_cap[r] * D);
   }
+  w.arrive = (int32_t*)take(4 * w.unit_cap[kRouteSplitk]);
   if (ws) *ws = w;
   return (size_t)off;
 }
@@ -244,21 +259,39 @@ struct PieceWalk {
   int64_t t0, t1;   // remaining tiles of this CTA in phase p
   int64_t u;        // next unit to look at
   int64_t lead;     // placeholder tiles ahead of each unit's key tiles
+  int64_t U;        // units of the route
+  int64_t pb0, pb1; // phase 0's tile range, and this CTA's first unit in it (loaded early)
+  int32_t fu0;
 };
 
-// Stream-K partition: CTA g of G owns flattened tiles [g*W/G, (g+1)*W/G).
-__host__ __device__ inline int64_t sk_start(int64_t g, int64_t W, int64_t G) { return g * W / G; }
-// CTA whose range holds tile x.
-__host__ __device__ inline int64_t sk_owner(int64_t x, int64_t W, int64_t G) {
-  return ((x + 1) * G - 1) / W;
+// a / b for a >= 0, b > 0: one 32-bit division when both fit in 32 bits (the usual case;
+// a 64-bit division is a long instruction sequence)
+__host__ __device__ __forceinline__ int64_t udiv(int64_t a, int64_t b) {
+  if ((((uint64_t)a | (uint64_t)b) >> 32) == 0) return (int64_t)((uint32_t)a / (uint32_t)b);
+  return a / b;
 }
 
+// Stream-K partition: CTA g of G owns flattened tiles [g*W/G, (g+1)*W/G).
+__host__ __device__ inline int64_t sk_start(int64_t g, int64_t W, int64_t G) { return udiv(g * W, G); }
+// CTA whose range holds tile x.
+__host__ __device__ inline int64_t sk_owner(int64_t x, int64_t W, int64_t G) {
+  return udiv((x + 1) * G - 1, W);
+}
+
+// All loads here are independent, so they travel together: the header, phase 0's bounds
+// and this CTA's entry in phase 0 (read with the launched grid, which is the grid the
+// scheduler planned for; the entry is only used if the CTA works in phase 0).
 __device__ inline void walk_begin(PieceWalk& w, const Workspace& W, int route) {
+  const SchedHdr* h = W.hdr;
   w.W = &W;
   w.route = route;
-  w.G = W.hdr->grid[route];
-  w.nphase = W.hdr->nphase[route];
-  w.lead = W.hdr->lead[route];
+  w.G = gridDim.x;
+  w.nphase = h->nphase[route];
+  w.lead = h->lead[route];
+  w.U = h->units[route];
+  w.pb0 = h->phase_base[route][0];
+  w.pb1 = h->phase_base[route][1];
+  w.fu0 = W.first_unit[route][blockIdx.x];
   w.p = -1;
   w.t0 = w.t1 = 0;
   w.u = 0;
@@ -268,7 +301,8 @@ __device__ inline void walk_begin(PieceWalk& w, const Workspace& W, int route) {
 __device__ inline bool walk_phase(PieceWalk& w) {
   const SchedHdr* h = w.W->hdr;
   while (++w.p < w.nphase) {
-    const int64_t b0 = h->phase_base[w.route][w.p], Wp = h->phase_base[w.route][w.p + 1] - b0;
+    const int64_t b0 = w.p == 0 ? w.pb0 : h->phase_base[w.route][w.p];
+    const int64_t Wp = (w.p == 0 ? w.pb1 : h->phase_base[w.route][w.p + 1]) - b0;
     if (Wp <= 0) continue;
     const int64_t Gp = min(w.G, Wp);  // at most one CTA per tile: nslots stays exact
     if ((int64_t)blockIdx.x >= Gp) continue;
@@ -276,7 +310,7 @@ __device__ inline bool walk_phase(PieceWalk& w) {
     w.t1 = b0 + sk_start(blockIdx.x + 1, Wp, Gp);
     if (w.t0 >= w.t1) continue;
     // the unit whose span holds tile t0, recorded by the scheduler
-    w.u = w.W->first_unit[w.route][w.p * w.G + blockIdx.x];
+    w.u = w.p == 0 ? w.fu0 : w.W->first_unit[w.route][w.p * w.G + blockIdx.x];
     return true;
   }
   return false;
@@ -285,8 +319,7 @@ __device__ inline bool walk_phase(PieceWalk& w) {
 // Next piece of this CTA: a unit and its tiles [ta, tb) that this CTA processes.
 __device__ inline bool walk_next(PieceWalk& w, UnitRec& ur, int64_t& ta, int64_t& tb) {
   for (;;) {
-    const int64_t U = w.W->hdr->units[w.route];
-    while (w.t0 < w.t1 && w.u < U) {
+    while (w.t0 < w.t1 && w.u < w.U) {
       const UnitRec r = w.W->units[w.route][w.u];
       const int64_t k0 = r.tile_base + w.lead, k1 = k0 + r.ntiles;  // the unit's key tiles
       if (r.ntiles == 0 || w.t0 >= k1) {
@@ -317,6 +350,13 @@ __device__ inline bool walk_next(PieceWalk& w, UnitRec& ur, int64_t& ta, int64_t
 // returns at once.  launch_dependents lets the next such kernel start launching.
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
 __device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;\n" :::); }
+
+// Atomic add with acquire-release semantics at GPU scope; returns the old value.
+__device__ __forceinline__ int atom_add_acq_rel_gpu(int* p, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;\n" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);

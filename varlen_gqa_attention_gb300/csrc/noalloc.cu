@@ -100,6 +100,7 @@ size_t layout_splitk_only(char* base, int64_t T, int Hq, int Hkv, int D, int S, 
   w.first_unit[kRouteSplitk] = (int32_t*)take(4 * (int64_t)kMaxPhases * grid);
   w.part_ml[kRouteSplitk] = (float2*)take(8 * w.part_cap[kRouteSplitk]);
   w.part_o[kRouteSplitk] = (float*)take(4 * w.part_cap[kRouteSplitk] * D);
+  w.arrive = (int32_t*)take(4 * w.unit_cap[kRouteSplitk]);
   if (ws) *ws = w;
   return (size_t)off;
 }

@@ -138,11 +138,12 @@ __global__ void __launch_bounds__(PfCfg<D>::THREADS, 1)
 
   griddep_wait();    // the scheduler's output
   griddep_launch();
-  if (A.ws.hdr->tiles[kRoutePrefill] == 0) return;  // whole CTA leaves before any setup
   {
+    // no tiles for this CTA in any phase (or none on the route): the whole CTA leaves
+    // before any setup, after one round of header loads
     PieceWalk probe;
     walk_begin(probe, A.ws, kRoutePrefill);
-    if (!walk_phase(probe)) return;  // no tiles for this CTA in any phase
+    if (!walk_phase(probe)) return;
   }
 
   uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);

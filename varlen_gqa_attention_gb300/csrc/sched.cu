@@ -95,7 +95,7 @@ __device__ __forceinline__ int route_of(const SchedArgs& A, const SegRec& r) {
     int64_t span = r.kv_end;
     if (r.window > 0) span = min(span, (int64_t)r.q_len + r.window - 1);
     const int64_t first = r.kv_end - span;
-    if (first / A.rows != (r.kv_end - 1) / A.rows) return kRouteSplitk;
+    if (udiv(first, A.rows) != udiv(r.kv_end - 1, A.rows)) return kRouteSplitk;
   }
   if (A.policy == SDPA_ROUTE_PREFILL) return kRoutePrefill;
   return R >= kPrefillRows ? kRoutePrefill : kRouteSplitk;
@@ -117,7 +117,7 @@ __global__ void __launch_bounds__(kSchedThreads) sdpa_sched_kernel(SchedArgs A) 
   __shared__ int64_t sh[4 * 32];
   __shared__ int64_t s_pb[3][kMaxPhases + 1];
   __shared__ int64_t s_U[3], s_np[3];
-  __shared__ int32_t s_status;
+  __shared__ int32_t s_status, s_work;
   int4* c_seg = reinterpret_cast<int4*>(smem);      // (q_start, q_len, col, kv_end)
   int2* c_mode = reinterpret_cast<int2*>(c_seg + kSegCache);  // (causal, window)
   int2* c_rn = c_mode + kSegCache;                  // (route, nrb)
@@ -135,7 +135,10 @@ __global__ void __launch_bounds__(kSchedThreads) sdpa_sched_kernel(SchedArgs A) 
   int32_t* row_map = rows_cached ? c_row : W.row_seg;
   int32_t* flag = cached ? c_flag : W.seg_flag;
   griddep_launch();  // the attention kernels may start launching; they wait for this grid
-  if (threadIdx.x == 0) s_status = 0;
+  if (threadIdx.x == 0) {
+    s_status = 0;
+    s_work = 0;
+  }
   __syncthreads();
 
   // 1. validate; clear overlap flags and the row owner map
@@ -198,7 +201,7 @@ __global__ void __launch_bounds__(kSchedThreads) sdpa_sched_kernel(SchedArgs A) 
   // the finished owner map goes out for the combine pass
   int64_t sa, sb;
   my_range(S, &sa, &sb);
-  int64_t cnt[2] = {0, 0};  // units on routes 1 and 2
+  int64_t cnt[3] = {0, 0, 0};  // units on routes 1 and 2, packed rows of live segments
   for (int64_t s = sa; s < sb; ++s) {
     const int32_t bits = bits_of((int)s);
     const int fl = flag[s];
@@ -212,8 +215,9 @@ __global__ void __launch_bounds__(kSchedThreads) sdpa_sched_kernel(SchedArgs A) 
       const int64_t R = (int64_t)g.y * A.group;
       route = route_of(A, r);
       const int rpu = rows_per_unit(route);
-      nrb = (int)((R + rpu - 1) / rpu);
+      nrb = (int)udiv(R + rpu - 1, rpu);
       cnt[route - 1] += (int64_t)A.Hkv * nrb;
+      cnt[2] += g.y;
     }
     if (cached) {
       c_rn[s] = make_int2(route, nrb);
@@ -225,13 +229,14 @@ __global__ void __launch_bounds__(kSchedThreads) sdpa_sched_kernel(SchedArgs A) 
   if (rows_cached)
     for (int64_t t = threadIdx.x; t < T; t += blockDim.x) W.row_seg[t] = c_row[t];
   {
-    int64_t tot[2];
-    block_scan<2>(cnt, tot, sh);
+    int64_t tot[3];
+    block_scan<3>(cnt, tot, sh);
     // Live segments cover disjoint rows, so tot <= unit_cap; units past the cap (none)
     // would simply not be generated.
     if (threadIdx.x == 0) {
       s_U[1] = min(tot[0], W.unit_cap[1]);
       s_U[2] = min(tot[1], W.unit_cap[2]);
+      if (tot[2] < T) s_work = 1;  // rows no live segment covers: the combine pass zeroes them
     }
   }
   for (int64_t s = sa; s < sb; ++s) {
@@ -256,6 +261,14 @@ __global__ void __launch_bounds__(kSchedThreads) sdpa_sched_kernel(SchedArgs A) 
   UnitRec* ubuf1 = units_cached ? c_unit : W.units[1];
   UnitRec* ubuf2 = units_cached ? c_unit + U1 : W.units[2];
   auto unit_at = [&](int64_t u) -> UnitRec& { return u < U1 ? ubuf1[u] : ubuf2[u - U1]; };
+  // phases each route may use: every phase adds at most G - 1 (unit, CTA) pairs to the one
+  // pair per unit, and the partial slots hold part_cap / rows-per-unit pairs
+  int64_t pmax[3] = {1, 1, 1};
+  for (int q = 1; q < 3; ++q) {
+    const int64_t G = A.grid[q];
+    const int64_t room = W.part_cap[q] / rows_per_unit(q) - s_U[q] - 1;
+    if (G > 0) pmax[q] = max((int64_t)1, min(room / G, (int64_t)kMaxPhases));
+  }
   int64_t ua, ub;
   my_range(U, &ua, &ub);
   int64_t acc[4] = {0, 0, 0, 0};  // key-line tiles on routes 1, 2; re-read bytes on routes 1, 2
@@ -283,6 +296,7 @@ __global__ void __launch_bounds__(kSchedThreads) sdpa_sched_kernel(SchedArgs A) 
     }
     UnitRec ur;
     const int64_t j = uq - g.ubase[q];
+    const int64_t jh = udiv(j, g.nrb);
     ur.seg = s;
     ur.q_start = g.q_start;
     ur.q_len = g.q_len;
@@ -290,17 +304,18 @@ __global__ void __launch_bounds__(kSchedThreads) sdpa_sched_kernel(SchedArgs A) 
     ur.kv_end = g.kv_end;
     ur.causal = g.causal;
     ur.window = g.window;
-    ur.hk = (int32_t)(j / g.nrb);
-    ur.rb = (int32_t)(j % g.nrb);
+    ur.hk = (int32_t)jh;
+    ur.rb = (int32_t)(j - jh * g.nrb);
     const int64_t R = (int64_t)g.q_len * A.group;
     const int64_t r0 = (int64_t)ur.rb * rpu;
     ur.rows = (int32_t)min((int64_t)rpu, R - r0);
-    const int i0 = (int)(r0 / A.group), i1 = (int)((r0 + ur.rows - 1) / A.group);
+    const int i0 = (int)udiv(r0, A.group), i1 = (int)udiv(r0 + ur.rows - 1, A.group);
     const RowWin w0 = row_window(i0, g.q_len, g.kv_end, g.causal, g.window);
     const RowWin w1 = row_window(i1, g.q_len, g.kv_end, g.causal, g.window);
     ur.lo = w0.lo;  // lo and hi grow with the query row
     ur.hi = max(w1.hi, w0.lo);
-    const int64_t nt = ur.hi > ur.lo ? ((int64_t)(ur.hi - ur.lo) + tl - 1) / tl : 0;
+    const int64_t nt = ur.hi > ur.lo ? udiv((int64_t)(ur.hi - ur.lo) + tl - 1, tl) : 0;
+    if (nt == 0) s_work = 1;  // rows of a unit with no keys: zeroed by the combine pass
     ur.nslots = 0;
     ur.g_first = 0;
     ur.ntiles = (int32_t)nt;
@@ -327,7 +342,7 @@ __global__ void __launch_bounds__(kSchedThreads) sdpa_sched_kernel(SchedArgs A) 
     UnitRec& ur = unit_at(u);
     const int64_t span = ur.tile_base, reuse = ur.slot_base;
     ur.tile_base = acc[q - 1];
-    ur.phase = (int32_t)min(acc[q + 1] / kPhaseBytes, (int64_t)kMaxPhases - 1);
+    ur.phase = (int32_t)min(acc[q + 1] / kPhaseBytes, pmax[q] - 1);
     acc[q - 1] += span;
     acc[q + 1] += reuse;
   }
@@ -371,15 +386,19 @@ __global__ void __launch_bounds__(kSchedThreads) sdpa_sched_kernel(SchedArgs A) 
       ur.g_first = (int32_t)g0;
       ur.nslots = (int32_t)(g1 - g0 + 1);
       if (ur.nslots > 1) prow[q - 1] += (int64_t)ur.nslots * ur.rows;
-      // CTAs whose share starts inside this unit's span begin their walk here
+      // split units the combine pass merges
+      if (ur.nslots > 1 && (q == kRoutePrefill || ur.rows > kMergeRows)) s_work = 1;
+      // CTAs whose share starts inside this unit's span begin their walk here: the ones
+      // after the owner of the tile before the span, up to the owner of its last tile
       const int64_t s0 = ur.tile_base - b0, s1 = k0 + nt;
-      for (int64_t c = sk_owner(s0, Wp, Gp); c <= sk_owner(s1 - 1, Wp, Gp); ++c)
-        if (sk_start(c, Wp, Gp) >= s0) W.first_unit[q][ur.phase * G + c] = (int32_t)uq;
+      const int64_t c0 = s0 > 0 ? sk_owner(s0 - 1, Wp, Gp) + 1 : 0;
+      for (int64_t c = c0; c <= sk_owner(s1 - 1, Wp, Gp); ++c) W.first_unit[q][ur.phase * G + c] = (int32_t)uq;
     }
   }
   {
     int64_t tot[2];
     block_scan<2>(prow, tot, sh);
+
   }
   for (int64_t u = ua; u < ub; ++u) {
     const int q = u < U1 ? 1 : 2;
@@ -399,6 +418,7 @@ __global__ void __launch_bounds__(kSchedThreads) sdpa_sched_kernel(SchedArgs A) 
       *dst = src[i];
     }
   }
+  for (int64_t u = threadIdx.x; u < U1; u += blockDim.x) W.arrive[u] = 0;
   if (cached) {
     for (int s = threadIdx.x; s < S; s += blockDim.x) {
       const int4 c = c_seg[s];
@@ -424,6 +444,7 @@ __global__ void __launch_bounds__(kSchedThreads) sdpa_sched_kernel(SchedArgs A) 
     W.hdr->nphase[q] = s_np[q];
   }
   if (threadIdx.x == 0) {
+    W.hdr->combine_work = s_work;
     W.hdr->status = s_status;
     if (A.status_dev && s_status) atomicOr(A.status_dev, s_status);
   }

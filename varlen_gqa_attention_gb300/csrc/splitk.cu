@@ -6,19 +6,22 @@
 //
 // A persistent grid (a multiple of the SM count) walks the stream-K tile line the scheduler
 // built: each CTA owns an equal share of key tiles across all units, a unit being
-// (segment, KV head, 64 packed rows r = i * group + g).  Per unit and CTA:
+// (segment, KV head, up to 32 packed rows r = i * group + g).  Per unit and CTA:
 //   * Q rows and 64-position K/V tiles are staged in shared memory with 16-byte cp.async
 //     (coalesced: a store row of one KV head is D*2 contiguous bytes, fetched from DRAM as
 //     one 256-byte block; ring rows wrap per row) through a three-stage ring (two at
 //     D = 256), so two tiles stream in while one is used; two CTAs share an SM at D <= 128;
-//   * each warp takes 16 packed rows and a slice of the tile: S = Q K^T and O += P V with
-//     bf16 m16n8k16 tensor-core MMAs and fp32 accumulation; with few rows (decode: q_len=1,
-//     group 8) the four warps split the tile's keys instead of the rows;
+//   * each warp takes a 16-row group and a slice of the tile: S = Q K^T and O += P V with
+//     bf16 m16n8k16 tensor-core MMAs and fp32 accumulation; two row groups split the tile's
+//     keys in halves, one row group (decode: q_len=1, group 8) in quarters, so no warp runs
+//     a whole tile of these legacy MMAs;
 //   * online softmax in base 2 with quad shuffles for the row max / sum, masks applied by
 //     select (never by adding), fully masked rows kept finite;
 //   * the warps' slices are merged through shared memory, then the CTA either writes `out`
-//     (it is the unit's only CTA) or a partial (max, sum, unnormalised O) that the combine
-//     pass merges by log-sum-exp.
+//     (it is the unit's only CTA) or a partial (max, sum, unnormalised O); for units of up
+//     to 16 rows the last of the unit's CTAs to finish (an arrival counter per unit) merges
+//     the partials by log-sum-exp and writes `out`, larger split units are merged by the
+//     combine pass.
 #include "common.cuh"
 
 namespace sdpa {
@@ -78,11 +81,92 @@ struct KvCursor {
   }
 };
 
+// The last CTA of a split unit: online log-sum-exp over the unit's slots (M' = max(M, m_c),
+// L' = L 2^(M - M') + l_c 2^(m_c - M'), O likewise), then `out`.  A unit's slots are one
+// contiguous block of nslots * rows partial rows, so when they fit in the CTA's shared
+// memory (free by now) they are staged there with 16-byte cp.async from L2 in one round
+// trip; otherwise four slots' loads at a time go straight to registers.  Kept out of line:
+// it runs once per split unit and must not crowd the registers of the tile loop.
+template <int D>
+__device__ __noinline__ void merge_slots(const AttnArgs& A, const UnitRec& ur, const SegRec& sg, int64_t r0,
+                                         char* smem) {
+  const int R = ur.rows, ns = ur.nslots;
+  const float2* ml = A.ws.part_ml[kRouteSplitk] + ur.slot_base;
+  const float* po = A.ws.part_o[kRouteSplitk] + ur.slot_base * D;
+  auto store_row = [&](int rl, int d0, const float* acc, float L) {
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    const int64_t r = r0 + rl;
+    const int64_t i = r / A.group;
+    const int h = ur.hk * A.group + (int)(r % A.group);
+    uint4 pk;
+    pk.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+    pk.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+    pk.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
+    pk.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
+    *reinterpret_cast<uint4*>(A.out + (sg.q_start + i) * A.o_rs + (int64_t)h * A.o_hs + d0) = pk;
+  };
+  auto fold = [](float& M, float& L, float* acc, float2 v, float4 u0, float4 u1) {
+    if (v.x == -INFINITY) return;  // an empty slot adds nothing
+    const float Mn = fmaxf(M, v.x);
+    const float fo = exp2_approx(M - Mn), fc = exp2_approx(v.x - Mn);
+    M = Mn;
+    L = L * fo + v.y * fc;
+    acc[0] = acc[0] * fo + u0.x * fc; acc[1] = acc[1] * fo + u0.y * fc;
+    acc[2] = acc[2] * fo + u0.z * fc; acc[3] = acc[3] * fo + u0.w * fc;
+    acc[4] = acc[4] * fo + u1.x * fc; acc[5] = acc[5] * fo + u1.y * fc;
+    acc[6] = acc[6] * fo + u1.z * fc; acc[7] = acc[7] * fo + u1.w * fc;
+  };
+  const int64_t o_bytes = (int64_t)ns * R * D * 4, m_bytes = (int64_t)ns * R * 8;
+  if (o_bytes + m_bytes <= SplitkSmem<D>::kBytes) {
+    float* so = reinterpret_cast<float*>(smem);
+    float2* sm = reinterpret_cast<float2*>(smem + o_bytes);
+    const int n16 = (int)(o_bytes / 16);
+    for (int k = threadIdx.x; k < n16; k += kSplitkThreads)
+      cp_async_16(smem_u32(so) + 16 * k, po + 4 * (int64_t)k, true);
+    cp_async_commit();
+    for (int k = threadIdx.x; k < ns * R; k += kSplitkThreads) sm[k] = __ldcg(ml + k);
+    cp_async_wait<0>();
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < R * (D / 8); idx += kSplitkThreads) {
+      const int rl = idx / (D / 8), d0 = (idx % (D / 8)) * 8;
+      float M = -INFINITY, L = 0.f, acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      for (int c = 0; c < ns; ++c) {
+        const float* src = so + ((int64_t)c * R + rl) * D + d0;
+        fold(M, L, acc, sm[c * R + rl], *reinterpret_cast<const float4*>(src),
+             *reinterpret_cast<const float4*>(src + 4));
+      }
+      store_row(rl, d0, acc, L);
+    }
+    return;
+  }
+  constexpr int kBatch = 4;
+  for (int idx = threadIdx.x; idx < R * (D / 8); idx += kSplitkThreads) {
+    const int rl = idx / (D / 8), d0 = (idx % (D / 8)) * 8;
+    float M = -INFINITY, L = 0.f, acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int c0 = 0; c0 < ns; c0 += kBatch) {
+      float2 v[kBatch];
+      float4 u0[kBatch], u1[kBatch];
+#pragma unroll
+      for (int b = 0; b < kBatch; ++b) {
+        v[b] = make_float2(-INFINITY, 0.f);
+        if (c0 + b < ns) {
+          const int64_t pi = (int64_t)(c0 + b) * R + rl;
+          v[b] = __ldcg(ml + pi);
+          u0[b] = __ldcg(reinterpret_cast<const float4*>(po + pi * D + d0));
+          u1[b] = __ldcg(reinterpret_cast<const float4*>(po + pi * D + d0 + 4));
+        }
+      }
+#pragma unroll
+      for (int b = 0; b < kBatch; ++b) fold(M, L, acc, v[b], u0[b], u1[b]);
+    }
+    store_row(rl, d0, acc, L);
+  }
+}
+
 // One warp's share of a unit: 16 packed rows x a slice of each key tile.
 template <int D, int NCS>
 __device__ __forceinline__ void splitk_unit(const AttnArgs& A, const UnitRec& ur, const SegRec& sg,
-                                            int64_t ta, int64_t tb, int slot, char* smem,
-                                            float2* s_ml) {
+                                            int64_t ta, int64_t tb, int slot, char* smem, float2* s_ml) {
   using S = SplitkSmem<D>;
   constexpr int RB = S::kRowBytes;
   constexpr int SW = kSplitkTile / NCS;  // keys per warp slice
@@ -289,6 +373,19 @@ __device__ __forceinline__ void splitk_unit(const AttnArgs& A, const UnitRec& ur
   __syncthreads();
 
   const bool direct = ur.nslots == 1;
+  // the output row of local row rl, dims d0 .. d0 + 7, normalised by 1 / L (0 when L = 0)
+  auto store_out = [&](int rl, int d0, const float* acc, float L) {
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    const int64_t r = r0 + rl;
+    const int64_t i = r / A.group;
+    const int h = ur.hk * A.group + (int)(r % A.group);
+    uint4 pk;
+    pk.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+    pk.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+    pk.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
+    pk.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
+    *reinterpret_cast<uint4*>(A.out + (sg.q_start + i) * A.o_rs + (int64_t)h * A.o_hs + d0) = pk;
+  };
   for (int idx = tid; idx < R * (D / 8); idx += kSplitkThreads) {
     const int rl = idx / (D / 8), d0 = (idx % (D / 8)) * 8;
     const int mtr = rl / 16, rin = rl % 16;
@@ -311,17 +408,8 @@ __device__ __forceinline__ void splitk_unit(const AttnArgs& A, const UnitRec& ur
       acc[0] += u0.x * f; acc[1] += u0.y * f; acc[2] += u0.z * f; acc[3] += u0.w * f;
       acc[4] += u1.x * f; acc[5] += u1.y * f; acc[6] += u1.z * f; acc[7] += u1.w * f;
     }
-    const int64_t r = r0 + rl;
     if (direct) {
-      const float inv = L > 0.f ? 1.f / L : 0.f;
-      const int64_t i = r / A.group;
-      const int h = ur.hk * A.group + (int)(r % A.group);
-      uint4 pk;
-      pk.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
-      pk.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
-      pk.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
-      pk.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
-      *reinterpret_cast<uint4*>(A.out + (sg.q_start + i) * A.o_rs + (int64_t)h * A.o_hs + d0) = pk;
+      store_out(rl, d0, acc, L);
     } else {
       const int64_t pi = ur.slot_base + (int64_t)slot * R + rl;
       if (d0 == 0) A.ws.part_ml[kRouteSplitk][pi] = make_float2(M, L);
@@ -337,11 +425,17 @@ template <int D>
 __global__ void __launch_bounds__(kSplitkThreads) sdpa_splitk_kernel(AttnArgs A) {
   extern __shared__ __align__(128) char smem[];
   __shared__ float2 s_ml[4 * 16];
+  // split pieces of this CTA (only the first and the last piece of a share in a phase can
+  // be split), their units and whether this CTA arrived last at each
+  constexpr int kPend = 2 * kMaxPhases;
+  __shared__ UnitRec s_pend[kPend];
+  __shared__ int64_t s_pidx[kPend];
+  __shared__ int s_plast[kPend];
+  int npend = 0;
   griddep_wait();    // the scheduler's output (and the prefill kernel's end)
   griddep_launch();
-  if (A.ws.hdr->tiles[kRouteSplitk] == 0) return;
   PieceWalk wk;
-  walk_begin(wk, A.ws, kRouteSplitk);
+  walk_begin(wk, A.ws, kRouteSplitk);  // no work on this route: the walk ends at once
   UnitRec ur;
   int64_t ta, tb;
   while (walk_next(wk, ur, ta, tb)) {
@@ -355,10 +449,39 @@ __global__ void __launch_bounds__(kSplitkThreads) sdpa_splitk_kernel(AttnArgs A)
     const int slot = (int)(blockIdx.x - ur.g_first);
     if (ur.rows <= 16)
       splitk_unit<D, 4>(A, ur, sg, ta, tb, slot, smem, s_ml);
-    else if (ur.rows <= 32)
-      splitk_unit<D, 2>(A, ur, sg, ta, tb, slot, smem, s_ml);
     else
-      splitk_unit<D, 1>(A, ur, sg, ta, tb, slot, smem, s_ml);
+      splitk_unit<D, 2>(A, ur, sg, ta, tb, slot, smem, s_ml);
+    if (ur.nslots > 1 && ur.rows <= kMergeRows && npend < kPend) {
+      if (threadIdx.x == 0) {
+        s_pend[npend] = ur;
+        s_pidx[npend] = wk.u - 1;  // the walk has moved past the unit it returned
+      }
+      ++npend;
+    }
+  }
+  if (npend == 0) return;
+  // Arrivals, once the CTA's work is done: the CTA that arrives last at a split unit merges
+  // its slots and writes `out`.  After the barrier (every slot store of the CTA issued) one
+  // thread counts each arrival with an acquire-release atomic: release publishes this CTA's
+  // slots, acquire (on the last arrival) makes the other CTAs' slots visible; the barrier
+  // after it extends that to the CTA, whose reads go to L2.  Nothing waits on another CTA.
+  __syncthreads();
+  if (threadIdx.x == 0)
+    for (int k = 0; k < npend; ++k)
+      s_plast[k] = atom_add_acq_rel_gpu(&A.ws.arrive[s_pidx[k]], 1) == s_pend[k].nslots - 1;
+  __syncthreads();
+  for (int k = 0; k < npend; ++k) {
+    if (!s_plast[k]) continue;
+    const UnitRec& pu = s_pend[k];
+    SegRec psg;
+    psg.q_start = pu.q_start;
+    psg.q_len = pu.q_len;
+    psg.col = pu.col;
+    psg.kv_end = pu.kv_end;
+    psg.causal = pu.causal;
+    psg.window = pu.window;
+    merge_slots<D>(A, pu, psg, (int64_t)pu.rb * kSplitkRows, smem);
+    __syncthreads();  // the staging buffer is reused by the next merge
   }
 }
 

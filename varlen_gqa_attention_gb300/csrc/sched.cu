@@ -59,7 +59,7 @@ __device__ void block_scan(int64_t (&v)[N], int64_t (&tot)[N], int64_t* sh /*[N 
 
 // Contiguous range of n items owned by this thread.
 __device__ __forceinline__ void my_range(int64_t n, int64_t* a, int64_t* b) {
-  int64_t per = (n + blockDim.x - 1) / blockDim.x;
+  const int64_t per = udiv(n + blockDim.x - 1, blockDim.x);
   *a = min(n, per * threadIdx.x);
   *b = min(n, *a + per);
 }
@@ -201,7 +201,7 @@ __global__ void __launch_bounds__(kSchedThreads) sdpa_sched_kernel(SchedArgs A) 
   // the finished owner map goes out for the combine pass
   int64_t sa, sb;
   my_range(S, &sa, &sb);
-  int64_t cnt[3] = {0, 0, 0};  // units on routes 1 and 2, packed rows of live segments
+  int64_t n1 = 0, n2 = 0, nrows = 0;  // units on routes 1 and 2, packed rows of live segments
   for (int64_t s = sa; s < sb; ++s) {
     const int32_t bits = bits_of((int)s);
     const int fl = flag[s];
@@ -216,8 +216,8 @@ __global__ void __launch_bounds__(kSchedThreads) sdpa_sched_kernel(SchedArgs A) 
       route = route_of(A, r);
       const int rpu = rows_per_unit(route);
       nrb = (int)udiv(R + rpu - 1, rpu);
-      cnt[route - 1] += (int64_t)A.Hkv * nrb;
-      cnt[2] += g.y;
+      if (route == kRouteSplitk) n1 += (int64_t)A.Hkv * nrb; else n2 += (int64_t)A.Hkv * nrb;
+      nrows += g.y;
     }
     if (cached) {
       c_rn[s] = make_int2(route, nrb);
@@ -229,8 +229,10 @@ __global__ void __launch_bounds__(kSchedThreads) sdpa_sched_kernel(SchedArgs A) 
   if (rows_cached)
     for (int64_t t = threadIdx.x; t < T; t += blockDim.x) W.row_seg[t] = c_row[t];
   {
-    int64_t tot[3];
+    int64_t cnt[3] = {n1, n2, nrows}, tot[3];
     block_scan<3>(cnt, tot, sh);
+    n1 = cnt[0];
+    n2 = cnt[1];
     // Live segments cover disjoint rows, so tot <= unit_cap; units past the cap (none)
     // would simply not be generated.
     if (threadIdx.x == 0) {
@@ -242,14 +244,15 @@ __global__ void __launch_bounds__(kSchedThreads) sdpa_sched_kernel(SchedArgs A) 
   for (int64_t s = sa; s < sb; ++s) {
     int2 rn;
     if (cached) {
-      c_ub[s] = make_int2((int32_t)cnt[0], (int32_t)cnt[1]);
+      c_ub[s] = make_int2((int32_t)n1, (int32_t)n2);
       rn = c_rn[s];
     } else {
-      W.segs[s].ubase[1] = (int32_t)cnt[0];
-      W.segs[s].ubase[2] = (int32_t)cnt[1];
+      W.segs[s].ubase[1] = (int32_t)n1;
+      W.segs[s].ubase[2] = (int32_t)n2;
       rn = make_int2(W.segs[s].route, W.segs[s].nrb);
     }
-    if (rn.x != kRouteNone) cnt[rn.x - 1] += (int64_t)A.Hkv * rn.y;
+    if (rn.x == kRouteSplitk) n1 += (int64_t)A.Hkv * rn.y;
+    else if (rn.x == kRoutePrefill) n2 += (int64_t)A.Hkv * rn.y;
   }
   __syncthreads();
 
@@ -262,16 +265,11 @@ __global__ void __launch_bounds__(kSchedThreads) sdpa_sched_kernel(SchedArgs A) 
   UnitRec* ubuf2 = units_cached ? c_unit + U1 : W.units[2];
   auto unit_at = [&](int64_t u) -> UnitRec& { return u < U1 ? ubuf1[u] : ubuf2[u - U1]; };
   // phases each route may use: every phase adds at most G - 1 (unit, CTA) pairs to the one
-  // pair per unit, and the partial slots hold part_cap / rows-per-unit pairs
-  int64_t pmax[3] = {1, 1, 1};
-  for (int q = 1; q < 3; ++q) {
-    const int64_t G = A.grid[q];
-    const int64_t room = W.part_cap[q] / rows_per_unit(q) - s_U[q] - 1;
-    if (G > 0) pmax[q] = max((int64_t)1, min(room / G, (int64_t)kMaxPhases));
-  }
+  // pair per unit, and the partial slots hold units + kPartPhases * G pairs
+  constexpr int64_t kPhases = kPartPhases < kMaxPhases ? kPartPhases : kMaxPhases;
   int64_t ua, ub;
   my_range(U, &ua, &ub);
-  int64_t acc[4] = {0, 0, 0, 0};  // key-line tiles on routes 1, 2; re-read bytes on routes 1, 2
+  int64_t t1 = 0, t2 = 0, b1 = 0, b2 = 0;  // key-line tiles and re-read bytes on routes 1, 2
   for (int64_t u = ua; u < ub; ++u) {
     const int q = u < U1 ? 1 : 2;
     const int64_t uq = q == 1 ? u : u - U1;
@@ -283,19 +281,26 @@ __global__ void __launch_bounds__(kSchedThreads) sdpa_sched_kernel(SchedArgs A) 
       const int32_t ubm = cached ? (q == 1 ? c_ub[mid].x : c_ub[mid].y) : W.segs[mid].ubase[q];
       if (ubm <= uq) { s = mid; lo = mid + 1; } else { hi = mid - 1; }
     }
-    SegRec g;
+    struct {
+      int32_t q_start, q_len, col, kv_end, nrb, ubase, causal, window;
+    } g;
     if (cached) {
       const int4 c = c_seg[s];
       g.q_start = c.x; g.q_len = c.y; g.col = c.z; g.kv_end = c.w;
       g.nrb = c_rn[s].y;
-      g.ubase[q] = q == 1 ? c_ub[s].x : c_ub[s].y;
+      g.ubase = q == 1 ? c_ub[s].x : c_ub[s].y;
       g.causal = c_mode[s].x;
       g.window = c_mode[s].y;
     } else {
-      g = W.segs[s];
+      const SegRec& r = W.segs[s];
+      g.q_start = r.q_start; g.q_len = r.q_len; g.col = r.col; g.kv_end = r.kv_end;
+      g.nrb = r.nrb;
+      g.ubase = q == 1 ? r.ubase[1] : r.ubase[2];
+      g.causal = r.causal;
+      g.window = r.window;
     }
     UnitRec ur;
-    const int64_t j = uq - g.ubase[q];
+    const int64_t j = uq - g.ubase;
     const int64_t jh = udiv(j, g.nrb);
     ur.seg = s;
     ur.q_start = g.q_start;
@@ -332,19 +337,30 @@ __global__ void __launch_bounds__(kSchedThreads) sdpa_sched_kernel(SchedArgs A) 
     }
     ur.slot_base = reuse;  // kept here until the phase pass below
     unit_at(u) = ur;
-    acc[q - 1] += span_tiles;
-    acc[q + 1] += reuse;
+    if (q == 1) {
+      t1 += span_tiles;
+      b1 += reuse;
+    } else {
+      t2 += span_tiles;
+      b2 += reuse;
+    }
   }
   int64_t tot4[4];
-  block_scan<4>(acc, tot4, sh);
+  {
+    int64_t v[4] = {t1, t2, b1, b2};
+    block_scan<4>(v, tot4, sh);
+    t1 = v[0]; t2 = v[1]; b1 = v[2]; b2 = v[3];
+  }
   for (int64_t u = ua; u < ub; ++u) {
-    const int q = u < U1 ? 1 : 2;
+    const bool r1 = u < U1;
     UnitRec& ur = unit_at(u);
     const int64_t span = ur.tile_base, reuse = ur.slot_base;
-    ur.tile_base = acc[q - 1];
-    ur.phase = (int32_t)min(acc[q + 1] / kPhaseBytes, pmax[q] - 1);
-    acc[q - 1] += span;
-    acc[q + 1] += reuse;
+    int64_t& tt = r1 ? t1 : t2;
+    int64_t& bb = r1 ? b1 : b2;
+    ur.tile_base = tt;
+    ur.phase = (int32_t)min(bb / kPhaseBytes, kPhases - 1);
+    tt += span;
+    bb += reuse;
   }
   __syncthreads();
 
@@ -361,14 +377,14 @@ __global__ void __launch_bounds__(kSchedThreads) sdpa_sched_kernel(SchedArgs A) 
     const int64_t np = Uq > 0 ? unit_at(q == 1 ? Uq - 1 : U1 + Uq - 1).phase + 1 : 0;
     s_np[q] = np;
     s_pb[q][0] = 0;
-    s_pb[q][np] = tot4[q - 1];
+    s_pb[q][np] = q == 1 ? tot4[0] : tot4[1];
   }
   __syncthreads();
 
   // 6. stream-K within each phase: CTA g of G_p = min(G, W_p) owns [g W_p / G_p, (g+1) W_p / G_p);
   // G_p <= W_p makes every working CTA own a tile, so the owners of a unit's tiles are
   // consecutive CTAs that all work on it (nslots is exact)
-  int64_t prow[2] = {0, 0};  // partial rows on routes 1, 2
+  int64_t p1 = 0, p2 = 0;  // partial rows on routes 1, 2
   for (int64_t u = ua; u < ub; ++u) {
     const int q = u < U1 ? 1 : 2;
     const int64_t uq = q == 1 ? u : u - U1;
@@ -385,7 +401,7 @@ __global__ void __launch_bounds__(kSchedThreads) sdpa_sched_kernel(SchedArgs A) 
       const int64_t g1 = sk_owner(k0 + nt - 1, Wp, Gp);
       ur.g_first = (int32_t)g0;
       ur.nslots = (int32_t)(g1 - g0 + 1);
-      if (ur.nslots > 1) prow[q - 1] += (int64_t)ur.nslots * ur.rows;
+      if (ur.nslots > 1) (q == 1 ? p1 : p2) += (int64_t)ur.nslots * ur.rows;
       // split units the combine pass merges
       if (ur.nslots > 1 && (q == kRoutePrefill || ur.rows > kMergeRows)) s_work = 1;
       // CTAs whose share starts inside this unit's span begin their walk here: the ones
@@ -396,15 +412,17 @@ __global__ void __launch_bounds__(kSchedThreads) sdpa_sched_kernel(SchedArgs A) 
     }
   }
   {
-    int64_t tot[2];
-    block_scan<2>(prow, tot, sh);
-
+    int64_t v[2] = {p1, p2}, tot[2];
+    block_scan<2>(v, tot, sh);
+    p1 = v[0];
+    p2 = v[1];
   }
   for (int64_t u = ua; u < ub; ++u) {
     const int q = u < U1 ? 1 : 2;
     UnitRec& ur = unit_at(u);
-    ur.slot_base = prow[q - 1];
-    if (ur.nslots > 1) prow[q - 1] += (int64_t)ur.nslots * ur.rows;
+    int64_t& pp = q == 1 ? p1 : p2;
+    ur.slot_base = pp;
+    if (ur.nslots > 1) pp += (int64_t)ur.nslots * ur.rows;
   }
   __syncthreads();
 

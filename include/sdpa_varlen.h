@@ -218,6 +218,14 @@ sdpa_status sdpa_varlen_splitk_static(const void* q, int64_t T, int Hq, int D, i
                                       int64_t o_row_stride, int64_t o_head_stride, int32_t* status_dev,
                                       void* stream);
 
+/*
+ * Whether the tensor-memory prefill kernel can run for head dim D on the current device:
+ * 1 yes, 0 no (every call then takes the split-K kernel, with the same results), -1 on a
+ * CUDA error or a head dim outside {64, 128, 256} (message in sdpa_last_error).  The answer
+ * is fixed once per device, on first use.
+ */
+int sdpa_prefill_available(int D);
+
 /* Message describing the last failure on this thread ("" if none). */
 const char* sdpa_last_error(void);
 

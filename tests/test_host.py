@@ -118,3 +118,9 @@ def test_seq_clone_rejects_bad_arguments_before_touching_the_device():
     assert lib.sdpa_seq_clone(p, p, 8, 2, 1, 128, 0, 2, 4, None) == ARG
     assert lib.sdpa_seq_clone(p, p, 8, 2, 1, 128, 1, 1, 4, None) == pkg.SDPA_OK  # same column
     assert lib.sdpa_seq_clone(p, p, 8, 2, 1, 128, 0, 1, 0, None) == pkg.SDPA_OK  # empty prefix
+
+
+def test_prefill_availability_rejects_unknown_head_dims_before_any_cuda_call():
+    lib = pkg.library()
+    assert lib.sdpa_prefill_available(96) == -1
+    assert "head dim 96" in lib.sdpa_last_error().decode()

@@ -318,3 +318,10 @@ def test_multi_phase_calls_stay_inside_the_workspace(dev, route, which):
     _, lo, hi, _ = O.visible_interval(call.seq_info, call.T, call.causal, call.window, call.rows, call.cols)
     assert int(status.item()) == st
     assert_matches(got, ref, seg_id, lo, hi, rows=rows, tag=which)
+
+
+@pytest.mark.parametrize("D", [64, 128, 256])
+def test_the_tensor_memory_prefill_kernel_is_usable(dev, D):
+    # if its set-up failed (e.g. more shared memory than an SM has), every call would quietly
+    # take the split-K kernel: same results, far slower
+    assert pkg.prefill_available(D)

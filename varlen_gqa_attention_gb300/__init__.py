@@ -38,7 +38,7 @@ STATUS_NAMES = {
 EXPORTS = [
     "sdpa_varlen_workspace_bytes", "sdpa_varlen", "sdpa_causal_prefill", "sdpa_set_route_policy",
     "sdpa_set_timing_events", "sdpa_last_error", "sdpa_version", "sdpa_varlen_splitk_static",
-    "sdpa_varlen_append", "sdpa_seq_clone", "sdpa_varlen_modes",
+    "sdpa_varlen_append", "sdpa_seq_clone", "sdpa_varlen_modes", "sdpa_prefill_available",
 ]
 
 
@@ -88,6 +88,8 @@ def library(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.sdpa_set_timing_events.argtypes = [ctypes.POINTER(c_vp), c_int]
     lib.sdpa_last_error.restype = ctypes.c_char_p
     lib.sdpa_last_error.argtypes = []
+    lib.sdpa_prefill_available.restype = c_int
+    lib.sdpa_prefill_available.argtypes = [c_int]
     lib.sdpa_version.restype = c_int
     lib.sdpa_version.argtypes = []
     _lib = lib
@@ -101,6 +103,15 @@ def _check(code: int):
 
 def workspace_bytes(T: int, Hq: int, Hkv: int, D: int, S: int) -> int:
     return int(library().sdpa_varlen_workspace_bytes(T, Hq, Hkv, D, S))
+
+
+def prefill_available(D: int) -> bool:
+    """Whether the tensor-memory prefill kernel runs for head dim D on the current device."""
+    lib = library()
+    r = lib.sdpa_prefill_available(D)
+    if r < 0:
+        raise SdpaError(9 if D in (64, 128, 256) else 3, lib.sdpa_last_error().decode())
+    return r == 1
 
 
 def set_route_policy(policy: int) -> None:

@@ -458,6 +458,17 @@ sdpa_status sdpa_causal_prefill(const void* q, const void* k, const void* v, int
              workspace, ws_bytes, nullptr, stream);
 }
 
+int sdpa_prefill_available(int D) {
+  g_err[0] = 0;
+  if (D != 64 && D != 128 && D != 256) {
+    fail(SDPA_ERR_HEAD_DIM, "head dim %d not in {64,128,256}", D);
+    return -1;
+  }
+  DevInfo di;
+  if (device_info(&di) != SDPA_OK) return -1;
+  return di.prefill_ok[d_index(D)] ? 1 : 0;
+}
+
 sdpa_status sdpa_set_route_policy(int policy) {
   if (policy != SDPA_ROUTE_AUTO && policy != SDPA_ROUTE_SPLITK && policy != SDPA_ROUTE_PREFILL)
     return fail(SDPA_ERR_ARG, "unknown route policy %d", policy);

@@ -122,7 +122,13 @@ struct PfPiece {
 
 __device__ __forceinline__ bool pf_next(PieceWalk& w, PfPiece& pc) {
   if (!walk_next(w, pc.ur, pc.ta, pc.tb)) return false;
-  pc.sg = w.W->segs[pc.ur.seg];
+  // the unit record carries its segment's entry and mode: no second dependent load
+  pc.sg.q_start = pc.ur.q_start;
+  pc.sg.q_len = pc.ur.q_len;
+  pc.sg.col = pc.ur.col;
+  pc.sg.kv_end = pc.ur.kv_end;
+  pc.sg.causal = pc.ur.causal;
+  pc.sg.window = pc.ur.window;
   pc.slot = (int)(blockIdx.x - pc.ur.g_first);
   return true;
 }

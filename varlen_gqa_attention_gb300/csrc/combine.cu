@@ -48,7 +48,7 @@ __global__ void __launch_bounds__(kCombineThreads) sdpa_combine_kernel(AttnArgs 
       if (u < (pf ? W.hdr->units[kRoutePrefill] : W.hdr->units[kRouteSplitk])) {
         const UnitRec ur = (pf ? W.units[kRoutePrefill] : W.units[kRouteSplitk])[u];
         // written by the unit's only CTA, or merged by the last of a split-K unit's CTAs
-        if (ur.nslots == 1 || (q == kRouteSplitk && ur.nslots > 1 && ur.rows <= kMergeRows)) return;
+        if (ur.nslots == 1 || (ur.nslots > 1 && !pf && ur.rows <= kMergeRows)) return;
         if (ur.nslots > 1) {
           zero = false;
           // online log-sum-exp over the slots, four slots' loads in flight at a time:

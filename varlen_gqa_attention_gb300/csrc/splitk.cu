@@ -81,88 +81,6 @@ struct KvCursor {
   }
 };
 
-// The last CTA of a split unit: online log-sum-exp over the unit's slots (M' = max(M, m_c),
-// L' = L 2^(M - M') + l_c 2^(m_c - M'), O likewise), then `out`.  A unit's slots are one
-// contiguous block of nslots * rows partial rows, so when they fit in the CTA's shared
-// memory (free by now) they are staged there with 16-byte cp.async from L2 in one round
-// trip; otherwise four slots' loads at a time go straight to registers.  Kept out of line:
-// it runs once per split unit and must not crowd the registers of the tile loop.
-template <int D>
-__device__ __noinline__ void merge_slots(const AttnArgs& A, const UnitRec& ur, const SegRec& sg, int64_t r0,
-                                         char* smem) {
-  const int R = ur.rows, ns = ur.nslots;
-  const float2* ml = A.ws.part_ml[kRouteSplitk] + ur.slot_base;
-  const float* po = A.ws.part_o[kRouteSplitk] + ur.slot_base * D;
-  auto store_row = [&](int rl, int d0, const float* acc, float L) {
-    const float inv = L > 0.f ? 1.f / L : 0.f;
-    const int64_t r = r0 + rl;
-    const int64_t i = r / A.group;
-    const int h = ur.hk * A.group + (int)(r % A.group);
-    uint4 pk;
-    pk.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
-    pk.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
-    pk.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
-    pk.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
-    *reinterpret_cast<uint4*>(A.out + (sg.q_start + i) * A.o_rs + (int64_t)h * A.o_hs + d0) = pk;
-  };
-  auto fold = [](float& M, float& L, float* acc, float2 v, float4 u0, float4 u1) {
-    if (v.x == -INFINITY) return;  // an empty slot adds nothing
-    const float Mn = fmaxf(M, v.x);
-    const float fo = exp2_approx(M - Mn), fc = exp2_approx(v.x - Mn);
-    M = Mn;
-    L = L * fo + v.y * fc;
-    acc[0] = acc[0] * fo + u0.x * fc; acc[1] = acc[1] * fo + u0.y * fc;
-    acc[2] = acc[2] * fo + u0.z * fc; acc[3] = acc[3] * fo + u0.w * fc;
-    acc[4] = acc[4] * fo + u1.x * fc; acc[5] = acc[5] * fo + u1.y * fc;
-    acc[6] = acc[6] * fo + u1.z * fc; acc[7] = acc[7] * fo + u1.w * fc;
-  };
-  const int64_t o_bytes = (int64_t)ns * R * D * 4, m_bytes = (int64_t)ns * R * 8;
-  if (o_bytes + m_bytes <= SplitkSmem<D>::kBytes) {
-    float* so = reinterpret_cast<float*>(smem);
-    float2* sm = reinterpret_cast<float2*>(smem + o_bytes);
-    const int n16 = (int)(o_bytes / 16);
-    for (int k = threadIdx.x; k < n16; k += kSplitkThreads)
-      cp_async_16(smem_u32(so) + 16 * k, po + 4 * (int64_t)k, true);
-    cp_async_commit();
-    for (int k = threadIdx.x; k < ns * R; k += kSplitkThreads) sm[k] = __ldcg(ml + k);
-    cp_async_wait<0>();
-    __syncthreads();
-    for (int idx = threadIdx.x; idx < R * (D / 8); idx += kSplitkThreads) {
-      const int rl = idx / (D / 8), d0 = (idx % (D / 8)) * 8;
-      float M = -INFINITY, L = 0.f, acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      for (int c = 0; c < ns; ++c) {
-        const float* src = so + ((int64_t)c * R + rl) * D + d0;
-        fold(M, L, acc, sm[c * R + rl], *reinterpret_cast<const float4*>(src),
-             *reinterpret_cast<const float4*>(src + 4));
-      }
-      store_row(rl, d0, acc, L);
-    }
-    return;
-  }
-  constexpr int kBatch = 4;
-  for (int idx = threadIdx.x; idx < R * (D / 8); idx += kSplitkThreads) {
-    const int rl = idx / (D / 8), d0 = (idx % (D / 8)) * 8;
-    float M = -INFINITY, L = 0.f, acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int c0 = 0; c0 < ns; c0 += kBatch) {
-      float2 v[kBatch];
-      float4 u0[kBatch], u1[kBatch];
-#pragma unroll
-      for (int b = 0; b < kBatch; ++b) {
-        v[b] = make_float2(-INFINITY, 0.f);
-        if (c0 + b < ns) {
-          const int64_t pi = (int64_t)(c0 + b) * R + rl;
-          v[b] = __ldcg(ml + pi);
-          u0[b] = __ldcg(reinterpret_cast<const float4*>(po + pi * D + d0));
-          u1[b] = __ldcg(reinterpret_cast<const float4*>(po + pi * D + d0 + 4));
-        }
-      }
-#pragma unroll
-      for (int b = 0; b < kBatch; ++b) fold(M, L, acc, v[b], u0[b], u1[b]);
-    }
-    store_row(rl, d0, acc, L);
-  }
-}
-
 // One warp's share of a unit: 16 packed rows x a slice of each key tile.
 template <int D, int NCS>
 __device__ __forceinline__ void splitk_unit(const AttnArgs& A, const UnitRec& ur, const SegRec& sg,
@@ -473,14 +391,8 @@ __global__ void __launch_bounds__(kSplitkThreads) sdpa_splitk_kernel(AttnArgs A)
   for (int k = 0; k < npend; ++k) {
     if (!s_plast[k]) continue;
     const UnitRec& pu = s_pend[k];
-    SegRec psg;
-    psg.q_start = pu.q_start;
-    psg.q_len = pu.q_len;
-    psg.col = pu.col;
-    psg.kv_end = pu.kv_end;
-    psg.causal = pu.causal;
-    psg.window = pu.window;
-    merge_slots<D>(A, pu, psg, (int64_t)pu.rb * kSplitkRows, smem);
+    merge_unit_slots<D, kSplitkThreads>(A, pu, kSplitkRows, A.ws.part_ml[kRouteSplitk],
+                                        A.ws.part_o[kRouteSplitk], smem, SplitkSmem<D>::kBytes);
     __syncthreads();  // the staging buffer is reused by the next merge
   }
 }

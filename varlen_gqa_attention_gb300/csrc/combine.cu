@@ -1,7 +1,7 @@
 // combine.cu - log-sum-exp merge of split partials, and zero rows.
 //
 // Runs only when the scheduler found work for it (combine_work); then one warp per
-// (packed row t, query head h):
+// (packed row t, query head h), which finds the row's unit through the scheduler's row record:
 //   * t owned by no live segment (uncovered, or an overlapping segment) -> 0
 //     ("[executorch][cuda] Add a length-aware Triton SDPA over per-sequence KV columns",
 //     PR description: rows no segment covers are zeroed);
@@ -24,28 +24,30 @@ __global__ void __launch_bounds__(kCombineThreads) sdpa_combine_kernel(AttnArgs 
   const int64_t gw = ((int64_t)blockIdx.x * kCombineThreads + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   griddep_wait();  // the attention kernels' slots and direct writes
-  if (!A.ws.hdr->combine_work || gw >= A.T * A.Hq) return;
+  if (gw >= A.T * A.Hq) return;
   const int64_t t = gw / A.Hq;
   const int h = (int)(gw % A.Hq);
   __nv_bfloat16* dst = A.out + t * A.o_rs + (int64_t)h * A.o_hs + lane * PER;
   const Workspace& W = A.ws;
+  // independent loads, issued together: whether there is work, the row's owner and the
+  // routes' unit counts
+  const int64_t work = W.hdr->combine_work;
+  const int4 ri = W.row_info[t];
+  const int64_t U1 = W.hdr->units[kRouteSplitk], U2 = W.hdr->units[kRoutePrefill];
+  if (!work) return;
 
   bool zero = true;
-  const int s = W.row_seg[t];
-  if (s >= 0) {
-    const SegRec sg = W.segs[s];
-    const int q = sg.route;
-    if (q != kRouteNone) {
-      const int rpu = q == kRoutePrefill ? kPrefillRows : kSplitkRows;
-      const int64_t i = t - sg.q_start;
-      const int hk = h / A.group;
-      const int64_t r = i * A.group + (h % A.group);
-      const int64_t rb = r / rpu;
+  const int q = ri.x;
+  if (q != kRouteNone) {
+    {
       // route-indexed fields picked by select: a runtime index would copy them to local memory
       const bool pf = q == kRoutePrefill;
-      const int64_t u = (int64_t)(pf ? sg.ubase[kRoutePrefill] : sg.ubase[kRouteSplitk]) +
-                        (int64_t)hk * sg.nrb + rb;
-      if (u < (pf ? W.hdr->units[kRoutePrefill] : W.hdr->units[kRouteSplitk])) {
+      const int rpu = pf ? kPrefillRows : kSplitkRows;
+      const int hk = h / A.group;
+      const int64_t r = (int64_t)ri.w * A.group + (h % A.group);
+      const int64_t rb = r / rpu;
+      const int64_t u = (int64_t)ri.y + (int64_t)hk * ri.z + rb;
+      if (u < (pf ? U2 : U1)) {
         const UnitRec ur = (pf ? W.units[kRoutePrefill] : W.units[kRouteSplitk])[u];
         // written by the unit's only CTA, or merged by the last of a split-K unit's CTAs
         if (ur.nslots == 1 || (ur.nslots > 1 && !pf && ur.rows <= kMergeRows)) return;

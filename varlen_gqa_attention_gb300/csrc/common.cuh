@@ -85,7 +85,10 @@ struct SchedHdr {
 struct Workspace {
   SchedHdr* hdr;
   SegRec* segs;
-  int32_t* row_seg;     // [T] owning segment or -1
+  int32_t* row_seg;     // [T] owning segment or -1 (the scheduler's claims)
+  int4* row_info;       // [T] for the combine pass: (route, the segment's first unit on that
+                        // route, units per KV head, row within the segment); route 0: no
+                        // live segment owns the row
   int32_t* seg_flag;    // [S] overlap flags
   UnitRec* units[3];    // [route][U_cap]
   int32_t* first_unit[3];  // [route][phase * grid + CTA]: unit whose span holds the CTA's first tile
@@ -129,6 +132,7 @@ __host__ inline size_t layout_workspace(char* base, int64_t T, int Hq, int Hkv, 
   w.hdr = (SchedHdr*)take(sizeof(SchedHdr));
   w.segs = (SegRec*)take((int64_t)sizeof(SegRec) * (S > 0 ? S : 1));
   w.row_seg = (int32_t*)take(4 * (T > 0 ? T : 1));
+  w.row_info = (int4*)take(16 * (T > 0 ? T : 1));
   w.seg_flag = (int32_t*)take(4 * (S > 0 ? S : 1));
   const int rpu[3] = {0, kSplitkRows, kPrefillRows};
   const int64_t grid[3] = {0, grid_splitk, grid_prefill};

@@ -93,6 +93,7 @@ size_t layout_splitk_only(char* base, int64_t T, int Hq, int Hkv, int D, int S, 
   w.hdr = (SchedHdr*)take(sizeof(SchedHdr));
   w.segs = (SegRec*)take((int64_t)sizeof(SegRec) * (S > 0 ? S : 1));
   w.row_seg = (int32_t*)take(4 * (T > 0 ? T : 1));
+  w.row_info = (int4*)take(16 * (T > 0 ? T : 1));
   w.seg_flag = (int32_t*)take(4 * (S > 0 ? S : 1));
   w.unit_cap[kRouteSplitk] = unit_cap(T, Hq, Hkv, S, kSplitkRows);
   w.part_cap[kRouteSplitk] = part_cap(w.unit_cap[kRouteSplitk], grid, kSplitkRows);

@@ -226,8 +226,6 @@ __global__ void __launch_bounds__(kSchedThreads) sdpa_sched_kernel(SchedArgs A) 
       W.segs[s].nrb = nrb;
     }
   }
-  if (rows_cached)
-    for (int64_t t = threadIdx.x; t < T; t += blockDim.x) W.row_seg[t] = c_row[t];
   {
     int64_t cnt[3] = {n1, n2, nrows}, tot[3];
     block_scan<3>(cnt, tot, sh);
@@ -448,6 +446,29 @@ __global__ void __launch_bounds__(kSchedThreads) sdpa_sched_kernel(SchedArgs A) 
       r.pad2[0] = r.pad2[1] = 0;
       W.segs[s] = r;
     }
+  }
+  // each packed row's owner as the combine pass needs it, so that it reaches the row's unit
+  // in one load
+  for (int64_t t = threadIdx.x; t < T; t += blockDim.x) {
+    const int s = row_map[t];
+    int4 ri = make_int4(kRouteNone, 0, 0, 0);
+    if (s >= 0) {
+      int route, nrb, ub, qs;
+      if (cached) {
+        route = c_rn[s].x;
+        nrb = c_rn[s].y;
+        ub = route == kRouteSplitk ? c_ub[s].x : c_ub[s].y;
+        qs = c_seg[s].x;
+      } else {
+        const SegRec& r = W.segs[s];
+        route = r.route;
+        nrb = r.nrb;
+        ub = route == kRouteSplitk ? r.ubase[kRouteSplitk] : r.ubase[kRoutePrefill];
+        qs = r.q_start;
+      }
+      if (route != kRouteNone) ri = make_int4(route, ub, nrb, (int)(t - qs));
+    }
+    W.row_info[t] = ri;
   }
   for (int i = threadIdx.x; i < 2 * (kMaxPhases + 1); i += blockDim.x) {
     const int q = 1 + i / (kMaxPhases + 1), k = i % (kMaxPhases + 1);

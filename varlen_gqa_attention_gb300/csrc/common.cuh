@@ -60,7 +60,8 @@ static_assert(sizeof(UnitRec) == 80, "unit record layout");
 // Phases: a route's tile line is cut at (segment, KV head) boundaries into phases whose
 // re-read K/V (units sharing a group's keys) fits a budget below the L2 size; every CTA
 // takes its stream-K share of phase 0, then of phase 1, ... so the K/V tiles the whole
-// grid touches at one time stay cached.
+// grid touches at one time stay cached.  The header and the per-CTA start tables have room
+// for kMaxPhases; the scheduler uses at most kPartPhases (the partial slots' sizing).
 constexpr int kMaxPhases = 16;
 constexpr int64_t kPhaseBytes = 48ll << 20;
 
@@ -111,8 +112,7 @@ __host__ __device__ inline int64_t unit_cap(int64_t T, int Hq, int Hkv, int S, i
 // Partial rows: each (unit, CTA) pair that is not the only CTA of its unit writes one slot
 // of `unit rows` rows.  Within one phase the CTAs' shares cut the units at most grid - 1
 // times, so there are at most units + phases * grid pairs; the slots are sized for
-// kPartPhases phases and the scheduler lowers a route's phase count below that whenever
-// its units leave less room.
+// kPartPhases phases, and the scheduler uses no more.
 constexpr int kPartPhases = 4;
 __host__ __device__ inline int64_t part_cap(int64_t ucap, int64_t grid, int rows_per_unit) {
   return (ucap + kPartPhases * grid + 1) * rows_per_unit;

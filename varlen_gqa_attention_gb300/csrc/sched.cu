@@ -9,12 +9,19 @@
 //   3. routes each remaining segment to the split-K or the tensor-memory prefill kernel and
 //      cuts it into units (segment, KV head, block of packed (query row, head) rows);
 //   4. counts each unit's key tiles over the union of its rows' visible intervals and lays
-//      all units' tiles end to end; CTA g of a route's persistent grid of G CTAs owns tiles
-//      [g*W/G, (g+1)*W/G) of that line (a stream-K split, so every CTA gets the same amount
-//      of key tiles whatever the length mix; G is capped at W so that no CTA is idle inside
-//      a unit's range), and each (unit, CTA) pair gets a slot of
-//      partial results unless the unit has a single CTA, which then writes `out` itself.
-// One CTA of 512 threads does all of it; block-wide scans give the prefix sums.
+//      all units' tiles end to end, each unit's behind a few placeholder tiles for the cost
+//      of starting a piece; the line is cut into at most four phases whose re-read K/V fits
+//      the L2 budget; within a phase CTA g of G owns tiles [g*W/G, (g+1)*W/G) (a stream-K
+//      split, so every CTA gets the same amount of key tiles whatever the length mix; G is
+//      capped at W so that no CTA is idle inside a unit's range), the CTAs whose share
+//      starts in a unit are recorded against it, and each (unit, CTA) pair gets a slot of
+//      partial results unless the unit has a single CTA, which then writes `out` itself;
+//   5. publishes the records, a per-row record for the combine pass, the arrival counters
+//      of the split units (zeroed) and a flag that tells the combine pass whether it has
+//      any work.
+// One CTA of 512 threads does all of it; block-wide scans give the prefix sums.  Segment
+// tables of up to 1024 segments, up to 8192 packed rows and up to 1024 units are built in
+// shared memory; larger calls run the same steps on the workspace copies.
 #include "common.cuh"
 
 namespace sdpa {

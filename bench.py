@@ -47,10 +47,10 @@ L2_FLUSH_BYTES = 512 << 20
 # named for the kernel and workload gives the command).  They describe the kernel source they
 # were taken on: a kernel change makes them stale until the capture is repeated.
 NCU_TRAFFIC_BYTES = {
-    "prefill_d128": 2198838016 + 37855232,  # sdpa_prefill_kernel<128>, one launch
+    "prefill_d128": 2304273152 + 37948416,  # sdpa_prefill_kernel<128>, one launch
     "prefill_d64": 9514752 + 0,             # sdpa_prefill_kernel<64>, one launch
-    "decode": 141783296 + 3000576,          # sdpa_splitk_kernel<128>, one launch
-    "mixed": 135065344 + 4560896 + 150354944 + 5475328,  # sdpa_splitk_kernel<128>, both calls
+    "decode": 141780224 + 3403008,          # sdpa_splitk_kernel<128>, one launch
+    "mixed": 135080704 + 4520448 + 150389248 + 5599488,  # sdpa_splitk_kernel<128>, both calls
 }
 
 

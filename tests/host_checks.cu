@@ -1,0 +1,116 @@
+// Host-side checks of the arithmetic the kernels share with the host (built with nvcc as a
+// host program, run by tests/test_host_arith.py):
+//   * udiv against plain 64-bit division, operands above 2^32 included;
+//   * the stream-K partition: shares are contiguous, cover [0, W) once, and sk_owner(x)
+//     names the CTA whose share holds x;
+//   * the workspace layout: every region 256-byte aligned, disjoint, inside the size it
+//     returns, and the partial slots sized for the phases the scheduler may use;
+//   * segment_bits for a grid of segments, printed one per line for comparison with the
+//     oracle's own rule.
+#include <cstdio>
+#include <cstdlib>
+#include <vector>
+#include <algorithm>
+
+#include "../varlen_gqa_attention_gb300/csrc/common.cuh"
+
+using namespace sdpa;
+
+static int failures = 0;
+#define CHECK(c)                                                              \
+  do {                                                                        \
+    if (!(c)) {                                                               \
+      std::printf("FAIL %s:%d %s\n", __FILE__, __LINE__, #c);                 \
+      ++failures;                                                             \
+    }                                                                         \
+  } while (0)
+
+static uint64_t rng_state = 0x9E3779B97F4A7C15ull;
+static uint64_t next_u64() {  // xorshift64*
+  rng_state ^= rng_state >> 12;
+  rng_state ^= rng_state << 25;
+  rng_state ^= rng_state >> 27;
+  return rng_state * 0x2545F4914F6CDD1Dull;
+}
+
+int main() {
+  // udiv
+  for (int i = 0; i < 200000; ++i) {
+    const int64_t a = (int64_t)(next_u64() >> (1 + next_u64() % 40));
+    const int64_t b = (int64_t)(next_u64() >> (1 + next_u64() % 60)) + 1;
+    CHECK(udiv(a, b) == a / b);
+  }
+  // stream-K partition
+  for (int i = 0; i < 20000; ++i) {
+    const int64_t W = 1 + (int64_t)(next_u64() % 100000);
+    const int64_t G = 1 + (int64_t)(next_u64() % std::min<int64_t>(W, 2000));
+    int64_t prev_end = 0;
+    for (int64_t g = 0; g < G; ++g) {
+      const int64_t a = sk_start(g, W, G), b = sk_start(g + 1, W, G);
+      CHECK(a == prev_end && b > a);
+      CHECK(sk_owner(a, W, G) == g && sk_owner(b - 1, W, G) == g);
+      prev_end = b;
+    }
+    CHECK(prev_end == W);
+  }
+  // workspace layout
+  const int64_t Ts[] = {1, 32, 513, 4096, 100000};
+  const int Ss[] = {1, 7, 32, 1500};
+  const int Ds[] = {64, 128, 256};
+  for (int64_t T : Ts)
+    for (int S : Ss)
+      for (int D : Ds) {
+        const int Hq = 16, Hkv = 2;
+        const int64_t gs = 304, gp = 152;
+        Workspace ws{};
+        const size_t need = layout_workspace(nullptr, T, Hq, Hkv, D, S, gs, gp, nullptr);
+        char* base = (char*)(uintptr_t)4096;  // addresses only, never dereferenced
+        const size_t need2 = layout_workspace(base, T, Hq, Hkv, D, S, gs, gp, &ws);
+        CHECK(need == need2);
+        struct R {
+          const void* p;
+          int64_t bytes;
+        };
+        std::vector<R> rs = {{ws.hdr, (int64_t)sizeof(SchedHdr)},
+                             {ws.segs, (int64_t)sizeof(SegRec) * S},
+                             {ws.row_seg, 4 * T},
+                             {ws.row_info, 16 * T},
+                             {ws.seg_flag, 4 * (int64_t)S},
+                             {ws.arrive, 4 * ws.unit_cap[kRouteSplitk]}};
+        const int64_t grid[3] = {0, gs, gp};
+        const int rpu[3] = {0, kSplitkRows, kPrefillRows};
+        for (int r = 1; r < 3; ++r) {
+          CHECK(ws.unit_cap[r] == unit_cap(T, Hq, Hkv, S, rpu[r]));
+          CHECK(ws.part_cap[r] >= (ws.unit_cap[r] + (int64_t)kPartPhases * grid[r] + 1) * rpu[r]);
+          rs.push_back({ws.units[r], (int64_t)sizeof(UnitRec) * ws.unit_cap[r]});
+          rs.push_back({ws.first_unit[r], 4 * (int64_t)kMaxPhases * grid[r]});
+          rs.push_back({ws.part_ml[r], 8 * ws.part_cap[r]});
+          rs.push_back({ws.part_o[r], 4 * ws.part_cap[r] * D});
+        }
+        std::sort(rs.begin(), rs.end(), [](const R& x, const R& y) { return x.p < y.p; });
+        for (size_t k = 0; k < rs.size(); ++k) {
+          const uintptr_t a = (uintptr_t)rs[k].p;
+          CHECK(a % 256 == 0);
+          CHECK(a >= (uintptr_t)base && a + rs[k].bytes <= (uintptr_t)base + need);
+          if (k + 1 < rs.size()) CHECK(a + rs[k].bytes <= (uintptr_t)rs[k + 1].p);
+        }
+        // every unit a route can produce fits: live segments cover disjoint rows
+        CHECK(ws.unit_cap[kRouteSplitk] >= (int64_t)Hkv * ((T * (Hq / Hkv) + kSplitkRows - 1) / kSplitkRows));
+      }
+  // segment_bits on a grid: "q_start q_len col kv_end T rows cols window bits"
+  const int64_t vals_q[] = {-1, 0, 3};
+  const int64_t lens[] = {-1, 0, 1, 5};
+  const int64_t colv[] = {-1, 0, 2};
+  const int64_t kvs[] = {-1, 0, 1, 6, 9, 40};
+  const int wins[] = {0, -2, 1, 3};
+  for (int64_t qs : vals_q)
+    for (int64_t ql : lens)
+      for (int64_t c : colv)
+        for (int64_t ke : kvs)
+          for (int w : wins)
+            std::printf("SEG %lld %lld %lld %lld %d %d %d %d %d\n", (long long)qs, (long long)ql,
+                        (long long)c, (long long)ke, 8, 8, 2, w,
+                        segment_bits(qs, ql, c, ke, 8, 8, 2, w));
+  std::printf("failures %d\n", failures);
+  return failures != 0;
+}

@@ -325,3 +325,20 @@ def test_the_tensor_memory_prefill_kernel_is_usable(dev, D):
     # if its set-up failed (e.g. more shared memory than an SM has), every call would quietly
     # take the split-K kernel: same results, far slower
     assert pkg.prefill_available(D)
+
+
+@pytest.mark.parametrize("D", [64, 128, 256])
+@pytest.mark.parametrize("q_len", [1, 2])
+def test_few_long_decode_sequences_split_over_dozens_of_ctas(dev, D, q_len):
+    # two sequences of 60000 and 30000 keys: each (sequence, KV head) unit is cut over tens
+    # of CTAs, more slots than the last CTA can stage in shared memory, so its merge reads
+    # them straight from L2
+    rows, Hq, Hkv = 65536, 16, 2
+    g = torch.Generator().manual_seed(D + q_len)
+    T = 2 * q_len
+    q = torch.randn(T, Hq, D, generator=g).to(torch.bfloat16)
+    k = torch.randn(rows, 3, Hkv, D, generator=g).to(torch.bfloat16)
+    v = torch.randn(rows, 3, Hkv, D, generator=g).to(torch.bfloat16)
+    si = np.array([(0, q_len, 0, 60000), (q_len, q_len, 2, 30000)], dtype=np.int32)
+    call = synth.Call(T, Hq, Hkv, D, rows, 3, si, True, 0, 1.0 / np.sqrt(D), q, k, v)
+    check_call(call, dev, tag=f"long decode D{D} q_len{q_len}")

@@ -71,8 +71,9 @@ static sdpa_status device_info(DevInfo* out) {
                              (int)sched_smem_bytes());
     if (e != cudaSuccess) return fail(SDPA_ERR_CUDA, "scheduler smem attribute: %s", cudaGetErrorString(e));
     // every kernel of a call asks for the whole shared-memory carveout, so that the SMs keep
-    // one L1 / shared split from kernel to kernel
-    const void* others[3] = {sched_kernel_ptr(), append_kernel_ptr(), clone_kernel_ptr()};
+    // one L1 / shared split from kernel to kernel (the clone kernel runs alone and keeps the
+    // default split, its L1 to itself)
+    const void* others[2] = {sched_kernel_ptr(), append_kernel_ptr()};
     for (const void* f : others) {
       e = cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
       if (e != cudaSuccess) return fail(SDPA_ERR_CUDA, "carveout attribute: %s", cudaGetErrorString(e));

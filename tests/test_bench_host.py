@@ -100,3 +100,22 @@ def test_useful_work_of_the_one_store_mixed_step_uses_each_segments_mode():
     f_t = O.useful_flops(c.seq_info[t], c.T, c.Hq, c.D, True, 4096, c.rows, c.cols)
     f_d = O.useful_flops(c.seq_info[d], c.T, c.Hq, c.D, False, 0, c.rows, c.cols)
     assert flops == f_t + f_d
+
+
+def test_reference_arm_prints_one_contract_line_on_the_cpu():
+    import json
+    import subprocess
+
+    out = subprocess.run([sys.executable, os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "bench.py"),
+                          "--impl", "reference", "--workload", "tiny", "--steps", "1", "--warmup", "3"],
+                         capture_output=True, text=True, timeout=240)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [ln for ln in out.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for key in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in d, key
+    assert d["impl"] == "reference" and d["steps"] == 1 and d["warmup"] >= 3 and d["value"] > 0
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}

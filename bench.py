@@ -51,6 +51,10 @@ NCU_TRAFFIC_BYTES = {
     "prefill_d64": 9514752 + 0,             # sdpa_prefill_kernel<64>, one launch
     "decode": 141780224 + 3403008,          # sdpa_splitk_kernel<128>, one launch
     "mixed": 135080704 + 4520448 + 150389248 + 5599488,  # sdpa_splitk_kernel<128>, both calls
+    "mixed_modes": 217293568 + 8046592,    # sdpa_splitk_kernel<128>, one launch
+    "decode_append": 141788928 + 3189504,  # sdpa_splitk_kernel<128>, one launch
+    # sdpa_clone_kernel: writes still dirty in L2 when the kernel ends are not counted
+    "seq_clone": 134240768 + 84825600,
 }
 
 
@@ -338,7 +342,7 @@ def run_clone(args, world, rank, local):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": name, "l2": "flushed between steps"},
         "roofline": {"bound": "hbm", "achieved": moved / (mean * 1e-3) / 1e9, "peak": hbm, "unit": "GB/s",
-                     "frac": moved / (mean * 1e-3) / 1e9 / hbm, "traffic": None, "kernel": "clone",
+                     "frac": moved / (mean * 1e-3) / 1e9 / hbm, "traffic": NCU_TRAFFIC_BYTES.get("seq_clone"), "kernel": "clone",
                      "peak_source": f"{src} HBM copy"},
         "e2e": {"value": moved / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": 2 * hk.numel() * 2,
                 "d2h_bytes_per_step": hcol.numel() * 2, "ms_per_step": e2e_ms},

@@ -559,8 +559,9 @@ def main():
     e2e_val = world * (flops if prefill_like else kv_bytes) / (e2e * 1e-3) / (1e12 if prefill_like else 1e9)
 
     # scheduler, split-K and combine per call, plus the prefill kernel when the head group
-    # divides its 128-row tile
-    launches = args.steps * sum(3 + (1 if 128 % (d["call"].Hq // d["call"].Hkv) == 0 else 0) for d in calls)
+    # divides its 128-row tile, plus the KV append kernel on the append workload
+    launches = args.steps * sum(3 + (1 if 128 % (d["call"].Hq // d["call"].Hkv) == 0 else 0) +
+                                (1 if "kn" in d else 0) for d in calls)
 
     if rank != 0:
         return

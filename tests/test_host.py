@@ -124,3 +124,16 @@ def test_prefill_availability_rejects_unknown_head_dims_before_any_cuda_call():
     lib = pkg.library()
     assert lib.sdpa_prefill_available(96) == -1
     assert "head dim 96" in lib.sdpa_last_error().decode()
+
+
+def _call_modes(seg_mode, S=1):
+    lib = pkg.library()
+    code = lib.sdpa_varlen_modes(FAKE, 8, 4, 64, 256, 64, FAKE, FAKE, 16, 2, 2, FAKE, seg_mode, S, 0.125,
+                                 FAKE, 256, 64, FAKE, 1 << 30, None, None)
+    return code, lib.sdpa_last_error().decode()
+
+
+def test_per_segment_mode_table_is_checked_before_any_cuda_call():
+    assert _call_modes(None)[0] == 1          # SDPA_ERR_NULL
+    code, msg = _call_modes(FAKE + 8)         # not 16-byte aligned
+    assert code == 6 and "seg_mode" in msg    # SDPA_ERR_ALIGN

@@ -272,6 +272,7 @@ static sdpa_status run(const void* q, int64_t T, int Hq, int D, int64_t q_rs, in
   if (q_rs % 8 || q_hs % 8 || o_rs % 8 || o_hs % 8 || q_rs < 0 || q_hs < 0 || o_rs < 0 || o_hs < 0)
     return fail(SDPA_ERR_STRIDE, "row/head strides must be non-negative multiples of 8 elements");
   if ((uintptr_t)ws % 256) return fail(SDPA_ERR_ALIGN, "workspace must be 256-byte aligned");
+  if (seg_mode && !aligned16(seg_mode)) return fail(SDPA_ERR_ALIGN, "seg_mode must be 16-byte aligned");
 
   DevInfo di;
   if ((st = device_info(&di))) return st;
@@ -281,7 +282,6 @@ static sdpa_status run(const void* q, int64_t T, int Hq, int D, int64_t q_rs, in
   if (ws_bytes < need)
     return fail(SDPA_ERR_WORKSPACE, "workspace of %zu bytes, %zu needed", ws_bytes, need);
 
-  if (seg_mode && !aligned16(seg_mode)) return fail(SDPA_ERR_ALIGN, "seg_mode must be 16-byte aligned");
   SchedArgs sa{};
   sa.seq_info = seq_info;
   sa.seg_mode = S > 0 ? seg_mode : nullptr;

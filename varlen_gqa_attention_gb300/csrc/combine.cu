@@ -39,72 +39,70 @@ __global__ void __launch_bounds__(kCombineThreads) sdpa_combine_kernel(AttnArgs 
   bool zero = true;
   const int q = ri.x;
   if (q != kRouteNone) {
-    {
-      // route-indexed fields picked by select: a runtime index would copy them to local memory
-      const bool pf = q == kRoutePrefill;
-      const int rpu = pf ? kPrefillRows : kSplitkRows;
-      const int hk = h / A.group;
-      const int64_t r = (int64_t)ri.w * A.group + (h % A.group);
-      const int64_t rb = r / rpu;
-      const int64_t u = (int64_t)ri.y + (int64_t)hk * ri.z + rb;
-      if (u < (pf ? U2 : U1)) {
-        const UnitRec ur = (pf ? W.units[kRoutePrefill] : W.units[kRouteSplitk])[u];
-        // written by the unit's only CTA, or merged by the last of a split-K unit's CTAs
-        if (ur.nslots == 1 || (ur.nslots > 1 && !pf && ur.rows <= kMergeRows)) return;
-        if (ur.nslots > 1) {
-          zero = false;
-          // online log-sum-exp over the slots, four slots' loads in flight at a time:
-          // M' = max(M, m_c), L' = L 2^(M - M') + l_c 2^(m_c - M'), O likewise
-          const int64_t rl = r - rb * rpu;
-          const float2* ml = (pf ? W.part_ml[kRoutePrefill] : W.part_ml[kRouteSplitk]) + ur.slot_base + rl;
-          const float* po = (pf ? W.part_o[kRoutePrefill] : W.part_o[kRouteSplitk]) +
-                            (ur.slot_base + rl) * D + lane * PER;
-          const int64_t stride = ur.rows;  // partial rows between one slot and the next
-          float M = -INFINITY, L = 0.f, acc[PER];
+    // route-indexed fields picked by select: a runtime index would copy them to local memory
+    const bool pf = q == kRoutePrefill;
+    const int rpu = pf ? kPrefillRows : kSplitkRows;
+    const int hk = h / A.group;
+    const int64_t r = (int64_t)ri.w * A.group + (h % A.group);
+    const int64_t rb = r / rpu;
+    const int64_t u = (int64_t)ri.y + (int64_t)hk * ri.z + rb;
+    if (u < (pf ? U2 : U1)) {
+      const UnitRec ur = (pf ? W.units[kRoutePrefill] : W.units[kRouteSplitk])[u];
+      // written by the unit's only CTA, or merged by the last of a split-K unit's CTAs
+      if (ur.nslots == 1 || (ur.nslots > 1 && !pf && ur.rows <= kMergeRows)) return;
+      if (ur.nslots > 1) {
+        zero = false;
+        // online log-sum-exp over the slots, four slots' loads in flight at a time:
+        // M' = max(M, m_c), L' = L 2^(M - M') + l_c 2^(m_c - M'), O likewise
+        const int64_t rl = r - rb * rpu;
+        const float2* ml = (pf ? W.part_ml[kRoutePrefill] : W.part_ml[kRouteSplitk]) + ur.slot_base + rl;
+        const float* po = (pf ? W.part_o[kRoutePrefill] : W.part_o[kRouteSplitk]) +
+                          (ur.slot_base + rl) * D + lane * PER;
+        const int64_t stride = ur.rows;  // partial rows between one slot and the next
+        float M = -INFINITY, L = 0.f, acc[PER];
 #pragma unroll
-          for (int k = 0; k < PER; ++k) acc[k] = 0.f;
-          constexpr int kBatch = 4;
-          for (int c0 = 0; c0 < ur.nslots; c0 += kBatch) {
-            float2 v[kBatch];
-            float o[kBatch][PER];
+        for (int k = 0; k < PER; ++k) acc[k] = 0.f;
+        constexpr int kBatch = 4;
+        for (int c0 = 0; c0 < ur.nslots; c0 += kBatch) {
+          float2 v[kBatch];
+          float o[kBatch][PER];
 #pragma unroll
-            for (int b = 0; b < kBatch; ++b) {
-              v[b] = make_float2(-INFINITY, 0.f);
-              if (c0 + b < ur.nslots) {
-                const int64_t c = c0 + b;
-                v[b] = ml[c * stride];
-                // PER = D / 32 floats per lane: 2, 4 or 8, so 8-byte loads at D = 64
-                if constexpr (PER % 4 == 0) {
+          for (int b = 0; b < kBatch; ++b) {
+            v[b] = make_float2(-INFINITY, 0.f);
+            if (c0 + b < ur.nslots) {
+              const int64_t c = c0 + b;
+              v[b] = ml[c * stride];
+              // PER = D / 32 floats per lane: 2, 4 or 8, so 8-byte loads at D = 64
+              if constexpr (PER % 4 == 0) {
 #pragma unroll
-                  for (int k = 0; k < PER; k += 4) {
-                    const float4 u = *reinterpret_cast<const float4*>(po + c * stride * D + k);
-                    o[b][k] = u.x; o[b][k + 1] = u.y; o[b][k + 2] = u.z; o[b][k + 3] = u.w;
-                  }
-                } else {
+                for (int k = 0; k < PER; k += 4) {
+                  const float4 u = *reinterpret_cast<const float4*>(po + c * stride * D + k);
+                  o[b][k] = u.x; o[b][k + 1] = u.y; o[b][k + 2] = u.z; o[b][k + 3] = u.w;
+                }
+              } else {
 #pragma unroll
-                  for (int k = 0; k < PER; k += 2) {
-                    const float2 u = *reinterpret_cast<const float2*>(po + c * stride * D + k);
-                    o[b][k] = u.x; o[b][k + 1] = u.y;
-                  }
+                for (int k = 0; k < PER; k += 2) {
+                  const float2 u = *reinterpret_cast<const float2*>(po + c * stride * D + k);
+                  o[b][k] = u.x; o[b][k + 1] = u.y;
                 }
               }
             }
-#pragma unroll
-            for (int b = 0; b < kBatch; ++b) {
-              if (v[b].x == -INFINITY) continue;  // an empty (or absent) slot adds nothing
-              const float Mn = fmaxf(M, v[b].x);
-              const float fo = exp2_approx(M - Mn), fc = exp2_approx(v[b].x - Mn);
-              M = Mn;
-              L = L * fo + v[b].y * fc;
-#pragma unroll
-              for (int k = 0; k < PER; ++k) acc[k] = acc[k] * fo + o[b][k] * fc;
-            }
           }
-          const float inv = L > 0.f ? 1.f / L : 0.f;
 #pragma unroll
-          for (int k = 0; k < PER; k += 2)
-            *reinterpret_cast<uint32_t*>(dst + k) = pack_bf16x2(acc[k] * inv, acc[k + 1] * inv);
+          for (int b = 0; b < kBatch; ++b) {
+            if (v[b].x == -INFINITY) continue;  // an empty (or absent) slot adds nothing
+            const float Mn = fmaxf(M, v[b].x);
+            const float fo = exp2_approx(M - Mn), fc = exp2_approx(v[b].x - Mn);
+            M = Mn;
+            L = L * fo + v[b].y * fc;
+#pragma unroll
+            for (int k = 0; k < PER; ++k) acc[k] = acc[k] * fo + o[b][k] * fc;
+          }
         }
+        const float inv = L > 0.f ? 1.f / L : 0.f;
+#pragma unroll
+        for (int k = 0; k < PER; k += 2)
+          *reinterpret_cast<uint32_t*>(dst + k) = pack_bf16x2(acc[k] * inv, acc[k + 1] * inv);
       }
     }
   }

@@ -2,7 +2,7 @@
 
 A thin ctypes binding over ``libsdpa_varlen.so`` (C interface in include/sdpa_varlen.h):
 it only checks tensor dtypes/devices, reads strides and pointers, allocates outputs and
-workspace with torch, and passes the current CUDA stream.  Every step of the computation
+workspace with torch, and passes the given (else the current) CUDA stream.  Every step of the computation
 runs in the library's CUDA kernels; there is no other implementation to fall back on, so a
 missing library is an error.
 """
@@ -19,8 +19,9 @@ import torch
 from . import _build
 
 __all__ = [
-    "sdpa_varlen", "sdpa_causal_prefill", "workspace_bytes", "set_route_policy", "set_timing_events",
-    "library",
+    "sdpa_varlen", "sdpa_varlen_modes", "sdpa_varlen_append", "sdpa_seq_clone", "sdpa_causal_prefill",
+    "sdpa_varlen_splitk_static", "workspace_bytes", "prefill_available", "set_route_policy",
+    "set_timing_events", "library",
     "SDPA_OK", "SEG_BAD_QRANGE", "SEG_BAD_COL", "SEG_BAD_KV", "SEG_SPAN", "SEG_OVERLAP",
     "DEV_TIMEOUT", "ROUTE_AUTO", "ROUTE_SPLITK", "ROUTE_PREFILL", "SdpaError",
 ]
@@ -129,8 +130,16 @@ def set_timing_events(events) -> None:
     _check(lib.sdpa_set_timing_events(arr, len(events)))
 
 
-def _workspace(nbytes: int, device) -> torch.Tensor:
-    return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+def _on_stream(t: torch.Tensor, stream) -> torch.Tensor:
+    """A tensor this module allocated on the current stream and hands to work on `stream`:
+    the caching allocator must not reuse its memory before that work is done."""
+    if stream is not None:
+        t.record_stream(stream)
+    return t
+
+
+def _workspace(nbytes: int, device, stream=None) -> torch.Tensor:
+    return _on_stream(torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device), stream)
 
 
 def _stream_ptr(stream) -> int:
@@ -168,12 +177,12 @@ def sdpa_varlen(q: torch.Tensor, k_store: torch.Tensor, v_store: torch.Tensor, s
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     if out is None:
-        out = torch.empty((T, Hq, D), dtype=torch.bfloat16, device=q.device)
+        out = _on_stream(torch.empty((T, Hq, D), dtype=torch.bfloat16, device=q.device), stream)
     elif out.dtype != torch.bfloat16 or tuple(out.shape) != (T, Hq, D) or out.stride(2) != 1:
         raise ValueError("out must be bf16 [T, Hq, D] with unit inner stride")
     need = workspace_bytes(T, Hq, Hkv, D, S)
     if workspace is None:
-        workspace = _workspace(need, q.device)
+        workspace = _workspace(need, q.device, stream)
     st_ptr = status.data_ptr() if status is not None else None
     code = lib.sdpa_varlen(q.data_ptr(), T, Hq, D, q.stride(0), q.stride(1), k_store.data_ptr(),
                            v_store.data_ptr(), rows, cols, Hkv, seq_info.data_ptr() if S else None,
@@ -217,11 +226,11 @@ def sdpa_varlen_append(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     if out is None:
-        out = torch.empty((T, Hq, D), dtype=torch.bfloat16, device=q.device)
+        out = _on_stream(torch.empty((T, Hq, D), dtype=torch.bfloat16, device=q.device), stream)
     elif out.dtype != torch.bfloat16 or tuple(out.shape) != (T, Hq, D) or out.stride(2) != 1:
         raise ValueError("out must be bf16 [T, Hq, D] with unit inner stride")
     if workspace is None:
-        workspace = _workspace(workspace_bytes(T, Hq, Hkv, D, S), q.device)
+        workspace = _workspace(workspace_bytes(T, Hq, Hkv, D, S), q.device, stream)
     st_ptr = status.data_ptr() if status is not None else None
     code = lib.sdpa_varlen_append(q.data_ptr(), T, Hq, D, q.stride(0), q.stride(1), k_new.data_ptr(),
                                   v_new.data_ptr(), k_new.stride(0), k_new.stride(1), k_store.data_ptr(),
@@ -260,11 +269,11 @@ def sdpa_varlen_modes(q: torch.Tensor, k_store: torch.Tensor, v_store: torch.Ten
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     if out is None:
-        out = torch.empty((T, Hq, D), dtype=torch.bfloat16, device=q.device)
+        out = _on_stream(torch.empty((T, Hq, D), dtype=torch.bfloat16, device=q.device), stream)
     elif out.dtype != torch.bfloat16 or tuple(out.shape) != (T, Hq, D) or out.stride(2) != 1:
         raise ValueError("out must be bf16 [T, Hq, D] with unit inner stride")
     if workspace is None:
-        workspace = _workspace(workspace_bytes(T, Hq, Hkv, D, S), q.device)
+        workspace = _workspace(workspace_bytes(T, Hq, Hkv, D, S), q.device, stream)
     st_ptr = status.data_ptr() if status is not None else None
     code = lib.sdpa_varlen_modes(q.data_ptr(), T, Hq, D, q.stride(0), q.stride(1), k_store.data_ptr(),
                                  v_store.data_ptr(), rows, cols, Hkv, seq_info.data_ptr() if S else None,
@@ -304,10 +313,10 @@ def sdpa_causal_prefill(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, scale
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     if out is None:
-        out = torch.empty_like(q)
+        out = _on_stream(torch.empty_like(q), stream)
     need = workspace_bytes(Lq, Hq, Hkv, D, 1)
     if workspace is None:
-        workspace = _workspace(need, q.device)
+        workspace = _workspace(need, q.device, stream)
     code = lib.sdpa_causal_prefill(q.data_ptr(), k.data_ptr(), v.data_ptr(), Lq, Lkv, Hq, Hkv, D,
                                    float(scale), out.data_ptr(), workspace.data_ptr(),
                                    workspace.numel(), _stream_ptr(stream))
@@ -335,7 +344,7 @@ def sdpa_varlen_splitk_static(q: torch.Tensor, k_store: torch.Tensor, v_store: t
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     if out is None:
-        out = torch.empty((T, Hq, D), dtype=torch.bfloat16, device=q.device)
+        out = _on_stream(torch.empty((T, Hq, D), dtype=torch.bfloat16, device=q.device), stream)
     code = fn(q.data_ptr(), T, Hq, D, q.stride(0), q.stride(1), k_store.data_ptr(), v_store.data_ptr(),
               rows, cols, Hkv, seq_info.data_ptr() if S else None, S, int(bool(causal)), int(window),
               float(scale), out.data_ptr(), out.stride(0), out.stride(1),

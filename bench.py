@@ -1,24 +1,34 @@
 """Benchmark of length-aware GQA attention on one GB300 (replicas on N GPUs).
 
 Prints one JSON line (rank 0).  A step is one pass of the whole path (scheduler, attention
-kernels, combine) over one synthetic batch, inputs resident in HBM.  The workload defaults to
-the long-context causal GQA prefill with D=128, Lq=4096, Lkv=131072, Hq=16, Hkv=2 (the
-D=128 row of the operator table on "[CUDA] Use Triton TMA for long-context causal prefill").
+kernels, combine) over one synthetic batch, inputs resident in HBM.  The headline workload is
+the long-context causal GQA prefill with D=128, Lq=4096, Lkv=131072, Hq=16, Hkv=2 (the D=128
+row of the operator table on "[CUDA] Use Triton TMA for long-context causal prefill"); the
+line also carries a `per_config` block with every other workload, each timed and clocked on
+its own.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+                  [--no-per-config] [--no-cpu-baseline]
 
 value: useful (mask-aware) TFLOP/s for prefill workloads, useful KV GB/s for decode-like
-ones, whole job (all ranks).  The L2 is flushed (a 512 MiB write) between timed steps,
-outside each step's events.  `roofline` reports the dominant kernel, timed with CUDA events
-recorded by the library on the launch stream; `e2e` repeats the measurement through the C
-interface from pinned host buffers (H2D of the step's inputs and D2H of its output inside
-the timed region); `cpu_baseline` times the fp64 CPU oracle on a bounded sample.
+ones, whole job (all ranks).  Each step is a CUDA-graph replay; the L2 is flushed (a 512 MiB
+write) between timed steps, outside each step's events; `ms_per_step` is the median step,
+with the mean and the 10th / 90th percentiles beside it.  `roofline` reports the dominant
+kernel, timed with CUDA events that the library records on the launch stream; `e2e` repeats
+the measurement through the C interface from pinned host buffers (H2D of the step's inputs
+and D2H of its output inside the timed region); `cpu_baseline` times the fp64 CPU oracle on
+a bounded sample.  Clocks and throttle reasons are sampled from NVML every ~2 ms (nvidia-smi
+every 100 ms where NVML cannot be loaded); each timed region reports the samples taken
+inside it.
 """
 
 from __future__ import annotations
 
 import argparse
+import ctypes
+import hashlib
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -33,29 +43,59 @@ sys.path.insert(0, ROOT)
 
 WORKLOADS = {
     "tiny": 0, "prefill_d64": 1, "prefill_d128": 2, "decode": 3, "mixed": 4, "decode_append": 3,
-    "seq_clone": -1, "mixed_modes": 5,
+    "seq_clone": -1, "mixed_modes": 5, "prefill_d256": 6, "ring_prefill": 7,
 }
+# the default line's per-config block, in this order (the headline workload first)
+PER_CONFIG = ["prefill_d128", "tiny", "prefill_d64", "prefill_d256", "ring_prefill", "decode",
+              "decode_append", "mixed", "mixed_modes", "seq_clone"]
 # seq_clone workload: one column of a [rows, cols, Hkv, D] store pair copied whole into another
 CLONE_SHAPE = (32768, 9, 8, 128)
 # workloads whose step first writes its new keys and values into the stores (sdpa_varlen_append)
 APPEND = {"decode_append"}
-PREFILL_LIKE = {"tiny", "prefill_d64", "prefill_d128"}
+PREFILL_LIKE = {"tiny", "prefill_d64", "prefill_d128", "prefill_d256", "ring_prefill"}
 METRIC = "varlen GQA attention TFLOP/s (prefill) & KV GB/s (decode), % of roofline"
 L2_FLUSH_BYTES = 512 << 20
+CSRC = os.path.join(ROOT, "varlen_gqa_attention_gb300", "csrc")
+# the sources each kernel is built from (their hash ties a traffic figure to the code it was
+# measured on)
+KERNEL_SOURCES = {
+    "prefill": ["prefill.cu", "tc.cuh", "common.cuh"],
+    "splitk": ["splitk.cu", "common.cuh"],
+    "clone": ["append.cu", "common.cuh"],
+}
 # DRAM bytes (read + write) of the dominant kernel per step, from one ncu capture of the same
 # bench line on a GB300 (dram__bytes_read.sum + dram__bytes_write.sum; the file under profiles/
-# named for the kernel and workload gives the command).  They describe the kernel source they
-# were taken on: a kernel change makes them stale until the capture is repeated.
-NCU_TRAFFIC_BYTES = {
-    "prefill_d128": 2304273152 + 37948416,  # sdpa_prefill_kernel<128>, one launch
-    "prefill_d64": 9514752 + 0,             # sdpa_prefill_kernel<64>, one launch
-    "decode": 141780224 + 3403008,          # sdpa_splitk_kernel<128>, one launch
-    "mixed": 135080704 + 4520448 + 150389248 + 5599488,  # sdpa_splitk_kernel<128>, both calls
-    "mixed_modes": 217293568 + 8046592,    # sdpa_splitk_kernel<128>, one launch
-    "decode_append": 141788928 + 3189504,  # sdpa_splitk_kernel<128>, one launch
+# named for the kernel and workload gives the command), with the hash of that kernel's sources
+# when it was taken.  A kernel whose sources hash differently now reports traffic null until
+# the capture is repeated.
+NCU_TRAFFIC = {
+    "prefill_d128": (2304273152 + 37948416, "prefill", "4b956d3df2670d5a"),
+    "prefill_d64": (9514752 + 0, "prefill", "4b956d3df2670d5a"),
+    "decode": (141780224 + 3403008, "splitk", "13b75fbc734f13b5"),
+    "mixed": (135080704 + 4520448 + 150389248 + 5599488, "splitk", "13b75fbc734f13b5"),
+    "mixed_modes": (217293568 + 8046592, "splitk", "13b75fbc734f13b5"),
+    "decode_append": (141788928 + 3189504, "splitk", "13b75fbc734f13b5"),
     # sdpa_clone_kernel: writes still dirty in L2 when the kernel ends are not counted
-    "seq_clone": 134240768 + 84825600,
+    "seq_clone": (134240768 + 84825600, "clone", "5986e1408fef5391"),
 }
+
+
+def kernel_sha(kind: str) -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES[kind]:
+        with open(os.path.join(CSRC, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload: str):
+    """The stored DRAM traffic of the workload's dominant kernel, or None when there is none
+    or the kernel's sources changed since it was captured."""
+    t = NCU_TRAFFIC.get(workload)
+    if t is None:
+        return None
+    nbytes, kind, sha = t
+    return nbytes if kernel_sha(kind) == sha else None
 
 
 def useful_work(call):
@@ -103,59 +143,148 @@ def read_peaks():
     return 6800.0, 1900.0, 1700.0, "fallback"
 
 
+def percentiles(ms):
+    """median, mean, 10th and 90th percentile of a list of step times."""
+    a = np.asarray(ms, dtype=np.float64)
+    return {"median": float(np.median(a)), "mean": float(a.mean()), "p10": float(np.percentile(a, 10)),
+            "p90": float(np.percentile(a, 90)), "n": int(a.size)}
+
+
+# ------------------------------------------------------------------------------------------
+# clocks
+# ------------------------------------------------------------------------------------------
+
+REASON_BITS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+
+def summarize_clocks(samples, t0: float, t1: float, source: str):
+    """Median SM clock, max clock and every throttle reason seen in the samples taken in
+    [t0, t1].  A sample is (time, sm_mhz, max_mhz, reason_bits, power_w)."""
+    win = [s for s in samples if t0 <= s[0] <= t1]
+    if not win:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "source": source,
+                "note": "no clock sample fell inside the timed region"}
+    sm = [s[1] for s in win]
+    reasons = sorted({name for s in win for bit, name in REASON_BITS.items() if s[3] & bit})
+    pw = [s[4] for s in win if s[4] is not None]
+    return {"sm_mhz": statistics.median(sm), "sm_min_mhz": min(sm), "sm_max_mhz": max(s[2] for s in win),
+            "reasons": reasons, "samples": len(win), "source": source,
+            "power_w_max": max(pw) if pw else None}
+
+
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons, sampled every 200 ms during the timed region."""
+    """SM clock, maximum clock, power and throttle reasons of one GPU, sampled in a background
+    thread: from NVML (libnvidia-ml through ctypes) every ~2 ms, else from `nvidia-smi -lms
+    100`.  Only reads; sets nothing.  Each sample carries the host time it was taken, so that
+    every timed region reports the samples inside it (`window`)."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    SMI_FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+                  "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+                  "clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
-        self.gpu = gpu_index
-        self.proc = None
-        self.lines = []
-        self.reader = None
+    def __init__(self, cuda_index: int, period_s: float = 0.002):
+        self.cuda_index = cuda_index
+        self.period = period_s
+        self.samples = []
+        self.source = "none"
+        self._stop = threading.Event()
+        self._thread = None
+        self._proc = None
+
+    def _nvml_handle(self):
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        h = ctypes.c_void_p()
+        bus = None
+        try:
+            import torch
+
+            p = torch.cuda.get_device_properties(self.cuda_index)
+            bus = f"{p.pci_domain_id:08X}:{p.pci_bus_id:02X}:{p.pci_device_id:02X}.0"
+        except Exception:  # noqa: BLE001 - fall back to the index
+            bus = None
+        rc = lib.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(h)) if bus else 1
+        if rc != 0:
+            rc = lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(self.cuda_index), ctypes.byref(h))
+        if rc != 0:
+            raise OSError("no NVML handle for the device")
+        reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        return lib, h, reasons
+
+    def _nvml_loop(self, lib, h, reasons_fn):
+        clk, mx, pw = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_uint()
+        rs = ctypes.c_ulonglong()
+        while not self._stop.is_set():
+            t = time.monotonic()
+            if lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0 and \
+                    lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:
+                r = reasons_fn(h, ctypes.byref(rs))
+                p = lib.nvmlDeviceGetPowerUsage(h, ctypes.byref(pw))
+                self.samples.append((t, float(clk.value), float(mx.value), int(rs.value) if r == 0 else 0,
+                                     pw.value / 1000.0 if p == 0 else None))
+            time.sleep(self.period)
+
+    def _smi_loop(self):
+        for line in self._proc.stdout:
+            t = time.monotonic()
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm, mx = float(parts[0]), float(parts[1])
+            except ValueError:
+                continue
+            try:
+                pw = float(parts[2])
+            except ValueError:
+                pw = None
+            bits = 0
+            for bit, val in zip((0x8, 0x40, 0x20, 0x4), parts[3:7]):
+                if val.lower().startswith("active"):
+                    bits |= bit
+            self.samples.append((t, sm, mx, bits, pw))
 
     def start(self):
         try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            self.reader = threading.Thread(target=self._read, daemon=True)
-            self.reader.start()
+            lib, h, rf = self._nvml_handle()
+            self.source = f"nvml every {self.period * 1e3:.0f} ms"
+            self._thread = threading.Thread(target=self._nvml_loop, args=(lib, h, rf), daemon=True)
+            self._thread.start()
+            return
+        except (OSError, AttributeError):
+            pass
+        try:
+            self._proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.cuda_index), f"--query-gpu={self.SMI_FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.source = "nvidia-smi every 100 ms"
+            self._thread = threading.Thread(target=self._smi_loop, daemon=True)
+            self._thread.start()
         except (OSError, FileNotFoundError):
-            self.proc = None
+            self.source = "unavailable"
 
-    def _read(self):
-        for line in self.proc.stdout:
-            self.lines.append(line.strip())
+    def window(self, t0: float, t1: float):
+        return summarize_clocks(list(self.samples), t0, t1, self.source)
 
     def stop(self):
-        if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        self.proc.terminate()
-        try:
-            self.proc.wait(timeout=5)
-        except subprocess.TimeoutExpired:
-            self.proc.kill()
-        self.reader.join(timeout=2)
-        sm, mx, reasons = [], None, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
-            parts = [p.strip() for p in ln.split(",")]
-            if len(parts) < 9:
-                continue
+        self._stop.set()
+        if self._proc is not None:
+            self._proc.terminate()
             try:
-                sm.append(float(parts[1]))
-                mx = float(parts[2])
-            except ValueError:
-                continue
-            for name, val in zip(names, parts[5:9]):
-                if val.lower().startswith("active"):
-                    reasons.add(name)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                self._proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self._proc.kill()
+        if self._thread is not None:
+            self._thread.join(timeout=2)
 
+
+# ------------------------------------------------------------------------------------------
+# ranks
+# ------------------------------------------------------------------------------------------
 
 def dist_setup():
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -184,6 +313,43 @@ def max_over_ranks(x: float, world: int) -> float:
     t = torch.tensor([x], dtype=torch.float64)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+# ------------------------------------------------------------------------------------------
+# the CPU oracle as a baseline
+# ------------------------------------------------------------------------------------------
+
+def cpu_info():
+    """CPU model and the BLAS thread count the oracle's NumPy runs with."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.startswith("Model name:"):
+                model = ln.split(":", 1)[1].strip()
+                break
+        if model is None:
+            vend = [ln.split(":", 1)[1].strip() for ln in out.splitlines() if ln.startswith("Vendor ID:")]
+            model = vend[0] if vend else None
+    except (OSError, subprocess.SubprocessError):
+        pass
+    blas = None
+    try:
+        for ln in open("/proc/self/maps"):
+            path = ln.split()[-1]
+            if "openblas" in path.lower() and ".so" in path:
+                lib = ctypes.CDLL(path)
+                for name in ("scipy_openblas_get_num_threads64_", "openblas_get_num_threads64_",
+                             "openblas_get_num_threads"):
+                    f = getattr(lib, name, None)
+                    if f is not None:
+                        blas = int(f())
+                        break
+                if blas is not None:
+                    break
+    except OSError:
+        pass
+    return model, blas
 
 
 def cpu_baseline(wl, prefill_like: bool, budget_s: float = 12.0):
@@ -220,11 +386,14 @@ def cpu_baseline(wl, prefill_like: bool, budget_s: float = 12.0):
             w = c.window if c.seg_mode is None else int(c.seg_mode[s][1])
             done_bytes += O.needed_span(ql, ke, w) * c.Hkv * c.D * 2 * 2
     cores = len(os.sched_getaffinity(0))
+    model, blas = cpu_info()
     el = max(el, 1e-9)
     value = done_flops / el / 1e12 if prefill_like else done_bytes / el / 1e9
     return {"value": value, "unit": "TFLOP/s" if prefill_like else "GB/s", "cores": cores, "kind": "oracle",
+            "cpu_model": model, "blas_threads": blas,
             "sample": f"the last {n_rows} packed rows (all heads) of {wl.name}: {el:.1f} s of fp64 NumPy "
-                      f"on {cores} host cores (BLAS threads: default)"}
+                      f"on {cores} host cores ({model or 'cpu model unknown'}; BLAS threads: "
+                      f"{blas if blas is not None else 'unknown'})"}
 
 
 def run_reference(args, wl, world, rank):
@@ -246,15 +415,275 @@ def run_reference(args, wl, world, rank):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": {"workload": wl.name, "description": wl.description},
         "cpu_baseline": {"value": v, "unit": unit, "cores": vals[0]["cores"], "kind": "oracle",
+                         "cpu_model": vals[0]["cpu_model"], "blas_threads": vals[0]["blas_threads"],
                          "sample": vals[0]["sample"]},
         "e2e": {"value": v, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
 
 
-def run_clone(args, world, rank, local):
+# ------------------------------------------------------------------------------------------
+# GPU timing
+# ------------------------------------------------------------------------------------------
+
+def time_replays(replay, n: int, flush, stream):
+    """n steps, each a call of `replay` bracketed by CUDA events on `stream`, the L2 flushed
+    before each step outside its events; one synchronisation at the end.  Returns the step
+    times (ms) and the host-time window the GPU work fell in."""
+    import torch
+
+    beg = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    end = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    torch.cuda.synchronize()
+    t0 = time.monotonic()
+    for k in range(n):
+        flush.fill_(k & 0xFF)
+        beg[k].record(stream)
+        replay()
+        end[k].record(stream)
+    torch.cuda.synchronize()
+    t1 = time.monotonic()
+    return [b.elapsed_time(e) for b, e in zip(beg, end)], t0, t1
+
+
+class Prepared:
+    """Device-resident inputs of one workload and the step that runs it through the binding."""
+
+    def __init__(self, name, seed, dev):
+        import torch
+
+        import varlen_gqa_attention_gb300 as pkg
+        from workloads import synth
+
+        self.name = name
+        self.pkg = pkg
+        self.wl = synth.workload(WORKLOADS[name], seed=seed)
+        wl = self.wl
+        self.prefill_like = name in PREFILL_LIKE
+        self.calls = []
+        T_total = max(c.row_end or c.T for c in wl.calls)
+        self.out = torch.empty((T_total, wl.calls[0].Hq, wl.calls[0].D), dtype=torch.bfloat16, device=dev)
+        for c in wl.calls:
+            d = dict(call=c, q=c.q.to(dev), k=c.k_store.to(dev), v=c.v_store.to(dev),
+                     seq=torch.from_numpy(c.seq_info).to(dev),
+                     ws=torch.empty(pkg.workspace_bytes(c.T, c.Hq, c.Hkv, c.D, len(c.seq_info)),
+                                    dtype=torch.uint8, device=dev))
+            d["out"] = self.out[c.row_begin:(c.row_end or c.T)]
+            if c.seg_mode is not None:
+                d["md"] = torch.from_numpy(np.ascontiguousarray(c.seg_mode, dtype=np.int32)).to(dev)
+            if name in APPEND:
+                g = torch.Generator().manual_seed(1000 + seed)
+                shape = (c.T, c.Hkv, c.D)
+                d["kn_host"] = torch.randn(shape, generator=g).to(torch.bfloat16)
+                d["vn_host"] = torch.randn(shape, generator=g).to(torch.bfloat16)
+                d["kn"], d["vn"] = d["kn_host"].to(dev), d["vn_host"].to(dev)
+            self.calls.append(d)
+        works = [useful_work(c) for c in wl.calls]
+        self.flops = sum(w[0] for w in works)
+        self.kv_bytes = sum(w[1] for w in works)
+        self.qo_bytes = sum(w[2] for w in works)
+        if name in APPEND:
+            # the step's new K and V rows, read once and written once (every covered row writes:
+            # kv_end >= q_len in these workloads)
+            self.kv_bytes += sum(w[2] // (4 * c.Hq * c.D) * c.Hkv * c.D * 2 * 2 * 2 for w, c in zip(works, wl.calls))
+        # scheduler, split-K and combine per call, plus the prefill kernel when the head group
+        # divides its 128-row tile, plus the KV append kernel on the append workload
+        self.launches_per_step = sum(3 + (1 if 128 % (d["call"].Hq // d["call"].Hkv) == 0 else 0) +
+                                     (1 if "kn" in d else 0) for d in self.calls)
+
+    def attend(self, d):
+        pkg, c = self.pkg, d["call"]
+        if "kn" in d:
+            pkg.sdpa_varlen_append(d["q"], d["kn"], d["vn"], d["k"], d["v"], d["seq"], causal=c.causal,
+                                   window=c.window, scale=c.scale, out=d["out"], workspace=d["ws"])
+        elif "md" in d:
+            pkg.sdpa_varlen_modes(d["q"], d["k"], d["v"], d["seq"], d["md"], scale=c.scale, out=d["out"],
+                                  workspace=d["ws"])
+        else:
+            pkg.sdpa_varlen(d["q"], d["k"], d["v"], d["seq"], causal=c.causal, window=c.window,
+                            scale=c.scale, out=d["out"], workspace=d["ws"])
+
+    def step(self, evs=None):
+        for i, d in enumerate(self.calls):
+            if evs is not None:
+                self.pkg.set_timing_events(evs[i])
+            self.attend(d)
+        if evs is not None:
+            self.pkg.set_timing_events(None)
+
+
+def measure(prep: Prepared, steps: int, warmup: int, flush, clocks, world, min_timed_s: float = 0.0):
+    """Times one workload: `steps` CUDA-graph replays of the step as a caller runs it (more
+    when `min_timed_s` asks for a longer timed region, so that it holds clock samples), then
+    the same number of replays of a graph with the library's timing events at every kernel
+    boundary (each kernel then runs alone) for the per-kernel times.  Returns the config
+    block (value, step-time statistics, roofline, kernel times, clocks)."""
+    import torch
+
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        prep.step()
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in prep.calls]
+    for e in (e for b in ev for e in b):
+        e.record(stream)  # torch creates the CUDA event on its first record
+    torch.cuda.synchronize()
+    graph_k = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph_k):
+        prep.step(ev)
+    graph_s = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph_s):
+        prep.step()
+    t0 = time.monotonic()
+    for _ in range(warmup):
+        graph_s.replay()
+        graph_k.replay()
+    torch.cuda.synchronize()
+    est = max((time.monotonic() - t0) / max(1, warmup) / 2, 1e-5)
+    n = steps
+    if min_timed_s > 0:
+        n = max(steps, min(20000, int(math.ceil(min_timed_s / (est + 2e-4)))))
+    barrier(world)
+    step_ms, w0, w1 = time_replays(graph_s.replay, n, flush, stream)
+    barrier(world)
+    clk = clocks.window(w0, w1)
+
+    # per-kernel breakdown, same L2 flush, outside the timed steps
+    nk = min(n, 200)
+    kern = {"sched": [], "prefill": [], "splitk": [], "combine": []}
+    for k in range(nk):
+        flush.fill_(k & 0xFF)
+        graph_k.replay()
+        torch.cuda.synchronize()
+        for i in range(len(prep.calls)):
+            e = [ev[i][a].elapsed_time(ev[i][a + 1]) for a in range(4)]
+            for key, val in zip(("sched", "prefill", "splitk", "combine"), e):
+                kern[key].append(val)
+    stats = percentiles(step_ms)
+    med = max_over_ranks(stats["median"], world)
+    if prep.prefill_like:
+        value = world * prep.flops / (med * 1e-3) / 1e12
+        unit = "TFLOP/s"
+    else:
+        value = world * prep.kv_bytes / (med * 1e-3) / 1e9
+        unit = "GB/s"
+    hbm, bf16, _, peak_src = read_peaks()
+    # per step: the median kernel time times the calls of a step
+    kmed = {k: statistics.median(v) * len(prep.calls) for k, v in kern.items()}
+    dom = max(("prefill", "splitk"), key=lambda k: kmed[k])
+    dom_ms = kmed[dom]
+    if prep.prefill_like:
+        achieved = prep.flops / (dom_ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": bf16, "unit": "TFLOP/s",
+                "frac": achieved / bf16, "traffic": ncu_traffic(prep.name), "kernel": dom,
+                "peak_source": f"{peak_src} bf16 dense (burst)"}
+    else:
+        alg = prep.kv_bytes + prep.qo_bytes
+        achieved = alg / (dom_ms * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                "frac": achieved / hbm, "traffic": ncu_traffic(prep.name), "kernel": dom,
+                "peak_source": f"{peak_src} HBM copy"}
+    return {
+        "workload": prep.wl.name + ("+kv_append" if prep.name in APPEND else ""),
+        "value": value, "unit": unit, "steps": n, "ms_per_step": med,
+        "ms": {"median": stats["median"], "mean": stats["mean"], "p10": stats["p10"], "p90": stats["p90"]},
+        "roofline": roof,
+        "kernel_ms": {k: v / len(prep.calls) for k, v in kmed.items()},  # median per call
+        "gpu_launches": n * prep.launches_per_step,
+        "clocks": clk,
+        "useful_tflop_per_step": prep.flops / 1e12, "kv_gb_per_step": prep.kv_bytes / 1e9,
+    }
+
+
+def measure_e2e(prep: Prepared, steps: int, flush, world):
+    """The same step through the public API from pinned host buffers: H2D of the step's inputs
+    and D2H of its output inside the timed region."""
+    import torch
+
+    stream = torch.cuda.current_stream()
+    host = []
+    h2d = 0
+    for d in prep.calls:
+        c = d["call"]
+        hq, hk, hv = c.q.pin_memory(), c.k_store.pin_memory(), c.v_store.pin_memory()
+        hs = torch.from_numpy(c.seq_info.copy()).pin_memory()
+        host.append((hq, hk, hv, hs))
+        h2d += hq.numel() * 2 + hk.numel() * 2 + hv.numel() * 2 + hs.numel() * 4
+        if "kn" in d:
+            d["kn_pin"], d["vn_pin"] = d["kn_host"].pin_memory(), d["vn_host"].pin_memory()
+            h2d += (d["kn_pin"].numel() + d["vn_pin"].numel()) * 2
+        if "md" in d:
+            d["md_pin"] = d["md"].cpu().pin_memory()
+            h2d += d["md_pin"].numel() * 4
+    hout = torch.empty(prep.out.shape, dtype=torch.bfloat16).pin_memory()
+    d2h = hout.numel() * 2
+
+    def e2e_step():
+        for d, (hq, hk, hv, hs) in zip(prep.calls, host):
+            d["q"].copy_(hq, non_blocking=True)
+            d["k"].copy_(hk, non_blocking=True)
+            d["v"].copy_(hv, non_blocking=True)
+            d["seq"].copy_(hs, non_blocking=True)
+            if "kn" in d:
+                d["kn"].copy_(d["kn_pin"], non_blocking=True)
+                d["vn"].copy_(d["vn_pin"], non_blocking=True)
+            if "md" in d:
+                d["md"].copy_(d["md_pin"], non_blocking=True)
+            prep.attend(d)
+        hout.copy_(prep.out, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    ms, _, _ = time_replays(e2e_step, steps, flush, stream)
+    med = max_over_ranks(statistics.median(ms), world)
+    denom = (1e12 if prep.prefill_like else 1e9)
+    work = prep.flops if prep.prefill_like else prep.kv_bytes
+    return {"value": world * work / (med * 1e-3) / denom, "unit": "TFLOP/s" if prep.prefill_like else "GB/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": med}
+
+
+def measure_clone(args, dev, flush, clocks, world, min_timed_s: float = 0.0):
     """The column clone: K and V of one whole column (rows x Hkv x D) read once and written
-    once per step, against the HBM copy roofline; the oracle's copy times the CPU leg."""
+    once per step, against the HBM copy roofline."""
+    import torch
+
+    import varlen_gqa_attention_gb300 as pkg
+
+    rows, cols, Hkv, D = CLONE_SHAPE
+    moved = 2 * 2 * rows * Hkv * D * 2  # K and V, read and written
+    g = torch.Generator().manual_seed(args.seed)
+    k = torch.randn((rows, cols, Hkv, D), generator=g).to(torch.bfloat16).to(dev)
+    v = torch.randn((rows, cols, Hkv, D), generator=g).to(torch.bfloat16).to(dev)
+    for _ in range(args.warmup):
+        pkg.sdpa_seq_clone(k, v, 0, cols - 1, rows)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    n = args.steps
+    if min_timed_s > 0:
+        n = max(n, int(math.ceil(min_timed_s / 2.5e-4)))
+    it = iter(range(10 ** 9))
+    barrier(world)
+    ms, w0, w1 = time_replays(lambda: pkg.sdpa_seq_clone(k, v, next(it) % (cols - 1), cols - 1, rows), n,
+                              flush, stream)
+    barrier(world)
+    stats = percentiles(ms)
+    med = max_over_ranks(stats["median"], world)
+    hbm, _, _, src = read_peaks()
+    achieved = moved / (med * 1e-3) / 1e9
+    block = {
+        "workload": f"seq_clone_store{rows}x{cols}x{Hkv}x{D}_full_column",
+        "value": world * achieved, "unit": "GB/s", "steps": n, "ms_per_step": med,
+        "ms": {"median": stats["median"], "mean": stats["mean"], "p10": stats["p10"], "p90": stats["p90"]},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                     "traffic": ncu_traffic("seq_clone"), "kernel": "clone", "peak_source": f"{src} HBM copy"},
+        "gpu_launches": n, "clocks": clocks.window(w0, w1),
+    }
+    return block, (k, v, moved)
+
+
+def run_clone(args, world, rank, local):
+    """`--workload seq_clone`: the clone as the headline; the oracle's copy times the CPU leg."""
     import torch
 
     import varlen_gqa_attention_gb300 as pkg
@@ -262,7 +691,6 @@ def run_clone(args, world, rank, local):
 
     rows, cols, Hkv, D = CLONE_SHAPE
     name = f"seq_clone_store{rows}x{cols}x{Hkv}x{D}_full_column"
-    moved = 2 * 2 * rows * Hkv * D * 2  # K and V, read and written
     if args.impl == "reference":
         if rank != 0:
             return
@@ -274,57 +702,38 @@ def run_clone(args, world, rank, local):
         el = (time.perf_counter() - t0) / (args.warmup + args.steps)
         v = 2 * 2 * n_cpu * Hkv * D * 2 / el / 1e9
         cores = len(os.sched_getaffinity(0))
+        model, blas = cpu_info()
         print(json.dumps({"impl": "reference", "metric": "seq_clone GB/s moved", "value": v, "unit": "GB/s",
                           "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": el * 1e3,
                           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
                           "data": "synthetic", "config": {"workload": name},
                           "cpu_baseline": {"value": v, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                                           "cpu_model": model, "blas_threads": blas,
                                            "sample": f"{n_cpu} rows of one column"},
                           "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}),
               flush=True)
         return
     dev = torch.device(f"cuda:{local}")
     torch.cuda.set_device(dev)
-    g = torch.Generator().manual_seed(args.seed)
-    k = torch.randn((rows, cols, Hkv, D), generator=g).to(torch.bfloat16).to(dev)
-    v = torch.randn((rows, cols, Hkv, D), generator=g).to(torch.bfloat16).to(dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    for _ in range(args.warmup):
-        pkg.sdpa_seq_clone(k, v, 0, cols - 1, rows)
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
     clocks.start()
-    barrier(world)
-    torch.cuda.synchronize()
-    ms = []
-    for i in range(args.steps):
-        flush.fill_(i & 0xFF)
-        e0.record()
-        pkg.sdpa_seq_clone(k, v, i % (cols - 1), cols - 1, rows)
-        e1.record()
-        torch.cuda.synchronize()
-        ms.append(e0.elapsed_time(e1))
-    barrier(world)
-    clk = clocks.stop()
-    mean = max_over_ranks(statistics.mean(ms), world)
-    value = world * moved / (mean * 1e-3) / 1e9
-    hbm, _, _, src = read_peaks()
+    block, (k, v, moved) = measure_clone(args, dev, flush, clocks, world)
     # end to end: the column pair goes up from pinned host memory, the clone runs, and the
     # destination column comes back
     hk, hv = k.cpu().pin_memory(), v.cpu().pin_memory()
     hcol = torch.empty((rows, Hkv, D), dtype=torch.bfloat16).pin_memory()
-    e2e = []
-    for i in range(max(2, args.steps // 2)):
-        e0.record()
+
+    def e2e_step():
         k.copy_(hk, non_blocking=True)
         v.copy_(hv, non_blocking=True)
         pkg.sdpa_seq_clone(k, v, 0, cols - 1, rows)
         hcol.copy_(k[:, cols - 1], non_blocking=True)
-        e1.record()
-        torch.cuda.synchronize()
-        e2e.append(e0.elapsed_time(e1))
-    e2e_ms = statistics.mean(e2e)
+
+    e2e_step()
+    ms, _, _ = time_replays(e2e_step, max(2, args.steps // 2), flush, torch.cuda.current_stream())
+    e2e_ms = max_over_ranks(statistics.median(ms), world)
+    clocks.stop()
     if rank != 0:
         return
     cpu = None
@@ -334,19 +743,20 @@ def run_clone(args, world, rank, local):
         t0 = time.perf_counter()
         O.seq_clone(kc, kc, 0, 1, n_cpu)
         el = time.perf_counter() - t0
-        cpu = {"value": 2 * 2 * n_cpu * Hkv * D * 2 / el / 1e9, "unit": "GB/s", "cores": len(os.sched_getaffinity(0)),
-               "kind": "oracle", "sample": f"{n_cpu} rows of one column ({el:.2f} s)"}
+        model, blas = cpu_info()
+        cpu = {"value": 2 * 2 * n_cpu * Hkv * D * 2 / el / 1e9, "unit": "GB/s",
+               "cores": len(os.sched_getaffinity(0)), "kind": "oracle", "cpu_model": model, "blas_threads": blas,
+               "sample": f"{n_cpu} rows of one column ({el:.2f} s)"}
     print(json.dumps({
-        "metric": "seq_clone GB/s moved", "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": mean, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "metric": "seq_clone GB/s moved", "value": block["value"], "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": block["ms_per_step"], "ms": block["ms"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": name, "l2": "flushed between steps"},
-        "roofline": {"bound": "hbm", "achieved": moved / (mean * 1e-3) / 1e9, "peak": hbm, "unit": "GB/s",
-                     "frac": moved / (mean * 1e-3) / 1e9 / hbm, "traffic": NCU_TRAFFIC_BYTES.get("seq_clone"), "kernel": "clone",
-                     "peak_source": f"{src} HBM copy"},
-        "e2e": {"value": moved / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s", "h2d_bytes_per_step": 2 * hk.numel() * 2,
-                "d2h_bytes_per_step": hcol.numel() * 2, "ms_per_step": e2e_ms},
-        "gpu_launches": args.steps, "clocks": clk, "cpu_baseline": cpu,
+        "roofline": block["roofline"],
+        "e2e": {"value": world * moved / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                "h2d_bytes_per_step": 2 * hk.numel() * 2, "d2h_bytes_per_step": hcol.numel() * 2,
+                "ms_per_step": e2e_ms},
+        "gpu_launches": block["gpu_launches"], "clocks": block["clocks"], "cpu_baseline": cpu,
     }), flush=True)
 
 
@@ -359,6 +769,10 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="time only the headline workload (default: also every other workload)")
+    ap.add_argument("--min-config-s", type=float, default=0.25,
+                    help="shortest timed region of a per-config block, in seconds (clock samples)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -368,226 +782,70 @@ def main():
     if args.workload == "seq_clone":
         run_clone(args, world, rank, local)
         return
-    wl = synth.workload(WORKLOADS[args.workload], seed=args.seed)
     if args.impl == "reference":
-        run_reference(args, wl, world, rank)
+        run_reference(args, synth.workload(WORKLOADS[args.workload], seed=args.seed), world, rank)
         return
 
     import torch
 
-    import varlen_gqa_attention_gb300 as pkg
-
     dev = torch.device(f"cuda:{local}")
     torch.cuda.set_device(dev)
-    prefill_like = args.workload in PREFILL_LIKE
-
-    # device-resident inputs, outputs and workspaces
-    calls = []
-    T_total = max(c.row_end or c.T for c in wl.calls)
-    out = torch.empty((T_total, wl.calls[0].Hq, wl.calls[0].D), dtype=torch.bfloat16, device=dev)
-    for c in wl.calls:
-        d = dict(call=c, q=c.q.to(dev), k=c.k_store.to(dev), v=c.v_store.to(dev),
-                 seq=torch.from_numpy(c.seq_info).to(dev),
-                 ws=torch.empty(pkg.workspace_bytes(c.T, c.Hq, c.Hkv, c.D, len(c.seq_info)),
-                                dtype=torch.uint8, device=dev))
-        d["out"] = out[c.row_begin:(c.row_end or c.T)]
-        if c.seg_mode is not None:
-            d["md"] = torch.from_numpy(np.ascontiguousarray(c.seg_mode, dtype=np.int32)).to(dev)
-        if args.workload in APPEND:
-            g = torch.Generator().manual_seed(1000 + args.seed)
-            shape = (c.T, c.Hkv, c.D)
-            d["kn_host"] = torch.randn(shape, generator=g).to(torch.bfloat16)
-            d["vn_host"] = torch.randn(shape, generator=g).to(torch.bfloat16)
-            d["kn"], d["vn"] = d["kn_host"].to(dev), d["vn_host"].to(dev)
-        calls.append(d)
-
-    def attend(d):
-        c = d["call"]
-        if "kn" in d:
-            pkg.sdpa_varlen_append(d["q"], d["kn"], d["vn"], d["k"], d["v"], d["seq"], causal=c.causal,
-                                   window=c.window, scale=c.scale, out=d["out"], workspace=d["ws"])
-        elif "md" in d:
-            pkg.sdpa_varlen_modes(d["q"], d["k"], d["v"], d["seq"], d["md"], scale=c.scale, out=d["out"],
-                                  workspace=d["ws"])
-        else:
-            pkg.sdpa_varlen(d["q"], d["k"], d["v"], d["seq"], causal=c.causal, window=c.window,
-                            scale=c.scale, out=d["out"], workspace=d["ws"])
-    flops = sum(useful_work(c)[0] for c in wl.calls)
-    kv_bytes = sum(useful_work(c)[1] for c in wl.calls)
-    qo_bytes = sum(useful_work(c)[2] for c in wl.calls)
-    if args.workload in APPEND:
-        # the step's new K and V rows, read once and written once (every covered row writes:
-        # kv_end >= q_len in these workloads)
-        kv_bytes += sum(useful_work(c)[2] // (4 * c.Hq * c.D) * c.Hkv * c.D * 2 * 2 * 2 for c in wl.calls)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    stream = torch.cuda.current_stream()
-
-    def step(evs=None):
-        for i, d in enumerate(calls):
-            if evs is not None:
-                pkg.set_timing_events(evs[i])
-            attend(d)
-        if evs is not None:
-            pkg.set_timing_events(None)
-
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-
-    # The step is captured as CUDA graphs and replayed: no host submission gaps inside a step.
-    # graph_s is the step as a caller runs it (the library chains its kernels with programmatic
-    # dependent launch) and gives the timed value; graph_k has the library's timing events at
-    # every kernel boundary (each kernel then runs alone) and gives the per-kernel times that
-    # the roofline uses.
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in calls]
-    for e in (e for b in ev for e in b):
-        e.record(stream)  # torch creates the CUDA event on its first record
-    torch.cuda.synchronize()
-    graph_k = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph_k):
-        step(ev)
-    graph_s = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph_s):
-        step()
-    for _ in range(args.warmup):
-        graph_s.replay()
-        graph_k.replay()
-    torch.cuda.synchronize()
-    e_beg = torch.cuda.Event(enable_timing=True)
-    e_end = torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local)
     clocks.start()
-    barrier(world)
-    torch.cuda.synchronize()
-    step_ms = []
-    for k in range(args.steps):
-        flush.fill_(k & 0xFF)  # L2 flush outside the step's events
-        e_beg.record(stream)
-        graph_s.replay()
-        e_end.record(stream)
-        torch.cuda.synchronize()
-        step_ms.append(e_beg.elapsed_time(e_end))
-    barrier(world)
-    clk = clocks.stop()
-
-    # per-kernel breakdown, same L2 flush, outside the timed steps
-    times = []
-    for k in range(args.steps):
-        flush.fill_(k & 0xFF)
-        graph_k.replay()
-        torch.cuda.synchronize()
-        times.append([[ev[i][a].elapsed_time(ev[i][a + 1]) for a in range(4)] for i in range(len(calls))])
-    kern_ms = {"sched": [], "prefill": [], "splitk": [], "combine": []}
-    for k in range(args.steps):
-        for i in range(len(calls)):
-            e = times[k][i]
-            kern_ms["sched"].append(e[0])
-            kern_ms["prefill"].append(e[1])
-            kern_ms["splitk"].append(e[2])
-            kern_ms["combine"].append(e[3])
-    ms = statistics.mean(step_ms)
-    ms_all = max_over_ranks(ms, world)
-    if prefill_like:
-        value = world * flops / (ms_all * 1e-3) / 1e12
-        unit = "TFLOP/s"
-    else:
-        value = world * kv_bytes / (ms_all * 1e-3) / 1e9
-        unit = "GB/s"
-
-    # dominant kernel and its roofline
-    hbm, bf16, bf16_sus, peak_src = read_peaks()
-    means = {k: statistics.mean(v) * len(calls) for k, v in kern_ms.items()}
-    dom = max(("prefill", "splitk"), key=lambda k: means[k])
-    dom_ms = means[dom]
-    if prefill_like:
-        achieved = flops / (dom_ms * 1e-3) / 1e12
-        roof = {"bound": "tensor", "achieved": achieved, "peak": bf16, "unit": "TFLOP/s",
-                "frac": achieved / bf16, "traffic": NCU_TRAFFIC_BYTES.get(args.workload), "kernel": dom,
-                "peak_source": f"{peak_src} bf16 dense (burst)"}
-    else:
-        alg = kv_bytes + qo_bytes
-        achieved = alg / (dom_ms * 1e-3) / 1e9
-        roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                "frac": achieved / hbm, "traffic": NCU_TRAFFIC_BYTES.get(args.workload), "kernel": dom,
-                "peak_source": f"{peak_src} HBM copy"}
-
-    # end to end through the C interface from pinned host buffers
-    host = []
-    h2d = 0
-    for d in calls:
-        c = d["call"]
-        hq, hk, hv = c.q.pin_memory(), c.k_store.pin_memory(), c.v_store.pin_memory()
-        hs = torch.from_numpy(c.seq_info.copy()).pin_memory()
-        host.append((hq, hk, hv, hs))
-        h2d += hq.numel() * 2 + hk.numel() * 2 + hv.numel() * 2 + hs.numel() * 4
-        if "kn" in d:
-            d["kn_pin"], d["vn_pin"] = d["kn_host"].pin_memory(), d["vn_host"].pin_memory()
-            h2d += (d["kn_pin"].numel() + d["vn_pin"].numel()) * 2
-        if "md" in d:
-            d["md_pin"] = d["md"].cpu().pin_memory()
-            h2d += d["md_pin"].numel() * 4
-    hout = torch.empty(out.shape, dtype=torch.bfloat16).pin_memory()
-    d2h = hout.numel() * 2
-
-    def e2e_step():
-        for d, (hq, hk, hv, hs) in zip(calls, host):
-            d["q"].copy_(hq, non_blocking=True)
-            d["k"].copy_(hk, non_blocking=True)
-            d["v"].copy_(hv, non_blocking=True)
-            d["seq"].copy_(hs, non_blocking=True)
-            if "kn" in d:
-                d["kn"].copy_(d["kn_pin"], non_blocking=True)
-                d["vn"].copy_(d["vn_pin"], non_blocking=True)
-            if "md" in d:
-                d["md"].copy_(d["md_pin"], non_blocking=True)
-            attend(d)
-        hout.copy_(out, non_blocking=True)
-
-    for _ in range(2):
-        e2e_step()
-    torch.cuda.synchronize()
-    e2e_ms = []
-    for k in range(args.steps):
-        flush.fill_(k & 0xFF)
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        e2e_step()
-        b.record(stream)
-        torch.cuda.synchronize()
-        e2e_ms.append(a.elapsed_time(b))
-    e2e = max_over_ranks(statistics.mean(e2e_ms), world)
-    e2e_val = world * (flops if prefill_like else kv_bytes) / (e2e * 1e-3) / (1e12 if prefill_like else 1e9)
-
-    # scheduler, split-K and combine per call, plus the prefill kernel when the head group
-    # divides its 128-row tile, plus the KV append kernel on the append workload
-    launches = args.steps * sum(3 + (1 if 128 % (d["call"].Hq // d["call"].Hkv) == 0 else 0) +
-                                (1 if "kn" in d else 0) for d in calls)
+    try:
+        prep = Prepared(args.workload, args.seed, dev)
+        head = measure(prep, args.steps, args.warmup, flush, clocks, world)
+        e2e = measure_e2e(prep, args.steps, flush, world)
+        per_config = None
+        if not args.no_per_config and args.workload == "prefill_d128":
+            per_config = {"prefill_d128": {k: head[k] for k in ("workload", "value", "unit", "steps", "ms_per_step",
+                                                                "ms", "roofline", "kernel_ms", "clocks")}}
+            del prep
+            torch.cuda.empty_cache()
+            for name in PER_CONFIG[1:]:
+                if name == "seq_clone":
+                    block, _ = measure_clone(args, dev, flush, clocks, world, args.min_config_s)
+                else:
+                    p = Prepared(name, args.seed, dev)
+                    block = measure(p, args.steps, args.warmup, flush, clocks, world, args.min_config_s)
+                    del p
+                torch.cuda.empty_cache()
+                block.pop("useful_tflop_per_step", None)
+                block.pop("kv_gb_per_step", None)
+                per_config[name] = block
+    finally:
+        clocks.stop()
 
     if rank != 0:
         return
+    wl = synth.workload(WORKLOADS[args.workload], seed=args.seed)
     base = None
     if not args.no_cpu_baseline:
-        base = cpu_baseline(wl, prefill_like)
+        base = cpu_baseline(wl, args.workload in PREFILL_LIKE)
     vs = None
     if args.workload == "prefill_d128":
-        vs = value / 160.1  # RTX 5090 Triton TMA, 27.039 ms on this shape (pages' operator table)
+        vs = head["value"] / 160.1  # RTX 5090 Triton TMA, 27.039 ms on this shape (pages' operator table)
+    # kernels of this library launched in the headline's timed region (each per-config block
+    # counts its own)
+    launches = head["gpu_launches"]
     line = {
-        "metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms_all, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": vs, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": wl.name + ("+kv_append" if args.workload in APPEND else ""),
-                   "description": wl.description, "seed": args.seed,
+        "metric": METRIC, "value": head["value"], "unit": head["unit"], "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "ms": head["ms"], "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": vs, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": head["workload"], "description": wl.description, "seed": args.seed,
                    "l2": "flushed between steps (512 MiB write outside the step's events)",
                    "parallelism": "replicas" if world > 1 else "single GPU",
-                   "useful_tflop_per_step": flops / 1e12, "kv_gb_per_step": kv_bytes / 1e9},
-        "roofline": roof,
-        "kernel_ms": {k: statistics.mean(v) for k, v in kern_ms.items()},
-        "e2e": {"value": e2e_val, "unit": unit, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": e2e},
+                   "useful_tflop_per_step": head["useful_tflop_per_step"], "kv_gb_per_step": head["kv_gb_per_step"]},
+        "roofline": head["roofline"],
+        "kernel_ms": head["kernel_ms"],
+        "e2e": e2e,
         "gpu_launches": launches,
-        "clocks": clk,
+        "clocks": head["clocks"],
         "cpu_baseline": base,
     }
+    if per_config:
+        line["per_config"] = per_config
     print(json.dumps(line), flush=True)
 
 

@@ -118,4 +118,46 @@ def test_reference_arm_prints_one_contract_line_on_the_cpu():
         assert key in d, key
     assert d["impl"] == "reference" and d["steps"] == 1 and d["warmup"] >= 3 and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
+    assert "cpu_model" in d["cpu_baseline"] and "blas_threads" in d["cpu_baseline"]
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_clock_window_takes_only_the_samples_inside_it():
+    # (time, sm_mhz, max_mhz, reason bits, power W)
+    samples = [(0.5, 900.0, 2070.0, 0x1, 100.0),        # before: idle, lower clock
+               (1.0, 2070.0, 2070.0, 0x0, 800.0),
+               (1.1, 2040.0, 2070.0, 0x4, 1390.0),      # power cap inside the window
+               (1.2, 2070.0, 2070.0, 0x0, 900.0),
+               (2.5, 1200.0, 2070.0, 0x40, 700.0)]      # after: thermal, outside the window
+    w = bench.summarize_clocks(samples, 1.0, 1.2, "test")
+    assert w["samples"] == 3 and w["sm_mhz"] == 2070.0 and w["sm_min_mhz"] == 2040.0
+    assert w["sm_max_mhz"] == 2070.0 and w["reasons"] == ["sw_power_cap"] and w["power_w_max"] == 1390.0
+    empty = bench.summarize_clocks(samples, 3.0, 4.0, "test")
+    assert empty["samples"] == 0 and empty["sm_mhz"] is None and "note" in empty
+
+
+def test_step_statistics_are_median_mean_and_deciles():
+    ms = [1.0 + 0.1 * k for k in range(11)]  # 1.0 .. 2.0
+    st = bench.percentiles(ms)
+    assert st["median"] == pytest.approx(1.5) and st["mean"] == pytest.approx(1.5)
+    assert st["p10"] == pytest.approx(1.1) and st["p90"] == pytest.approx(1.9) and st["n"] == 11
+
+
+def test_stored_traffic_goes_null_when_the_kernel_source_changes(monkeypatch):
+    name = next(iter(bench.NCU_TRAFFIC))
+    nbytes, kind, sha = bench.NCU_TRAFFIC[name]
+    monkeypatch.setitem(bench.NCU_TRAFFIC, name, (nbytes, kind, bench.kernel_sha(kind)))
+    assert bench.ncu_traffic(name) == nbytes
+    monkeypatch.setitem(bench.NCU_TRAFFIC, name, (nbytes, kind, "0" * 16))
+    assert bench.ncu_traffic(name) is None
+    assert bench.ncu_traffic("no such workload") is None
+
+
+def test_every_per_config_workload_is_known_and_builds():
+    for name in bench.PER_CONFIG:
+        assert name in bench.WORKLOADS
+    for name in ("prefill_d256", "ring_prefill"):
+        wl = synth.workload(bench.WORKLOADS[name])
+        flops, kv, _ = bench.useful_work(wl.calls[0])
+        c = wl.calls[0]
+        assert flops == O.useful_flops(c.seq_info, c.T, c.Hq, c.D, c.causal, c.window, c.rows, c.cols) > 0

@@ -191,9 +191,29 @@ def mixed_step_one_store(seed: int = 0, n_target: int = 8, n_draft: int = 8, Hq:
                     f"(per-segment modes)")
 
 
+def ring_window_prefill(seed: int = 0, Hq: int = 16, Hkv: int = 2, D: int = 128, window: int = 4096,
+                        q_len: int = 2048, kv_end: int = 60000) -> Workload:
+    """A long sliding-window prefill chunk on a ring store: one segment of q_len queries whose
+    keys [kv_end - q_len - window + 1, kv_end) wrap around a ring of window + q_len - 1 rows
+    (the ring size of "[executorch][cuda] Add a length-aware Triton SDPA over per-sequence KV
+    columns", #24073 commit: window + max_write - 1, with max_write = q_len).  Column 1 is the
+    scratch column."""
+    rows, cols = window + q_len - 1, 2
+    gen = torch.Generator().manual_seed(seed)
+    q = _randn_bf16(gen, (q_len, Hq, D))
+    k = _randn_bf16(gen, (rows, cols, Hkv, D))
+    v = _randn_bf16(gen, (rows, cols, Hkv, D))
+    c = Call(q_len, Hq, Hkv, D, rows, cols, _seq_info([(0, q_len, 0, kv_end)]), True, window,
+             1.0 / math.sqrt(D), q, k, v)
+    return Workload(f"ring_window_prefill_w{window}_q{q_len}_kv{kv_end}_d{D}", [c],
+                    f"S=1 Hq={Hq} Hkv={Hkv} D={D} causal W={window} q_len={q_len} kv_end={kv_end} "
+                    f"on a ring of {rows} rows (keys wrap)")
+
+
 def workload(index: int, seed: int = 0) -> Workload:
-    """The measured shapes, in order: tiny, D=64 prefill, D=128 prefill, decode, mixed, and the
-    mixed step as one call with per-segment modes."""
+    """The measured shapes, in order: tiny, D=64 prefill, D=128 prefill, decode, mixed, the
+    mixed step as one call with per-segment modes, a D=256 prefill, and a windowed prefill
+    chunk on a ring store."""
     if index == 0:
         return tiny_causal_prefill(seed)
     if index == 1:
@@ -206,6 +226,10 @@ def workload(index: int, seed: int = 0) -> Workload:
         return mixed_step(seed)
     if index == 5:
         return mixed_step_one_store(seed)
+    if index == 6:
+        return long_causal_prefill(256, 4096, 32768, seed)
+    if index == 7:
+        return ring_window_prefill(seed)
     raise ValueError(f"no workload {index}")
 
 

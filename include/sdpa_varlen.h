@@ -22,8 +22,9 @@
  *  - bf16 tensors hold IEEE bfloat16 values (uint16 bit patterns).
  *  - Strides are in elements.  The innermost (head-dim) stride is always 1.
  *  - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default stream).  No call
- *    synchronises the host, so all of them may be captured into a CUDA graph.  Lengths
- *    are read on the device: one captured graph serves any seq_info contents.
+ *    but the status read-back sdpa_workspace_status synchronises the host, so all the others
+ *    may be captured into a CUDA graph.  Lengths are read on the device: one captured graph
+ *    serves any seq_info contents.
  *  - The return value reports argument checks (made before any CUDA call) and launch
  *    errors.  Errors inside a segment table are reported through `status_dev`.
  *  - sdpa_last_error() returns a thread-local message describing the last failure.
@@ -207,6 +208,8 @@ sdpa_status sdpa_set_timing_events(void* const* events, int n);
  * does not fit return SDPA_ERR_WORKSPACE (sdpa_last_error() says how much they need).
  * The first call on each device looks up the array's device address (with that device
  * current) and configures the kernels: make that first call before any stream capture.
+ * The address is kept until the process exits, which assumes the device's primary context
+ * lives as long: after cudaDeviceReset on a device, do not call this entry point there again.
  * All calls on a device share the one array and it keeps the last call's contents; nothing
  * in it needs to start at zero, but calls that overlap on the GPU (different streams, or
  * graphs replayed at the same time) race on it and must be serialised by the caller.
@@ -225,6 +228,18 @@ sdpa_status sdpa_varlen_splitk_static(const void* q, int64_t T, int Hq, int D, i
  * is fixed once per device, on first use.
  */
 int sdpa_prefill_available(int D);
+
+/*
+ * Status of the last call that used `workspace` (sdpa_varlen, _append, _modes or
+ * sdpa_causal_prefill), for callers that passed no status_dev: the OR of the SDPA_SEG_* bits
+ * its scheduler found and SDPA_DEV_TIMEOUT when one of its bounded device waits gave up (its
+ * output is then unspecified).  Waits for `stream` (cudaStream_t) to finish, then copies the
+ * word to *status_host, so it synchronises the host and cannot be captured in a graph; a
+ * caller that checks every replay of a graph passes status_dev instead.  Errors:
+ * SDPA_ERR_NULL, _ALIGN (workspace not 256-byte aligned), _WORKSPACE (ws_bytes smaller than
+ * the header), _CUDA.
+ */
+sdpa_status sdpa_workspace_status(const void* workspace, size_t ws_bytes, int32_t* status_host, void* stream);
 
 /* Message describing the last failure on this thread ("" if none). */
 const char* sdpa_last_error(void);

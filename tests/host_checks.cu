@@ -97,6 +97,49 @@ int main() {
         // every unit a route can produce fits: live segments cover disjoint rows
         CHECK(ws.unit_cap[kRouteSplitk] >= (int64_t)Hkv * ((T * (Hq / Hkv) + kSplitkRows - 1) / kSplitkRows));
       }
+  // the split-K-only layout of the allocation-free entry: the same regions, the prefill
+  // route's tables empty, inside the bytes it reports and no larger than the full layout
+  for (int64_t T : Ts)
+    for (int S : Ss)
+      for (int D : Ds) {
+        const int Hq = 16, Hkv = 2;
+        const int64_t gs = 304;
+        Workspace ws{};
+        char* base = (char*)(uintptr_t)4096;
+        const size_t need = layout_workspace(base, T, Hq, Hkv, D, S, gs, 0, &ws, false);
+        CHECK(need == layout_workspace(nullptr, T, Hq, Hkv, D, S, gs, 0, nullptr, false));
+        CHECK(need <= layout_workspace(nullptr, T, Hq, Hkv, D, S, gs, 152, nullptr, true));
+        CHECK(ws.unit_cap[kRoutePrefill] == 0 && ws.part_cap[kRoutePrefill] == 0);
+        CHECK(ws.unit_cap[kRouteSplitk] == unit_cap(T, Hq, Hkv, S, kSplitkRows));
+        CHECK(ws.part_cap[kRouteSplitk] >= (ws.unit_cap[kRouteSplitk] + (int64_t)kPartPhases * gs + 1) * kSplitkRows);
+        struct R {
+          const void* p;
+          int64_t bytes;
+        };
+        std::vector<R> rs = {{ws.hdr, (int64_t)sizeof(SchedHdr)},
+                             {ws.segs, (int64_t)sizeof(SegRec) * S},
+                             {ws.row_seg, 4 * T},
+                             {ws.row_info, 16 * T},
+                             {ws.seg_flag, 4 * (int64_t)S},
+                             {ws.arrive, 4 * ws.unit_cap[kRouteSplitk]},
+                             {ws.units[kRouteSplitk], (int64_t)sizeof(UnitRec) * ws.unit_cap[kRouteSplitk]},
+                             {ws.first_unit[kRouteSplitk], 4 * (int64_t)kMaxPhases * gs},
+                             {ws.part_ml[kRouteSplitk], 8 * ws.part_cap[kRouteSplitk]},
+                             {ws.part_o[kRouteSplitk], 4 * ws.part_cap[kRouteSplitk] * D}};
+        std::sort(rs.begin(), rs.end(), [](const R& x, const R& y) { return x.p < y.p; });
+        for (size_t k = 0; k < rs.size(); ++k) {
+          const uintptr_t a = (uintptr_t)rs[k].p;
+          CHECK(a % 256 == 0);
+          CHECK(a >= (uintptr_t)base && a + rs[k].bytes <= (uintptr_t)base + need);
+          if (k + 1 < rs.size()) CHECK(a + rs[k].bytes <= (uintptr_t)rs[k + 1].p);
+        }
+      }
+  // scratch the allocation-free entry needs for the fallback-grid test case (T=2048 packed
+  // rows, Hq=16, Hkv=2, D=128, S=8) at the general grid of a 152-SM GB300 (2 split-K CTAs per
+  // SM at D=128) and at one CTA per SM: "STATIC_NEED grid bytes"
+  for (int64_t g : {304, 152})
+    std::printf("STATIC_NEED %lld %zu\n", (long long)g,
+                layout_workspace(nullptr, 2048, 16, 2, 128, 8, g, 0, nullptr, false));
   // segment_bits on a grid: "q_start q_len col kv_end T rows cols window bits"
   const int64_t vals_q[] = {-1, 0, 3};
   const int64_t lens[] = {-1, 0, 1, 5};

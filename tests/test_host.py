@@ -137,3 +137,97 @@ def test_per_segment_mode_table_is_checked_before_any_cuda_call():
     assert _call_modes(None)[0] == 1          # SDPA_ERR_NULL
     code, msg = _call_modes(FAKE + 8)         # not 16-byte aligned
     assert code == 6 and "seg_mode" in msg    # SDPA_ERR_ALIGN
+
+
+def _call_static(**kw):
+    a = dict(q=FAKE, T=8, Hq=4, D=64, q_rs=256, q_hs=64, k=FAKE, v=FAKE, rows=16, cols=2, Hkv=2,
+             seq=FAKE, S=1, causal=1, window=0, scale=0.125, out=FAKE, o_rs=256, o_hs=64, status=None,
+             stream=None)
+    a.update(kw)
+    lib = pkg.library()
+    code = lib.sdpa_varlen_splitk_static(a["q"], a["T"], a["Hq"], a["D"], a["q_rs"], a["q_hs"], a["k"], a["v"],
+                                         a["rows"], a["cols"], a["Hkv"], a["seq"], a["S"], a["causal"],
+                                         a["window"], a["scale"], a["out"], a["o_rs"], a["o_hs"], a["status"],
+                                         a["stream"])
+    return code, lib.sdpa_last_error().decode()
+
+
+@pytest.mark.parametrize("kw", [
+    dict(D=96), dict(Hq=6, Hkv=4), dict(Hq=256, Hkv=1), dict(T=-1), dict(S=-1), dict(rows=0), dict(cols=0),
+    dict(window=-3), dict(scale=float("nan")), dict(q=None), dict(out=None), dict(seq=None),
+    dict(q=FAKE + 2), dict(out=FAKE + 8), dict(q_rs=250), dict(o_hs=3),
+    dict(T=(1 << 40) // 64 + 1, Hq=128, Hkv=1),  # Hq * T beyond 2^40
+])
+def test_static_entry_rejects_what_sdpa_varlen_rejects_with_the_same_message(kw):
+    code, msg = _call_static(**kw)
+    ref_code, ref_msg = _call(**kw)
+    assert code == ref_code and code != 0, (code, msg)
+    assert msg == ref_msg
+
+
+def test_workspace_status_checks_its_arguments_before_any_cuda_call():
+    import ctypes
+
+    lib = pkg.library()
+    v = ctypes.c_int32(0)
+    assert lib.sdpa_workspace_status(None, 1 << 20, ctypes.byref(v), None) == 1
+    assert lib.sdpa_workspace_status(FAKE, 1 << 20, None, None) == 1
+    assert lib.sdpa_workspace_status(FAKE + 16, 1 << 20, ctypes.byref(v), None) == 6
+    assert lib.sdpa_workspace_status(FAKE, 8, ctypes.byref(v), None) == 7
+
+
+def _cpu_args(**kw):
+    import torch
+
+    a = dict(q=torch.zeros(8, 4, 64, dtype=torch.bfloat16), k=torch.zeros(16, 2, 2, 64, dtype=torch.bfloat16),
+             v=torch.zeros(16, 2, 2, 64, dtype=torch.bfloat16), seq=torch.zeros(1, 4, dtype=torch.int32))
+    a.update(kw)
+    return a
+
+
+def _bad_inputs():
+    import torch
+
+    bf = torch.bfloat16
+    return [
+        ("fp16 q", _cpu_args(q=torch.zeros(8, 4, 64, dtype=torch.float16)), "q must be bf16"),
+        ("fp32 store", _cpu_args(k=torch.zeros(16, 2, 2, 64)), "k_store must be bf16"),
+        ("int64 table", _cpu_args(seq=torch.zeros(1, 4, dtype=torch.int64)), "seq_info"),
+        ("table of 3 columns", _cpu_args(seq=torch.zeros(1, 3, dtype=torch.int32)), "seq_info"),
+        ("strided store", _cpu_args(k=torch.zeros(16, 4, 2, 64, dtype=bf)[:, ::2],
+                                    v=torch.zeros(16, 4, 2, 64, dtype=bf)[:, ::2]), "contiguous"),
+        ("q inner stride 2", _cpu_args(q=torch.zeros(8, 4, 128, dtype=bf)[:, :, ::2]), "inner stride"),
+        ("head dims differ", _cpu_args(q=torch.zeros(8, 4, 128, dtype=bf)), "head dims"),
+        ("3-d store", _cpu_args(k=torch.zeros(16, 2, 64, dtype=bf), v=torch.zeros(16, 2, 64, dtype=bf)), "stores"),
+        ("host tensors", _cpu_args(), "CUDA device"),
+    ]
+
+
+@pytest.mark.parametrize("entry", ["sdpa_varlen", "sdpa_varlen_splitk_static", "sdpa_varlen_modes",
+                                   "sdpa_varlen_append"])
+def test_python_entries_reject_bad_tensors_before_the_library_call(entry):
+    import torch
+
+    for what, a, needle in _bad_inputs():
+        f = getattr(pkg, entry)
+        with pytest.raises(ValueError) as ei:
+            if entry == "sdpa_varlen_modes":
+                f(a["q"], a["k"], a["v"], a["seq"], torch.zeros(a["seq"].shape[0], 2, dtype=torch.int32))
+            elif entry == "sdpa_varlen_append":
+                kn = torch.zeros(a["q"].shape[0], a["k"].shape[-2] if a["k"].dim() == 4 else 2, a["q"].shape[-1],
+                                 dtype=torch.bfloat16)
+                f(a["q"], kn, kn, a["k"], a["v"], a["seq"], causal=True)
+            else:
+                f(a["q"], a["k"], a["v"], a["seq"], causal=True)
+        assert needle in str(ei.value), (entry, what, str(ei.value))
+
+
+def test_python_static_entry_checks_out_and_status():
+    import torch
+
+    a = _cpu_args()
+    with pytest.raises(ValueError, match="out must be bf16"):
+        pkg.sdpa_varlen_splitk_static(a["q"], a["k"], a["v"], a["seq"], causal=True,
+                                      out=torch.zeros(8, 4, 32, dtype=torch.bfloat16))
+    with pytest.raises(ValueError, match="seg_mode"):
+        pkg.sdpa_varlen_modes(a["q"], a["k"], a["v"], a["seq"], torch.zeros(1, 3, dtype=torch.int32))

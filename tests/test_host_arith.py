@@ -42,3 +42,13 @@ def test_segment_validity_rule_matches_the_oracle(host_checks):
         qs, ql, col, ke, T, nrows, cols, w, bits = (int(x) for x in r)
         want = O.segment_status(np.array([qs, ql, col, ke]), T, nrows, cols, w)
         assert bits == want, (qs, ql, col, ke, w, bits, want)
+
+
+def test_the_static_entry_fallback_case_needs_the_reduced_grid(host_checks):
+    """The case tests/test_zz_no_alloc.py runs to reach the allocation-free entry's reduced
+    grid: its scratch does not fit the 32 MiB array at the general grid (two split-K CTAs
+    per SM on a 152-SM GB300) but fits at one CTA per SM."""
+    _, out = host_checks
+    need = {int(g): int(b) for g, b in (ln.split()[1:] for ln in out.splitlines() if ln.startswith("STATIC_NEED"))}
+    cap = 32 << 20
+    assert need[304] > cap >= need[152], need

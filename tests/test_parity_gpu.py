@@ -119,6 +119,23 @@ def test_invalid_segments_set_status_and_zero_rows(dev, route):
     check_call(call, dev, tag="invalid")
 
 
+def test_workspace_status_reads_back_the_calls_status_bits(dev, route):
+    """Without status_dev, the status of the last call is read back from its workspace."""
+    call = synth.random_call(np.random.default_rng(9), D=64, Hq=4, Hkv=2, T=40, S=2, rows=64, cols=2,
+                             causal=True, window=0, max_q=8, max_kv=60, gen_seed=4, allow_gaps=False)
+    tables = [np.array([[0, 5, 0, 20], [5, 3, 2, 10], [9, 4, 1, 65], [20, 3, 1, 12], [22, 2, 0, 5]],
+                       dtype=np.int32),
+              np.array([[0, 5, 0, 20], [20, 3, 1, 12]], dtype=np.int32)]
+    ws = torch.full((pkg.workspace_bytes(call.T, call.Hq, call.Hkv, call.D, 5),), 255, dtype=torch.uint8,
+                    device=dev)
+    q, k, v = call.q.to(dev), call.k_store.to(dev), call.v_store.to(dev)
+    for tab in tables:
+        seq = torch.from_numpy(tab).to(dev)
+        pkg.sdpa_varlen(q, k, v, seq, causal=True, scale=call.scale, workspace=ws)
+        _, _, _, st = O.visible_interval(tab, call.T, True, 0, call.rows, call.cols)
+        assert pkg.workspace_status(ws) == st  # the second table is clean: 0
+
+
 def test_nan_in_invisible_cells_changes_no_output_bit(dev, route):
     wl = synth.batched_decode(seed=1, S=8, rows=2048)
     call = wl.calls[0]

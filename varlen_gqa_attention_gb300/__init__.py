@@ -20,7 +20,7 @@ from . import _build
 
 __all__ = [
     "sdpa_varlen", "sdpa_varlen_modes", "sdpa_varlen_append", "sdpa_seq_clone", "sdpa_causal_prefill",
-    "sdpa_varlen_splitk_static", "workspace_bytes", "prefill_available", "set_route_policy",
+    "sdpa_varlen_splitk_static", "workspace_bytes", "workspace_status", "prefill_available", "set_route_policy",
     "set_timing_events", "library",
     "SDPA_OK", "SEG_BAD_QRANGE", "SEG_BAD_COL", "SEG_BAD_KV", "SEG_SPAN", "SEG_OVERLAP",
     "DEV_TIMEOUT", "ROUTE_AUTO", "ROUTE_SPLITK", "ROUTE_PREFILL", "SdpaError",
@@ -40,6 +40,7 @@ EXPORTS = [
     "sdpa_varlen_workspace_bytes", "sdpa_varlen", "sdpa_causal_prefill", "sdpa_set_route_policy",
     "sdpa_set_timing_events", "sdpa_last_error", "sdpa_version", "sdpa_varlen_splitk_static",
     "sdpa_varlen_append", "sdpa_seq_clone", "sdpa_varlen_modes", "sdpa_prefill_available",
+    "sdpa_workspace_status",
 ]
 
 
@@ -93,6 +94,12 @@ def library(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.sdpa_prefill_available.argtypes = [c_int]
     lib.sdpa_version.restype = c_int
     lib.sdpa_version.argtypes = []
+    lib.sdpa_varlen_splitk_static.restype = c_int
+    lib.sdpa_varlen_splitk_static.argtypes = [c_vp, c_i64, c_int, c_int, c_i64, c_i64, c_vp, c_vp, c_i64, c_int,
+                                              c_int, c_vp, c_int, c_int, c_int, c_f, c_vp, c_i64, c_i64, c_vp,
+                                              c_vp]
+    lib.sdpa_workspace_status.restype = c_int
+    lib.sdpa_workspace_status.argtypes = [c_vp, ctypes.c_size_t, ctypes.POINTER(ctypes.c_int32), c_vp]
     _lib = lib
     return lib
 
@@ -104,6 +111,15 @@ def _check(code: int):
 
 def workspace_bytes(T: int, Hq: int, Hkv: int, D: int, S: int) -> int:
     return int(library().sdpa_varlen_workspace_bytes(T, Hq, Hkv, D, S))
+
+
+def workspace_status(workspace: torch.Tensor, stream=None) -> int:
+    """Status word of the last call that used ``workspace``: its SDPA_SEG_* bits and
+    DEV_TIMEOUT.  Waits for the stream, so it is not for use inside graph capture."""
+    v = ctypes.c_int32(0)
+    _check(library().sdpa_workspace_status(workspace.data_ptr(), workspace.numel(), ctypes.byref(v),
+                                           _stream_ptr(stream)))
+    return int(v.value)
 
 
 def prefill_available(D: int) -> bool:
@@ -147,6 +163,38 @@ def _stream_ptr(stream) -> int:
     return s.cuda_stream
 
 
+def _check_attention_args(q, k_store, v_store, seq_info, out=None, seg_mode=None):
+    """The tensor checks every attention entry makes before its C call: shapes, dtypes
+    (bf16 data, int32 tables), layouts (contiguous stores and tables, unit inner strides) and
+    one CUDA device for all of them.  Raises ValueError; returns (T, Hq, D, rows, cols, Hkv, S)."""
+    if q.dim() != 3 or k_store.dim() != 4 or tuple(v_store.shape) != tuple(k_store.shape):
+        raise ValueError("q must be [T, Hq, D] and the stores [rows, cols, Hkv, D]")
+    for name, t in (("q", q), ("k_store", k_store), ("v_store", v_store)):
+        if t.dtype != torch.bfloat16:
+            raise ValueError(f"{name} must be bf16, not {t.dtype}")
+    T, Hq, D = q.shape
+    rows, cols, Hkv, Dk = k_store.shape
+    if Dk != D:
+        raise ValueError("head dims of q and the stores differ")
+    if q.stride(2) != 1:
+        raise ValueError("q must have unit inner stride")
+    if not (k_store.is_contiguous() and v_store.is_contiguous()):
+        raise ValueError("k_store and v_store must be contiguous")
+    if seq_info.dtype != torch.int32 or not seq_info.is_contiguous() or \
+            (seq_info.numel() and (seq_info.dim() != 2 or seq_info.shape[1] != 4)):
+        raise ValueError("seq_info must be a contiguous int32 [S, 4] tensor")
+    S = seq_info.shape[0] if seq_info.numel() else 0
+    if out is not None and (out.dtype != torch.bfloat16 or tuple(out.shape) != (T, Hq, D) or out.stride(2) != 1):
+        raise ValueError("out must be bf16 [T, Hq, D] with unit inner stride")
+    if seg_mode is not None:
+        if seg_mode.dtype != torch.int32 or not seg_mode.is_contiguous() or (S and tuple(seg_mode.shape) != (S, 2)):
+            raise ValueError("seg_mode must be a contiguous int32 [S, 2] tensor")
+    tensors = [q, k_store, v_store, seq_info] + [t for t in (out, seg_mode) if t is not None]
+    if not all(t.is_cuda for t in tensors) or len({t.device for t in tensors}) != 1:
+        raise ValueError("every tensor must be on the same CUDA device")
+    return T, Hq, D, rows, cols, Hkv, S
+
+
 def sdpa_varlen(q: torch.Tensor, k_store: torch.Tensor, v_store: torch.Tensor, seq_info: torch.Tensor,
                 *, causal: bool, window: int = 0, scale: Optional[float] = None,
                 out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
@@ -157,29 +205,12 @@ def sdpa_varlen(q: torch.Tensor, k_store: torch.Tensor, v_store: torch.Tensor, s
     contiguous; seq_info: int32 [S, 4] contiguous on the same device.  ``status`` (an int32
     device tensor, optional) receives the OR of the device status bits.
     """
+    T, Hq, D, rows, cols, Hkv, S = _check_attention_args(q, k_store, v_store, seq_info, out)
     lib = library()
-    if q.dim() != 3 or k_store.dim() != 4 or tuple(v_store.shape) != tuple(k_store.shape):
-        raise ValueError("q must be [T, Hq, D] and the stores [rows, cols, Hkv, D]")
-    for name, t in (("q", q), ("k_store", k_store), ("v_store", v_store)):
-        if t.dtype != torch.bfloat16 or not t.is_cuda:
-            raise ValueError(f"{name} must be a bf16 CUDA tensor")
-    if not (k_store.is_contiguous() and v_store.is_contiguous()):
-        raise ValueError("k_store and v_store must be contiguous")
-    if seq_info.dtype != torch.int32 or not seq_info.is_cuda or not seq_info.is_contiguous():
-        raise ValueError("seq_info must be a contiguous int32 CUDA tensor")
-    T, Hq, D = q.shape
-    rows, cols, Hkv, Dk = k_store.shape
-    if Dk != D:
-        raise ValueError("head dims of q and the stores differ")
-    if q.stride(2) != 1:
-        raise ValueError("q must have unit inner stride")
-    S = seq_info.shape[0] if seq_info.numel() else 0
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     if out is None:
         out = _on_stream(torch.empty((T, Hq, D), dtype=torch.bfloat16, device=q.device), stream)
-    elif out.dtype != torch.bfloat16 or tuple(out.shape) != (T, Hq, D) or out.stride(2) != 1:
-        raise ValueError("out must be bf16 [T, Hq, D] with unit inner stride")
     need = workspace_bytes(T, Hq, Hkv, D, S)
     if workspace is None:
         workspace = _workspace(need, q.device, stream)
@@ -204,31 +235,19 @@ def sdpa_varlen_append(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor
     query row t; they go to store row (kv_end - q_len + i) % rows of each live segment's
     column.  The stores are modified in place; everything else is as ``sdpa_varlen``.
     """
-    lib = library()
-    if q.dim() != 3 or k_store.dim() != 4 or tuple(v_store.shape) != tuple(k_store.shape):
-        raise ValueError("q must be [T, Hq, D] and the stores [rows, cols, Hkv, D]")
-    T, Hq, D = q.shape
-    rows, cols, Hkv, Dk = k_store.shape
-    for name, t in (("q", q), ("k_new", k_new), ("v_new", v_new), ("k_store", k_store), ("v_store", v_store)):
-        if t.dtype != torch.bfloat16 or not t.is_cuda:
-            raise ValueError(f"{name} must be a bf16 CUDA tensor")
+    T, Hq, D, rows, cols, Hkv, S = _check_attention_args(q, k_store, v_store, seq_info, out)
+    for name, t in (("k_new", k_new), ("v_new", v_new)):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or t.device != q.device:
+            raise ValueError(f"{name} must be a bf16 tensor on q's CUDA device")
     if tuple(k_new.shape) != (T, Hkv, D) or tuple(v_new.shape) != (T, Hkv, D):
         raise ValueError("k_new and v_new must be [T, Hkv, D]")
     if k_new.stride() != v_new.stride() or k_new.stride(2) != 1:
         raise ValueError("k_new and v_new must share strides, with unit inner stride")
-    if not (k_store.is_contiguous() and v_store.is_contiguous()):
-        raise ValueError("k_store and v_store must be contiguous")
-    if seq_info.dtype != torch.int32 or not seq_info.is_cuda or not seq_info.is_contiguous():
-        raise ValueError("seq_info must be a contiguous int32 CUDA tensor")
-    if Dk != D or q.stride(2) != 1:
-        raise ValueError("head dims differ, or q has a non-unit inner stride")
-    S = seq_info.shape[0] if seq_info.numel() else 0
+    lib = library()
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     if out is None:
         out = _on_stream(torch.empty((T, Hq, D), dtype=torch.bfloat16, device=q.device), stream)
-    elif out.dtype != torch.bfloat16 or tuple(out.shape) != (T, Hq, D) or out.stride(2) != 1:
-        raise ValueError("out must be bf16 [T, Hq, D] with unit inner stride")
     if workspace is None:
         workspace = _workspace(workspace_bytes(T, Hq, Hkv, D, S), q.device, stream)
     st_ptr = status.data_ptr() if status is not None else None
@@ -248,30 +267,12 @@ def sdpa_varlen_modes(q: torch.Tensor, k_store: torch.Tensor, v_store: torch.Ten
                       stream=None) -> torch.Tensor:
     """``sdpa_varlen`` with a mask mode per segment: seg_mode int32 [S, 2] = (causal, window)
     on the device, in place of the call's causal / window."""
+    T, Hq, D, rows, cols, Hkv, S = _check_attention_args(q, k_store, v_store, seq_info, out, seg_mode)
     lib = library()
-    if q.dim() != 3 or k_store.dim() != 4 or tuple(v_store.shape) != tuple(k_store.shape):
-        raise ValueError("q must be [T, Hq, D] and the stores [rows, cols, Hkv, D]")
-    for name, t in (("q", q), ("k_store", k_store), ("v_store", v_store)):
-        if t.dtype != torch.bfloat16 or not t.is_cuda:
-            raise ValueError(f"{name} must be a bf16 CUDA tensor")
-    if not (k_store.is_contiguous() and v_store.is_contiguous()):
-        raise ValueError("k_store and v_store must be contiguous")
-    for name, t in (("seq_info", seq_info), ("seg_mode", seg_mode)):
-        if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
-            raise ValueError(f"{name} must be a contiguous int32 CUDA tensor")
-    T, Hq, D = q.shape
-    rows, cols, Hkv, Dk = k_store.shape
-    S = seq_info.shape[0] if seq_info.numel() else 0
-    if tuple(seg_mode.shape) != (S, 2) and S:
-        raise ValueError("seg_mode must be [S, 2]")
-    if Dk != D or q.stride(2) != 1:
-        raise ValueError("head dims differ, or q has a non-unit inner stride")
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     if out is None:
         out = _on_stream(torch.empty((T, Hq, D), dtype=torch.bfloat16, device=q.device), stream)
-    elif out.dtype != torch.bfloat16 or tuple(out.shape) != (T, Hq, D) or out.stride(2) != 1:
-        raise ValueError("out must be bf16 [T, Hq, D] with unit inner stride")
     if workspace is None:
         workspace = _workspace(workspace_bytes(T, Hq, Hkv, D, S), q.device, stream)
     st_ptr = status.data_ptr() if status is not None else None
@@ -331,23 +332,19 @@ def sdpa_varlen_splitk_static(q: torch.Tensor, k_store: torch.Tensor, v_store: t
     """sdpa_varlen for callers that cannot allocate device scratch: the library's own static
     device array (SDPA_STATIC_SCRATCH_BYTES) serves as the workspace and every segment runs on
     the split-K kernel.  Pass ``out`` to allocate nothing at all.  Calls must not overlap on
-    the GPU (they share the array); make the first call on a device outside stream capture."""
+    the GPU (they share the array); make the first call on a device outside stream capture.
+    The tensors are checked as for ``sdpa_varlen``."""
+    T, Hq, D, rows, cols, Hkv, S = _check_attention_args(q, k_store, v_store, seq_info, out)
+    if status is not None and (status.dtype != torch.int32 or status.device != q.device):
+        raise ValueError("status must be an int32 tensor on q's CUDA device")
     lib = library()
-    fn = lib.sdpa_varlen_splitk_static
-    c_i64, c_int, c_vp, c_f = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_float
-    fn.restype = c_int
-    fn.argtypes = [c_vp, c_i64, c_int, c_int, c_i64, c_i64, c_vp, c_vp, c_i64, c_int, c_int, c_vp,
-                   c_int, c_int, c_int, c_f, c_vp, c_i64, c_i64, c_vp, c_vp]
-    T, Hq, D = q.shape
-    rows, cols, Hkv, _ = k_store.shape
-    S = seq_info.shape[0] if seq_info.numel() else 0
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     if out is None:
         out = _on_stream(torch.empty((T, Hq, D), dtype=torch.bfloat16, device=q.device), stream)
-    code = fn(q.data_ptr(), T, Hq, D, q.stride(0), q.stride(1), k_store.data_ptr(), v_store.data_ptr(),
-              rows, cols, Hkv, seq_info.data_ptr() if S else None, S, int(bool(causal)), int(window),
-              float(scale), out.data_ptr(), out.stride(0), out.stride(1),
-              status.data_ptr() if status is not None else None, _stream_ptr(stream))
+    code = lib.sdpa_varlen_splitk_static(
+        q.data_ptr(), T, Hq, D, q.stride(0), q.stride(1), k_store.data_ptr(), v_store.data_ptr(), rows, cols, Hkv,
+        seq_info.data_ptr() if S else None, S, int(bool(causal)), int(window), float(scale), out.data_ptr(),
+        out.stride(0), out.stride(1), status.data_ptr() if status is not None else None, _stream_ptr(stream))
     _check(code)
     return out

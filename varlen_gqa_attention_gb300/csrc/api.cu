@@ -160,8 +160,8 @@ static Grids grids_for(const DevInfo& di, int D) {
   return g;
 }
 
-static sdpa_status check_common(int64_t T, int Hq, int Hkv, int D, int S, int64_t rows, int cols,
-                                int window, float scale) {
+sdpa_status check_common(int64_t T, int Hq, int Hkv, int D, int S, int64_t rows, int cols, int window,
+                         float scale) {
   if (T < 0 || S < 0 || Hq <= 0 || Hkv <= 0 || rows <= 0 || cols <= 0)
     return fail(SDPA_ERR_SHAPE, "bad sizes: T=%lld S=%d Hq=%d Hkv=%d rows=%lld cols=%d",
                 (long long)T, S, Hq, Hkv, (long long)rows, cols);
@@ -172,6 +172,16 @@ static sdpa_status check_common(int64_t T, int Hq, int Hkv, int D, int S, int64_
     return fail(SDPA_ERR_GQA, "Hq=%d is not a multiple of Hkv=%d (group <= 128)", Hq, Hkv);
   if (window < 0) return fail(SDPA_ERR_ARG, "window %d < 0", window);
   if (!std::isfinite(scale)) return fail(SDPA_ERR_ARG, "scale is not finite");
+  return SDPA_OK;
+}
+
+sdpa_status check_tensors(const void* q, const void* k, const void* v, void* out, const int32_t* seq_info,
+                          int S, int64_t q_rs, int64_t q_hs, int64_t o_rs, int64_t o_hs) {
+  if (!q || !k || !v || !out || (!seq_info && S > 0)) return fail(SDPA_ERR_NULL, "a required pointer is NULL");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || (seq_info && !aligned16(seq_info)))
+    return fail(SDPA_ERR_ALIGN, "tensor pointers must be 16-byte aligned");
+  if (q_rs % 8 || q_hs % 8 || o_rs % 8 || o_hs % 8 || q_rs < 0 || q_hs < 0 || o_rs < 0 || o_hs < 0)
+    return fail(SDPA_ERR_STRIDE, "row/head strides must be non-negative multiples of 8 elements");
   return SDPA_OK;
 }
 
@@ -263,14 +273,9 @@ static sdpa_status run(const void* q, int64_t T, int Hq, int D, int64_t q_rs, in
   g_err[0] = 0;
   sdpa_status st = check_common(T, Hq, Hkv, D, S, rows, cols, window, scale);
   if (st) return st;
-  if (!q || !k || !v || !out || (!seq_info && !inl && S > 0))
-    return fail(SDPA_ERR_NULL, "a required pointer is NULL");
+  // the dense entry passes its one segment by value: no table pointer to check
+  if ((st = check_tensors(q, k, v, out, seq_info, inl ? 0 : S, q_rs, q_hs, o_rs, o_hs))) return st;
   if (!ws) return fail(SDPA_ERR_WORKSPACE, "workspace is NULL");
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(ws) ||
-      (seq_info && !aligned16(seq_info)))
-    return fail(SDPA_ERR_ALIGN, "tensor pointers must be 16-byte aligned");
-  if (q_rs % 8 || q_hs % 8 || o_rs % 8 || o_hs % 8 || q_rs < 0 || q_hs < 0 || o_rs < 0 || o_hs < 0)
-    return fail(SDPA_ERR_STRIDE, "row/head strides must be non-negative multiples of 8 elements");
   if ((uintptr_t)ws % 256) return fail(SDPA_ERR_ALIGN, "workspace must be 256-byte aligned");
   if (seg_mode && !aligned16(seg_mode)) return fail(SDPA_ERR_ALIGN, "seg_mode must be 16-byte aligned");
 
@@ -488,6 +493,23 @@ sdpa_status sdpa_set_timing_events(void* const* events, int n) {
     g_ev[i] = (cudaEvent_t)events[i];
   }
   g_ev_on = true;
+  return SDPA_OK;
+}
+
+sdpa_status sdpa_workspace_status(const void* workspace, size_t ws_bytes, int32_t* status_host, void* stream) {
+  g_err[0] = 0;
+  if (!workspace || !status_host) return fail(SDPA_ERR_NULL, "workspace or status_host is NULL");
+  if ((uintptr_t)workspace % 256) return fail(SDPA_ERR_ALIGN, "workspace must be 256-byte aligned");
+  if (ws_bytes < sizeof(SchedHdr)) return fail(SDPA_ERR_WORKSPACE, "workspace of %zu bytes has no header", ws_bytes);
+  // the header opens every workspace layout; its status word is rewritten by each call's
+  // scheduler and ORed by the attention kernels (SDPA_DEV_TIMEOUT)
+  const SchedHdr* h = reinterpret_cast<const SchedHdr*>(workspace);
+  int64_t v = 0;
+  cudaStream_t st = (cudaStream_t)stream;
+  cudaError_t e = cudaMemcpyAsync(&v, &h->status, sizeof(v), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return fail(SDPA_ERR_CUDA, "status read-back: %s", cudaGetErrorString(e));
+  *status_host = (int32_t)v;
   return SDPA_OK;
 }
 

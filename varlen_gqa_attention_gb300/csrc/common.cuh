@@ -119,9 +119,11 @@ __host__ __device__ inline int64_t part_cap(int64_t ucap, int64_t grid, int rows
 }
 
 // Lays the workspace out from `base` (base may be null to only measure). Returns bytes.
+// Without the prefill route (`with_prefill` false: every segment takes the split-K kernel)
+// that route's unit table and partial slots are empty.
 __host__ inline size_t layout_workspace(char* base, int64_t T, int Hq, int Hkv, int D, int S,
                                         int64_t grid_splitk, int64_t grid_prefill,
-                                        Workspace* ws) {
+                                        Workspace* ws, bool with_prefill = true) {
   int64_t off = 0;
   auto take = [&](int64_t bytes) {
     int64_t o = off;
@@ -137,8 +139,9 @@ __host__ inline size_t layout_workspace(char* base, int64_t T, int Hq, int Hkv, 
   const int rpu[3] = {0, kSplitkRows, kPrefillRows};
   const int64_t grid[3] = {0, grid_splitk, grid_prefill};
   for (int r = 1; r < 3; ++r) {
-    w.unit_cap[r] = unit_cap(T, Hq, Hkv, S, rpu[r]);
-    w.part_cap[r] = part_cap(w.unit_cap[r], grid[r], rpu[r]);
+    const bool used = r == kRouteSplitk || with_prefill;
+    w.unit_cap[r] = used ? unit_cap(T, Hq, Hkv, S, rpu[r]) : 0;
+    w.part_cap[r] = used ? part_cap(w.unit_cap[r], grid[r], rpu[r]) : 0;
     w.units[r] = (UnitRec*)take((int64_t)sizeof(UnitRec) * w.unit_cap[r]);
     w.first_unit[r] = (int32_t*)take(4 * (int64_t)kMaxPhases * (grid[r] > 0 ? grid[r] : 1));
     w.part_ml[r] = (float2*)take(8 * w.part_cap[r]);
@@ -222,6 +225,12 @@ int prefill_tile_keys(int D);
 int prefill_block_threads(int D);
 // Sets the message sdpa_last_error() returns on this thread.
 void set_last_error(const char* msg);
+// Argument checks shared by the attention entry points (api.cu); each sets the message of
+// sdpa_last_error() and returns its code, SDPA_OK when the arguments pass.
+sdpa_status check_common(int64_t T, int Hq, int Hkv, int D, int S, int64_t rows, int cols, int window,
+                         float scale);
+sdpa_status check_tensors(const void* q, const void* k, const void* v, void* out, const int32_t* seq_info,
+                          int S, int64_t q_rs, int64_t q_hs, int64_t o_rs, int64_t o_hs);
 
 // Segment validity (SDPA_SEG_* bits), same rule on host and device.
 __host__ __device__ inline int32_t segment_bits(int64_t q_start, int64_t q_len, int64_t col,

@@ -10,7 +10,9 @@
 // The array is a host-side stand-in symbol in host code, not a device address: its device
 // address is fetched with cudaGetSymbolAddress once per device (with that device current)
 // on the first call there, and passed to the kernels.  That first call should come before
-// any stream capture.  Every call on a device shares the one array, which keeps the last
+// any stream capture.  The address is kept for the life of the process: it assumes the
+// device's primary context does too (after cudaDeviceReset it would be stale, so a caller
+// that resets a device must not call this entry point on it again).  Every call on a device shares the one array, which keeps the last
 // call's contents; nothing in it needs to start at zero (the scheduler kernel writes every
 // field the later kernels read), but two calls that overlap on the GPU (different streams,
 // or graphs replayed concurrently) race on it.
@@ -79,33 +81,6 @@ sdpa_status static_setup(StaticDev* out) {
   return SDPA_OK;
 }
 
-// Workspace layout with the split-K route only (no prefill tables); same records as the
-// general layout.  Returns the bytes it needs.
-size_t layout_splitk_only(char* base, int64_t T, int Hq, int Hkv, int D, int S, int64_t grid,
-                          Workspace* ws) {
-  int64_t off = 0;
-  auto take = [&](int64_t bytes) {
-    const int64_t o = off;
-    off = align_up(off + bytes, 256);
-    return base ? base + o : nullptr;
-  };
-  Workspace w{};
-  w.hdr = (SchedHdr*)take(sizeof(SchedHdr));
-  w.segs = (SegRec*)take((int64_t)sizeof(SegRec) * (S > 0 ? S : 1));
-  w.row_seg = (int32_t*)take(4 * (T > 0 ? T : 1));
-  w.row_info = (int4*)take(16 * (T > 0 ? T : 1));
-  w.seg_flag = (int32_t*)take(4 * (S > 0 ? S : 1));
-  w.unit_cap[kRouteSplitk] = unit_cap(T, Hq, Hkv, S, kSplitkRows);
-  w.part_cap[kRouteSplitk] = part_cap(w.unit_cap[kRouteSplitk], grid, kSplitkRows);
-  w.units[kRouteSplitk] = (UnitRec*)take((int64_t)sizeof(UnitRec) * w.unit_cap[kRouteSplitk]);
-  w.first_unit[kRouteSplitk] = (int32_t*)take(4 * (int64_t)kMaxPhases * grid);
-  w.part_ml[kRouteSplitk] = (float2*)take(8 * w.part_cap[kRouteSplitk]);
-  w.part_o[kRouteSplitk] = (float*)take(4 * w.part_cap[kRouteSplitk] * D);
-  w.arrive = (int32_t*)take(4 * w.unit_cap[kRouteSplitk]);
-  if (ws) *ws = w;
-  return (size_t)off;
-}
-
 }  // namespace
 }  // namespace sdpa
 
@@ -117,28 +92,22 @@ extern "C" sdpa_status sdpa_varlen_splitk_static(
     int S, int causal, int window, float scale, void* out, int64_t o_row_stride, int64_t o_head_stride,
     int32_t* status_dev, void* stream) {
   set_last_error("");
-  if (T < 0 || S < 0 || Hq <= 0 || Hkv <= 0 || rows <= 0 || cols <= 0 || T > INT32_MAX || rows > INT32_MAX)
-    return static_fail(SDPA_ERR_SHAPE, "bad sizes");
-  if (D != 64 && D != 128 && D != 256) return static_fail(SDPA_ERR_HEAD_DIM, "head dim not in {64,128,256}");
-  if (Hq % Hkv != 0 || Hq / Hkv > 128) return static_fail(SDPA_ERR_GQA, "Hq must be a multiple of Hkv (group <= 128)");
-  if (window < 0 || !std::isfinite(scale)) return static_fail(SDPA_ERR_ARG, "window < 0 or scale not finite");
-  if (!q || !k_store || !v_store || !out || (!seq_info && S > 0))
-    return static_fail(SDPA_ERR_NULL, "a required pointer is NULL");
-  if (((uintptr_t)q | (uintptr_t)k_store | (uintptr_t)v_store | (uintptr_t)out | (uintptr_t)seq_info) & 15u)
-    return static_fail(SDPA_ERR_ALIGN, "tensor pointers must be 16-byte aligned");
-  if (q_row_stride % 8 || q_head_stride % 8 || o_row_stride % 8 || o_head_stride % 8 || q_row_stride < 0 ||
-      q_head_stride < 0 || o_row_stride < 0 || o_head_stride < 0)
-    return static_fail(SDPA_ERR_STRIDE, "row/head strides must be non-negative multiples of 8 elements");
+  // the same argument checks, with the same messages, as sdpa_varlen
+  sdpa_status st = check_common(T, Hq, Hkv, D, S, rows, cols, window, scale);
+  if (st) return st;
+  if ((st = check_tensors(q, k_store, v_store, out, seq_info, S, q_row_stride, q_head_stride, o_row_stride,
+                          o_head_stride)))
+    return st;
 
   StaticDev sd;
-  sdpa_status st = static_setup(&sd);
-  if (st) return st;
-  // The general grid if its scratch fits; otherwise fewer CTAs, down to one per SM.
+  if ((st = static_setup(&sd))) return st;
+  // sdpa_varlen's workspace layout without the prefill route's tables.  The general grid if
+  // its scratch fits; otherwise one CTA per SM (fewer partial slots).
   int64_t grid = (int64_t)sd.sms * sd.per_sm[dix(D)];
-  size_t need = layout_splitk_only(nullptr, T, Hq, Hkv, D, S, grid, nullptr);
+  size_t need = layout_workspace(nullptr, T, Hq, Hkv, D, S, grid, 0, nullptr, false);
   if (need > kStaticScratchBytes) {
     grid = sd.sms;
-    need = layout_splitk_only(nullptr, T, Hq, Hkv, D, S, grid, nullptr);
+    need = layout_workspace(nullptr, T, Hq, Hkv, D, S, grid, 0, nullptr, false);
   }
   if (need > kStaticScratchBytes) {
     char msg[256];
@@ -149,7 +118,7 @@ extern "C" sdpa_status sdpa_varlen_splitk_static(
     return static_fail(SDPA_ERR_WORKSPACE, msg);
   }
   Workspace W;
-  layout_splitk_only((char*)sd.scratch, T, Hq, Hkv, D, S, grid, &W);
+  layout_workspace((char*)sd.scratch, T, Hq, Hkv, D, S, grid, 0, &W, false);
 
   SchedArgs sa{};
   sa.seq_info = seq_info;

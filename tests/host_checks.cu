@@ -3,6 +3,7 @@
 //   * udiv against plain 64-bit division, operands above 2^32 included;
 //   * the stream-K partition: shares are contiguous, cover [0, W) once, and sk_owner(x)
 //     names the CTA whose share holds x;
+//   * the key tiles of a prefill unit: they cover its keys once and never wrap a ring;
 //   * the workspace layout: every region 256-byte aligned, disjoint, inside the size it
 //     returns, and the partial slots sized for the phases the scheduler may use;
 //   * segment_bits for a grid of segments, printed one per line for comparison with the
@@ -53,6 +54,27 @@ int main() {
     }
     CHECK(prev_end == W);
   }
+  // key tiles of a prefill unit: the tiles cover [lo, hi) once, in order, each 1..bn keys,
+  // and no tile's store rows wrap (its first and last key sit in one block of `rows`)
+  for (int i = 0; i < 200000; ++i) {
+    const int64_t rows = 1 + (int64_t)(next_u64() % 5000);
+    const int bn = (next_u64() & 1) ? 128 : 64;
+    const int64_t lo = (int64_t)(next_u64() % 100000);
+    const int64_t span = (int64_t)(next_u64() % (rows + 1));  // a unit's keys span <= rows
+    const int64_t hi = lo + span;
+    const KeyTiles kt = key_tiles(lo, hi, rows, bn);
+    int64_t expect = lo;
+    for (int64_t t = 0; t < kt.n; ++t) {
+      int64_t j0;
+      int valid;
+      key_tile(kt, t, bn, &j0, &valid);
+      CHECK(j0 == expect && valid >= 1 && valid <= bn);
+      CHECK(j0 / rows == (j0 + valid - 1) / rows);
+      expect = j0 + valid;
+    }
+    CHECK(expect == (span > 0 ? hi : lo));
+    CHECK(kt.n <= (span + bn - 1) / bn + 1);
+  }
   // workspace layout
   const int64_t Ts[] = {1, 32, 513, 4096, 100000};
   const int Ss[] = {1, 7, 32, 1500};
@@ -78,7 +100,7 @@ int main() {
                              {ws.seg_flag, 4 * (int64_t)S},
                              {ws.arrive, 4 * ws.unit_cap[kRouteSplitk]}};
         const int64_t grid[3] = {0, gs, gp};
-        const int rpu[3] = {0, kSplitkRows, kPrefillRows};
+        const int rpu[3] = {0, kSplitkRows, prefill_unit_rows(D)};
         for (int r = 1; r < 3; ++r) {
           CHECK(ws.unit_cap[r] == unit_cap(T, Hq, Hkv, S, rpu[r]));
           CHECK(ws.part_cap[r] >= (ws.unit_cap[r] + (int64_t)kPartPhases * grid[r] + 1) * rpu[r]);

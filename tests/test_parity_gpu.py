@@ -58,9 +58,45 @@ def test_d64_long_prefill_full(dev, route, seed):
 
 def test_d128_long_prefill_sampled_rows(dev, route):
     call = synth.long_causal_prefill(128, 4096, 131072, seed=0).calls[0]
-    rows = sorted(set([0, 1, 15, 16, 17, 127, 128, 2047, 2048, 4094, 4095] +
-                      list(np.random.default_rng(0).integers(0, 4096, 20))))
+    # both ends, both sides of every 256-query-row boundary (units hold 32 query rows at group
+    # 8, key tiles 128 positions), and random rows in between
+    edges = [b + d for b in range(0, 4097, 256) for d in (-1, 0) if 0 <= b + d < 4096]
+    rows = sorted(set([0, 1, 15, 16, 17, 31, 32, 127, 128, 2047, 2048, 4094, 4095] + edges +
+                      list(np.random.default_rng(0).integers(0, 4096, 40))))
     check_call(call, dev, rows_subset=rows, tag="d128 sampled")
+
+
+def test_d128_prefill_full_over_several_units(dev, route):
+    # every row of a 768 x 6000 causal prefill (24 units of 256 packed rows, ragged last
+    # key tile)
+    call = synth.long_causal_prefill(128, 768, 6000, seed=4).calls[0]
+    check_call(call, dev, tag="d128 768x6000")
+
+
+@pytest.mark.parametrize("D", [64, 128, 256])
+def test_windowed_prefill_whose_keys_wrap_the_ring(dev, route, D):
+    """Long sliding-window chunks on a ring store of window + q_len - 1 rows whose keys cross
+    the ring's end (the prefill kernel tiles them in two parts at the wrap)."""
+    W, q_len, Hq, Hkv = 300, 64, 8, 2
+    rows, cols = W + q_len - 1, 4
+    segs = [(0, q_len, 0, 2000), (q_len, q_len, 1, 363 * 3 + 40), (2 * q_len, 40, 2, 1700), (2 * q_len + 40, 1, 3, 900)]
+    g = torch.Generator().manual_seed(D)
+    T = 2 * q_len + 41
+    call = synth.Call(T, Hq, Hkv, D, rows, cols, np.array(segs, dtype=np.int32), True, W, D ** -0.5,
+                      torch.randn((T, Hq, D), generator=g).to(torch.bfloat16),
+                      torch.randn((rows, cols, Hkv, D), generator=g).to(torch.bfloat16),
+                      torch.randn((rows, cols, Hkv, D), generator=g).to(torch.bfloat16))
+    for qs, ql, col, ke in segs[:3]:
+        first = ke - min(ke, ql + W - 1)
+        assert first // rows != (ke - 1) // rows  # the keys wrap
+    check_call(call, dev, tag=f"ring wrap D={D}")
+
+
+def test_ring_window_prefill_workload_sampled_rows(dev, route):
+    call = synth.ring_window_prefill(seed=0).calls[0]
+    rows = sorted(set([0, 1, 15, 16, 31, 32, 1023, 1024, 2046, 2047] +
+                      list(np.random.default_rng(1).integers(0, call.T, 24))))
+    check_call(call, dev, rows_subset=rows, tag="ring prefill")
 
 
 @pytest.mark.parametrize("seed", [0, 1, 2])

@@ -41,7 +41,7 @@ __global__ void __launch_bounds__(kCombineThreads) sdpa_combine_kernel(AttnArgs 
   if (q != kRouteNone) {
     // route-indexed fields picked by select: a runtime index would copy them to local memory
     const bool pf = q == kRoutePrefill;
-    const int rpu = pf ? kPrefillRows : kSplitkRows;
+    const int rpu = pf ? prefill_unit_rows(D) : kSplitkRows;
     const int hk = h / A.group;
     const int64_t r = (int64_t)ri.w * A.group + (h % A.group);
     const int64_t rb = r / rpu;

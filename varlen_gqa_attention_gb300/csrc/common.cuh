@@ -22,6 +22,9 @@ constexpr int kMergeRows = 16;
 constexpr int kSplitkThreads = 128;  // split-K kernel: four warps
 constexpr int kPrefillRows = 128;  // tensor-memory prefill kernel: one 128-lane accumulator
 constexpr int kPrefillTile = 128;  // prefill kernel: key positions per tile
+// Packed rows of a prefill unit: two 128-row halves that share every K/V tile (D = 64, 128),
+// or one (D = 256, whose output accumulator alone fills the tensor memory).
+__host__ __device__ constexpr int prefill_unit_rows(int D) { return D == 256 ? kPrefillRows : 2 * kPrefillRows; }
 
 constexpr int kRouteNone = 0;
 constexpr int kRouteSplitk = 1;
@@ -136,7 +139,7 @@ __host__ inline size_t layout_workspace(char* base, int64_t T, int Hq, int Hkv, 
   w.row_seg = (int32_t*)take(4 * (T > 0 ? T : 1));
   w.row_info = (int4*)take(16 * (T > 0 ? T : 1));
   w.seg_flag = (int32_t*)take(4 * (S > 0 ? S : 1));
-  const int rpu[3] = {0, kSplitkRows, kPrefillRows};
+  const int rpu[3] = {0, kSplitkRows, prefill_unit_rows(D)};
   const int64_t grid[3] = {0, grid_splitk, grid_prefill};
   for (int r = 1; r < 3; ++r) {
     const bool used = r == kRouteSplitk || with_prefill;
@@ -220,6 +223,9 @@ const void* splitk_kernel_ptr(int D);
 int splitk_smem_bytes(int D);
 const void* combine_kernel_ptr(int D);
 const void* prefill_kernel_ptr(int D);
+const void* prefill_pair_kernel_ptr(int D);  // D = 64, 128
+int prefill_pair_smem_bytes(int D);
+int prefill_pair_block_threads(int D);
 int prefill_smem_bytes(int D);
 int prefill_tile_keys(int D);
 int prefill_block_threads(int D);
@@ -282,6 +288,43 @@ struct PieceWalk {
 __host__ __device__ __forceinline__ int64_t udiv(int64_t a, int64_t b) {
   if ((((uint64_t)a | (uint64_t)b) >> 32) == 0) return (int64_t)((uint32_t)a / (uint32_t)b);
   return a / b;
+}
+
+// Key tiles of a prefill unit.  The unit's keys [lo, hi) span at most `rows` store rows, so on
+// a ring store they cross a multiple of `rows` (where the store row wraps to 0) at most once;
+// such a range is tiled in two parts, [lo, wrap) and [wrap, hi), so that the store rows of
+// every tile are consecutive (one TMA box).  The tile that ends at the wrap may be short.
+struct KeyTiles {
+  int64_t lo, wrap, hi;  // wrap = hi when the range does not wrap
+  int64_t na, n;         // tiles of [lo, wrap), and of the whole range
+};
+__host__ __device__ inline KeyTiles key_tiles(int64_t lo, int64_t hi, int64_t rows, int bn) {
+  KeyTiles k;
+  k.lo = lo;
+  k.hi = hi;
+  if (hi <= lo) {
+    k.wrap = hi;
+    k.na = k.n = 0;
+    return k;
+  }
+  const int64_t w = (udiv(lo, rows) + 1) * rows;  // first position after lo in store row 0
+  k.wrap = w < hi ? w : hi;
+  k.na = udiv(k.wrap - lo + bn - 1, bn);
+  k.n = k.na + udiv(hi - k.wrap + bn - 1, bn);
+  return k;
+}
+// First key position of tile t and how many of its bn positions exist (the rest is masked).
+__host__ __device__ inline void key_tile(const KeyTiles& k, int64_t t, int bn, int64_t* j0, int* valid) {
+  int64_t end;
+  if (t < k.na) {
+    *j0 = k.lo + t * bn;
+    end = k.wrap;
+  } else {
+    *j0 = k.wrap + (t - k.na) * bn;
+    end = k.hi;
+  }
+  const int64_t v = end - *j0;
+  *valid = (int)(v < bn ? v : bn);
 }
 
 // Stream-K partition: CTA g of G owns flattened tiles [g*W/G, (g+1)*W/G).

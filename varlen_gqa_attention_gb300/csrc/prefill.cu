@@ -1,4 +1,6 @@
-// prefill.cu - tensor-memory attention kernel for long segments on sm_103a.
+// prefill.cu - tensor-memory attention kernel for long segments on sm_103a at D = 256 (one
+// 128-row query tile per CTA: its output accumulator alone takes half the tensor memory);
+// D = 64 and 128 use the two-tile kernel of prefill_pair.cu.
 //
 // "[CUDA] Use Triton TMA for long-context causal prefill" (Summary: TMA-staged tiles,
 // per-head-dim tile configurations, guarded online softmax so fully masked rows stay finite,
@@ -13,7 +15,8 @@
 //     heads sharing a KV head fill the MMA's M dimension together (GQA packing);
 //   * two producer warps move Q and K tiles, and V tiles, with TMA (128-byte swizzle) into
 //     rings of shared-memory stages; the store is a 4-d tensor [rows, cols, Hkv, D], so a tile of one
-//     column and KV head is one box;
+//     column and KV head is one box (a key range that wraps around a ring store is tiled in
+//     two parts at the wrap, so no tile's store rows wrap);
 //   * the MMA warp issues tcgen05.mma (the whole warp runs the loop, one elected lane
 //     issues): S = Q K^T into one of two tensor-memory buffers (fp32, 128 lanes x BN
 //     columns) and O += P V with P read from tensor memory; S(g+2) goes out as soon as the
@@ -21,7 +24,7 @@
 //     tcgen05.commit on mbarriers;
 //   * two softmax warpgroups each take half of every tile's key columns, one thread per row
 //     (= tensor-memory lane): the thread reads its S half-row, masks by select (causal,
-//     window, piece bounds), keeps a base-2 running max shared by the two halves with lazy
+//     window, the tile's end), keeps a base-2 running max shared by the two halves with lazy
 //     rescaling (one barrier per tile checks that no row's tile max left the 2^8 window; only
 //     then are maxima swapped and O rescaled) and writes P as bf16 pairs into tensor memory;
 //     at the end of a piece the two row-sum halves are added and each warpgroup writes its
@@ -60,13 +63,9 @@ struct PfCfg {
   static constexpr int BAR_BYTES = 512;
   static constexpr int SMEM = OFF_BAR + BAR_BYTES + 1024;  // + alignment slack
 };
-static_assert(PfCfg<64>::STAGES <= 6 && PfCfg<128>::STAGES <= 6 && PfCfg<256>::STAGES <= 6,
-              "K/V ring deeper than the barrier arrays");
-static_assert(PfCfg<128>::SMEM <= 232448, "prefill D=128 shared memory");
-static_assert(PfCfg<64>::SMEM <= 232448, "prefill D=64 shared memory");
+static_assert(PfCfg<256>::STAGES <= 6, "K/V ring deeper than the barrier arrays");
 static_assert(PfCfg<256>::SMEM <= 232448, "prefill D=256 shared memory");
-static_assert(PfCfg<64>::O_COL + 64 <= 512 && PfCfg<128>::O_COL + 128 <= 512 &&
-                  PfCfg<256>::O_COL + 256 <= 512 && PfCfg<256>::P_COL + 64 <= PfCfg<256>::O_COL,
+static_assert(PfCfg<256>::O_COL + 256 <= 512 && PfCfg<256>::P_COL + 64 <= PfCfg<256>::O_COL,
               "prefill tensor-memory layout");
 
 // barrier slots (8 bytes each) inside the barrier block
@@ -116,12 +115,15 @@ __device__ __forceinline__ void add2f(float& s0, float& s1, float x0, float x1) 
 struct PfPiece {
   UnitRec ur;
   SegRec sg;
+  KeyTiles kt;
   int64_t ta, tb;
   int slot;
 };
 
-__device__ __forceinline__ bool pf_next(PieceWalk& w, PfPiece& pc) {
+template <int BN>
+__device__ __forceinline__ bool pf_next(PieceWalk& w, PfPiece& pc, int64_t rows) {
   if (!walk_next(w, pc.ur, pc.ta, pc.tb)) return false;
+  pc.kt = key_tiles(pc.ur.lo, pc.ur.hi, rows, BN);
   // the unit record carries its segment's entry and mode: no second dependent load
   pc.sg.q_start = pc.ur.q_start;
   pc.sg.q_len = pc.ur.q_len;
@@ -197,9 +199,9 @@ __global__ void __launch_bounds__(PfCfg<D>::THREADS, 1)
     PieceWalk wk;
     walk_begin(wk, A.ws, kRoutePrefill);
     PfPiece pc;
-    uint32_t gt = 0, pi = 0;
+    uint32_t gt = 0, pi = 0;  // tiles and pieces whose copies this warp started
     bool ok = true;
-    while (ok && pf_next(wk, pc)) {
+    while (ok && pf_next<C::BN>(wk, pc, A.rows)) {
       const int hk = pc.ur.hk;
       if (is_k && lane == 0) {
         ok = mbar_wait(bar(PfBars::Q_EMPTY), (pi & 1) ^ 1, abort);
@@ -212,14 +214,15 @@ __global__ void __launch_bounds__(PfCfg<D>::THREADS, 1)
         }
       }
       ok = __shfl_sync(0xffffffffu, ok, 0);
-      const int64_t pos_lo = (int64_t)pc.ur.lo + pc.ta * C::BN;
-      const int64_t pos_hi = min((int64_t)pc.ur.lo + pc.tb * C::BN, (int64_t)pc.ur.hi);
+      if (!ok) break;
+      if (is_k) ++pi;
       const int n = (int)(pc.tb - pc.ta);
       for (int j = 0; ok && j < n; ++j, ++gt) {
         const int s = gt % C::STAGES;
         const uint32_t use = gt / C::STAGES;
-        const int64_t j0 = pos_lo + (int64_t)j * C::BN;
-        const int valid = (int)min((int64_t)C::BN, pos_hi - j0);
+        int64_t j0;
+        int valid;
+        key_tile(pc.kt, pc.ta + j, C::BN, &j0, &valid);
         const int row0 = (int)(j0 % A.rows);
         if (is_k) {
           if (lane == 0) {
@@ -233,6 +236,7 @@ __global__ void __launch_bounds__(PfCfg<D>::THREADS, 1)
             }
           }
           ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) break;  // this tile's copy was not started
           continue;
         }
         if (lane == 0) {
@@ -254,7 +258,10 @@ __global__ void __launch_bounds__(PfCfg<D>::THREADS, 1)
           // V rows past the last visible key: wait for the tile, then zero them
           ok = mbar_wait(bar(PfBars::V_FULL + s), use & 1, abort);
           ok = __all_sync(0xffffffffu, ok);
-          if (!ok) break;
+          if (!ok) {
+            ++gt;  // its copy was started
+            break;
+          }
           const int bytes = (C::BN - valid) * 128;
 #pragma unroll
           for (int c = 0; c < C::NREG; ++c) {
@@ -267,16 +274,20 @@ __global__ void __launch_bounds__(PfCfg<D>::THREADS, 1)
           if (lane == 0) mbar_arrive(bar(PfBars::V_READY + s));
         }
       }
-      ++pi;
     }
     // drain: the copies this warp started must land before the CTA can exit (immediate on
-    // the normal path, where the MMA warp already consumed every stage and Q tile)
+    // the normal path, where the MMA warp already consumed every stage and Q tile); each
+    // wait is bounded on its own
     if (lane == 0) {
-      int dummy = 0;
       const uint32_t first = gt > (uint32_t)C::STAGES ? gt - C::STAGES : 0u;
-      for (uint32_t g = first; g < gt; ++g)
-        mbar_wait(bar((is_k ? PfBars::K_FULL : PfBars::V_FULL) + g % C::STAGES), (g / C::STAGES) & 1, &dummy);
-      if (is_k && pi > 0) mbar_wait(bar(PfBars::Q_FULL), (pi - 1) & 1, &dummy);
+      for (uint32_t g = first; g < gt; ++g) {
+        int own = 0;
+        mbar_wait(bar((is_k ? PfBars::K_FULL : PfBars::V_FULL) + g % C::STAGES), (g / C::STAGES) & 1, &own);
+      }
+      if (is_k && pi > 0) {
+        int own = 0;
+        mbar_wait(bar(PfBars::Q_FULL), (pi - 1) & 1, &own);
+      }
     }
     __syncwarp();
   } else if (warp == W_MMA) {
@@ -348,12 +359,8 @@ __global__ void __launch_bounds__(PfCfg<D>::THREADS, 1)
         tc_commit_w(bar(PfBars::V_EMPTY + s));  // V(g) free, and PV(g) done with P_b and O
         return test && __all_sync(0xffffffffu, pre);
       };
-      while (ok && pf_next(wk, pc)) {
+      while (ok && pf_next<C::BN>(wk, pc, A.rows)) {
         const int n = (int)(pc.tb - pc.ta);
-        // keys of the piece's last tile (the V producer zeroes the rest of that tile)
-        const int64_t span = min((int64_t)pc.ur.lo + pc.tb * C::BN, (int64_t)pc.ur.hi) -
-                             ((int64_t)pc.ur.lo + pc.ta * C::BN);
-        const bool ragged = span < (int64_t)n * C::BN;
         ok = __all_sync(0xffffffffu, mbar_wait(bar(PfBars::Q_FULL), pi & 1, abort)) && s_deps(gt) &&
              (n < 2 || s_deps(gt + 1));
         if (!ok) break;
@@ -365,10 +372,14 @@ __global__ void __launch_bounds__(PfCfg<D>::THREADS, 1)
         for (int j = 0; j < n; ++j) {
           const uint32_t g = gt + j;
           const int b = g & 1, s = g % C::STAGES;
-          // V_READY is awaited on the ragged tile only: the producer arrives on it for every
-          // tile (before the copy, or after zeroing the rows past the last key), so at this
-          // wait the barrier has completed exactly the phases of earlier uses and this one.
-          const bool tail = ragged && j + 1 == n;
+          // V_READY is awaited on short tiles only (the V producer zeroes the rest of such a
+          // tile): the producer arrives on it for every tile (before the copy, or after
+          // zeroing the rows past the last key), so at this wait the barrier has completed
+          // exactly the phases of earlier uses and this one.
+          int64_t tj0;
+          int tvalid;
+          key_tile(pc.kt, pc.ta + j, C::BN, &tj0, &tvalid);
+          const bool tail = tvalid < C::BN;
           bool pre_pv = false;
           if (j + 2 < n) {
             if (!pre_s) {
@@ -428,19 +439,17 @@ __global__ void __launch_bounds__(PfCfg<D>::THREADS, 1)
     PfPiece pc;
     uint32_t gt = 0;
     bool ok = true;
-    while (ok && pf_next(wk, pc)) {
+    while (ok && pf_next<C::BN>(wk, pc, A.rows)) {
       const UnitRec& ur = pc.ur;
       const SegRec& sg = pc.sg;
       const bool live = row < ur.rows;
       const int64_t r = (int64_t)ur.rb * C::BM + row;
       const int qi = (int)(r / A.group);
-      const int64_t pos_lo = (int64_t)ur.lo + pc.ta * C::BN;
-      const int64_t pos_hi = min((int64_t)ur.lo + pc.tb * C::BN, (int64_t)ur.hi);
       int64_t rlo = 1, rhi = 0;  // padding rows see nothing
       if (live) {
         const RowWin w = row_window(qi, sg.q_len, sg.kv_end, sg.causal, sg.window);
-        rlo = max((int64_t)w.lo, pos_lo);
-        rhi = min((int64_t)w.hi, pos_hi);
+        rlo = w.lo;
+        rhi = w.hi;
       }
       const int n = (int)(pc.tb - pc.ta);
       float m_use = -INFINITY, l = 0.f;
@@ -452,10 +461,14 @@ __global__ void __launch_bounds__(PfCfg<D>::THREADS, 1)
         // P_b was last read by PV(g-2): tested here, its answer used after the max
         const uint32_t g2 = g - 2;
         const bool pv2 = g < 2 || mbar_test_wait(bar(PfBars::V_EMPTY + g2 % C::STAGES), (g2 / C::STAGES) & 1);
-        // this half's visible columns of the tile
-        const int64_t j0 = pos_lo + (int64_t)j * C::BN + wg * C::HALF;
-        const int vlo = okw ? (int)min(max(rlo - j0, (int64_t)0), (int64_t)C::HALF) : 0;
-        const int vhi = okw ? (int)min(max(rhi - j0, (int64_t)0), (int64_t)C::HALF) : 0;
+        // this half's visible columns of the tile (its keys [tj0, tj0 + tvalid) exist)
+        int64_t tj0;
+        int tvalid;
+        key_tile(pc.kt, pc.ta + j, C::BN, &tj0, &tvalid);
+        const int64_t j0 = tj0 + wg * C::HALF;
+        const int64_t hv = min(max((int64_t)tvalid - wg * C::HALF, (int64_t)0), (int64_t)C::HALF);
+        const int vlo = okw ? (int)min(max(rlo - j0, (int64_t)0), hv) : 0;
+        const int vhi = okw ? (int)min(max(rhi - j0, (int64_t)0), hv) : 0;
         float x[C::HALF];
         if (okw) {
           tc_fence_after();
@@ -605,37 +618,16 @@ __global__ void __launch_bounds__(PfCfg<D>::THREADS, 1)
   if (warp == W_MMA) tmem_dealloc(tmem, C::TMEM_COLS);
 }
 
-template __global__ void sdpa_prefill_kernel<64>(const AttnArgs, const __grid_constant__ CUtensorMap,
-                                                 const __grid_constant__ CUtensorMap,
-                                                 const __grid_constant__ CUtensorMap);
-template __global__ void sdpa_prefill_kernel<128>(const AttnArgs, const __grid_constant__ CUtensorMap,
-                                                  const __grid_constant__ CUtensorMap,
-                                                  const __grid_constant__ CUtensorMap);
 template __global__ void sdpa_prefill_kernel<256>(const AttnArgs, const __grid_constant__ CUtensorMap,
                                                   const __grid_constant__ CUtensorMap,
                                                   const __grid_constant__ CUtensorMap);
 
+// The prefill kernel of a head dim: this one at D = 256, the two-tile kernel otherwise.
 const void* prefill_kernel_ptr(int D) {
-  switch (D) {
-    case 64: return (const void*)sdpa_prefill_kernel<64>;
-    case 128: return (const void*)sdpa_prefill_kernel<128>;
-    default: return (const void*)sdpa_prefill_kernel<256>;
-  }
+  return D == 256 ? (const void*)sdpa_prefill_kernel<256> : prefill_pair_kernel_ptr(D);
 }
-int prefill_smem_bytes(int D) {
-  switch (D) {
-    case 64: return PfCfg<64>::SMEM;
-    case 128: return PfCfg<128>::SMEM;
-    default: return PfCfg<256>::SMEM;
-  }
-}
-int prefill_block_threads(int D) {
-  switch (D) {
-    case 64: return PfCfg<64>::THREADS;
-    case 128: return PfCfg<128>::THREADS;
-    default: return PfCfg<256>::THREADS;
-  }
-}
-int prefill_tile_keys(int D) { return D == 256 ? PfCfg<256>::BN : PfCfg<128>::BN; }
+int prefill_smem_bytes(int D) { return D == 256 ? PfCfg<256>::SMEM : prefill_pair_smem_bytes(D); }
+int prefill_block_threads(int D) { return D == 256 ? PfCfg<256>::THREADS : prefill_pair_block_threads(D); }
+int prefill_tile_keys(int D) { return D == 256 ? PfCfg<256>::BN : kPrefillTile; }
 
 }  // namespace sdpa

@@ -80,8 +80,8 @@ __device__ __forceinline__ void load_seg(const SchedArgs& A, int s, int32_t* seg
   }
 }
 
-__device__ __forceinline__ int rows_per_unit(int route) {
-  return route == kRoutePrefill ? kPrefillRows : kSplitkRows;
+__device__ __forceinline__ int rows_per_unit(const SchedArgs& A, int route) {
+  return route == kRoutePrefill ? prefill_unit_rows(A.D) : kSplitkRows;
 }
 __device__ __forceinline__ int tile_len(const SchedArgs& A, int route) {
   return route == kRoutePrefill ? A.tile_pf : kSplitkTile;
@@ -92,18 +92,12 @@ __device__ __forceinline__ int tile_len(const SchedArgs& A, int route) {
 __device__ __forceinline__ int64_t lead_tiles(int route) { return route == kRoutePrefill ? 6 : 3; }
 
 // Route of a live segment.  The prefill kernel takes segments that fill at least one
-// 128-row tile and whose visible keys do not wrap around a ring store (a TMA box cannot
-// wrap); everything else, and everything when the prefill kernel is unusable, goes to
-// the split-K kernel.
+// 128-row tile (on a ring store too: its key tiles stop at the wrap, so a TMA box never
+// wraps); everything else, and everything when the prefill kernel is unusable, goes to the
+// split-K kernel.
 __device__ __forceinline__ int route_of(const SchedArgs& A, const SegRec& r) {
   const int64_t R = (int64_t)r.q_len * A.group;
   if (A.policy == SDPA_ROUTE_SPLITK || !A.prefill_ok) return kRouteSplitk;
-  if (r.kv_end > 0) {
-    int64_t span = r.kv_end;
-    if (r.window > 0) span = min(span, (int64_t)r.q_len + r.window - 1);
-    const int64_t first = r.kv_end - span;
-    if (udiv(first, A.rows) != udiv(r.kv_end - 1, A.rows)) return kRouteSplitk;
-  }
   if (A.policy == SDPA_ROUTE_PREFILL) return kRoutePrefill;
   return R >= kPrefillRows ? kRoutePrefill : kRouteSplitk;
 }
@@ -221,7 +215,7 @@ __global__ void __launch_bounds__(kSchedThreads) sdpa_sched_kernel(SchedArgs A) 
       r.window = cached ? c_mode[s].y : W.segs[s].window;
       const int64_t R = (int64_t)g.y * A.group;
       route = route_of(A, r);
-      const int rpu = rows_per_unit(route);
+      const int rpu = rows_per_unit(A, route);
       nrb = (int)udiv(R + rpu - 1, rpu);
       if (route == kRouteSplitk) n1 += (int64_t)A.Hkv * nrb; else n2 += (int64_t)A.Hkv * nrb;
       nrows += g.y;
@@ -278,7 +272,7 @@ __global__ void __launch_bounds__(kSchedThreads) sdpa_sched_kernel(SchedArgs A) 
   for (int64_t u = ua; u < ub; ++u) {
     const int q = u < U1 ? 1 : 2;
     const int64_t uq = q == 1 ? u : u - U1;
-    const int rpu = rows_per_unit(q), tl = tile_len(A, q);
+    const int rpu = rows_per_unit(A, q), tl = tile_len(A, q);
     // owning segment: the last one whose route-q unit base is <= uq
     int lo = 0, hi = S - 1, s = 0;
     while (lo <= hi) {
@@ -324,7 +318,10 @@ __global__ void __launch_bounds__(kSchedThreads) sdpa_sched_kernel(SchedArgs A) 
     const RowWin w1 = row_window(i1, g.q_len, g.kv_end, g.causal, g.window);
     ur.lo = w0.lo;  // lo and hi grow with the query row
     ur.hi = max(w1.hi, w0.lo);
-    const int64_t nt = ur.hi > ur.lo ? udiv((int64_t)(ur.hi - ur.lo) + tl - 1, tl) : 0;
+    // key tiles: the prefill kernel's stop at a ring wrap (two TMA ranges), the split-K
+    // kernel's wrap per row
+    const int64_t nt = q == kRoutePrefill ? key_tiles(ur.lo, ur.hi, A.rows, tl).n
+                                          : (ur.hi > ur.lo ? udiv((int64_t)(ur.hi - ur.lo) + tl - 1, tl) : 0);
     if (nt == 0) s_work = 1;  // rows of a unit with no keys: zeroed by the combine pass
     ur.nslots = 0;
     ur.g_first = 0;

@@ -49,8 +49,10 @@ template <int D>
 struct PpCfg {
   static constexpr int BM = kPrefillRows;  // rows per half
   static constexpr int BN = kPrefillTile;  // keys per tile
-  static constexpr int KSTAGES = D == 64 ? 6 : 3;
-  static constexpr int VSTAGES = D == 64 ? 6 : 2;
+  // K(j+1) is loaded once S(j-1) is done and V(j+1) once PV(j-2) is done, so each has more
+  // than a tile's time to land
+  static constexpr int KSTAGES = D == 64 ? 6 : 2;
+  static constexpr int VSTAGES = D == 64 ? 6 : 3;
   static constexpr int NREG = D / 64;      // 64-element (128-byte) column regions
   static constexpr int QH_BYTES = BM * D * 2;
   static constexpr int KV_BYTES = BN * D * 2;
@@ -479,45 +481,85 @@ __global__ void __launch_bounds__(PpCfg<D>::THREADS, 1)
     auto wait_all = [&](uint32_t b, uint32_t parity) -> bool {
       return __all_sync(0xffffffffu, mbar_wait(b, parity, abort));
     };
+    // V(j) (and, on a short tile, its zeroed tail) for PV(j); K(j+1) for S(j+1).  The barriers
+    // a group of MMAs will need next are tested (non-blocking) right after the group before
+    // it has been issued, so the test's latency hides behind the MMA issue, which waits for
+    // room in the tensor pipe; a blocking wait runs only when a test came back negative.  So
+    // the one wait left between two groups is the one for a half's P.
+    auto v_short = [&](int64_t t) -> bool {
+      int64_t j0;
+      int valid;
+      key_tile(pc.kt, t, C::BN, &j0, &valid);
+      return valid < C::BN;
+    };
+    auto test_v = [&](uint32_t g, bool shortv) -> bool {
+      const uint32_t vs = g % C::VSTAGES, vph = (g / C::VSTAGES) & 1;
+      return mbar_test_wait(bar(PpBars::V_FULL + vs), vph) &&
+             (!shortv || mbar_test_wait(bar(PpBars::V_READY + vs), vph));
+    };
+    auto wait_v = [&](uint32_t g, bool shortv) -> bool {
+      const uint32_t vs = g % C::VSTAGES, vph = (g / C::VSTAGES) & 1;
+      return wait_all(bar(PpBars::V_FULL + vs), vph) && (!shortv || wait_all(bar(PpBars::V_READY + vs), vph));
+    };
+    auto test_k = [&](uint32_t g) -> bool {
+      return mbar_test_wait(bar(PpBars::K_FULL + g % C::KSTAGES), (g / C::KSTAGES) & 1);
+    };
+    auto wait_k = [&](uint32_t g) -> bool {
+      return wait_all(bar(PpBars::K_FULL + g % C::KSTAGES), (g / C::KSTAGES) & 1);
+    };
     while (ok && pp_next(wk, pc, A.rows)) {
       const int n = (int)(pc.tb - pc.ta);
       const int nh = pc.has1 ? 2 : 1;
-      ok = wait_all(bar(PpBars::Q_FULL), pi & 1) &&
-           wait_all(bar(PpBars::K_FULL + gk % C::KSTAGES), (gk / C::KSTAGES) & 1);
+      ok = wait_all(bar(PpBars::Q_FULL), pi & 1) && wait_k(gk);
       if (!ok) break;
       tc_fence_after();
       for (int h = 0; h < nh; ++h) issue_s(h, gk);
       tc_commit_w(bar(PpBars::K_EMPTY + gk % C::KSTAGES));
       if (n == 1) tc_commit_w(bar(PpBars::Q_EMPTY));
+      ok = wait_v(gv, v_short(pc.ta));
+      if (!ok) break;
+      bool next_short = n > 1 && v_short(pc.ta + 1);
       for (int j = 0; j < n; ++j) {
-        // V of tile j (and, on a short tile, its zeroed tail)
-        int64_t j0;
-        int valid;
-        key_tile(pc.kt, pc.ta + j, C::BN, &j0, &valid);
-        const uint32_t vs = gv % C::VSTAGES, vph = (gv / C::VSTAGES) & 1;
-        ok = wait_all(bar(PpBars::V_FULL + vs), vph) && (valid == C::BN || wait_all(bar(PpBars::V_READY + vs), vph));
-        if (!ok) break;
         const bool more = j + 1 < n;
-        if (more) {
-          ok = wait_all(bar(PpBars::K_FULL + (gk + 1) % C::KSTAGES), ((gk + 1) / C::KSTAGES) & 1);
-          if (!ok) break;
-        }
-        for (int h = 0; h < nh; ++h) {
-          // PV_h(j) once half h wrote P_h(j); then S_h(j+1) over the same columns
-          ok = wait_all(bar(PpBars::P_FULL + h), gp[h] & 1);
-          if (!ok) break;
-          tc_fence_after();
-          issue_pv(h, gv, j > 0 ? 1u : 0u);
-          if (more) issue_s(h, gk + 1);
-          ++gp[h];
-        }
+        // half 0: PV_0(j) once P_0(j) is written, then S_0(j+1) over the same columns
+        ok = wait_all(bar(PpBars::P_FULL + 0), gp[0] & 1);
         if (!ok) break;
-        tc_commit_w(bar(PpBars::V_EMPTY + vs));
+        tc_fence_after();
+        issue_pv(0, gv, j > 0 ? 1u : 0u);
+        // tested while the PV MMAs queue: K(j+1), P_1(j), and with one half V(j+1)
+        const bool ready_k = !more || test_k(gk + 1);
+        const bool ready_p1 = nh == 1 || mbar_test_wait(bar(PpBars::P_FULL + 1), gp[1] & 1);
+        bool ready_v = !more || nh == 2 || test_v(gv + 1, next_short);
+        if (more) {
+          if (!__all_sync(0xffffffffu, ready_k)) {
+            ok = wait_k(gk + 1);
+            if (!ok) break;
+          }
+          issue_s(0, gk + 1);
+        }
+        ++gp[0];
+        if (nh == 2) {
+          if (!__all_sync(0xffffffffu, ready_p1)) {
+            ok = wait_all(bar(PpBars::P_FULL + 1), gp[1] & 1);
+            if (!ok) break;
+          }
+          tc_fence_after();
+          issue_pv(1, gv, j > 0 ? 1u : 0u);
+          if (more) ready_v = test_v(gv + 1, next_short);  // tested while the PV MMAs queue
+          if (more) issue_s(1, gk + 1);
+          ++gp[1];
+        }
+        tc_commit_w(bar(PpBars::V_EMPTY + gv % C::VSTAGES));
         ++gv;
         if (more) {
           ++gk;
           tc_commit_w(bar(PpBars::K_EMPTY + gk % C::KSTAGES));
           if (j + 2 == n) tc_commit_w(bar(PpBars::Q_EMPTY));  // the piece's last S are issued
+          if (!__all_sync(0xffffffffu, ready_v)) {  // the next tile's V
+            ok = wait_v(gv, next_short);
+            if (!ok) break;
+          }
+          next_short = j + 2 < n && v_short(pc.ta + j + 2);
         }
       }
       if (!ok) break;

@@ -97,8 +97,7 @@ int main() {
                              {ws.segs, (int64_t)sizeof(SegRec) * S},
                              {ws.row_seg, 4 * T},
                              {ws.row_info, 16 * T},
-                             {ws.seg_flag, 4 * (int64_t)S},
-                             {ws.arrive, 4 * ws.unit_cap[kRouteSplitk]}};
+                             {ws.seg_flag, 4 * (int64_t)S}};
         const int64_t grid[3] = {0, gs, gp};
         const int rpu[3] = {0, kSplitkRows, prefill_unit_rows(D)};
         for (int r = 1; r < 3; ++r) {
@@ -143,7 +142,6 @@ int main() {
                              {ws.row_seg, 4 * T},
                              {ws.row_info, 16 * T},
                              {ws.seg_flag, 4 * (int64_t)S},
-                             {ws.arrive, 4 * ws.unit_cap[kRouteSplitk]},
                              {ws.units[kRouteSplitk], (int64_t)sizeof(UnitRec) * ws.unit_cap[kRouteSplitk]},
                              {ws.first_unit[kRouteSplitk], 4 * (int64_t)kMaxPhases * gs},
                              {ws.part_ml[kRouteSplitk], 8 * ws.part_cap[kRouteSplitk]},

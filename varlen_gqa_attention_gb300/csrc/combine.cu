@@ -5,8 +5,7 @@
 //   * t owned by no live segment (uncovered, or an overlapping segment) -> 0
 //     ("[executorch][cuda] Add a length-aware Triton SDPA over per-sequence KV columns",
 //     PR description: rows no segment covers are zeroed);
-//   * the unit holding (t, h) had a single CTA, or is a split-K unit of at most kMergeRows
-//     rows (its last CTA merged the slots) -> already written; skip;
+//   * the unit holding (t, h) had a single CTA -> already written; skip;
 //   * no keys at all -> 0 (finite output for fully masked rows, "[CUDA] Use Triton TMA for
 //     long-context causal prefill", Summary);
 //   * otherwise merge the unit's slots: M = max m_c, L = sum l_c 2^(m_c - M),
@@ -48,8 +47,7 @@ __global__ void __launch_bounds__(kCombineThreads) sdpa_combine_kernel(AttnArgs 
     const int64_t u = (int64_t)ri.y + (int64_t)hk * ri.z + rb;
     if (u < (pf ? U2 : U1)) {
       const UnitRec ur = (pf ? W.units[kRoutePrefill] : W.units[kRouteSplitk])[u];
-      // written by the unit's only CTA, or merged by the last of a split-K unit's CTAs
-      if (ur.nslots == 1 || (ur.nslots > 1 && !pf && ur.rows <= kMergeRows)) return;
+      if (ur.nslots == 1) return;  // written by the unit's only CTA
       if (ur.nslots > 1) {
         zero = false;
         // online log-sum-exp over the slots, four slots' loads in flight at a time:

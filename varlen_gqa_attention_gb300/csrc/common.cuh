@@ -16,9 +16,6 @@ namespace sdpa {
 // them; more rows per unit would leave each warp a whole tile of legacy tensor-core work
 constexpr int kSplitkRows = 32;
 constexpr int kSplitkTile = 64;    // split-K kernel: key positions per tile
-// split-K units of up to this many rows are merged by their last CTA (a few KB of slots);
-// larger split units leave it to the combine pass, which spreads it over the whole GPU
-constexpr int kMergeRows = 16;
 constexpr int kSplitkThreads = 128;  // split-K kernel: four warps
 constexpr int kPrefillRows = 128;  // tensor-memory prefill kernel: one 128-lane accumulator
 constexpr int kPrefillTile = 128;  // prefill kernel: key positions per tile
@@ -81,8 +78,7 @@ struct SchedHdr {
   // starts a unit gets that many fewer key tiles.
   int64_t lead[3];
   // Non-zero when the combine pass has rows to write: rows no live segment covers, units
-  // with no keys, or units split over several CTAs other than split-K units of at most
-  // kMergeRows rows (those merge their own partial results).
+  // with no keys, or units split over several CTAs.
   int64_t combine_work;
 };
 
@@ -98,7 +94,6 @@ struct Workspace {
   int32_t* first_unit[3];  // [route][phase * grid + CTA]: unit whose span holds the CTA's first tile
   float2* part_ml[3];   // [route][P_cap] (running max in log2 units, sum)
   float* part_o[3];     // [route][P_cap * D] unnormalised output
-  int32_t* arrive;       // [split-K unit_cap]: CTAs of the unit that finished (zeroed by the scheduler)
   int64_t unit_cap[3];
   int64_t part_cap[3];
 };
@@ -150,7 +145,6 @@ __host__ inline size_t layout_workspace(char* base, int64_t T, int Hq, int Hkv, 
     w.part_ml[r] = (float2*)take(8 * w.part_cap[r]);
     w.part_o[r] = (float*)take(4 * w.part_cap[r] * D);
   }
-  w.arrive = (int32_t*)take(4 * w.unit_cap[kRouteSplitk]);
   if (ws) *ws = w;
   return (size_t)off;
 }
@@ -407,13 +401,6 @@ __device__ inline bool walk_next(PieceWalk& w, UnitRec& ur, int64_t& ta, int64_t
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
 __device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;\n" :::); }
 
-// Atomic add with acquire-release semantics at GPU scope; returns the old value.
-__device__ __forceinline__ int atom_add_acq_rel_gpu(int* p, int v) {
-  int old;
-  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;\n" : "=r"(old) : "l"(p), "r"(v) : "memory");
-  return old;
-}
-
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
 }
@@ -473,92 +460,6 @@ __device__ __forceinline__ float exp2_approx(float x) {
 // eight consecutive rows at one logical chunk hit eight different bank groups.
 __device__ __forceinline__ uint32_t swz(int r, int c, int row_bytes) {
   return (uint32_t)(r * row_bytes + ((c ^ (r & 7)) << 4));
-}
-
-// The last CTA of a split unit merges the unit's slots and writes `out`: online log-sum-exp
-// over the slots (M' = max(M, m_c), L' = L 2^(M - M') + l_c 2^(m_c - M'), O likewise, m in
-// base-2 units), then O / L (0 where L = 0) rounded to bf16.  A unit's slots are one
-// contiguous block of nslots * rows partial rows, so when they fit in `cap` bytes of the
-// CTA's shared memory (idle by then) they are staged there with 16-byte cp.async in one
-// round trip from L2; otherwise four slots' loads at a time go straight to registers.  NT
-// threads, all of the CTA's; kept out of line so that it does not crowd the registers of
-// the kernels' main loops.
-template <int D, int NT>
-__device__ __noinline__ void merge_unit_slots(const AttnArgs& A, const UnitRec& ur, int rows_per_unit,
-                                              const float2* part_ml, const float* part_o, char* smem,
-                                              int64_t cap) {
-  const int R = ur.rows, ns = ur.nslots;
-  const int64_t r0 = (int64_t)ur.rb * rows_per_unit;
-  const float2* ml = part_ml + ur.slot_base;
-  const float* po = part_o + ur.slot_base * D;
-  auto store_row = [&](int rl, int d0, const float* acc, float L) {
-    const float inv = L > 0.f ? 1.f / L : 0.f;
-    const int64_t r = r0 + rl;
-    const int64_t i = r / A.group;
-    const int h = ur.hk * A.group + (int)(r % A.group);
-    uint4 pk;
-    pk.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
-    pk.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
-    pk.z = pack_bf16x2(acc[4] * inv, acc[5] * inv);
-    pk.w = pack_bf16x2(acc[6] * inv, acc[7] * inv);
-    *reinterpret_cast<uint4*>(A.out + (ur.q_start + i) * A.o_rs + (int64_t)h * A.o_hs + d0) = pk;
-  };
-  auto fold = [](float& M, float& L, float* acc, float2 v, float4 u0, float4 u1) {
-    if (v.x == -INFINITY) return;  // an empty slot adds nothing
-    const float Mn = fmaxf(M, v.x);
-    const float fo = exp2_approx(M - Mn), fc = exp2_approx(v.x - Mn);
-    M = Mn;
-    L = L * fo + v.y * fc;
-    acc[0] = acc[0] * fo + u0.x * fc; acc[1] = acc[1] * fo + u0.y * fc;
-    acc[2] = acc[2] * fo + u0.z * fc; acc[3] = acc[3] * fo + u0.w * fc;
-    acc[4] = acc[4] * fo + u1.x * fc; acc[5] = acc[5] * fo + u1.y * fc;
-    acc[6] = acc[6] * fo + u1.z * fc; acc[7] = acc[7] * fo + u1.w * fc;
-  };
-  const int64_t o_bytes = (int64_t)ns * R * D * 4, m_bytes = (int64_t)ns * R * 8;
-  if (o_bytes + m_bytes <= cap) {
-    float* so = reinterpret_cast<float*>(smem);
-    float2* sm = reinterpret_cast<float2*>(smem + o_bytes);
-    const int64_t n16 = o_bytes / 16;
-    for (int64_t k = threadIdx.x; k < n16; k += NT)
-      cp_async_16(smem_u32(so) + 16 * (uint32_t)k, po + 4 * k, true);
-    cp_async_commit();
-    for (int k = threadIdx.x; k < ns * R; k += NT) sm[k] = __ldcg(ml + k);
-    cp_async_wait<0>();
-    __syncthreads();
-    for (int idx = threadIdx.x; idx < R * (D / 8); idx += NT) {
-      const int rl = idx / (D / 8), d0 = (idx % (D / 8)) * 8;
-      float M = -INFINITY, L = 0.f, acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      for (int c = 0; c < ns; ++c) {
-        const float* src = so + ((int64_t)c * R + rl) * D + d0;
-        fold(M, L, acc, sm[c * R + rl], *reinterpret_cast<const float4*>(src),
-             *reinterpret_cast<const float4*>(src + 4));
-      }
-      store_row(rl, d0, acc, L);
-    }
-    return;
-  }
-  constexpr int kBatch = 4;
-  for (int idx = threadIdx.x; idx < R * (D / 8); idx += NT) {
-    const int rl = idx / (D / 8), d0 = (idx % (D / 8)) * 8;
-    float M = -INFINITY, L = 0.f, acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int c0 = 0; c0 < ns; c0 += kBatch) {
-      float2 v[kBatch];
-      float4 u0[kBatch], u1[kBatch];
-#pragma unroll
-      for (int b = 0; b < kBatch; ++b) {
-        v[b] = make_float2(-INFINITY, 0.f);
-        if (c0 + b < ns) {
-          const int64_t pi = (int64_t)(c0 + b) * R + rl;
-          v[b] = __ldcg(ml + pi);
-          u0[b] = __ldcg(reinterpret_cast<const float4*>(po + pi * D + d0));
-          u1[b] = __ldcg(reinterpret_cast<const float4*>(po + pi * D + d0 + 4));
-        }
-      }
-#pragma unroll
-      for (int b = 0; b < kBatch; ++b) fold(M, L, acc, v[b], u0[b], u1[b]);
-    }
-    store_row(rl, d0, acc, L);
-  }
 }
 
 }  // namespace sdpa

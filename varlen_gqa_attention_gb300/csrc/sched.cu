@@ -405,7 +405,7 @@ __global__ void __launch_bounds__(kSchedThreads) sdpa_sched_kernel(SchedArgs A) 
       ur.nslots = (int32_t)(g1 - g0 + 1);
       if (ur.nslots > 1) (q == 1 ? p1 : p2) += (int64_t)ur.nslots * ur.rows;
       // split units the combine pass merges
-      if (ur.nslots > 1 && (q == kRoutePrefill || ur.rows > kMergeRows)) s_work = 1;
+      if (ur.nslots > 1) s_work = 1;
       // CTAs whose share starts inside this unit's span begin their walk here: the ones
       // after the owner of the tile before the span, up to the owner of its last tile
       const int64_t s0 = ur.tile_base - b0, s1 = k0 + nt;
@@ -438,7 +438,6 @@ __global__ void __launch_bounds__(kSchedThreads) sdpa_sched_kernel(SchedArgs A) 
       *dst = src[i];
     }
   }
-  for (int64_t u = threadIdx.x; u < U1; u += blockDim.x) W.arrive[u] = 0;
   if (cached) {
     for (int s = threadIdx.x; s < S; s += blockDim.x) {
       const int4 c = c_seg[s];

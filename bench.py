@@ -503,9 +503,12 @@ class Prepared:
             # kv_end >= q_len in these workloads)
             self.kv_bytes += sum(w[2] // (4 * c.Hq * c.D) * c.Hkv * c.D * 2 * 2 * 2 for w, c in zip(works, wl.calls))
         # scheduler, split-K and combine per call, plus the prefill kernel when the head group
-        # divides its 128-row tile, plus the KV append kernel on the append workload
-        self.launches_per_step = sum(3 + (1 if 128 % (d["call"].Hq // d["call"].Hkv) == 0 else 0) +
-                                     (1 if "kn" in d else 0) for d in self.calls)
+        # divides its 128-row tile and the call's packed rows can fill one, plus the KV append
+        # kernel on the append workload
+        def pf(c):
+            g = c.Hq // c.Hkv
+            return 1 if 128 % g == 0 and c.T * g >= 128 else 0
+        self.launches_per_step = sum(3 + pf(d["call"]) + (1 if "kn" in d else 0) for d in self.calls)
 
     def attend(self, d):
         pkg, c = self.pkg, d["call"]

@@ -239,10 +239,21 @@ static sdpa_status launch_all(const SchedArgs& sa, const AttnArgs& aa, int D, co
     if (e != cudaSuccess) return fail(SDPA_ERR_CUDA, "append launch: %s", cudaGetErrorString(e));
   }
   if (e == cudaSuccess) e = mark(1, st);
-  if (e == cudaSuccess && sa.prefill_ok) {
+  // The prefill kernel is launched only when some segment can reach its route: not under the
+  // split-K policy, and (automatic routing) not when T * group < 128, where no segment fills
+  // a 128-row tile.  Chained to the scheduler (programmatic dependent launch: its launch
+  // overlaps the scheduler) when the average segment fills less than one tile, so that the
+  // launch is most likely empty; launched after the scheduler otherwise (measured: the
+  // chained launch saves ~6 us on a decode step whose prefill kernel has nothing to do, and
+  // costs ~5 us on prefill steps of a few tiles per CTA).
+  const int64_t packed = aa.T * aa.group;
+  const bool pf_possible = sa.prefill_ok && sa.policy != SDPA_ROUTE_SPLITK &&
+                           (sa.policy == SDPA_ROUTE_PREFILL || packed >= kPrefillRows);
+  if (e == cudaSuccess && pf_possible) {
     void* args[] = {(void*)&aa, (void*)&tm.q, (void*)&tm.k, (void*)&tm.v};
+    const bool chained = packed < (int64_t)kPrefillRows * std::max(sa.S, 1);
     e = launch_k(prefill_kernel_ptr(D), (unsigned)g.prefill, prefill_block_threads(D), args,
-                 prefill_smem_bytes(D), st, true);
+                 prefill_smem_bytes(D), st, chained);
     if (e != cudaSuccess) return fail(SDPA_ERR_CUDA, "prefill launch: %s", cudaGetErrorString(e));
   }
   if (e == cudaSuccess) e = mark(2, st);

@@ -75,7 +75,7 @@ CSRC = os.path.join(ROOT, "varlen_gqa_attention_gb300", "csrc")
 # the sources each kernel is built from (their hash ties a traffic figure to the code it was
 # measured on)
 KERNEL_SOURCES = {
-    "prefill": ["prefill.cu", "tc.cuh", "common.cuh"],
+    "prefill": ["prefill.cu", "prefill_pair.cu", "tc.cuh", "common.cuh"],
     "splitk": ["splitk.cu", "common.cuh"],
     "clone": ["append.cu", "common.cuh"],
 }
@@ -85,14 +85,17 @@ KERNEL_SOURCES = {
 # when it was taken.  A kernel whose sources hash differently now reports traffic null until
 # the capture is repeated.
 NCU_TRAFFIC = {
-    "prefill_d128": (2304273152 + 37948416, "prefill", "4b956d3df2670d5a"),
-    "prefill_d64": (9514752 + 0, "prefill", "4b956d3df2670d5a"),
-    "decode": (141780224 + 3403008, "splitk", "13b75fbc734f13b5"),
-    "mixed": (135080704 + 4520448 + 150389248 + 5599488, "splitk", "13b75fbc734f13b5"),
-    "mixed_modes": (217293568 + 8046592, "splitk", "13b75fbc734f13b5"),
-    "decode_append": (141788928 + 3189504, "splitk", "13b75fbc734f13b5"),
+    "prefill_d128": (1167303424 + 66042624, "prefill", "c7229c3d43514587"),  # sdpa_prefill_pair_kernel<128>
+    "prefill_d64": (9747200 + 256, "prefill", "c7229c3d43514587"),           # sdpa_prefill_pair_kernel<64>
+    "prefill_d256": (329988608 + 45937920, "prefill", "c7229c3d43514587"),   # sdpa_prefill_kernel<256>
+    "ring_prefill": (15011840 + 213760, "prefill", "c7229c3d43514587"),      # sdpa_prefill_pair_kernel<128>
+    "tiny": (209152 + 0, "prefill", "c7229c3d43514587"),                     # sdpa_prefill_pair_kernel<64>
+    "decode": (141731840 + 3812096, "splitk", "1794387a881b41bc"),            # sdpa_splitk_kernel<128>
+    "decode_append": (141737472 + 3909632, "splitk", "1794387a881b41bc"),
+    "mixed": (285201152 + 9822720, "splitk", "1794387a881b41bc"),             # both calls
+    "mixed_modes": (216732416 + 8007680, "splitk", "1794387a881b41bc"),
     # sdpa_clone_kernel: writes still dirty in L2 when the kernel ends are not counted
-    "seq_clone": (134240768 + 84825600, "clone", "5986e1408fef5391"),
+    "seq_clone": (134260224 + 84899840, "clone", "4ba20d84435abfcc"),
 }
 
 
@@ -533,10 +536,11 @@ class Prepared:
 
 def measure(prep: Prepared, steps: int, warmup: int, flush, clocks, world, min_timed_s: float = 0.0):
     """Times one workload: `steps` CUDA-graph replays of the step as a caller runs it (more
-    when `min_timed_s` asks for a longer timed region, so that it holds clock samples), then
-    the same number of replays of a graph with the library's timing events at every kernel
-    boundary (each kernel then runs alone) for the per-kernel times.  Returns the config
-    block (value, step-time statistics, roofline, kernel times, clocks)."""
+    when `min_timed_s` asks for a longer timed region, so that it holds clock samples), each
+    followed, inside the same timed region, by a replay of a graph with the library's timing
+    events at every kernel boundary (each kernel then runs alone) for the per-kernel times, so
+    that both see the same clocks.  The L2 is flushed before every replay, outside the events.
+    Returns the config block (value, step-time statistics, roofline, kernel times, clocks)."""
     import torch
 
     stream = torch.cuda.current_stream()
@@ -558,26 +562,33 @@ def measure(prep: Prepared, steps: int, warmup: int, flush, clocks, world, min_t
         graph_s.replay()
         graph_k.replay()
     torch.cuda.synchronize()
-    est = max((time.monotonic() - t0) / max(1, warmup) / 2, 1e-5)
+    est = max((time.monotonic() - t0) / max(1, warmup), 1e-5)
     n = steps
     if min_timed_s > 0:
-        n = max(steps, min(20000, int(math.ceil(min_timed_s / (est + 2e-4)))))
-    barrier(world)
-    step_ms, w0, w1 = time_replays(graph_s.replay, n, flush, stream)
-    barrier(world)
-    clk = clocks.window(w0, w1)
-
-    # per-kernel breakdown, same L2 flush, outside the timed steps
-    nk = min(n, 200)
+        n = max(steps, min(20000, int(math.ceil(min_timed_s / (est + 4e-4)))))
     kern = {"sched": [], "prefill": [], "splitk": [], "combine": []}
-    for k in range(nk):
+    e_beg = torch.cuda.Event(enable_timing=True)
+    e_end = torch.cuda.Event(enable_timing=True)
+    step_ms = []
+    barrier(world)
+    torch.cuda.synchronize()
+    w0 = time.monotonic()
+    for k in range(n):
+        flush.fill_(k & 0xFF)
+        e_beg.record(stream)
+        graph_s.replay()
+        e_end.record(stream)
         flush.fill_(k & 0xFF)
         graph_k.replay()
         torch.cuda.synchronize()
+        step_ms.append(e_beg.elapsed_time(e_end))
         for i in range(len(prep.calls)):
             e = [ev[i][a].elapsed_time(ev[i][a + 1]) for a in range(4)]
             for key, val in zip(("sched", "prefill", "splitk", "combine"), e):
                 kern[key].append(val)
+    w1 = time.monotonic()
+    barrier(world)
+    clk = clocks.window(w0, w1)
     stats = percentiles(step_ms)
     med = max_over_ranks(stats["median"], world)
     if prep.prefill_like:
@@ -608,7 +619,7 @@ def measure(prep: Prepared, steps: int, warmup: int, flush, clocks, world, min_t
         "ms": {"median": stats["median"], "mean": stats["mean"], "p10": stats["p10"], "p90": stats["p90"]},
         "roofline": roof,
         "kernel_ms": {k: v / len(prep.calls) for k, v in kmed.items()},  # median per call
-        "gpu_launches": n * prep.launches_per_step,
+        "gpu_launches": 2 * n * prep.launches_per_step,  # the step and its timed-kernels copy
         "clocks": clk,
         "useful_tflop_per_step": prep.flops / 1e12, "kv_gb_per_step": prep.kv_bytes / 1e9,
     }

@@ -338,6 +338,51 @@ def test_more_rows_and_units_than_the_scheduler_stages(dev, route, T, Hq, Hkv, s
     check_call(call, dev, rows_subset=sorted(sample), tag=f"T={T}")
 
 
+def _table_call(S, Hq, Hkv, q_len, seed, edit=None):
+    # S segments of q_len rows (an int, or a cycle of lengths), packed in order with a 5-row
+    # uncovered tail, over a 1024-row store (one column each); `edit` may rewrite the table
+    D, rows, cols = 64, 1024, S + 1
+    rng = np.random.default_rng(seed)
+    lens = [q_len] * S if isinstance(q_len, int) else [q_len[s % len(q_len)] for s in range(S)]
+    starts = np.concatenate([[0], np.cumsum(lens)]).tolist()
+    segs = [[starts[s], lens[s], s, int(rng.integers(lens[s], rows + 1))] for s in range(S)]
+    if edit is not None:
+        edit(segs, cols)
+    T = starts[S] + 5
+    g = torch.Generator().manual_seed(seed)
+    q = torch.randn(T, Hq, D, generator=g).to(torch.bfloat16)
+    k = torch.randn(rows, cols, Hkv, D, generator=g).to(torch.bfloat16)
+    v = torch.randn(rows, cols, Hkv, D, generator=g).to(torch.bfloat16)
+    return synth.Call(T, Hq, Hkv, D, rows, cols, np.array(segs, dtype=np.int32), True, 0,
+                      1.0 / np.sqrt(D), q, k, v)
+
+
+def _messy(segs, cols):
+    segs[4][0] = segs[3][0] + 1   # 3 and 4 share rows: both dropped
+    segs[7][2] = cols             # column out of range
+    segs[9][1] = 0                # empty
+    segs[11][3] = -1              # negative kv_end
+    segs[20][0] = segs[31][0]     # 20 and 31 share rows, far apart in the table
+
+
+def _reversed(segs, cols):
+    segs.reverse()                # disjoint rows, but not in row order
+
+
+@pytest.mark.parametrize("S,Hq,Hkv,q_len,edit", [
+    (32, 32, 8, 16, None),     # 32 segments, 512 split-K units: the shortest chains
+    (32, 32, 8, 17, None),     # 32 segments, 768 units: unit steps over ranges per thread
+    (33, 16, 2, 1, None),      # 33 segments, 66 units: block-wide segment steps, one unit per thread
+    (32, 16, 2, 3, _messy),    # invalid, empty and overlapping segments in the one-warp steps
+    (40, 16, 2, 3, _messy),    # the same table shape through the block-wide steps
+    (32, 16, 2, 3, _reversed),  # disjoint segments out of row order: the pairwise overlap test
+    (20, 32, 8, (40, 3), None),  # 80 prefill and 80 split-K units (auto route) in one block
+], ids=["s32_u512", "s32_u768", "s33_u66", "s32_messy", "s40_messy", "s32_reversed", "s20_two_routes"])
+def test_scheduler_paths_at_their_limits(dev, route, S, Hq, Hkv, q_len, edit):
+    call = _table_call(S, Hq, Hkv, q_len, seed=S * 100 + int(np.sum(q_len)), edit=edit)
+    check_call(call, dev, tag=f"S={S} q_len={q_len}")
+
+
 def _multi_phase_prefill_call():
     # 8 prefill segments of 512 rows over 16384 keys each: 16 (segment, KV head) groups whose
     # units re-read 8 MB of K/V each, so the tile line is cut into several phases

@@ -73,7 +73,7 @@ static sdpa_status device_info(DevInfo* out) {
     // every kernel of a call asks for the whole shared-memory carveout, so that the SMs keep
     // one L1 / shared split from kernel to kernel (the clone kernel runs alone and keeps the
     // default split, its L1 to itself)
-    const void* others[2] = {sched_kernel_ptr(), append_kernel_ptr()};
+    const void* others[3] = {sched_kernel_ptr(), sched_small_kernel_ptr(), append_kernel_ptr()};
     for (const void* f : others) {
       e = cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
       if (e != cudaSuccess) return fail(SDPA_ERR_CUDA, "carveout attribute: %s", cudaGetErrorString(e));
@@ -213,8 +213,7 @@ static sdpa_status launch_all(const SchedArgs& sa, const AttnArgs& aa, int D, co
                               const TensorMaps& tm, const AppendArgs* ap, cudaStream_t st) {
   cudaError_t e = mark(0, st);
   if (e == cudaSuccess) {
-    void* args[] = {(void*)&sa};
-    e = cudaLaunchKernel(sched_kernel_ptr(), dim3(1), dim3(kSchedThreads), args, sched_smem_bytes(), st);
+    e = launch_sched(sa, st);
     if (e != cudaSuccess) return fail(SDPA_ERR_CUDA, "scheduler launch: %s", cudaGetErrorString(e));
   }
   if (e == cudaSuccess && ap && sa.S > 0) {

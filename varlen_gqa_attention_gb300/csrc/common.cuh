@@ -207,9 +207,22 @@ struct SchedArgs {
 };
 
 constexpr int kSchedThreads = 512;
+// Calls the small scheduler kernel takes: at most kSmallSegs segments and at most 8192 packed
+// rows, and units that fit one per thread with route 2's starting at a warp boundary.  Live
+// segments cover disjoint rows and a unit holds at least 32 packed rows, so the units number
+// at most Hkv * (ceil(T * group / 32) + S).
+constexpr int kSmallSegs = 32;
+__host__ __device__ inline bool sched_small_ok(int64_t T, int Hq, int Hkv, int S) {
+  if (S > kSmallSegs || T > 8192 || Hkv <= 0) return false;
+  const int64_t units = (int64_t)Hkv * ((T * (Hq / Hkv) + 31) / 32 + S);
+  return units + 31 <= kSchedThreads;
+}
 
 // Kernel entry points (defined in their own translation units).
 const void* sched_kernel_ptr();
+const void* sched_small_kernel_ptr();  // calls with sched_small_ok
+// Launches the scheduler kernel that suits the call (one CTA of kSchedThreads threads).
+cudaError_t launch_sched(const SchedArgs& sa, cudaStream_t st);
 size_t sched_smem_bytes();  // dynamic shared memory of the scheduler kernel
 const void* append_kernel_ptr();
 const void* clone_kernel_ptr();
@@ -277,11 +290,19 @@ struct PieceWalk {
   int32_t fu0;
 };
 
-// a / b for a >= 0, b > 0: one 32-bit division when both fit in 32 bits (the usual case;
-// a 64-bit division is a long instruction sequence)
+// a / b for a >= 0, b > 0: one 32-bit division when both fit in 32 bits (the usual case).
+// On the device the 64-bit division, a long instruction sequence, is a call: kept out of
+// line, it does not spread the code that runs over more instruction-cache lines.
+#ifdef __CUDA_ARCH__
+static __device__ __noinline__ int64_t udiv64(int64_t a, int64_t b) { return a / b; }
+#endif
 __host__ __device__ __forceinline__ int64_t udiv(int64_t a, int64_t b) {
   if ((((uint64_t)a | (uint64_t)b) >> 32) == 0) return (int64_t)((uint32_t)a / (uint32_t)b);
+#ifdef __CUDA_ARCH__
+  return udiv64(a, b);
+#else
   return a / b;
+#endif
 }
 
 // Key tiles of a prefill unit.  The unit's keys [lo, hi) span at most `rows` store rows, so on

@@ -165,10 +165,7 @@ extern "C" sdpa_status sdpa_varlen_splitk_static(
 
   cudaStream_t s = (cudaStream_t)stream;
   cudaError_t e;
-  {
-    void* args[] = {(void*)&sa};
-    e = cudaLaunchKernel(sched_kernel_ptr(), dim3(1), dim3(kSchedThreads), args, sched_smem_bytes(), s);
-  }
+  e = launch_sched(sa, s);
   if (e == cudaSuccess) {
     void* args[] = {(void*)&aa};
     e = cudaLaunchKernel(splitk_kernel_ptr(D), dim3((unsigned)grid), dim3(kSplitkThreads), args,

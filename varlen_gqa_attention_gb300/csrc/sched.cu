@@ -16,12 +16,19 @@
 //      capped at W so that no CTA is idle inside a unit's range), the CTAs whose share
 //      starts in a unit are recorded against it, and each (unit, CTA) pair gets a slot of
 //      partial results unless the unit has a single CTA, which then writes `out` itself;
-//   5. publishes the records, a per-row record for the combine pass, the arrival counters
-//      of the split units (zeroed) and a flag that tells the combine pass whether it has
-//      any work.
-// One CTA of 512 threads does all of it; block-wide scans give the prefix sums.  Segment
-// tables of up to 1024 segments, up to 8192 packed rows and up to 1024 units are built in
-// shared memory; larger calls run the same steps on the workspace copies.
+//   5. publishes the records, a per-row record for the combine pass and a flag that tells
+//      the combine pass whether it has any work.
+// One CTA of 512 threads does all of it.  The work is small and serial (a chain of dependent
+// steps with a barrier between each), so the cost of a call is the length of that chain, not
+// its arithmetic; two shorter chains cover the usual decode and mixed steps:
+//   * at most 32 segments (and 8192 packed rows): steps 1-3 run in warp 0, one segment per
+//     lane, with shuffles (pairwise overlap test, unit-base scan) and no barrier, while the
+//     other warps clear the row owner map;
+//   * at most 512 units: one unit per thread, its record kept in registers; one-barrier scans,
+//     and each thread writes the phase bases that start at the next unit from its own prefix.
+// Otherwise block-wide steps over contiguous ranges per thread.  Segment tables of up to 1024
+// segments, up to 8192 packed rows and up to 1024 units are built in shared memory; larger
+// calls run the same steps on the workspace copies.
 #include "common.cuh"
 
 namespace sdpa {
@@ -64,6 +71,51 @@ __device__ void block_scan(int64_t (&v)[N], int64_t (&tot)[N], int64_t* sh /*[N 
   __syncthreads();
 }
 
+// Exclusive scan of N int64 values per thread over one route's threads, with one barrier.
+// The threads of a route are whole warps (route r of warp w: wroute(w), 0 for none); warps of
+// no route skip the shuffles (a shuffle takes the SM's shuffle unit for a cycle, whichever
+// warp issues it, so idle warps would slow the others).  tot: the route's totals.
+template <int N, typename F>
+__device__ void route_scan(int64_t (&v)[N], int64_t (&tot)[N], int64_t* sh /*[N * 32]*/, F wroute) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const int r = wroute(warp);
+  int64_t x[N];
+  if (r != 0) {
+#pragma unroll
+    for (int k = 0; k < N; ++k) {
+      x[k] = v[k];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int64_t y = __shfl_up_sync(0xffffffffu, x[k], o);
+        if (lane >= o) x[k] += y;
+      }
+      if (lane == 31) sh[k * 32 + warp] = x[k];
+    }
+  }
+  __syncthreads();
+  if (r == 0) return;
+  const bool mine = lane < nw && wroute(lane) == r;
+#pragma unroll
+  for (int k = 0; k < N; ++k) {
+    int64_t w = mine ? sh[k * 32 + lane] : 0;
+    for (int o = 1; o < nw; o <<= 1) {
+      const int64_t y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    const int64_t base = __shfl_sync(0xffffffffu, w, warp > 0 ? warp - 1 : 0);
+    tot[k] = __shfl_sync(0xffffffffu, w, nw - 1);
+    v[k] = (warp > 0 ? base : 0) + x[k] - v[k];
+  }
+}
+
+// Phase of a unit whose route's earlier units re-read `bytes` of K/V: bytes / kPhaseBytes,
+// capped (kPhaseBytes = 3 * 2^24, so a shift and a 32-bit division by 3).
+static_assert(kPhaseBytes == (3ll << 24), "phase budget");
+__device__ __forceinline__ int phase_of(int64_t bytes, int cap) {
+  const uint64_t m = (uint64_t)bytes >> 24;
+  return m >= 3ull * (uint64_t)cap ? cap : (int)((uint32_t)m / 3u);
+}
+
 // Contiguous range of n items owned by this thread.
 __device__ __forceinline__ void my_range(int64_t n, int64_t* a, int64_t* b) {
   const int64_t per = udiv(n + blockDim.x - 1, blockDim.x);
@@ -95,11 +147,91 @@ __device__ __forceinline__ int64_t lead_tiles(int route) { return route == kRout
 // 128-row tile (on a ring store too: its key tiles stop at the wrap, so a TMA box never
 // wraps); everything else, and everything when the prefill kernel is unusable, goes to the
 // split-K kernel.
-__device__ __forceinline__ int route_of(const SchedArgs& A, const SegRec& r) {
-  const int64_t R = (int64_t)r.q_len * A.group;
+__device__ __forceinline__ int route_of(const SchedArgs& A, int32_t q_len) {
+  const int64_t R = (int64_t)q_len * A.group;
   if (A.policy == SDPA_ROUTE_SPLITK || !A.prefill_ok) return kRouteSplitk;
   if (A.policy == SDPA_ROUTE_PREFILL) return kRoutePrefill;
   return R >= kPrefillRows ? kRoutePrefill : kRouteSplitk;
+}
+
+// A segment's entry as the unit builder reads it.
+struct SegView {
+  int32_t q_start, q_len, col, kv_end, nrb, ubase, causal, window;
+};
+
+// Record of unit uq of route q, which belongs to segment s: its (KV head, row block), rows,
+// key range and key tiles.  *span: the unit's length on its route's tile line (the lead
+// placeholders and its key tiles; 0 when no key is visible); *reuse: the K/V bytes its
+// (segment, KV head) group reads again, counted once, on the group's last unit, and only for
+// groups of several units (phases are cut on these).
+__device__ __forceinline__ UnitRec make_unit(const SchedArgs& A, int s, const SegView& g, int q, int64_t uq,
+                                             int64_t* span, int64_t* reuse) {
+  const int rpu = rows_per_unit(A, q), tl = tile_len(A, q);
+  UnitRec ur;
+  const int64_t j = uq - g.ubase;
+  const int64_t jh = udiv(j, g.nrb);
+  ur.seg = s;
+  ur.q_start = g.q_start;
+  ur.q_len = g.q_len;
+  ur.col = g.col;
+  ur.kv_end = g.kv_end;
+  ur.causal = g.causal;
+  ur.window = g.window;
+  ur.hk = (int32_t)jh;
+  ur.rb = (int32_t)(j - jh * g.nrb);
+  const int64_t R = (int64_t)g.q_len * A.group;
+  const int64_t r0 = (int64_t)ur.rb * rpu;
+  ur.rows = (int32_t)min((int64_t)rpu, R - r0);
+  const int i0 = (int)udiv(r0, A.group), i1 = (int)udiv(r0 + ur.rows - 1, A.group);
+  const RowWin w0 = row_window(i0, g.q_len, g.kv_end, g.causal, g.window);
+  const RowWin w1 = row_window(i1, g.q_len, g.kv_end, g.causal, g.window);
+  ur.lo = w0.lo;  // lo and hi grow with the query row
+  ur.hi = max(w1.hi, w0.lo);
+  // key tiles: the prefill kernel's stop at a ring wrap (two TMA ranges), the split-K
+  // kernel's wrap per row
+  const int64_t nt = q == kRoutePrefill ? key_tiles(ur.lo, ur.hi, A.rows, tl).n
+                                        : (ur.hi > ur.lo ? udiv((int64_t)(ur.hi - ur.lo) + tl - 1, tl) : 0);
+  ur.nslots = 0;
+  ur.g_first = 0;
+  ur.ntiles = (int32_t)nt;
+  ur.phase = 0;
+  ur.tile_base = 0;
+  ur.slot_base = 0;
+  *span = nt > 0 ? nt + lead_tiles(q) : 0;
+  *reuse = 0;
+  if (g.nrb >= 2 && ur.rb == g.nrb - 1) {
+    int64_t sp = g.kv_end;
+    if (g.window > 0) sp = min(sp, (int64_t)g.q_len + g.window - 1);
+    *reuse = sp * (int64_t)A.D * 4;
+  }
+  return ur;
+}
+
+// Stream-K placement of a unit whose tile_base and phase are set, within its phase: CTA g of
+// G_p = min(G, W_p) owns [g W_p / G_p, (g+1) W_p / G_p); G_p <= W_p makes every working CTA
+// own a tile, so the owners of a unit's tiles are consecutive CTAs that all work on it
+// (nslots is exact).  Records the CTAs whose share starts inside the unit's span in the
+// per-CTA start table.  pb: the route's phase bases.  Returns the unit's partial rows (its
+// slots, when several CTAs share it).
+__device__ __forceinline__ int64_t place_unit(const SchedArgs& A, UnitRec& ur, int q, int64_t uq,
+                                              const int64_t* pb) {
+  const int64_t nt = ur.ntiles;
+  if (nt <= 0) return 0;
+  const int64_t G = A.grid[q];
+  const int64_t lead = lead_tiles(q);
+  const int64_t b0 = pb[ur.phase];
+  const int64_t Wp = pb[ur.phase + 1] - b0;
+  const int64_t Gp = min(G, Wp);
+  const int64_t k0 = ur.tile_base + lead - b0;  // the key tiles, phase-relative
+  const int64_t g0 = sk_owner(k0, Wp, Gp);
+  const int64_t g1 = sk_owner(k0 + nt - 1, Wp, Gp);
+  ur.g_first = (int32_t)g0;
+  ur.nslots = (int32_t)(g1 - g0 + 1);
+  // the CTAs after the owner of the tile before the span, up to the owner of its last tile
+  const int64_t s0 = ur.tile_base - b0;
+  const int64_t c0 = s0 > 0 ? sk_owner(s0 - 1, Wp, Gp) + 1 : 0;
+  for (int64_t c = c0; c <= g1; ++c) A.ws.first_unit[q][ur.phase * G + c] = (int32_t)uq;
+  return ur.nslots > 1 ? (int64_t)ur.nslots * ur.rows : 0;
 }
 
 // Shared-memory staging: segment tables of up to kSegCache rows, the row-owner map of up
@@ -135,41 +267,6 @@ __global__ void __launch_bounds__(kSchedThreads) sdpa_sched_kernel(SchedArgs A) 
   const bool rows_cached = cached && T <= kRowCache;
   int32_t* row_map = rows_cached ? c_row : W.row_seg;
   int32_t* flag = cached ? c_flag : W.seg_flag;
-  griddep_launch();  // the attention kernels may start launching; they wait for this grid
-  if (threadIdx.x == 0) {
-    s_status = 0;
-    s_work = 0;
-  }
-  __syncthreads();
-
-  // 1. validate; clear overlap flags and the row owner map
-  for (int s = threadIdx.x; s < S; s += blockDim.x) {
-    int32_t g[4];
-    load_seg(A, s, g);
-    int2 md = make_int2(A.causal, A.window);
-    if (A.seg_mode) {
-      md = reinterpret_cast<const int2*>(A.seg_mode)[s];
-      md.x = md.x != 0;
-    }
-    const int32_t bits = segment_bits(g[0], g[1], g[2], g[3], T, A.rows, A.cols, md.y);
-    if (cached) {
-      c_seg[s] = make_int4(g[0], g[1], g[2], g[3]);
-      c_bits[s] = bits;
-      c_mode[s] = md;
-    } else {
-      SegRec r;
-      r.q_start = g[0]; r.q_len = g[1]; r.col = g[2]; r.kv_end = g[3];
-      r.route = kRouteNone; r.nrb = 0; r.bits = bits; r.pad = 0;
-      r.ubase[0] = r.ubase[1] = r.ubase[2] = r.ubase[3] = 0;
-      r.causal = md.x; r.window = md.y;
-      r.pad2[0] = r.pad2[1] = 0;
-      W.segs[s] = r;
-    }
-    flag[s] = 0;
-    if (bits) atomicOr(&s_status, bits);
-  }
-  for (int64_t t = threadIdx.x; t < T; t += blockDim.x) row_map[t] = -1;
-  __syncthreads();
   auto seg_of = [&](int s) -> int4 {
     if (cached) return c_seg[s];
     const SegRec r = W.segs[s];
@@ -177,112 +274,137 @@ __global__ void __launch_bounds__(kSchedThreads) sdpa_sched_kernel(SchedArgs A) 
   };
   auto bits_of = [&](int s) -> int32_t { return cached ? c_bits[s] : W.segs[s].bits; };
 
-  // 2. claim rows; a segment that meets another one marks both.  Teams of threads take
-  // segments round-robin: the whole block per segment when segments are few, one warp per
-  // segment when there are at least as many segments as warps.
   {
-    int team = blockDim.x;
-    while (team > 32 && team * S > (int)blockDim.x * 2) team >>= 1;
-    const int nteam = blockDim.x / team, tm = threadIdx.x / team, ti = threadIdx.x % team;
-    for (int s = tm; s < S; s += nteam) {
-      if (bits_of(s)) continue;
-      const int4 g = seg_of(s);
-      for (int i = ti; i < g.y; i += team) {
-        const int old = atomicCAS(&row_map[g.x + i], -1, s);
-        if (old != -1) {
-          atomicExch(&flag[s], 1);
-          atomicExch(&flag[old], 1);
+    griddep_launch();  // the attention kernels may start launching; they wait for this grid
+    if (threadIdx.x == 0) {
+      s_status = 0;
+      s_work = 0;
+    }
+    __syncthreads();
+
+    // 1. validate; clear overlap flags and the row owner map
+    for (int s = threadIdx.x; s < S; s += blockDim.x) {
+      int32_t g[4];
+      load_seg(A, s, g);
+      int2 md = make_int2(A.causal, A.window);
+      if (A.seg_mode) {
+        md = reinterpret_cast<const int2*>(A.seg_mode)[s];
+        md.x = md.x != 0;
+      }
+      const int32_t bits = segment_bits(g[0], g[1], g[2], g[3], T, A.rows, A.cols, md.y);
+      if (cached) {
+        c_seg[s] = make_int4(g[0], g[1], g[2], g[3]);
+        c_bits[s] = bits;
+        c_mode[s] = md;
+      } else {
+        SegRec r;
+        r.q_start = g[0]; r.q_len = g[1]; r.col = g[2]; r.kv_end = g[3];
+        r.route = kRouteNone; r.nrb = 0; r.bits = bits; r.pad = 0;
+        r.ubase[0] = r.ubase[1] = r.ubase[2] = r.ubase[3] = 0;
+        r.causal = md.x; r.window = md.y;
+        r.pad2[0] = r.pad2[1] = 0;
+        W.segs[s] = r;
+      }
+      flag[s] = 0;
+      if (bits) atomicOr(&s_status, bits);
+    }
+    for (int64_t t = threadIdx.x; t < T; t += blockDim.x) row_map[t] = -1;
+    __syncthreads();
+
+    // 2. claim rows; a segment that meets another one marks both.  Teams of threads take
+    // segments round-robin: the whole block per segment when segments are few, one warp per
+    // segment when there are at least as many segments as warps.
+    {
+      int team = blockDim.x;
+      while (team > 32 && team * S > (int)blockDim.x * 2) team >>= 1;
+      const int nteam = blockDim.x / team, tm = threadIdx.x / team, ti = threadIdx.x % team;
+      for (int s = tm; s < S; s += nteam) {
+        if (bits_of(s)) continue;
+        const int4 g = seg_of(s);
+        for (int i = ti; i < g.y; i += team) {
+          const int old = atomicCAS(&row_map[g.x + i], -1, s);
+          if (old != -1) {
+            atomicExch(&flag[s], 1);
+            atomicExch(&flag[old], 1);
+          }
         }
       }
     }
-  }
-  __syncthreads();
+    __syncthreads();
 
-  // 3. route each live segment and count its units (contiguous segment ranges per thread);
-  // the finished owner map goes out for the combine pass
-  int64_t sa, sb;
-  my_range(S, &sa, &sb);
-  int64_t n1 = 0, n2 = 0, nrows = 0;  // units on routes 1 and 2, packed rows of live segments
-  for (int64_t s = sa; s < sb; ++s) {
-    const int32_t bits = bits_of((int)s);
-    const int fl = flag[s];
-    if (bits == 0 && fl) atomicOr(&s_status, SDPA_SEG_OVERLAP);
-    const int4 g = seg_of((int)s);
-    int route = kRouteNone, nrb = 0;
-    if (bits == 0 && !fl && g.y > 0) {
-      SegRec r;
-      r.q_start = g.x; r.q_len = g.y; r.col = g.z; r.kv_end = g.w;
-      r.window = cached ? c_mode[s].y : W.segs[s].window;
-      const int64_t R = (int64_t)g.y * A.group;
-      route = route_of(A, r);
-      const int rpu = rows_per_unit(A, route);
-      nrb = (int)udiv(R + rpu - 1, rpu);
-      if (route == kRouteSplitk) n1 += (int64_t)A.Hkv * nrb; else n2 += (int64_t)A.Hkv * nrb;
-      nrows += g.y;
+    // 3. route each live segment and count its units (contiguous segment ranges per thread)
+    int64_t sa, sb;
+    my_range(S, &sa, &sb);
+    int64_t n1 = 0, n2 = 0, nrows = 0;  // units on routes 1 and 2, packed rows of live segments
+    for (int64_t s = sa; s < sb; ++s) {
+      const int32_t bits = bits_of((int)s);
+      const int fl = flag[s];
+      if (bits == 0 && fl) atomicOr(&s_status, SDPA_SEG_OVERLAP);
+      const int4 g = seg_of((int)s);
+      int route = kRouteNone, nrb = 0;
+      if (bits == 0 && !fl && g.y > 0) {
+        const int64_t R = (int64_t)g.y * A.group;
+        route = route_of(A, g.y);
+        const int rpu = rows_per_unit(A, route);
+        nrb = (int)udiv(R + rpu - 1, rpu);
+        if (route == kRouteSplitk) n1 += (int64_t)A.Hkv * nrb; else n2 += (int64_t)A.Hkv * nrb;
+        nrows += g.y;
+      }
+      if (cached) {
+        c_rn[s] = make_int2(route, nrb);
+      } else {
+        W.segs[s].route = route;
+        W.segs[s].nrb = nrb;
+      }
     }
-    if (cached) {
-      c_rn[s] = make_int2(route, nrb);
-    } else {
-      W.segs[s].route = route;
-      W.segs[s].nrb = nrb;
+    {
+      int64_t cnt[3] = {n1, n2, nrows}, tot[3];
+      block_scan<3>(cnt, tot, sh);
+      n1 = cnt[0];
+      n2 = cnt[1];
+      // Live segments cover disjoint rows, so tot <= unit_cap; units past the cap (none)
+      // would simply not be generated.
+      if (threadIdx.x == 0) {
+        s_U[1] = min(tot[0], W.unit_cap[1]);
+        s_U[2] = min(tot[1], W.unit_cap[2]);
+        if (tot[2] < T) s_work = 1;  // rows no live segment covers: the combine pass zeroes them
+      }
     }
+    for (int64_t s = sa; s < sb; ++s) {
+      int2 rn;
+      if (cached) {
+        c_ub[s] = make_int2((int32_t)n1, (int32_t)n2);
+        rn = c_rn[s];
+      } else {
+        W.segs[s].ubase[1] = (int32_t)n1;
+        W.segs[s].ubase[2] = (int32_t)n2;
+        rn = make_int2(W.segs[s].route, W.segs[s].nrb);
+      }
+      if (rn.x == kRouteSplitk) n1 += (int64_t)A.Hkv * rn.y;
+      else if (rn.x == kRoutePrefill) n2 += (int64_t)A.Hkv * rn.y;
+    }
+    __syncthreads();
   }
-  {
-    int64_t cnt[3] = {n1, n2, nrows}, tot[3];
-    block_scan<3>(cnt, tot, sh);
-    n1 = cnt[0];
-    n2 = cnt[1];
-    // Live segments cover disjoint rows, so tot <= unit_cap; units past the cap (none)
-    // would simply not be generated.
-    if (threadIdx.x == 0) {
-      s_U[1] = min(tot[0], W.unit_cap[1]);
-      s_U[2] = min(tot[1], W.unit_cap[2]);
-      if (tot[2] < T) s_work = 1;  // rows no live segment covers: the combine pass zeroes them
-    }
-  }
-  for (int64_t s = sa; s < sb; ++s) {
-    int2 rn;
-    if (cached) {
-      c_ub[s] = make_int2((int32_t)n1, (int32_t)n2);
-      rn = c_rn[s];
-    } else {
-      W.segs[s].ubase[1] = (int32_t)n1;
-      W.segs[s].ubase[2] = (int32_t)n2;
-      rn = make_int2(W.segs[s].route, W.segs[s].nrb);
-    }
-    if (rn.x == kRouteSplitk) n1 += (int64_t)A.Hkv * rn.y;
-    else if (rn.x == kRoutePrefill) n2 += (int64_t)A.Hkv * rn.y;
-  }
-  __syncthreads();
 
-  // 4. the units of both routes in one index space, [0, U1) on route 1 and [U1, U1 + U2) on
-  // route 2, each thread a contiguous range: records, key tiles and re-read bytes, then
-  // each unit's place on its route's tile line and its phase
+  // 4-6. the units of both routes in one index space, [0, U1) on route 1 and [U1, U1 + U2) on
+  // route 2: records, key tiles and re-read bytes, then each unit's place on its route's tile
+  // line, its phase and its stream-K split
   const int64_t U1 = s_U[1], U2 = s_U[2], U = U1 + U2;
-  const bool units_cached = U <= kUnitCache;
-  UnitRec* ubuf1 = units_cached ? c_unit : W.units[1];
-  UnitRec* ubuf2 = units_cached ? c_unit + U1 : W.units[2];
-  auto unit_at = [&](int64_t u) -> UnitRec& { return u < U1 ? ubuf1[u] : ubuf2[u - U1]; };
   // phases each route may use: every phase adds at most G - 1 (unit, CTA) pairs to the one
   // pair per unit, and the partial slots hold units + kPartPhases * G pairs
   constexpr int64_t kPhases = kPartPhases < kMaxPhases ? kPartPhases : kMaxPhases;
-  int64_t ua, ub;
-  my_range(U, &ua, &ub);
-  int64_t t1 = 0, t2 = 0, b1 = 0, b2 = 0;  // key-line tiles and re-read bytes on routes 1, 2
-  for (int64_t u = ua; u < ub; ++u) {
-    const int q = u < U1 ? 1 : 2;
-    const int64_t uq = q == 1 ? u : u - U1;
-    const int rpu = rows_per_unit(A, q), tl = tile_len(A, q);
-    // owning segment: the last one whose route-q unit base is <= uq
+  // owning segment of unit uq of route q: the last one whose route-q unit base is <= uq
+  auto owner = [&](int q, int64_t uq) -> int {
     int lo = 0, hi = S - 1, s = 0;
     while (lo <= hi) {
       const int mid = (lo + hi) >> 1;
       const int32_t ubm = cached ? (q == 1 ? c_ub[mid].x : c_ub[mid].y) : W.segs[mid].ubase[q];
       if (ubm <= uq) { s = mid; lo = mid + 1; } else { hi = mid - 1; }
     }
-    struct {
-      int32_t q_start, q_len, col, kv_end, nrb, ubase, causal, window;
-    } g;
+    return s;
+  };
+  auto view_of = [&](int s, int q) -> SegView {
+    SegView g;
     if (cached) {
       const int4 c = c_seg[s];
       g.q_start = c.x; g.q_len = c.y; g.col = c.z; g.kv_end = c.w;
@@ -298,133 +420,94 @@ __global__ void __launch_bounds__(kSchedThreads) sdpa_sched_kernel(SchedArgs A) 
       g.causal = r.causal;
       g.window = r.window;
     }
-    UnitRec ur;
-    const int64_t j = uq - g.ubase;
-    const int64_t jh = udiv(j, g.nrb);
-    ur.seg = s;
-    ur.q_start = g.q_start;
-    ur.q_len = g.q_len;
-    ur.col = g.col;
-    ur.kv_end = g.kv_end;
-    ur.causal = g.causal;
-    ur.window = g.window;
-    ur.hk = (int32_t)jh;
-    ur.rb = (int32_t)(j - jh * g.nrb);
-    const int64_t R = (int64_t)g.q_len * A.group;
-    const int64_t r0 = (int64_t)ur.rb * rpu;
-    ur.rows = (int32_t)min((int64_t)rpu, R - r0);
-    const int i0 = (int)udiv(r0, A.group), i1 = (int)udiv(r0 + ur.rows - 1, A.group);
-    const RowWin w0 = row_window(i0, g.q_len, g.kv_end, g.causal, g.window);
-    const RowWin w1 = row_window(i1, g.q_len, g.kv_end, g.causal, g.window);
-    ur.lo = w0.lo;  // lo and hi grow with the query row
-    ur.hi = max(w1.hi, w0.lo);
-    // key tiles: the prefill kernel's stop at a ring wrap (two TMA ranges), the split-K
-    // kernel's wrap per row
-    const int64_t nt = q == kRoutePrefill ? key_tiles(ur.lo, ur.hi, A.rows, tl).n
-                                          : (ur.hi > ur.lo ? udiv((int64_t)(ur.hi - ur.lo) + tl - 1, tl) : 0);
-    if (nt == 0) s_work = 1;  // rows of a unit with no keys: zeroed by the combine pass
-    ur.nslots = 0;
-    ur.g_first = 0;
-    ur.ntiles = (int32_t)nt;
-    ur.phase = 0;
-    const int64_t span_tiles = nt > 0 ? nt + lead_tiles(q) : 0;
-    ur.tile_base = span_tiles;  // the span, until the scan below
-    // K/V bytes the group's units read again (counted once, on the group's last unit;
-    // only groups of several units re-read them): phases are cut on these
-    int64_t reuse = 0;
-    if (g.nrb >= 2 && ur.rb == g.nrb - 1) {
-      int64_t span = g.kv_end;
-      if (g.window > 0) span = min(span, (int64_t)g.q_len + g.window - 1);
-      reuse = span * (int64_t)A.D * 4;
-    }
-    ur.slot_base = reuse;  // kept here until the phase pass below
-    unit_at(u) = ur;
-    if (q == 1) {
-      t1 += span_tiles;
-      b1 += reuse;
-    } else {
-      t2 += span_tiles;
-      b2 += reuse;
-    }
-  }
-  int64_t tot4[4];
+    return g;
+  };
+  const bool units_cached = U <= kUnitCache;
   {
-    int64_t v[4] = {t1, t2, b1, b2};
-    block_scan<4>(v, tot4, sh);
-    t1 = v[0]; t2 = v[1]; b1 = v[2]; b2 = v[3];
-  }
-  for (int64_t u = ua; u < ub; ++u) {
-    const bool r1 = u < U1;
-    UnitRec& ur = unit_at(u);
-    const int64_t span = ur.tile_base, reuse = ur.slot_base;
-    int64_t& tt = r1 ? t1 : t2;
-    int64_t& bb = r1 ? b1 : b2;
-    ur.tile_base = tt;
-    ur.phase = (int32_t)min(bb / kPhaseBytes, kPhases - 1);
-    tt += span;
-    bb += reuse;
-  }
-  __syncthreads();
-
-  // 5. phase bases: phase k of a route starts at the first unit whose phase is >= k
-  for (int64_t u = ua; u < ub; ++u) {
-    const int q = u < U1 ? 1 : 2;
-    const int64_t uq = q == 1 ? u : u - U1;
-    const int cp = unit_at(u).phase, pp = uq > 0 ? unit_at(u - 1).phase : -1;
-    for (int k = pp + 1; k <= cp; ++k) s_pb[q][k] = unit_at(u).tile_base;
-  }
-  if (threadIdx.x < 2) {
-    const int q = 1 + threadIdx.x;
-    const int64_t Uq = s_U[q];
-    const int64_t np = Uq > 0 ? unit_at(q == 1 ? Uq - 1 : U1 + Uq - 1).phase + 1 : 0;
-    s_np[q] = np;
-    s_pb[q][0] = 0;
-    s_pb[q][np] = q == 1 ? tot4[0] : tot4[1];
-  }
-  __syncthreads();
-
-  // 6. stream-K within each phase: CTA g of G_p = min(G, W_p) owns [g W_p / G_p, (g+1) W_p / G_p);
-  // G_p <= W_p makes every working CTA own a tile, so the owners of a unit's tiles are
-  // consecutive CTAs that all work on it (nslots is exact)
-  int64_t p1 = 0, p2 = 0;  // partial rows on routes 1, 2
-  for (int64_t u = ua; u < ub; ++u) {
-    const int q = u < U1 ? 1 : 2;
-    const int64_t uq = q == 1 ? u : u - U1;
-    UnitRec& ur = unit_at(u);
-    const int64_t nt = ur.ntiles;
-    if (nt > 0) {
-      const int64_t G = A.grid[q];
-      const int64_t lead = lead_tiles(q);
-      const int64_t b0 = s_pb[q][ur.phase];
-      const int64_t Wp = s_pb[q][ur.phase + 1] - b0;
-      const int64_t Gp = min(G, Wp);
-      const int64_t k0 = ur.tile_base + lead - b0;  // the key tiles, phase-relative
-      const int64_t g0 = sk_owner(k0, Wp, Gp);
-      const int64_t g1 = sk_owner(k0 + nt - 1, Wp, Gp);
-      ur.g_first = (int32_t)g0;
-      ur.nslots = (int32_t)(g1 - g0 + 1);
-      if (ur.nslots > 1) (q == 1 ? p1 : p2) += (int64_t)ur.nslots * ur.rows;
-      // split units the combine pass merges
-      if (ur.nslots > 1) s_work = 1;
-      // CTAs whose share starts inside this unit's span begin their walk here: the ones
-      // after the owner of the tile before the span, up to the owner of its last tile
-      const int64_t s0 = ur.tile_base - b0, s1 = k0 + nt;
-      const int64_t c0 = s0 > 0 ? sk_owner(s0 - 1, Wp, Gp) + 1 : 0;
-      for (int64_t c = c0; c <= sk_owner(s1 - 1, Wp, Gp); ++c) W.first_unit[q][ur.phase * G + c] = (int32_t)uq;
+    UnitRec* ubuf1 = units_cached ? c_unit : W.units[1];
+    UnitRec* ubuf2 = units_cached ? c_unit + U1 : W.units[2];
+    auto unit_at = [&](int64_t u) -> UnitRec& { return u < U1 ? ubuf1[u] : ubuf2[u - U1]; };
+    int64_t ua, ub;
+    my_range(U, &ua, &ub);
+    // 4. records; the span and the re-read bytes wait in tile_base and slot_base
+    int64_t t1 = 0, t2 = 0, b1 = 0, b2 = 0;  // key-line tiles and re-read bytes on routes 1, 2
+    for (int64_t u = ua; u < ub; ++u) {
+      const int q = u < U1 ? 1 : 2;
+      const int64_t uq = q == 1 ? u : u - U1;
+      const int s = owner(q, uq);
+      int64_t span, reuse;
+      UnitRec ur = make_unit(A, s, view_of(s, q), q, uq, &span, &reuse);
+      if (ur.ntiles == 0) s_work = 1;  // rows of a unit with no keys: zeroed by the combine pass
+      ur.tile_base = span;
+      ur.slot_base = reuse;
+      unit_at(u) = ur;
+      if (q == 1) {
+        t1 += span;
+        b1 += reuse;
+      } else {
+        t2 += span;
+        b2 += reuse;
+      }
     }
-  }
-  {
-    int64_t v[2] = {p1, p2}, tot[2];
-    block_scan<2>(v, tot, sh);
-    p1 = v[0];
-    p2 = v[1];
-  }
-  for (int64_t u = ua; u < ub; ++u) {
-    const int q = u < U1 ? 1 : 2;
-    UnitRec& ur = unit_at(u);
-    int64_t& pp = q == 1 ? p1 : p2;
-    ur.slot_base = pp;
-    if (ur.nslots > 1) pp += (int64_t)ur.nslots * ur.rows;
+    int64_t tot4[4];
+    {
+      int64_t v[4] = {t1, t2, b1, b2};
+      block_scan<4>(v, tot4, sh);
+      t1 = v[0]; t2 = v[1]; b1 = v[2]; b2 = v[3];
+    }
+    for (int64_t u = ua; u < ub; ++u) {
+      const bool r1 = u < U1;
+      UnitRec& ur = unit_at(u);
+      const int64_t span = ur.tile_base, reuse = ur.slot_base;
+      int64_t& tt = r1 ? t1 : t2;
+      int64_t& bb = r1 ? b1 : b2;
+      ur.tile_base = tt;
+      ur.phase = phase_of(bb, (int)kPhases - 1);
+      tt += span;
+      bb += reuse;
+    }
+    __syncthreads();
+
+    // 5. phase bases: phase k of a route starts at the first unit whose phase is >= k
+    for (int64_t u = ua; u < ub; ++u) {
+      const int q = u < U1 ? 1 : 2;
+      const int64_t uq = q == 1 ? u : u - U1;
+      const int cp = unit_at(u).phase, pp = uq > 0 ? unit_at(u - 1).phase : -1;
+      for (int k = pp + 1; k <= cp; ++k) s_pb[q][k] = unit_at(u).tile_base;
+    }
+    if (threadIdx.x < 2) {
+      const int q = 1 + threadIdx.x;
+      const int64_t Uq = s_U[q];
+      const int64_t np = Uq > 0 ? unit_at(q == 1 ? Uq - 1 : U1 + Uq - 1).phase + 1 : 0;
+      s_np[q] = np;
+      s_pb[q][0] = 0;
+      s_pb[q][np] = q == 1 ? tot4[0] : tot4[1];
+    }
+    __syncthreads();
+
+    // 6. stream-K within each phase, then each split unit's first partial row
+    int64_t p1 = 0, p2 = 0;  // partial rows on routes 1, 2
+    for (int64_t u = ua; u < ub; ++u) {
+      const int q = u < U1 ? 1 : 2;
+      const int64_t uq = q == 1 ? u : u - U1;
+      UnitRec& ur = unit_at(u);
+      const int64_t pr = place_unit(A, ur, q, uq, s_pb[q]);
+      if (ur.nslots > 1) s_work = 1;  // split units the combine pass merges
+      (q == 1 ? p1 : p2) += pr;
+    }
+    {
+      int64_t v[2] = {p1, p2}, tot[2];
+      block_scan<2>(v, tot, sh);
+      p1 = v[0];
+      p2 = v[1];
+    }
+    for (int64_t u = ua; u < ub; ++u) {
+      const int q = u < U1 ? 1 : 2;
+      UnitRec& ur = unit_at(u);
+      int64_t& pp = q == 1 ? p1 : p2;
+      ur.slot_base = pp;
+      if (ur.nslots > 1) pp += (int64_t)ur.nslots * ur.rows;
+    }
   }
   __syncthreads();
 
@@ -492,7 +575,205 @@ __global__ void __launch_bounds__(kSchedThreads) sdpa_sched_kernel(SchedArgs A) 
   }
 }
 
+
+// Scheduler for small calls (sched_small_ok: at most 32 segments, units one per thread): the
+// records of the kernel above, from a short chain in compact code.  The scheduler runs once
+// per call, from a cold instruction cache (the attention kernels ran in between), so its
+// time is mostly the instruction fetch along the path it takes and the dependent steps on
+// that path:
+//   - warp 0 validates the segments (one per lane), tests them for shared rows with
+//     shuffles (one test when the live segments are in row order, else every pair), routes
+//     them and scans the unit bases, while the other warps clear the row records;
+//   - after one barrier, warps take the live segments' row records and every thread one
+//     unit: its record, then two scans over the warps of its route (route 2's units start
+//     at a warp boundary, so a warp holds one route) with one barrier each, and one barrier
+//     for the phase bases, which each thread writes for the next unit of its route from its
+//     own prefix and span.
+__global__ void __launch_bounds__(kSchedThreads) sdpa_sched_small_kernel(SchedArgs A) {
+  __shared__ int4 c_seg[kSmallSegs];   // (q_start, q_len, col, kv_end)
+  __shared__ int2 c_mode[kSmallSegs];  // (causal, window)
+  __shared__ int2 c_rn[kSmallSegs];    // (route, nrb)
+  __shared__ int2 c_ub[kSmallSegs];    // unit bases on routes 1 and 2
+  __shared__ int64_t sh[3 * 32];
+  __shared__ int64_t s_pb[3][kMaxPhases + 1];
+  __shared__ int32_t s_U[3], s_np[3], s_status, s_work;
+  const Workspace& W = A.ws;
+  const int S = A.S;
+  const int T = (int)A.T;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  constexpr uint32_t kAll = 0xffffffffu;
+
+  if (warp == 0) {
+    const bool have = lane < S;
+    int32_t g[4] = {0, 0, 0, 0};
+    int2 md = make_int2(A.causal, A.window);
+    if (have) {
+      load_seg(A, lane, g);
+      if (A.seg_mode) md = reinterpret_cast<const int2*>(A.seg_mode)[lane];
+    }
+    // the attention kernels may start launching (they wait for this grid); the trigger takes
+    // a while, and the loads above are in flight meanwhile
+    griddep_launch();
+    md.x = md.x != 0;
+    const int32_t bits = have ? segment_bits(g[0], g[1], g[2], g[3], T, A.rows, A.cols, md.y) : 0;
+    const bool ok = have && bits == 0 && g[1] > 0;
+    const uint32_t okm = __ballot_sync(kAll, ok);
+    // a valid segment that shares a packed row with another valid one: both are dropped
+    const int32_t a0 = ok ? g[0] : 0, a1 = ok ? g[0] + g[1] : 0;  // in [0, T] when ok
+    const int nxt = __ffs(okm & ~((2u << lane) - 1u)) - 1;       // next valid lane, or -1
+    const int32_t n0 = __shfl_sync(kAll, a0, nxt < 0 ? lane : nxt);
+    bool ov = false;
+    if (!__all_sync(kAll, !ok || nxt < 0 || a1 <= n0)) {
+#pragma unroll 1
+      for (int o = 0; o < kSmallSegs; ++o) {
+        const int32_t b0 = __shfl_sync(kAll, a0, o), b1 = __shfl_sync(kAll, a1, o);
+        ov |= o != lane && ((okm >> o) & 1u) && max(a0, b0) < min(a1, b1);
+      }
+      ov = ov && ok;
+    }
+    const bool live = ok && !ov;
+    int route = kRouteNone, nrb = 0;
+    if (live) {
+      route = route_of(A, g[1]);
+      const int rpu = rows_per_unit(A, route);
+      nrb = (int)(((uint32_t)g[1] * (uint32_t)A.group + rpu - 1) / (uint32_t)rpu);
+    }
+    const int32_t n1 = route == kRouteSplitk ? A.Hkv * nrb : 0, n2 = route == kRoutePrefill ? A.Hkv * nrb : 0;
+    int32_t x1 = n1, x2 = n2;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int32_t y1 = __shfl_up_sync(kAll, x1, o), y2 = __shfl_up_sync(kAll, x2, o);
+      if (lane >= o) {
+        x1 += y1;
+        x2 += y2;
+      }
+    }
+    const int32_t covered = (int32_t)__reduce_add_sync(kAll, live ? (uint32_t)g[1] : 0u);
+    const int32_t st = (int32_t)__reduce_or_sync(kAll, (uint32_t)(bits | (ov ? SDPA_SEG_OVERLAP : 0)));
+    if (have) {
+      c_seg[lane] = make_int4(g[0], g[1], g[2], g[3]);
+      c_mode[lane] = md;
+      c_rn[lane] = make_int2(route, nrb);
+      c_ub[lane] = make_int2(x1 - n1, x2 - n2);
+      SegRec r;
+      r.q_start = g[0]; r.q_len = g[1]; r.col = g[2]; r.kv_end = g[3];
+      r.route = route; r.nrb = nrb; r.bits = bits; r.pad = 0;
+      r.ubase[0] = 0; r.ubase[1] = x1 - n1; r.ubase[2] = x2 - n2; r.ubase[3] = 0;
+      r.causal = md.x; r.window = md.y;
+      r.pad2[0] = r.pad2[1] = 0;
+      W.segs[lane] = r;
+    }
+    if (lane == 31) {
+      s_status = st;
+      s_work = covered < T;  // rows no live segment covers: the combine pass zeroes them
+      s_U[1] = (int32_t)min((int64_t)x1, W.unit_cap[1]);
+      s_U[2] = (int32_t)min((int64_t)x2, W.unit_cap[2]);
+    }
+  } else {
+    griddep_launch();
+    for (int t = threadIdx.x - 32; t < T; t += blockDim.x - 32) W.row_info[t] = make_int4(kRouteNone, 0, 0, 0);
+  }
+  __syncthreads();  // (also orders the row records above before the ones below)
+
+  // each live segment's row records
+  for (int s = warp; s < S; s += nw) {
+    const int2 rn = c_rn[s];
+    if (rn.x == kRouteNone) continue;
+    const int4 g = c_seg[s];
+    const int ub = rn.x == kRouteSplitk ? c_ub[s].x : c_ub[s].y;
+    for (int i = lane; i < g.y; i += 32) W.row_info[g.x + i] = make_int4(rn.x, ub, rn.y, i);
+  }
+
+  // one unit per thread
+  const int U1 = s_U[1], U2 = s_U[2], U1w = (U1 + 31) & ~31;
+  constexpr int kPhases = kPartPhases < kMaxPhases ? kPartPhases : kMaxPhases;
+  const int i = threadIdx.x;
+  const int q = i < U1 ? 1 : (i >= U1w && i < U1w + U2 ? 2 : 0);
+  const int uq = q == 1 ? i : i - U1w;
+  auto wroute = [&](int w) -> int {
+    const int w0 = w * 32;
+    return w0 < U1 ? 1 : (w0 >= U1w && w0 < U1w + U2 ? 2 : 0);
+  };
+  UnitRec ur;
+  int64_t span = 0, reuse = 0;
+  if (q != 0) {
+    // owning segment: the last one whose route-q unit base is <= uq
+    int lo = 0, hi = S - 1, s = 0;
+#pragma unroll 1
+    while (lo <= hi) {
+      const int mid = (lo + hi) >> 1;
+      if ((q == 1 ? c_ub[mid].x : c_ub[mid].y) <= uq) { s = mid; lo = mid + 1; } else { hi = mid - 1; }
+    }
+    const int4 c = c_seg[s];
+    SegView gv;
+    gv.q_start = c.x; gv.q_len = c.y; gv.col = c.z; gv.kv_end = c.w;
+    gv.nrb = c_rn[s].y;
+    gv.ubase = q == 1 ? c_ub[s].x : c_ub[s].y;
+    gv.causal = c_mode[s].x;
+    gv.window = c_mode[s].y;
+    ur = make_unit(A, s, gv, q, uq, &span, &reuse);
+    if (ur.ntiles == 0) s_work = 1;  // rows of a unit with no keys: zeroed by the combine pass
+  }
+  int64_t v[2] = {span, reuse}, tot[2];
+  route_scan<2>(v, tot, sh, wroute);
+  if (q != 0) {
+    const int64_t tb = v[0], bb = v[1];
+    ur.tile_base = tb;
+    ur.phase = phase_of(bb, kPhases - 1);
+    if (uq == 0) s_pb[q][0] = 0;
+    if (uq + 1 < (q == 1 ? U1 : U2)) {
+      const int pn = phase_of(bb + reuse, kPhases - 1);
+      for (int k = ur.phase + 1; k <= pn; ++k) s_pb[q][k] = tb + span;
+    } else {
+      s_np[q] = ur.phase + 1;
+      s_pb[q][ur.phase + 1] = tot[0];
+    }
+  }
+  if (i < 2 && s_U[1 + i] == 0) {
+    s_np[1 + i] = 0;
+    s_pb[1 + i][0] = 0;
+  }
+  __syncthreads();
+  int64_t pv[1] = {0}, ptot[1];
+  if (q != 0) {
+    pv[0] = place_unit(A, ur, q, uq, s_pb[q]);
+    if (ur.nslots > 1) s_work = 1;  // split units the combine pass merges
+  }
+  route_scan<1>(pv, ptot, sh + 2 * 32, wroute);  // (its barrier also publishes s_work)
+  if (q != 0) {
+    ur.slot_base = pv[0];
+    W.units[q][uq] = ur;
+  }
+
+  // the header
+  if (i < 2 * (kMaxPhases + 1)) {
+    const int hq = 1 + i / (kMaxPhases + 1), k = i % (kMaxPhases + 1);
+    if (k <= s_np[hq]) W.hdr->phase_base[hq][k] = s_pb[hq][k];
+  }
+  if (i < 2) {
+    const int hq = 1 + i;
+    W.hdr->tiles[hq] = s_pb[hq][s_np[hq]];
+    W.hdr->units[hq] = s_U[hq];
+    W.hdr->grid[hq] = A.grid[hq];
+    W.hdr->lead[hq] = lead_tiles(hq);
+    W.hdr->nphase[hq] = s_np[hq];
+  }
+  if (i == 0) {
+    W.hdr->combine_work = s_work;
+    W.hdr->status = s_status;
+    if (A.status_dev && s_status) atomicOr(A.status_dev, s_status);
+  }
+}
+
 const void* sched_kernel_ptr() { return (const void*)sdpa_sched_kernel; }
+const void* sched_small_kernel_ptr() { return (const void*)sdpa_sched_small_kernel; }
+
+cudaError_t launch_sched(const SchedArgs& sa, cudaStream_t st) {
+  void* args[] = {(void*)&sa};
+  if (sched_small_ok(sa.T, sa.group * sa.Hkv, sa.Hkv, sa.S))
+    return cudaLaunchKernel(sched_small_kernel_ptr(), dim3(1), dim3(kSchedThreads), args, 0, st);
+  return cudaLaunchKernel(sched_kernel_ptr(), dim3(1), dim3(kSchedThreads), args, sched_smem_bytes(), st);
+}
 size_t sched_smem_bytes() { return kSchedSmem; }
 
 }  // namespace sdpa

@@ -506,11 +506,13 @@ class Prepared:
             # kv_end >= q_len in these workloads)
             self.kv_bytes += sum(w[2] // (4 * c.Hq * c.D) * c.Hkv * c.D * 2 * 2 * 2 for w, c in zip(works, wl.calls))
         # scheduler, split-K and combine per call, plus the prefill kernel when the head group
-        # divides its 128-row tile and the call's packed rows can fill one, plus the KV append
-        # kernel on the append workload
+        # divides its 128-row tile, the call's packed rows can fill one and the call can hold
+        # the prefill route's minimum work (packed rows * Hkv * D * longest key span >= 2^30),
+        # plus the KV append kernel on the append workload
         def pf(c):
             g = c.Hq // c.Hkv
-            return 1 if 128 % g == 0 and c.T * g >= 128 else 0
+            span = c.rows if (c.seg_mode is not None or c.window <= 0) else min(c.rows, c.T + c.window - 1)
+            return 1 if 128 % g == 0 and c.T * g >= 128 and c.T * g * c.Hkv * c.D * span >= 2 ** 30 else 0
         self.launches_per_step = sum(3 + pf(d["call"]) + (1 if "kn" in d else 0) for d in self.calls)
 
     def attend(self, d):

@@ -239,15 +239,21 @@ static sdpa_status launch_all(const SchedArgs& sa, const AttnArgs& aa, int D, co
   }
   if (e == cudaSuccess) e = mark(1, st);
   // The prefill kernel is launched only when some segment can reach its route: not under the
-  // split-K policy, and (automatic routing) not when T * group < 128, where no segment fills
-  // a 128-row tile.  Chained to the scheduler (programmatic dependent launch: its launch
-  // overlaps the scheduler) when the average segment fills less than one tile, so that the
-  // launch is most likely empty; launched after the scheduler otherwise (measured: the
-  // chained launch saves ~6 us on a decode step whose prefill kernel has nothing to do, and
-  // costs ~5 us on prefill steps of a few tiles per CTA).
+  // split-K policy, and (automatic routing) not when no segment can fill a 128-row tile
+  // (T * group < 128) or the call cannot hold kPrefillMinWork of prefill work: that is at
+  // most packed rows * Hkv * D * the longest needed key span, which is at most the store's
+  // rows (longer spans are invalid) and, with a call-wide window, T + window - 1.  Chained to
+  // the scheduler (programmatic dependent launch: its launch overlaps the scheduler) when the
+  // average segment fills less than one tile, so that the launch is most likely empty;
+  // launched after the scheduler otherwise (measured: the chained launch saves ~6 us on a
+  // decode step whose prefill kernel has nothing to do, and costs ~5 us on prefill steps of
+  // a few tiles per CTA).
   const int64_t packed = aa.T * aa.group;
+  int64_t span_max = sa.rows;
+  if (!sa.seg_mode && sa.window > 0) span_max = std::min<int64_t>(span_max, aa.T + sa.window - 1);
+  const bool pf_work = (double)packed * sa.Hkv * D * (double)span_max >= kPrefillMinWork;
   const bool pf_possible = sa.prefill_ok && sa.policy != SDPA_ROUTE_SPLITK &&
-                           (sa.policy == SDPA_ROUTE_PREFILL || packed >= kPrefillRows);
+                           (sa.policy == SDPA_ROUTE_PREFILL || (packed >= kPrefillRows && pf_work));
   if (e == cudaSuccess && pf_possible) {
     void* args[] = {(void*)&aa, (void*)&tm.q, (void*)&tm.k, (void*)&tm.v};
     const bool chained = packed < (int64_t)kPrefillRows * std::max(sa.S, 1);

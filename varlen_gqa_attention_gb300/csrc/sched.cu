@@ -116,6 +116,19 @@ __device__ __forceinline__ int phase_of(int64_t bytes, int cap) {
   return m >= 3ull * (uint64_t)cap ? cap : (int)((uint32_t)m / 3u);
 }
 
+// Sum of one double per thread, the same value (same order) in every thread; one barrier.
+// sh: 32 doubles used by this call only.
+__device__ double block_sum(double v, double* sh) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  if (lane == 0) sh[warp] = v;
+  __syncthreads();
+  double t = 0.0;
+  for (int w = 0; w < nw; ++w) t += sh[w];
+  return t;
+}
+
 // Contiguous range of n items owned by this thread.
 __device__ __forceinline__ void my_range(int64_t n, int64_t* a, int64_t* b) {
   const int64_t per = udiv(n + blockDim.x - 1, blockDim.x);
@@ -145,13 +158,23 @@ __device__ __forceinline__ int64_t lead_tiles(int route) { return route == kRout
 
 // Route of a live segment.  The prefill kernel takes segments that fill at least one
 // 128-row tile (on a ring store too: its key tiles stop at the wrap, so a TMA box never
-// wraps); everything else, and everything when the prefill kernel is unusable, goes to the
-// split-K kernel.
-__device__ __forceinline__ int route_of(const SchedArgs& A, int32_t q_len) {
+// wraps), when the call holds enough such work to pay for that kernel's fixed cost (`big`:
+// the segments' prefill_work sums to at least kPrefillMinWork); everything else, and
+// everything when the prefill kernel is unusable, goes to the split-K kernel.
+__device__ __forceinline__ int route_of(const SchedArgs& A, int32_t q_len, bool big) {
   const int64_t R = (int64_t)q_len * A.group;
   if (A.policy == SDPA_ROUTE_SPLITK || !A.prefill_ok) return kRouteSplitk;
   if (A.policy == SDPA_ROUTE_PREFILL) return kRoutePrefill;
-  return R >= kPrefillRows ? kRoutePrefill : kRouteSplitk;
+  return R >= kPrefillRows && big ? kRoutePrefill : kRouteSplitk;
+}
+// A live segment's share of the prefill route's work measure: packed rows * needed key
+// span * Hkv * D when it fills a 128-row tile, else 0 (in double: no overflow).
+__device__ __forceinline__ double prefill_work(const SchedArgs& A, int32_t q_len, int32_t kv_end, int32_t window) {
+  const int64_t R = (int64_t)q_len * A.group;
+  if (R < kPrefillRows) return 0.0;
+  int64_t span = kv_end;
+  if (window > 0) span = min(span, (int64_t)q_len + window - 1);
+  return (double)R * (double)span * (double)A.Hkv * (double)A.D;
 }
 
 // A segment's entry as the unit builder reads it.
@@ -248,6 +271,7 @@ constexpr size_t kSchedSmem = (size_t)kSegCache * (16 + 8 + 8 + 8 + 4 + 4) + (si
 __global__ void __launch_bounds__(kSchedThreads) sdpa_sched_kernel(SchedArgs A) {
   extern __shared__ __align__(16) unsigned char smem[];
   __shared__ int64_t sh[4 * 32];
+  __shared__ double s_dsum[32];
   __shared__ int64_t s_pb[3][kMaxPhases + 1];
   __shared__ int64_t s_U[3], s_np[3];
   __shared__ int32_t s_status, s_work;
@@ -332,9 +356,17 @@ __global__ void __launch_bounds__(kSchedThreads) sdpa_sched_kernel(SchedArgs A) 
     }
     __syncthreads();
 
-    // 3. route each live segment and count its units (contiguous segment ranges per thread)
+    // 3. route each live segment and count its units (contiguous segment ranges per thread);
+    // first the call's prefill work, which decides whether the prefill route is taken
     int64_t sa, sb;
     my_range(S, &sa, &sb);
+    double pw = 0.0;
+    for (int64_t s = sa; s < sb; ++s) {
+      const int4 g = seg_of((int)s);
+      if (bits_of((int)s) == 0 && !flag[s] && g.y > 0)
+        pw += prefill_work(A, g.y, g.w, cached ? c_mode[s].y : W.segs[s].window);
+    }
+    const bool big = block_sum(pw, s_dsum) >= (double)kPrefillMinWork;
     int64_t n1 = 0, n2 = 0, nrows = 0;  // units on routes 1 and 2, packed rows of live segments
     for (int64_t s = sa; s < sb; ++s) {
       const int32_t bits = bits_of((int)s);
@@ -344,7 +376,7 @@ __global__ void __launch_bounds__(kSchedThreads) sdpa_sched_kernel(SchedArgs A) 
       int route = kRouteNone, nrb = 0;
       if (bits == 0 && !fl && g.y > 0) {
         const int64_t R = (int64_t)g.y * A.group;
-        route = route_of(A, g.y);
+        route = route_of(A, g.y, big);
         const int rpu = rows_per_unit(A, route);
         nrb = (int)udiv(R + rpu - 1, rpu);
         if (route == kRouteSplitk) n1 += (int64_t)A.Hkv * nrb; else n2 += (int64_t)A.Hkv * nrb;
@@ -632,9 +664,12 @@ __global__ void __launch_bounds__(kSchedThreads) sdpa_sched_small_kernel(SchedAr
       ov = ov && ok;
     }
     const bool live = ok && !ov;
+    double pw = live ? prefill_work(A, g[1], g[3], md.y) : 0.0;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) pw += __shfl_xor_sync(kAll, pw, o);
     int route = kRouteNone, nrb = 0;
     if (live) {
-      route = route_of(A, g[1]);
+      route = route_of(A, g[1], pw >= (double)kPrefillMinWork);
       const int rpu = rows_per_unit(A, route);
       nrb = (int)(((uint32_t)g[1] * (uint32_t)A.group + rpu - 1) / (uint32_t)rpu);
     }

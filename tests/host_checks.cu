@@ -108,6 +108,7 @@ int main() {
           rs.push_back({ws.part_ml[r], 8 * ws.part_cap[r]});
           rs.push_back({ws.part_o[r], 4 * ws.part_cap[r] * D});
         }
+        rs.push_back({ws.unit_done, 4 * ws.unit_cap[kRouteSplitk]});
         std::sort(rs.begin(), rs.end(), [](const R& x, const R& y) { return x.p < y.p; });
         for (size_t k = 0; k < rs.size(); ++k) {
           const uintptr_t a = (uintptr_t)rs[k].p;

@@ -11,18 +11,49 @@
 //   * otherwise merge the unit's slots: M = max m_c, L = sum l_c 2^(m_c - M),
 //     O = sum o_c 2^(m_c - M) / L (m in base-2 units, accumulated online over the slots, four
 //     slots' loads in flight at a time), L = 0 -> 0; round to bf16.
+// The pass does not wait for the attention kernels to finish: it is launched (programmatic
+// dependent launch) once the split-K kernel has passed its own wait, i.e. once the scheduler
+// and the prefill kernel have finished, and each warp waits only for its split-K unit's CTAs
+// (the unit's done count reaches nslots; bounded, SDPA_DEV_TIMEOUT past two seconds).  Units
+// that finish early are merged while the split-K kernel's last CTAs still stream.  Every
+// workspace read bypasses L1 (written by kernels still running, or by earlier calls).
 #include "common.cuh"
 
 namespace sdpa {
 
 constexpr int kCombineThreads = 256;
 
+// A unit record read through L2 (five 16-byte loads in flight together).
+__device__ __forceinline__ UnitRec load_unit(const UnitRec* p) {
+  static_assert(sizeof(UnitRec) == 80, "unit record layout");
+  UnitRec r;
+  const int4* s = reinterpret_cast<const int4*>(p);
+  int4* d = reinterpret_cast<int4*>(&r);
+#pragma unroll
+  for (int k = 0; k < 5; ++k) d[k] = __ldcg(s + k);
+  return r;
+}
+
+// Waits until *count reaches n (the unit's CTAs have written their slots); false after about
+// two seconds.
+__device__ __forceinline__ bool wait_done(const int32_t* count, int32_t n) {
+  if (ld_acquire(count) >= n) return true;
+  uint64_t t0;
+  asm volatile("mov.u64 %0, %%globaltimer;\n" : "=l"(t0));
+  for (;;) {
+    __nanosleep(200);
+    if (ld_acquire(count) >= n) return true;
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;\n" : "=l"(t));
+    if (t - t0 > 2000000000ull) return false;
+  }
+}
+
 template <int D>
 __global__ void __launch_bounds__(kCombineThreads) sdpa_combine_kernel(AttnArgs A) {
   constexpr int PER = D / 32;  // elements per lane
   const int64_t gw = ((int64_t)blockIdx.x * kCombineThreads + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
-  griddep_wait();  // the attention kernels' slots and direct writes
   if (gw >= A.T * A.Hq) return;
   const int64_t t = gw / A.Hq;
   const int h = (int)(gw % A.Hq);
@@ -30,9 +61,9 @@ __global__ void __launch_bounds__(kCombineThreads) sdpa_combine_kernel(AttnArgs 
   const Workspace& W = A.ws;
   // independent loads, issued together: whether there is work, the row's owner and the
   // routes' unit counts
-  const int64_t work = W.hdr->combine_work;
-  const int4 ri = W.row_info[t];
-  const int64_t U1 = W.hdr->units[kRouteSplitk], U2 = W.hdr->units[kRoutePrefill];
+  const int64_t work = __ldcg(&W.hdr->combine_work);
+  const int4 ri = __ldcg(&W.row_info[t]);
+  const int64_t U1 = __ldcg(&W.hdr->units[kRouteSplitk]), U2 = __ldcg(&W.hdr->units[kRoutePrefill]);
   if (!work) return;
 
   bool zero = true;
@@ -46,10 +77,17 @@ __global__ void __launch_bounds__(kCombineThreads) sdpa_combine_kernel(AttnArgs 
     const int64_t rb = r / rpu;
     const int64_t u = (int64_t)ri.y + (int64_t)hk * ri.z + rb;
     if (u < (pf ? U2 : U1)) {
-      const UnitRec ur = (pf ? W.units[kRoutePrefill] : W.units[kRouteSplitk])[u];
+      const UnitRec ur = load_unit(pf ? W.units[kRoutePrefill] + u : W.units[kRouteSplitk] + u);
       if (ur.nslots == 1) return;  // written by the unit's only CTA
       if (ur.nslots > 1) {
         zero = false;
+        if (!pf && !wait_done(W.unit_done + u, ur.nslots)) {
+          if (lane == 0) {
+            atomicOr((unsigned long long*)&W.hdr->status, (unsigned long long)SDPA_DEV_TIMEOUT);
+            if (A.status_dev) atomicOr(A.status_dev, SDPA_DEV_TIMEOUT);
+          }
+          return;
+        }
         // online log-sum-exp over the slots, four slots' loads in flight at a time:
         // M' = max(M, m_c), L' = L 2^(M - M') + l_c 2^(m_c - M'), O likewise
         const int64_t rl = r - rb * rpu;
@@ -69,18 +107,18 @@ __global__ void __launch_bounds__(kCombineThreads) sdpa_combine_kernel(AttnArgs 
             v[b] = make_float2(-INFINITY, 0.f);
             if (c0 + b < ur.nslots) {
               const int64_t c = c0 + b;
-              v[b] = ml[c * stride];
+              v[b] = __ldcg(ml + c * stride);
               // PER = D / 32 floats per lane: 2, 4 or 8, so 8-byte loads at D = 64
               if constexpr (PER % 4 == 0) {
 #pragma unroll
                 for (int k = 0; k < PER; k += 4) {
-                  const float4 u = *reinterpret_cast<const float4*>(po + c * stride * D + k);
+                  const float4 u = __ldcg(reinterpret_cast<const float4*>(po + c * stride * D + k));
                   o[b][k] = u.x; o[b][k + 1] = u.y; o[b][k + 2] = u.z; o[b][k + 3] = u.w;
                 }
               } else {
 #pragma unroll
                 for (int k = 0; k < PER; k += 2) {
-                  const float2 u = *reinterpret_cast<const float2*>(po + c * stride * D + k);
+                  const float2 u = __ldcg(reinterpret_cast<const float2*>(po + c * stride * D + k));
                   o[b][k] = u.x; o[b][k + 1] = u.y;
                 }
               }

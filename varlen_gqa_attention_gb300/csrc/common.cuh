@@ -102,6 +102,10 @@ struct Workspace {
   float* part_o[3];     // [route][P_cap * D] unnormalised output
   int64_t unit_cap[3];
   int64_t part_cap[3];
+  // [U_cap of the split-K route] CTAs of each split-K unit that have written their partial
+  // slot (zeroed by the scheduler, counted by the split-K kernel with release semantics, read
+  // by the combine pass with acquire semantics)
+  int32_t* unit_done;
 };
 
 __host__ __device__ inline int64_t align_up(int64_t x, int64_t a) { return (x + a - 1) / a * a; }
@@ -151,6 +155,7 @@ __host__ inline size_t layout_workspace(char* base, int64_t T, int Hq, int Hkv, 
     w.part_ml[r] = (float2*)take(8 * w.part_cap[r]);
     w.part_o[r] = (float*)take(4 * w.part_cap[r] * D);
   }
+  w.unit_done = (int32_t*)take(4 * (w.unit_cap[kRouteSplitk] > 0 ? w.unit_cap[kRouteSplitk] : 1));
   if (ws) *ws = w;
   return (size_t)off;
 }
@@ -427,6 +432,19 @@ __device__ inline bool walk_next(PieceWalk& w, UnitRec& ur, int64_t& ta, int64_t
 // returns at once.  launch_dependents lets the next such kernel start launching.
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
 __device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;\n" :::); }
+
+// A count that one kernel publishes and a concurrently running one waits for: a CTA's writes
+// before a barrier, then one thread's release add, are visible to a reader whose acquire load
+// sees the add.  (The callers put a barrier right before the add, which also keeps the
+// compiler from moving the CTA's writes past it.)
+__device__ __forceinline__ void red_add_release(int32_t* p, int32_t v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;\n" ::"l"(p), "r"(v));
+}
+__device__ __forceinline__ int32_t ld_acquire(const int32_t* p) {
+  int32_t v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];\n" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);

@@ -470,6 +470,7 @@ __global__ void __launch_bounds__(kSchedThreads) sdpa_sched_kernel(SchedArgs A) 
       int64_t span, reuse;
       UnitRec ur = make_unit(A, s, view_of(s, q), q, uq, &span, &reuse);
       if (ur.ntiles == 0) s_work = 1;  // rows of a unit with no keys: zeroed by the combine pass
+      if (q == kRouteSplitk) W.unit_done[uq] = 0;
       ur.tile_base = span;
       ur.slot_base = reuse;
       unit_at(u) = ur;
@@ -748,6 +749,7 @@ __global__ void __launch_bounds__(kSchedThreads) sdpa_sched_small_kernel(SchedAr
     gv.window = c_mode[s].y;
     ur = make_unit(A, s, gv, q, uq, &span, &reuse);
     if (ur.ntiles == 0) s_work = 1;  // rows of a unit with no keys: zeroed by the combine pass
+    if (q == kRouteSplitk) W.unit_done[uq] = 0;
   }
   int64_t v[2] = {span, reuse}, tot[2];
   route_scan<2>(v, tot, sh, wroute);

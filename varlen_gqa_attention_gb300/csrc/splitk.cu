@@ -82,9 +82,12 @@ struct KvCursor {
 };
 
 // One warp's share of a unit: 16 packed rows x a slice of each key tile.
+// s_count: [0] the done count of the CTA's previous piece, not yet counted (or null); [1] this
+// piece's (null when it writes `out` directly).
 template <int D, int NCS>
 __device__ __forceinline__ void splitk_unit(const AttnArgs& A, const UnitRec& ur, const SegRec& sg,
-                                            int64_t ta, int64_t tb, int slot, char* smem, float2* s_ml) {
+                                            int64_t ta, int64_t tb, int slot, char* smem, float2* s_ml,
+                                            int32_t** s_count) {
   using S = SplitkSmem<D>;
   constexpr int RB = S::kRowBytes;
   constexpr int SW = kSplitkTile / NCS;  // keys per warp slice
@@ -290,6 +293,13 @@ __device__ __forceinline__ void splitk_unit(const AttnArgs& A, const UnitRec& ur
   }
   __syncthreads();
 
+  // the previous piece's partial slot, written a whole piece ago, is counted now: a release
+  // waits for the CTA's earlier writes to land, which by now they have (counted at the end
+  // of their own piece, it would wait on the slot just written, under full memory load)
+  if (tid == 0 && s_count[0] != nullptr) {
+    red_add_release(s_count[0], 1);
+    s_count[0] = nullptr;
+  }
   const bool direct = ur.nslots == 1;
   // the output row of local row rl, dims d0 .. d0 + 7, normalised by 1 / L (0 when L = 0)
   auto store_out = [&](int rl, int d0, const float* acc, float L) {
@@ -343,12 +353,17 @@ template <int D>
 __global__ void __launch_bounds__(kSplitkThreads) sdpa_splitk_kernel(AttnArgs A) {
   extern __shared__ __align__(128) char smem[];
   __shared__ float2 s_ml[4 * 16];
+  __shared__ int32_t* s_count[2];
   griddep_wait();    // the scheduler's output (and the prefill kernel's end)
   griddep_launch();
   PieceWalk wk;
   walk_begin(wk, A.ws, kRouteSplitk);  // no work on this route: the walk ends at once
   UnitRec ur;
   int64_t ta, tb;
+  // Done counts (kept in shared memory, not in registers across a piece): the combine pass
+  // merges a split unit as soon as all its CTAs have counted its slot, while other CTAs still
+  // stream.  A piece's slot is counted in the next piece's epilogue, or as the CTA ends.
+  if (threadIdx.x == 0) s_count[0] = nullptr;
   while (walk_next(wk, ur, ta, tb)) {
     SegRec sg;  // the unit record carries its segment's entry: no second dependent load
     sg.q_start = ur.q_start;
@@ -358,11 +373,17 @@ __global__ void __launch_bounds__(kSplitkThreads) sdpa_splitk_kernel(AttnArgs A)
     sg.causal = ur.causal;
     sg.window = ur.window;
     const int slot = (int)(blockIdx.x - ur.g_first);
+    // the walk has moved past the piece's unit
+    if (threadIdx.x == 0) s_count[1] = ur.nslots > 1 ? A.ws.unit_done + (wk.u - 1) : nullptr;
     if (ur.rows <= 16)
-      splitk_unit<D, 4>(A, ur, sg, ta, tb, slot, smem, s_ml);
+      splitk_unit<D, 4>(A, ur, sg, ta, tb, slot, smem, s_ml, s_count);
     else
-      splitk_unit<D, 2>(A, ur, sg, ta, tb, slot, smem, s_ml);
+      splitk_unit<D, 2>(A, ur, sg, ta, tb, slot, smem, s_ml, s_count);
+    if (threadIdx.x == 0) s_count[0] = s_count[1];
   }
+  // the last piece ended on a barrier: its slot is complete (the release add is cumulative
+  // over the CTA's writes before it)
+  if (threadIdx.x == 0 && s_count[0] != nullptr) red_add_release(s_count[0], 1);
 }
 
 template __global__ void sdpa_splitk_kernel<64>(AttnArgs);

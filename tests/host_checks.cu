@@ -3,6 +3,8 @@
 //   * udiv against plain 64-bit division, operands above 2^32 included;
 //   * the stream-K partition: shares are contiguous, cover [0, W) once, and sk_owner(x)
 //     names the CTA whose share holds x;
+//   * the cost-weighted tile line: each tile owned once, a unit's owners consecutive, each
+//     owning a tile;
 //   * the key tiles of a prefill unit: they cover its keys once and never wrap a ring;
 //   * the workspace layout: every region 256-byte aligned, disjoint, inside the size it
 //     returns, and the partial slots sized for the phases the scheduler may use;
@@ -53,6 +55,46 @@ int main() {
       prev_end = b;
     }
     CHECK(prev_end == W);
+  }
+  // the cost-weighted tile line of one phase: units of nt tiles of tile_cost units each,
+  // behind lead_cost placeholders, shared by phase_ctas CTAs.  Every tile is owned by exactly
+  // one CTA (the one whose share holds its start, line_tiles), the owners of a unit's tiles
+  // are the CTAs from sk_owner(first start) to sk_owner(last start), and each of them owns
+  // at least one of its tiles (so a unit's slot count is exact)
+  for (int i = 0; i < 3000; ++i) {
+    const int route = (next_u64() & 1) ? kRouteSplitk : kRoutePrefill;
+    const int nu = 1 + (int)(next_u64() % 40);
+    std::vector<int64_t> base(nu), nts(nu), tws(nu);
+    int64_t Wp = 0;
+    for (int u = 0; u < nu; ++u) {
+      nts[u] = (next_u64() % 5 == 0) ? 0 : 1 + (int64_t)(next_u64() % ((next_u64() & 1) ? 4 : 300));
+      tws[u] = tile_cost(route, 1 + (int)(next_u64() % 32));
+      base[u] = Wp;
+      Wp += nts[u] > 0 ? lead_cost(route) + nts[u] * tws[u] : 0;
+    }
+    if (Wp == 0) continue;
+    const int64_t G = 1 + (int64_t)(next_u64() % 400);
+    const int64_t Gp = phase_ctas(G, Wp, route);
+    CHECK(Gp >= 1 && Gp <= G);
+    for (int u = 0; u < nu; ++u) {
+      if (nts[u] == 0) continue;
+      const int64_t k0 = base[u] + lead_cost(route);
+      std::vector<int> owner(nts[u], -1);
+      for (int64_t g = 0; g < Gp; ++g) {
+        int64_t ta, tb;
+        line_tiles(sk_start(g, Wp, Gp), sk_start(g + 1, Wp, Gp), k0, nts[u], tws[u], &ta, &tb);
+        for (int64_t t = ta; t < tb; ++t) {
+          CHECK(owner[t] == -1);
+          owner[t] = (int)g;
+        }
+      }
+      const int64_t g0 = sk_owner(k0, Wp, Gp), g1 = sk_owner(k0 + (nts[u] - 1) * tws[u], Wp, Gp);
+      CHECK(owner[0] == g0 && owner[nts[u] - 1] == g1);
+      for (int64_t t = 0; t < nts[u]; ++t) {
+        CHECK(owner[t] >= 0);
+        if (t > 0) CHECK(owner[t] == owner[t - 1] || owner[t] == owner[t - 1] + 1);
+      }
+    }
   }
   // key tiles of a prefill unit: the tiles cover [lo, hi) once, in order, each 1..bn keys,
   // and no tile's store rows wrap (its first and last key sit in one block of `rows`)

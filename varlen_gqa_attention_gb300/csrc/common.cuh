@@ -353,6 +353,31 @@ __host__ __device__ inline void key_tile(const KeyTiles& k, int64_t t, int bn, i
   *valid = (int)(v < bn ? v : bn);
 }
 
+// Line cost of a key tile.  A split-K tile of a unit with more than 16 rows (two MMA row
+// groups per warp) costs about 1.25x one of at most 16 rows (measured: CTAs' finishing times
+// follow the row-weighted tile count, not the tile count), so the split-K route's tile line
+// counts 4 and 5 units per tile; the prefill route's tiles all cost the same (1).  The lead
+// placeholders ahead of a unit's tiles are in the same units.
+__host__ __device__ __forceinline__ int64_t tile_cost(int route, int rows) {
+  return route == kRouteSplitk ? (rows > 16 ? 5 : 4) : 1;
+}
+__host__ __device__ __forceinline__ int64_t lead_cost(int route) { return route == kRoutePrefill ? 6 : 3 * 4; }
+// CTAs that share a phase of Wp line units: at most one per costliest tile, so that every
+// CTA's share holds the start of a tile of each unit it crosses (nslots stays exact).
+__host__ __device__ __forceinline__ int64_t phase_ctas(int64_t G, int64_t Wp, int route) {
+  const int64_t g = Wp / (route == kRouteSplitk ? 5 : 1);
+  return g < 1 ? 1 : (g < G ? g : G);
+}
+// The tiles [ta, tb) of a unit whose first tile starts at line position k0 (nt tiles of tw
+// units each) that a share [t0, t1) owns: those whose start lies in the share.
+__host__ __device__ inline void line_tiles(int64_t t0, int64_t t1, int64_t k0, int64_t nt, int64_t tw,
+                                           int64_t* ta, int64_t* tb) {
+  const int64_t a = t0 > k0 ? t0 - k0 : 0, e = nt * tw, b = t1 - k0 < e ? t1 - k0 : e;
+  *ta = (a + tw - 1) / tw;
+  *tb = b > 0 ? (b + tw - 1) / tw : 0;
+  if (*ta > nt) *ta = nt;
+}
+
 // Stream-K partition: CTA g of G owns flattened tiles [g*W/G, (g+1)*W/G).
 __host__ __device__ inline int64_t sk_start(int64_t g, int64_t W, int64_t G) { return udiv(g * W, G); }
 // CTA whose range holds tile x.
@@ -386,7 +411,7 @@ __device__ inline bool walk_phase(PieceWalk& w) {
     const int64_t b0 = w.p == 0 ? w.pb0 : h->phase_base[w.route][w.p];
     const int64_t Wp = (w.p == 0 ? w.pb1 : h->phase_base[w.route][w.p + 1]) - b0;
     if (Wp <= 0) continue;
-    const int64_t Gp = min(w.G, Wp);  // at most one CTA per tile: nslots stays exact
+    const int64_t Gp = phase_ctas(w.G, Wp, w.route);
     if ((int64_t)blockIdx.x >= Gp) continue;
     w.t0 = b0 + sk_start(blockIdx.x, Wp, Gp);
     w.t1 = b0 + sk_start(blockIdx.x + 1, Wp, Gp);
@@ -403,19 +428,23 @@ __device__ inline bool walk_next(PieceWalk& w, UnitRec& ur, int64_t& ta, int64_t
   for (;;) {
     while (w.t0 < w.t1 && w.u < w.U) {
       const UnitRec r = w.W->units[w.route][w.u];
-      const int64_t k0 = r.tile_base + w.lead, k1 = k0 + r.ntiles;  // the unit's key tiles
+      const int64_t tw = tile_cost(w.route, r.rows);
+      const int64_t k0 = r.tile_base + w.lead, k1 = k0 + r.ntiles * tw;  // the unit's key tiles
       if (r.ntiles == 0 || w.t0 >= k1) {
         ++w.u;
         continue;
       }
-      if (w.t1 <= k0) {  // the share ends among the unit's placeholders
-        w.t0 = w.t1;
-        break;
+      line_tiles(w.t0, w.t1, k0, r.ntiles, tw, &ta, &tb);
+      if (ta >= tb) {
+        if (w.t1 <= k1) {  // the share ends before the unit's next tile starts
+          w.t0 = w.t1;
+          break;
+        }
+        ++w.u;  // the share starts past the unit's last tile start
+        continue;
       }
       ur = r;
-      ta = max(w.t0, k0) - k0;
-      tb = min(w.t1, k1) - k0;
-      w.t0 = k0 + tb;
+      w.t0 = k0 + tb * tw;
       ++w.u;
       return true;
     }

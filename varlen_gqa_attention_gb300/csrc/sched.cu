@@ -9,13 +9,15 @@
 //   3. routes each remaining segment to the split-K or the tensor-memory prefill kernel and
 //      cuts it into units (segment, KV head, block of packed (query row, head) rows);
 //   4. counts each unit's key tiles over the union of its rows' visible intervals and lays
-//      all units' tiles end to end, each unit's behind a few placeholder tiles for the cost
-//      of starting a piece; the line is cut into at most four phases whose re-read K/V fits
-//      the L2 budget; within a phase CTA g of G owns tiles [g*W/G, (g+1)*W/G) (a stream-K
-//      split, so every CTA gets the same amount of key tiles whatever the length mix; G is
-//      capped at W so that no CTA is idle inside a unit's range), the CTAs whose share
-//      starts in a unit are recorded against it, and each (unit, CTA) pair gets a slot of
-//      partial results unless the unit has a single CTA, which then writes `out` itself;
+//      all units' tiles end to end on a line of cost units (tile_cost: 4 or 5 per split-K
+//      tile by its unit's rows, 1 per prefill tile), each unit's behind lead placeholders
+//      for the cost of starting a piece; the line is cut into at most four phases whose
+//      re-read K/V fits the L2 budget; within a phase CTA g of G owns the tiles whose start
+//      lies in [g*W/G, (g+1)*W/G) (a stream-K split, so every CTA gets the same cost whatever
+//      the length mix; G is capped at W over the costliest tile, so that every CTA owns a
+//      tile of each unit its share crosses), the CTAs whose share starts in a unit are
+//      recorded against it, and each (unit, CTA) pair gets a slot of partial results unless
+//      the unit has a single CTA, which then writes `out` itself;
 //   5. publishes the records, a per-row record for the combine pass and a flag that tells
 //      the combine pass whether it has any work.
 // One CTA of 512 threads does all of it.  The work is small and serial (a chain of dependent
@@ -151,10 +153,9 @@ __device__ __forceinline__ int rows_per_unit(const SchedArgs& A, int route) {
 __device__ __forceinline__ int tile_len(const SchedArgs& A, int route) {
   return route == kRoutePrefill ? A.tile_pf : kSplitkTile;
 }
-// Start-up cost of a piece in key tiles of its route (operand loads, pipeline fill, the
-// epilogue): about 4 us per prefill piece of 128-key tiles that take about 0.7 us, about
-// 4 us per split-K piece of 64-key tiles that stream at about 1.6 us.
-__device__ __forceinline__ int64_t lead_tiles(int route) { return route == kRoutePrefill ? 6 : 3; }
+// Start-up cost of a piece (operand loads, pipeline fill, the epilogue), lead_cost: about
+// 4 us per prefill piece of 128-key tiles that take about 0.7 us (6 tiles), about 4 us per
+// split-K piece of 64-key tiles that stream at about 1.6 us (3 tiles of 4 units).
 
 // Route of a live segment.  The prefill kernel takes segments that fill at least one
 // 128-row tile (on a ring store too: its key tiles stop at the wrap, so a TMA box never
@@ -220,7 +221,7 @@ __device__ __forceinline__ UnitRec make_unit(const SchedArgs& A, int s, const Se
   ur.phase = 0;
   ur.tile_base = 0;
   ur.slot_base = 0;
-  *span = nt > 0 ? nt + lead_tiles(q) : 0;
+  *span = nt > 0 ? nt * tile_cost(q, ur.rows) + lead_cost(q) : 0;
   *reuse = 0;
   if (g.nrb >= 2 && ur.rb == g.nrb - 1) {
     int64_t sp = g.kv_end;
@@ -241,19 +242,21 @@ __device__ __forceinline__ int64_t place_unit(const SchedArgs& A, UnitRec& ur, i
   const int64_t nt = ur.ntiles;
   if (nt <= 0) return 0;
   const int64_t G = A.grid[q];
-  const int64_t lead = lead_tiles(q);
+  const int64_t tw = tile_cost(q, ur.rows);
   const int64_t b0 = pb[ur.phase];
   const int64_t Wp = pb[ur.phase + 1] - b0;
-  const int64_t Gp = min(G, Wp);
-  const int64_t k0 = ur.tile_base + lead - b0;  // the key tiles, phase-relative
+  const int64_t Gp = phase_ctas(G, Wp, q);
+  const int64_t k0 = ur.tile_base + lead_cost(q) - b0;  // the key tiles, phase-relative
   const int64_t g0 = sk_owner(k0, Wp, Gp);
-  const int64_t g1 = sk_owner(k0 + nt - 1, Wp, Gp);
+  const int64_t g1 = sk_owner(k0 + (nt - 1) * tw, Wp, Gp);  // the owners of the first and last tile starts
   ur.g_first = (int32_t)g0;
   ur.nslots = (int32_t)(g1 - g0 + 1);
-  // the CTAs after the owner of the tile before the span, up to the owner of its last tile
-  const int64_t s0 = ur.tile_base - b0;
+  // the CTAs whose share starts inside the unit's span: after the owner of the position
+  // before the span, up to the owner of its last position
+  const int64_t s0 = ur.tile_base - b0, s1 = k0 + nt * tw;
   const int64_t c0 = s0 > 0 ? sk_owner(s0 - 1, Wp, Gp) + 1 : 0;
-  for (int64_t c = c0; c <= g1; ++c) A.ws.first_unit[q][ur.phase * G + c] = (int32_t)uq;
+  const int64_t c1 = sk_owner(s1 - 1, Wp, Gp);
+  for (int64_t c = c0; c <= c1; ++c) A.ws.first_unit[q][ur.phase * G + c] = (int32_t)uq;
   return ur.nslots > 1 ? (int64_t)ur.nslots * ur.rows : 0;
 }
 
@@ -598,7 +601,7 @@ __global__ void __launch_bounds__(kSchedThreads) sdpa_sched_kernel(SchedArgs A) 
     W.hdr->tiles[q] = s_pb[q][s_np[q]];
     W.hdr->units[q] = s_U[q];
     W.hdr->grid[q] = A.grid[q];
-    W.hdr->lead[q] = lead_tiles(q);
+    W.hdr->lead[q] = lead_cost(q);
     W.hdr->nphase[q] = s_np[q];
   }
   if (threadIdx.x == 0) {
@@ -792,7 +795,7 @@ __global__ void __launch_bounds__(kSchedThreads) sdpa_sched_small_kernel(SchedAr
     W.hdr->tiles[hq] = s_pb[hq][s_np[hq]];
     W.hdr->units[hq] = s_U[hq];
     W.hdr->grid[hq] = A.grid[hq];
-    W.hdr->lead[hq] = lead_tiles(hq);
+    W.hdr->lead[hq] = lead_cost(hq);
     W.hdr->nphase[hq] = s_np[hq];
   }
   if (i == 0) {

@@ -64,13 +64,15 @@ int main() {
   for (int i = 0; i < 3000; ++i) {
     const int route = (next_u64() & 1) ? kRouteSplitk : kRoutePrefill;
     const int nu = 1 + (int)(next_u64() % 40);
-    std::vector<int64_t> base(nu), nts(nu), tws(nu);
+    std::vector<int64_t> base(nu), nts(nu), tws(nu), lds(nu);
     int64_t Wp = 0;
     for (int u = 0; u < nu; ++u) {
       nts[u] = (next_u64() % 5 == 0) ? 0 : 1 + (int64_t)(next_u64() % ((next_u64() & 1) ? 4 : 300));
-      tws[u] = tile_cost(route, 1 + (int)(next_u64() % 32));
+      const int rows = 1 + (int)(next_u64() % 32);
+      tws[u] = tile_cost(route, rows);
+      lds[u] = lead_cost(route);
       base[u] = Wp;
-      Wp += nts[u] > 0 ? lead_cost(route) + nts[u] * tws[u] : 0;
+      Wp += nts[u] > 0 ? lds[u] + nts[u] * tws[u] : 0;
     }
     if (Wp == 0) continue;
     const int64_t G = 1 + (int64_t)(next_u64() % 400);
@@ -78,7 +80,7 @@ int main() {
     CHECK(Gp >= 1 && Gp <= G);
     for (int u = 0; u < nu; ++u) {
       if (nts[u] == 0) continue;
-      const int64_t k0 = base[u] + lead_cost(route);
+      const int64_t k0 = base[u] + lds[u];
       std::vector<int> owner(nts[u], -1);
       for (int64_t g = 0; g < Gp; ++g) {
         int64_t ta, tb;

@@ -56,8 +56,8 @@ struct UnitRec {
   int32_t phase;              // scheduling phase of the unit (see SchedHdr)
   int32_t q_start, q_len, col, kv_end;  // the segment's entry and mask mode, copied so
   int32_t causal, window;               // that one record (80 bytes) describes a piece
-  int64_t tile_base;          // start of the unit's span in the flattened tile line: `lead`
-                              // placeholder tiles, then its ntiles key tiles
+  int64_t tile_base;          // start of the unit's span on its route's line of cost units:
+                              // lead_cost placeholders, then its ntiles key tiles
   int64_t slot_base;          // first partial row of the unit's slots
 };
 static_assert(sizeof(UnitRec) == 80, "unit record layout");
@@ -73,16 +73,12 @@ constexpr int64_t kPhaseBytes = 48ll << 20;
 
 // Scheduler header (int64 words).
 struct SchedHdr {
-  int64_t tiles[3];   // total tiles per route (index = route)
+  int64_t tiles[3];   // length of each route's line, in cost units (index = route)
   int64_t units[3];   // units per route
   int64_t grid[3];    // CTAs per route as launched
   int64_t status;     // OR of the status bits of this call
   int64_t nphase[3];  // phases per route
-  int64_t phase_base[3][kMaxPhases + 1];  // first tile of each phase; [nphase] = tiles
-  // Placeholder tiles ahead of each unit's key tiles on the line: they stand for the cost of
-  // starting a piece (operand loads, pipeline fill, the epilogue), so a CTA whose share
-  // starts a unit gets that many fewer key tiles.
-  int64_t lead[3];
+  int64_t phase_base[3][kMaxPhases + 1];  // start of each phase on the line; [nphase] = tiles
   // Non-zero when the combine pass has rows to write: rows no live segment covers, units
   // with no keys, or units split over several CTAs.
   int64_t combine_work;
@@ -293,9 +289,8 @@ struct PieceWalk {
   int64_t G;        // launched grid
   int64_t nphase;
   int64_t p;        // current phase
-  int64_t t0, t1;   // remaining tiles of this CTA in phase p
+  int64_t t0, t1;   // remaining share of this CTA in phase p (line cost units)
   int64_t u;        // next unit to look at
-  int64_t lead;     // placeholder tiles ahead of each unit's key tiles
   int64_t U;        // units of the route
   int64_t pb0, pb1; // phase 0's tile range, and this CTA's first unit in it (loaded early)
   int32_t fu0;
@@ -353,19 +348,23 @@ __host__ __device__ inline void key_tile(const KeyTiles& k, int64_t t, int bn, i
   *valid = (int)(v < bn ? v : bn);
 }
 
-// Line cost of a key tile.  A split-K tile of a unit with more than 16 rows (two MMA row
-// groups per warp) costs about 1.25x one of at most 16 rows (measured: CTAs' finishing times
-// follow the row-weighted tile count, not the tile count), so the split-K route's tile line
-// counts 4 and 5 units per tile; the prefill route's tiles all cost the same (1).  The lead
-// placeholders ahead of a unit's tiles are in the same units.
+// Line cost of a key tile, and of the lead placeholders ahead of a unit's tiles (the cost of
+// starting a piece: operand loads, pipeline fill, the epilogue).  A split-K tile of a unit
+// with more than 16 rows (two MMA row groups per warp) costs about 1.5x one of at most 16
+// rows, and a piece 4-6 small tiles (a least-squares fit of the split-K CTAs' finishing times
+// on their tile counts by row class and their piece counts, on decode and mixed steps: 0.6-0.8
+// us per small tile, 1.0-1.1 us per large one, 3.2 us per piece of 8-row units, 4-4.9 us on
+// the mixed steps), so the split-K route's line counts 4 and 6 units per tile and 20 units
+// of lead (leads of 16 or 24 by rows measured no better).  Prefill tiles cost 1 and a prefill
+// piece 6 (about 4 us against 0.7 us per 128-key tile).
 __host__ __device__ __forceinline__ int64_t tile_cost(int route, int rows) {
-  return route == kRouteSplitk ? (rows > 16 ? 5 : 4) : 1;
+  return route == kRouteSplitk ? (rows > 16 ? 6 : 4) : 1;
 }
-__host__ __device__ __forceinline__ int64_t lead_cost(int route) { return route == kRoutePrefill ? 6 : 3 * 4; }
+__host__ __device__ __forceinline__ int64_t lead_cost(int route) { return route == kRouteSplitk ? 20 : 6; }
 // CTAs that share a phase of Wp line units: at most one per costliest tile, so that every
 // CTA's share holds the start of a tile of each unit it crosses (nslots stays exact).
 __host__ __device__ __forceinline__ int64_t phase_ctas(int64_t G, int64_t Wp, int route) {
-  const int64_t g = Wp / (route == kRouteSplitk ? 5 : 1);
+  const int64_t g = Wp / (route == kRouteSplitk ? 6 : 1);
   return g < 1 ? 1 : (g < G ? g : G);
 }
 // The tiles [ta, tb) of a unit whose first tile starts at line position k0 (nt tiles of tw
@@ -394,7 +393,6 @@ __device__ inline void walk_begin(PieceWalk& w, const Workspace& W, int route) {
   w.route = route;
   w.G = gridDim.x;
   w.nphase = h->nphase[route];
-  w.lead = h->lead[route];
   w.U = h->units[route];
   w.pb0 = h->phase_base[route][0];
   w.pb1 = h->phase_base[route][1];
@@ -429,7 +427,7 @@ __device__ inline bool walk_next(PieceWalk& w, UnitRec& ur, int64_t& ta, int64_t
     while (w.t0 < w.t1 && w.u < w.U) {
       const UnitRec r = w.W->units[w.route][w.u];
       const int64_t tw = tile_cost(w.route, r.rows);
-      const int64_t k0 = r.tile_base + w.lead, k1 = k0 + r.ntiles * tw;  // the unit's key tiles
+      const int64_t k0 = r.tile_base + lead_cost(w.route), k1 = k0 + r.ntiles * tw;  // its key tiles
       if (r.ntiles == 0 || w.t0 >= k1) {
         ++w.u;
         continue;

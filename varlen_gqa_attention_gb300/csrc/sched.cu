@@ -9,9 +9,9 @@
 //   3. routes each remaining segment to the split-K or the tensor-memory prefill kernel and
 //      cuts it into units (segment, KV head, block of packed (query row, head) rows);
 //   4. counts each unit's key tiles over the union of its rows' visible intervals and lays
-//      all units' tiles end to end on a line of cost units (tile_cost: 4 or 5 per split-K
+//      all units' tiles end to end on a line of cost units (tile_cost: 4 or 6 per split-K
 //      tile by its unit's rows, 1 per prefill tile), each unit's behind lead placeholders
-//      for the cost of starting a piece; the line is cut into at most four phases whose
+//      for the cost of starting a piece (lead_cost); the line is cut into at most four phases whose
 //      re-read K/V fits the L2 budget; within a phase CTA g of G owns the tiles whose start
 //      lies in [g*W/G, (g+1)*W/G) (a stream-K split, so every CTA gets the same cost whatever
 //      the length mix; G is capped at W over the costliest tile, so that every CTA owns a
@@ -153,9 +153,6 @@ __device__ __forceinline__ int rows_per_unit(const SchedArgs& A, int route) {
 __device__ __forceinline__ int tile_len(const SchedArgs& A, int route) {
   return route == kRoutePrefill ? A.tile_pf : kSplitkTile;
 }
-// Start-up cost of a piece (operand loads, pipeline fill, the epilogue), lead_cost: about
-// 4 us per prefill piece of 128-key tiles that take about 0.7 us (6 tiles), about 4 us per
-// split-K piece of 64-key tiles that stream at about 1.6 us (3 tiles of 4 units).
 
 // Route of a live segment.  The prefill kernel takes segments that fill at least one
 // 128-row tile (on a ring store too: its key tiles stop at the wrap, so a TMA box never
@@ -601,7 +598,6 @@ __global__ void __launch_bounds__(kSchedThreads) sdpa_sched_kernel(SchedArgs A) 
     W.hdr->tiles[q] = s_pb[q][s_np[q]];
     W.hdr->units[q] = s_U[q];
     W.hdr->grid[q] = A.grid[q];
-    W.hdr->lead[q] = lead_cost(q);
     W.hdr->nphase[q] = s_np[q];
   }
   if (threadIdx.x == 0) {
@@ -795,7 +791,6 @@ __global__ void __launch_bounds__(kSchedThreads) sdpa_sched_small_kernel(SchedAr
     W.hdr->tiles[hq] = s_pb[hq][s_np[hq]];
     W.hdr->units[hq] = s_U[hq];
     W.hdr->grid[hq] = A.grid[hq];
-    W.hdr->lead[hq] = lead_cost(hq);
     W.hdr->nphase[hq] = s_np[hq];
   }
   if (i == 0) {

@@ -209,6 +209,21 @@ static cudaError_t launch_k(const void* f, unsigned grid, unsigned block, void**
   return cudaLaunchKernelExC(&cfg, f, args);
 }
 
+// Whether a call may route segments to the prefill kernel: not under the split-K policy, and
+// (automatic routing) not when no segment can fill a 128-row tile (T * group < 128) or the
+// call cannot hold kPrefillMinWork of prefill work: that is at most packed rows * Hkv * D *
+// the longest needed key span, which is at most the store's rows (longer spans are invalid)
+// and, with a call-wide window, T + window - 1.  The scheduler takes the result as
+// prefill_ok, so it never routes work to a prefill kernel that is not launched.
+static bool prefill_launch(const SchedArgs& sa, int64_t T) {
+  if (sa.policy == SDPA_ROUTE_SPLITK) return false;
+  if (sa.policy == SDPA_ROUTE_PREFILL) return true;
+  const int64_t packed = T * sa.group;
+  int64_t span_max = sa.rows;
+  if (!sa.seg_mode && sa.window > 0) span_max = std::min<int64_t>(span_max, T + sa.window - 1);
+  return packed >= kPrefillRows && (double)packed * sa.Hkv * sa.D * (double)span_max >= (double)kPrefillMinWork;
+}
+
 static sdpa_status launch_all(const SchedArgs& sa, const AttnArgs& aa, int D, const Grids& g,
                               const TensorMaps& tm, const AppendArgs* ap, cudaStream_t st) {
   cudaError_t e = mark(0, st);
@@ -238,22 +253,14 @@ static sdpa_status launch_all(const SchedArgs& sa, const AttnArgs& aa, int D, co
     if (e != cudaSuccess) return fail(SDPA_ERR_CUDA, "append launch: %s", cudaGetErrorString(e));
   }
   if (e == cudaSuccess) e = mark(1, st);
-  // The prefill kernel is launched only when some segment can reach its route: not under the
-  // split-K policy, and (automatic routing) not when no segment can fill a 128-row tile
-  // (T * group < 128) or the call cannot hold kPrefillMinWork of prefill work: that is at
-  // most packed rows * Hkv * D * the longest needed key span, which is at most the store's
-  // rows (longer spans are invalid) and, with a call-wide window, T + window - 1.  Chained to
-  // the scheduler (programmatic dependent launch: its launch overlaps the scheduler) when the
-  // average segment fills less than one tile, so that the launch is most likely empty;
-  // launched after the scheduler otherwise (measured: the chained launch saves ~6 us on a
-  // decode step whose prefill kernel has nothing to do, and costs ~5 us on prefill steps of
-  // a few tiles per CTA).
+  // The prefill kernel is launched when the call's schedule may use it (prefill_ok, see
+  // prefill_launch).  Chained to the scheduler (programmatic dependent launch: its launch
+  // overlaps the scheduler) when the average segment fills less than one tile, so that the
+  // launch is most likely empty; launched after the scheduler otherwise (measured: the
+  // chained launch saves ~6 us on a decode step whose prefill kernel has nothing to do, and
+  // costs ~5 us on prefill steps of a few tiles per CTA).
   const int64_t packed = aa.T * aa.group;
-  int64_t span_max = sa.rows;
-  if (!sa.seg_mode && sa.window > 0) span_max = std::min<int64_t>(span_max, aa.T + sa.window - 1);
-  const bool pf_work = (double)packed * sa.Hkv * D * (double)span_max >= kPrefillMinWork;
-  const bool pf_possible = sa.prefill_ok && sa.policy != SDPA_ROUTE_SPLITK &&
-                           (sa.policy == SDPA_ROUTE_PREFILL || (packed >= kPrefillRows && pf_work));
+  const bool pf_possible = sa.prefill_ok;
   if (e == cudaSuccess && pf_possible) {
     void* args[] = {(void*)&aa, (void*)&tm.q, (void*)&tm.k, (void*)&tm.v};
     const bool chained = packed < (int64_t)kPrefillRows * std::max(sa.S, 1);
@@ -323,7 +330,7 @@ static sdpa_status run(const void* q, int64_t T, int Hq, int D, int64_t q_rs, in
   const int group = Hq / Hkv;
   const bool group_fits = group <= kPrefillRows && (kPrefillRows % group) == 0;
   sa.tile_pf = prefill_tile_keys(D);
-  sa.prefill_ok = di.prefill_ok[d_index(D)] && group_fits &&
+  sa.prefill_ok = di.prefill_ok[d_index(D)] && group_fits && prefill_launch(sa, T) &&
                   make_tensor_maps(q, T, Hq, D, q_rs, q_hs, k, v, rows, cols, Hkv, group, sa.tile_pf,
                                    &tm.q, &tm.k, &tm.v);
   sa.grid[0] = 0;

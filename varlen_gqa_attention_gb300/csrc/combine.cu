@@ -15,24 +15,15 @@
 // dependent launch) once the split-K kernel has passed its own wait, i.e. once the scheduler
 // and the prefill kernel have finished, and each warp waits only for its split-K unit's CTAs
 // (the unit's done count reaches nslots; bounded, SDPA_DEV_TIMEOUT past two seconds).  Units
-// that finish early are merged while the split-K kernel's last CTAs still stream.  Every
-// workspace read bypasses L1 (written by kernels still running, or by earlier calls).
+// that finish early are merged while the split-K kernel's last CTAs still stream.  The
+// scheduler's records and the prefill kernel's slots come from grids that finished before
+// this one was launched, so plain loads see them; the split-K slots are read after the
+// acquire, through L2.
 #include "common.cuh"
 
 namespace sdpa {
 
 constexpr int kCombineThreads = 256;
-
-// A unit record read through L2 (five 16-byte loads in flight together).
-__device__ __forceinline__ UnitRec load_unit(const UnitRec* p) {
-  static_assert(sizeof(UnitRec) == 80, "unit record layout");
-  UnitRec r;
-  const int4* s = reinterpret_cast<const int4*>(p);
-  int4* d = reinterpret_cast<int4*>(&r);
-#pragma unroll
-  for (int k = 0; k < 5; ++k) d[k] = __ldcg(s + k);
-  return r;
-}
 
 // Waits until *count reaches n (the unit's CTAs have written their slots); false after about
 // two seconds.
@@ -61,9 +52,9 @@ __global__ void __launch_bounds__(kCombineThreads) sdpa_combine_kernel(AttnArgs 
   const Workspace& W = A.ws;
   // independent loads, issued together: whether there is work, the row's owner and the
   // routes' unit counts
-  const int64_t work = __ldcg(&W.hdr->combine_work);
-  const int4 ri = __ldcg(&W.row_info[t]);
-  const int64_t U1 = __ldcg(&W.hdr->units[kRouteSplitk]), U2 = __ldcg(&W.hdr->units[kRoutePrefill]);
+  const int64_t work = W.hdr->combine_work;
+  const int4 ri = W.row_info[t];
+  const int64_t U1 = W.hdr->units[kRouteSplitk], U2 = W.hdr->units[kRoutePrefill];
   if (!work) return;
 
   bool zero = true;
@@ -77,7 +68,7 @@ __global__ void __launch_bounds__(kCombineThreads) sdpa_combine_kernel(AttnArgs 
     const int64_t rb = r / rpu;
     const int64_t u = (int64_t)ri.y + (int64_t)hk * ri.z + rb;
     if (u < (pf ? U2 : U1)) {
-      const UnitRec ur = load_unit(pf ? W.units[kRoutePrefill] + u : W.units[kRouteSplitk] + u);
+      const UnitRec ur = (pf ? W.units[kRoutePrefill] : W.units[kRouteSplitk])[u];
       if (ur.nslots == 1) return;  // written by the unit's only CTA
       if (ur.nslots > 1) {
         zero = false;

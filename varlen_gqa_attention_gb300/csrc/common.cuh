@@ -23,7 +23,7 @@ constexpr int kPrefillRows = 128;  // tensor-memory prefill kernel: one 128-lane
 // it the tensor-memory kernel's fixed cost (set-up, first loads, epilogue: ~15 us) is more
 // than the split-K kernel's extra time (measured crossover: ~2^30 at D = 64 and D = 128,
 // about 2 GFLOP of causal work).
-constexpr double kPrefillMinWork = 1073741824.0;
+constexpr float kPrefillMinWork = 1073741824.0f;
 constexpr int kPrefillTile = 128;  // prefill kernel: key positions per tile
 // Packed rows of a prefill unit: two 128-row halves that share every K/V tile (D = 64, 128),
 // or one (D = 256, whose output accumulator alone fills the tensor memory).

@@ -118,15 +118,15 @@ __device__ __forceinline__ int phase_of(int64_t bytes, int cap) {
   return m >= 3ull * (uint64_t)cap ? cap : (int)((uint32_t)m / 3u);
 }
 
-// Sum of one double per thread, the same value (same order) in every thread; one barrier.
-// sh: 32 doubles used by this call only.
-__device__ double block_sum(double v, double* sh) {
+// Sum of one float per thread, the same value (same order) in every thread; one barrier.
+// sh: 32 floats used by this call only.
+__device__ float block_sum(float v, float* sh) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
   if (lane == 0) sh[warp] = v;
   __syncthreads();
-  double t = 0.0;
+  float t = 0.f;
   for (int w = 0; w < nw; ++w) t += sh[w];
   return t;
 }
@@ -166,13 +166,14 @@ __device__ __forceinline__ int route_of(const SchedArgs& A, int32_t q_len, bool 
   return R >= kPrefillRows && big ? kRoutePrefill : kRouteSplitk;
 }
 // A live segment's share of the prefill route's work measure: packed rows * needed key
-// span * Hkv * D when it fills a 128-row tile, else 0 (in double: no overflow).
-__device__ __forceinline__ double prefill_work(const SchedArgs& A, int32_t q_len, int32_t kv_end, int32_t window) {
+// span * Hkv * D when it fills a 128-row tile, else 0 (in fp32: no overflow, ample for a
+// threshold, and fast; fp64 runs at a small fraction of the fp32 rate here).
+__device__ __forceinline__ float prefill_work(const SchedArgs& A, int32_t q_len, int32_t kv_end, int32_t window) {
   const int64_t R = (int64_t)q_len * A.group;
-  if (R < kPrefillRows) return 0.0;
+  if (R < kPrefillRows) return 0.f;
   int64_t span = kv_end;
   if (window > 0) span = min(span, (int64_t)q_len + window - 1);
-  return (double)R * (double)span * (double)A.Hkv * (double)A.D;
+  return (float)R * (float)span * (float)A.Hkv * (float)A.D;
 }
 
 // A segment's entry as the unit builder reads it.
@@ -271,7 +272,7 @@ constexpr size_t kSchedSmem = (size_t)kSegCache * (16 + 8 + 8 + 8 + 4 + 4) + (si
 __global__ void __launch_bounds__(kSchedThreads) sdpa_sched_kernel(SchedArgs A) {
   extern __shared__ __align__(16) unsigned char smem[];
   __shared__ int64_t sh[4 * 32];
-  __shared__ double s_dsum[32];
+  __shared__ float s_fsum[32];
   __shared__ int64_t s_pb[3][kMaxPhases + 1];
   __shared__ int64_t s_U[3], s_np[3];
   __shared__ int32_t s_status, s_work;
@@ -360,13 +361,13 @@ __global__ void __launch_bounds__(kSchedThreads) sdpa_sched_kernel(SchedArgs A) 
     // first the call's prefill work, which decides whether the prefill route is taken
     int64_t sa, sb;
     my_range(S, &sa, &sb);
-    double pw = 0.0;
+    float pw = 0.f;
     for (int64_t s = sa; s < sb; ++s) {
       const int4 g = seg_of((int)s);
       if (bits_of((int)s) == 0 && !flag[s] && g.y > 0)
         pw += prefill_work(A, g.y, g.w, cached ? c_mode[s].y : W.segs[s].window);
     }
-    const bool big = block_sum(pw, s_dsum) >= (double)kPrefillMinWork;
+    const bool big = block_sum(pw, s_fsum) >= kPrefillMinWork;
     int64_t n1 = 0, n2 = 0, nrows = 0;  // units on routes 1 and 2, packed rows of live segments
     for (int64_t s = sa; s < sb; ++s) {
       const int32_t bits = bits_of((int)s);
@@ -664,12 +665,12 @@ __global__ void __launch_bounds__(kSchedThreads) sdpa_sched_small_kernel(SchedAr
       ov = ov && ok;
     }
     const bool live = ok && !ov;
-    double pw = live ? prefill_work(A, g[1], g[3], md.y) : 0.0;
+    float pw = live ? prefill_work(A, g[1], g[3], md.y) : 0.f;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) pw += __shfl_xor_sync(kAll, pw, o);
     int route = kRouteNone, nrb = 0;
     if (live) {
-      route = route_of(A, g[1], pw >= (double)kPrefillMinWork);
+      route = route_of(A, g[1], pw >= kPrefillMinWork);
       const int rpu = rows_per_unit(A, route);
       nrb = (int)(((uint32_t)g[1] * (uint32_t)A.group + rpu - 1) / (uint32_t)rpu);
     }

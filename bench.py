@@ -85,17 +85,17 @@ KERNEL_SOURCES = {
 # when it was taken.  A kernel whose sources hash differently now reports traffic null until
 # the capture is repeated.
 NCU_TRAFFIC = {
-    "prefill_d128": (1167303424 + 66042624, "prefill", "c7229c3d43514587"),  # sdpa_prefill_pair_kernel<128>
-    "prefill_d64": (9747200 + 256, "prefill", "c7229c3d43514587"),           # sdpa_prefill_pair_kernel<64>
-    "prefill_d256": (329988608 + 45937920, "prefill", "c7229c3d43514587"),   # sdpa_prefill_kernel<256>
-    "ring_prefill": (15011840 + 213760, "prefill", "c7229c3d43514587"),      # sdpa_prefill_pair_kernel<128>
-    "tiny": (209152 + 0, "prefill", "c7229c3d43514587"),                     # sdpa_prefill_pair_kernel<64>
-    "decode": (141731840 + 3812096, "splitk", "1794387a881b41bc"),            # sdpa_splitk_kernel<128>
-    "decode_append": (141737472 + 3909632, "splitk", "1794387a881b41bc"),
-    "mixed": (285201152 + 9822720, "splitk", "1794387a881b41bc"),             # both calls
-    "mixed_modes": (216732416 + 8007680, "splitk", "1794387a881b41bc"),
+    "prefill_d128": (1237094656 + 65428480, "prefill", "fa5647a7b80fc120"),  # sdpa_prefill_pair_kernel<128>
+    "prefill_d64": (9902080 + 512, "prefill", "fa5647a7b80fc120"),  # sdpa_prefill_pair_kernel<64>
+    "prefill_d256": (334974464 + 46728192, "prefill", "fa5647a7b80fc120"),  # sdpa_prefill_kernel<256>
+    "ring_prefill": (15016704 + 176128, "prefill", "fa5647a7b80fc120"),  # sdpa_prefill_pair_kernel<128>
+    "tiny": (158976 + 0, "splitk", "b2ea96bb9d5f324b"),  # sdpa_splitk_kernel<64> (tiny calls take the split-K route)
+    "decode": (141723136 + 3245568, "splitk", "b2ea96bb9d5f324b"),  # sdpa_splitk_kernel<128>
+    "decode_append": (141721856 + 3546880, "splitk", "b2ea96bb9d5f324b"),
+    "mixed": (285227776 + 10821888, "splitk", "b2ea96bb9d5f324b"),  # both calls
+    "mixed_modes": (219486464 + 8172800, "splitk", "b2ea96bb9d5f324b"),
     # sdpa_clone_kernel: writes still dirty in L2 when the kernel ends are not counted
-    "seq_clone": (134260224 + 84899840, "clone", "4ba20d84435abfcc"),
+    "seq_clone": (134238720 + 84515072, "clone", "429f90f2e11ceea7"),
 }
 
 

@@ -5,6 +5,7 @@
 //     names the CTA whose share holds x;
 //   * the cost-weighted tile line: each tile owned once, a unit's owners consecutive, each
 //     owning a tile;
+//   * the small scheduler's admission bound on the units of any live table;
 //   * the key tiles of a prefill unit: they cover its keys once and never wrap a ring;
 //   * the workspace layout: every region 256-byte aligned, disjoint, inside the size it
 //     returns, and the partial slots sized for the phases the scheduler may use;
@@ -96,6 +97,39 @@ int main() {
         CHECK(owner[t] >= 0);
         if (t > 0) CHECK(owner[t] == owner[t - 1] || owner[t] == owner[t - 1] + 1);
       }
+    }
+  }
+  // the small scheduler's admission bound: for every call sched_small_ok admits, any table
+  // of disjoint live segments, routed any way, gives at most kSchedThreads threads of units
+  // with route 2's starting at a warp boundary
+  for (int i = 0; i < 20000; ++i) {
+    const int Hkv = 1 << (int)(next_u64() % 4);
+    const int group = 1 + (int)(next_u64() % 16);
+    const int Hq = Hkv * group;
+    const int S = 1 + (int)(next_u64() % 40);
+    const int64_t T = 1 + (int64_t)(next_u64() % ((next_u64() & 1) ? 300 : 9000));
+    if (!sched_small_ok(T, Hq, Hkv, S)) continue;
+    CHECK(S <= kSmallSegs && T <= 8192);
+    int64_t left = T, u1 = 0, u2 = 0;
+    for (int s = 0; s < S && left > 0; ++s) {
+      const int64_t ql = 1 + (int64_t)(next_u64() % (uint64_t)left);
+      left -= ql;
+      const int64_t R = ql * group;
+      if (next_u64() & 1) u1 += Hkv * ((R + kSplitkRows - 1) / kSplitkRows);
+      else {
+        const int rpu = prefill_unit_rows(64 << (int)(next_u64() % 3));
+        u2 += Hkv * ((R + rpu - 1) / rpu);
+      }
+    }
+    CHECK(((u1 + 31) / 32) * 32 + u2 <= kSchedThreads);
+    // the table that comes closest to the bound: S - 1 one-row segments and one long one, all
+    // on the split-K route but the first, on the prefill route (route 2 after padding)
+    if (T >= S) {
+      int64_t w1 = 0;
+      for (int s = 1; s < S - 1; ++s) w1 += Hkv * ((group + kSplitkRows - 1) / kSplitkRows);
+      if (S > 1) w1 += Hkv * (((T - S + 1) * group + kSplitkRows - 1) / kSplitkRows);
+      const int64_t w2 = S > 1 ? Hkv * ((group + 255) / 256) : 0;
+      CHECK(((w1 + 31) / 32) * 32 + w2 <= kSchedThreads);
     }
   }
   // key tiles of a prefill unit: the tiles cover [lo, hi) once, in order, each 1..bn keys,

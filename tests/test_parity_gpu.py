@@ -383,6 +383,38 @@ def test_scheduler_paths_at_their_limits(dev, route, S, Hq, Hkv, q_len, edit):
     check_call(call, dev, tag=f"S={S} q_len={q_len}")
 
 
+def _equal_length_call(S, Hq, Hkv, q_len, kv_lo, kv_hi, seed, window=0):
+    # S segments of q_len rows with kv_end in [kv_lo, kv_hi], one column each
+    D, cols = 64, S + 1
+    rows = kv_hi
+    rng = np.random.default_rng(seed)
+    segs = [[s * q_len, q_len, s, int(rng.integers(kv_lo, kv_hi + 1))] for s in range(S)]
+    T = S * q_len
+    g = torch.Generator().manual_seed(seed)
+    q = torch.randn(T, Hq, D, generator=g).to(torch.bfloat16)
+    k = torch.randn(rows, cols, Hkv, D, generator=g).to(torch.bfloat16)
+    v = torch.randn(rows, cols, Hkv, D, generator=g).to(torch.bfloat16)
+    return synth.Call(T, Hq, Hkv, D, rows, cols, np.array(segs, dtype=np.int32), True, window,
+                      1.0 / np.sqrt(D), q, k, v)
+
+
+@pytest.mark.parametrize("S,Hq,Hkv,q_len,kv_lo,kv_hi,window", [
+    (19, 128, 16, 1, 2000, 2000, 0),     # 304 equal split-K units, one per CTA (small scheduler)
+    (19, 128, 16, 1, 1950, 2000, 0),     # near-equal lengths: still whole units
+    (37, 64, 8, 1, 1980, 2000, 0),       # 296 units through the block-wide scheduler
+    (1, 16, 2, 2048, 8192, 8192, 1024),  # 128 windowed prefill units of one long segment
+    (1, 16, 2, 2048, 8192, 8192, 0),     # the same without a window: long, uneven units split
+], ids=["s19_equal", "s19_near_equal", "s37_general", "prefill_window", "prefill_no_window"])
+def test_whole_unit_phases(dev, route, S, Hq, Hkv, q_len, kv_lo, kv_hi, window):
+    # phases of short, even units give each CTA one whole unit (no partial slots)
+    call = _equal_length_call(S, Hq, Hkv, q_len, kv_lo, kv_hi, seed=S + q_len + kv_lo, window=window)
+    rows = None
+    if call.T > 256:
+        rng = np.random.default_rng(5)
+        rows = sorted(set(rng.choice(call.T, size=160, replace=False).tolist()) | {0, call.T - 1})
+    check_call(call, dev, rows_subset=rows, tag=f"S={S} q_len={q_len}")
+
+
 def _multi_phase_prefill_call():
     # 8 prefill segments of 512 rows over 16384 keys each: 16 (segment, KV head) groups whose
     # units re-read 8 MB of K/V each, so the tile line is cut into several phases

@@ -79,6 +79,11 @@ struct SchedHdr {
   int64_t status;     // OR of the status bits of this call
   int64_t nphase[3];  // phases per route
   int64_t phase_base[3][kMaxPhases + 1];  // start of each phase on the line; [nphase] = tiles
+  // Phases of short, even units take one whole unit per CTA ("aligned": CTA g of the phase
+  // works on its unit u0 + g alone, so no unit is cut and no partial slot is written; the
+  // scheduler's phase_is_aligned decides); phase_unit0[p] = the phase's first unit.
+  int64_t aligned[3];  // bit p: phase p is aligned
+  int64_t phase_unit0[3][kMaxPhases + 1];
   // Non-zero when the combine pass has rows to write: rows no live segment covers, units
   // with no keys, or units split over several CTAs.
   int64_t combine_work;
@@ -294,6 +299,7 @@ struct PieceWalk {
   int64_t U;        // units of the route
   int64_t pb0, pb1; // phase 0's tile range, and this CTA's first unit in it (loaded early)
   int32_t fu0;
+  int64_t amask;    // the route's aligned phases (bit p)
 };
 
 // a / b for a >= 0, b > 0: one 32-bit division when both fit in 32 bits (the usual case).
@@ -397,6 +403,7 @@ __device__ inline void walk_begin(PieceWalk& w, const Workspace& W, int route) {
   w.pb0 = h->phase_base[route][0];
   w.pb1 = h->phase_base[route][1];
   w.fu0 = W.first_unit[route][blockIdx.x];
+  w.amask = h->aligned[route];
   w.p = -1;
   w.t0 = w.t1 = 0;
   w.u = 0;
@@ -409,6 +416,17 @@ __device__ inline bool walk_phase(PieceWalk& w) {
     const int64_t b0 = w.p == 0 ? w.pb0 : h->phase_base[w.route][w.p];
     const int64_t Wp = (w.p == 0 ? w.pb1 : h->phase_base[w.route][w.p + 1]) - b0;
     if (Wp <= 0) continue;
+    if ((w.amask >> w.p) & 1) {
+      // one whole unit per CTA: its span, and the walk starts at it
+      const int64_t u = h->phase_unit0[w.route][w.p] + blockIdx.x;
+      if (u >= h->phase_unit0[w.route][w.p + 1]) continue;
+      const UnitRec& r = w.W->units[w.route][u];
+      if (r.ntiles == 0) continue;
+      w.t0 = r.tile_base;
+      w.t1 = r.tile_base + lead_cost(w.route) + (int64_t)r.ntiles * tile_cost(w.route, r.rows);
+      w.u = u;
+      return true;
+    }
     const int64_t Gp = phase_ctas(w.G, Wp, w.route);
     if ((int64_t)blockIdx.x >= Gp) continue;
     w.t0 = b0 + sk_start(blockIdx.x, Wp, Gp);

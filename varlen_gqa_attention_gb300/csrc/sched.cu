@@ -235,11 +235,32 @@ __device__ __forceinline__ UnitRec make_unit(const SchedArgs& A, int s, const Se
 // (nslots is exact).  Records the CTAs whose share starts inside the unit's span in the
 // per-CTA start table.  pb: the route's phase bases.  Returns the unit's partial rows (its
 // slots, when several CTAs share it).
+// Whether phase p of route q takes one whole unit per CTA: its units (pu0[p], pu0[p+1]) are
+// at most the CTAs, and the longest (pmax, in line units) costs no more than an even
+// stream-K share of the phase (W_p / G) plus what cutting units costs: partial slots written
+// by the attention kernel and merged by the combine pass, about 12 prefill tiles (~8 us) on the
+// prefill route and 8 units (2 small tiles) on the split-K route, whose merges overlap its
+// tail.  Short, even units (a windowed prefill of many row blocks) then avoid the merges;
+// long ones (a 131072-key prefill) keep the stream-K split, which leaves no CTA idle.
+__device__ __forceinline__ bool phase_is_aligned(const int64_t* pb, const int64_t* pu0, const int32_t* pmax,
+                                                 int p, int64_t G, int q) {
+  const int64_t Up = pu0[p + 1] - pu0[p], Wp = pb[p + 1] - pb[p];
+  const int64_t M = q == kRouteSplitk ? 8 : 12;
+  return Up > 0 && Up <= G && (int64_t)pmax[p] * G <= Wp + M * G;
+}
+
 __device__ __forceinline__ int64_t place_unit(const SchedArgs& A, UnitRec& ur, int q, int64_t uq,
-                                              const int64_t* pb) {
+                                              const int64_t* pb, const int64_t* pu0, bool aligned) {
   const int64_t nt = ur.ntiles;
   if (nt <= 0) return 0;
   const int64_t G = A.grid[q];
+  if (aligned) {  // CTA g of the phase takes its unit g whole and writes `out` itself
+    const int64_t g = uq - pu0[ur.phase];
+    ur.g_first = (int32_t)g;
+    ur.nslots = 1;
+    A.ws.first_unit[q][ur.phase * G + g] = (int32_t)uq;
+    return 0;
+  }
   const int64_t tw = tile_cost(q, ur.rows);
   const int64_t b0 = pb[ur.phase];
   const int64_t Wp = pb[ur.phase + 1] - b0;
@@ -274,6 +295,8 @@ __global__ void __launch_bounds__(kSchedThreads) sdpa_sched_kernel(SchedArgs A) 
   __shared__ int64_t sh[4 * 32];
   __shared__ float s_fsum[32];
   __shared__ int64_t s_pb[3][kMaxPhases + 1];
+  __shared__ int64_t s_pu0[3][kMaxPhases + 1];  // first unit of each phase; [np] = units
+  __shared__ int32_t s_pmax[3][kMaxPhases];      // longest unit span of each phase
   __shared__ int64_t s_U[3], s_np[3];
   __shared__ int32_t s_status, s_work;
   int4* c_seg = reinterpret_cast<int4*>(smem);      // (q_start, q_len, col, kv_end)
@@ -305,6 +328,7 @@ __global__ void __launch_bounds__(kSchedThreads) sdpa_sched_kernel(SchedArgs A) 
       s_status = 0;
       s_work = 0;
     }
+    if (threadIdx.x < 3 * kMaxPhases) (&s_pmax[0][0])[threadIdx.x] = 0;
     __syncthreads();
 
     // 1. validate; clear overlap flags and the row owner map
@@ -502,12 +526,19 @@ __global__ void __launch_bounds__(kSchedThreads) sdpa_sched_kernel(SchedArgs A) 
     }
     __syncthreads();
 
-    // 5. phase bases: phase k of a route starts at the first unit whose phase is >= k
+    // 5. phase bases: phase k of a route starts at the first unit whose phase is >= k; each
+    // phase's longest unit span
     for (int64_t u = ua; u < ub; ++u) {
       const int q = u < U1 ? 1 : 2;
       const int64_t uq = q == 1 ? u : u - U1;
-      const int cp = unit_at(u).phase, pp = uq > 0 ? unit_at(u - 1).phase : -1;
-      for (int k = pp + 1; k <= cp; ++k) s_pb[q][k] = unit_at(u).tile_base;
+      const UnitRec& ur = unit_at(u);
+      const int cp = ur.phase, pp = uq > 0 ? unit_at(u - 1).phase : -1;
+      for (int k = pp + 1; k <= cp; ++k) {
+        s_pb[q][k] = ur.tile_base;
+        s_pu0[q][k] = uq;
+      }
+      if (ur.ntiles > 0)
+        atomicMax(&s_pmax[q][cp], (int32_t)(ur.ntiles * tile_cost(q, ur.rows) + lead_cost(q)));
     }
     if (threadIdx.x < 2) {
       const int q = 1 + threadIdx.x;
@@ -515,7 +546,9 @@ __global__ void __launch_bounds__(kSchedThreads) sdpa_sched_kernel(SchedArgs A) 
       const int64_t np = Uq > 0 ? unit_at(q == 1 ? Uq - 1 : U1 + Uq - 1).phase + 1 : 0;
       s_np[q] = np;
       s_pb[q][0] = 0;
+      s_pu0[q][0] = 0;
       s_pb[q][np] = q == 1 ? tot4[0] : tot4[1];
+      s_pu0[q][np] = Uq;
     }
     __syncthreads();
 
@@ -525,7 +558,8 @@ __global__ void __launch_bounds__(kSchedThreads) sdpa_sched_kernel(SchedArgs A) 
       const int q = u < U1 ? 1 : 2;
       const int64_t uq = q == 1 ? u : u - U1;
       UnitRec& ur = unit_at(u);
-      const int64_t pr = place_unit(A, ur, q, uq, s_pb[q]);
+      const int64_t pr = place_unit(A, ur, q, uq, s_pb[q], s_pu0[q],
+                                    phase_is_aligned(s_pb[q], s_pu0[q], s_pmax[q], ur.phase, A.grid[q], q));
       if (ur.nslots > 1) s_work = 1;  // split units the combine pass merges
       (q == 1 ? p1 : p2) += pr;
     }
@@ -592,10 +626,18 @@ __global__ void __launch_bounds__(kSchedThreads) sdpa_sched_kernel(SchedArgs A) 
   }
   for (int i = threadIdx.x; i < 2 * (kMaxPhases + 1); i += blockDim.x) {
     const int q = 1 + i / (kMaxPhases + 1), k = i % (kMaxPhases + 1);
-    if (k <= s_np[q]) W.hdr->phase_base[q][k] = s_pb[q][k];
+    if (k <= s_np[q]) {
+      W.hdr->phase_base[q][k] = s_pb[q][k];
+      W.hdr->phase_unit0[q][k] = s_pu0[q][k];
+
+    }
   }
   if (threadIdx.x < 2) {
     const int q = 1 + threadIdx.x;
+    int64_t am = 0;
+    for (int k = 0; k < s_np[q]; ++k)
+      if (phase_is_aligned(s_pb[q], s_pu0[q], s_pmax[q], k, A.grid[q], q)) am |= (int64_t)1 << k;
+    W.hdr->aligned[q] = am;
     W.hdr->tiles[q] = s_pb[q][s_np[q]];
     W.hdr->units[q] = s_U[q];
     W.hdr->grid[q] = A.grid[q];
@@ -629,6 +671,8 @@ __global__ void __launch_bounds__(kSchedThreads) sdpa_sched_small_kernel(SchedAr
   __shared__ int2 c_ub[kSmallSegs];    // unit bases on routes 1 and 2
   __shared__ int64_t sh[3 * 32];
   __shared__ int64_t s_pb[3][kMaxPhases + 1];
+  __shared__ int64_t s_pu0[3][kMaxPhases + 1];  // first unit of each phase; [np] = units
+  __shared__ int32_t s_pmax[3][kMaxPhases];      // longest unit span of each phase
   __shared__ int32_t s_U[3], s_np[3], s_status, s_work;
   const Workspace& W = A.ws;
   const int S = A.S;
@@ -707,6 +751,7 @@ __global__ void __launch_bounds__(kSchedThreads) sdpa_sched_small_kernel(SchedAr
     }
   } else {
     griddep_launch();
+    if (threadIdx.x - 32 < 3 * kMaxPhases) (&s_pmax[0][0])[threadIdx.x - 32] = 0;
     for (int t = threadIdx.x - 32; t < T; t += blockDim.x - 32) W.row_info[t] = make_int4(kRouteNone, 0, 0, 0);
   }
   __syncthreads();  // (also orders the row records above before the ones below)
@@ -757,23 +802,33 @@ __global__ void __launch_bounds__(kSchedThreads) sdpa_sched_small_kernel(SchedAr
     const int64_t tb = v[0], bb = v[1];
     ur.tile_base = tb;
     ur.phase = phase_of(bb, kPhases - 1);
-    if (uq == 0) s_pb[q][0] = 0;
+    atomicMax(&s_pmax[q][ur.phase], (int32_t)span);
+    if (uq == 0) {
+      s_pb[q][0] = 0;
+      s_pu0[q][0] = 0;
+    }
     if (uq + 1 < (q == 1 ? U1 : U2)) {
       const int pn = phase_of(bb + reuse, kPhases - 1);
-      for (int k = ur.phase + 1; k <= pn; ++k) s_pb[q][k] = tb + span;
+      for (int k = ur.phase + 1; k <= pn; ++k) {
+        s_pb[q][k] = tb + span;
+        s_pu0[q][k] = uq + 1;
+      }
     } else {
       s_np[q] = ur.phase + 1;
       s_pb[q][ur.phase + 1] = tot[0];
+      s_pu0[q][ur.phase + 1] = uq + 1;
     }
   }
   if (i < 2 && s_U[1 + i] == 0) {
     s_np[1 + i] = 0;
     s_pb[1 + i][0] = 0;
+    s_pu0[1 + i][0] = 0;
   }
   __syncthreads();
   int64_t pv[1] = {0}, ptot[1];
   if (q != 0) {
-    pv[0] = place_unit(A, ur, q, uq, s_pb[q]);
+    pv[0] = place_unit(A, ur, q, uq, s_pb[q], s_pu0[q],
+                       phase_is_aligned(s_pb[q], s_pu0[q], s_pmax[q], ur.phase, A.grid[q], q));
     if (ur.nslots > 1) s_work = 1;  // split units the combine pass merges
   }
   route_scan<1>(pv, ptot, sh + 2 * 32, wroute);  // (its barrier also publishes s_work)
@@ -785,10 +840,18 @@ __global__ void __launch_bounds__(kSchedThreads) sdpa_sched_small_kernel(SchedAr
   // the header
   if (i < 2 * (kMaxPhases + 1)) {
     const int hq = 1 + i / (kMaxPhases + 1), k = i % (kMaxPhases + 1);
-    if (k <= s_np[hq]) W.hdr->phase_base[hq][k] = s_pb[hq][k];
+    if (k <= s_np[hq]) {
+      W.hdr->phase_base[hq][k] = s_pb[hq][k];
+      W.hdr->phase_unit0[hq][k] = s_pu0[hq][k];
+
+    }
   }
   if (i < 2) {
     const int hq = 1 + i;
+    int64_t am = 0;
+    for (int k = 0; k < s_np[hq]; ++k)
+      if (phase_is_aligned(s_pb[hq], s_pu0[hq], s_pmax[hq], k, A.grid[hq], hq)) am |= (int64_t)1 << k;
+    W.hdr->aligned[hq] = am;
     W.hdr->tiles[hq] = s_pb[hq][s_np[hq]];
     W.hdr->units[hq] = s_U[hq];
     W.hdr->grid[hq] = A.grid[hq];

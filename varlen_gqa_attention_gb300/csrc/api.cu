@@ -278,7 +278,7 @@ static sdpa_status launch_all(const SchedArgs& sa, const AttnArgs& aa, int D, co
   if (e == cudaSuccess && aa.T > 0) {
     void* args[] = {(void*)&aa};
     const int64_t warps = aa.T * aa.Hq;
-    const int64_t blocks = (warps * 32 + 255) / 256;
+    const int64_t blocks = std::min<int64_t>((warps * 32 + 255) / 256, 8 * (int64_t)g.prefill);
     e = launch_k(combine_kernel_ptr(D), (unsigned)blocks, 256, args, 0, st, true);
     if (e != cudaSuccess) return fail(SDPA_ERR_CUDA, "combine launch: %s", cudaGetErrorString(e));
   }

@@ -40,22 +40,15 @@ __device__ __forceinline__ bool wait_done(const int32_t* count, int32_t n) {
   }
 }
 
+// One warp: packed row t, query head h (gw = t * Hq + h).
 template <int D>
-__global__ void __launch_bounds__(kCombineThreads) sdpa_combine_kernel(AttnArgs A) {
+__device__ __forceinline__ void combine_row(const AttnArgs& A, int64_t gw, int lane, int64_t U1, int64_t U2) {
   constexpr int PER = D / 32;  // elements per lane
-  const int64_t gw = ((int64_t)blockIdx.x * kCombineThreads + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (gw >= A.T * A.Hq) return;
   const int64_t t = gw / A.Hq;
   const int h = (int)(gw % A.Hq);
   __nv_bfloat16* dst = A.out + t * A.o_rs + (int64_t)h * A.o_hs + lane * PER;
   const Workspace& W = A.ws;
-  // independent loads, issued together: whether there is work, the row's owner and the
-  // routes' unit counts
-  const int64_t work = W.hdr->combine_work;
   const int4 ri = W.row_info[t];
-  const int64_t U1 = W.hdr->units[kRouteSplitk], U2 = W.hdr->units[kRoutePrefill];
-  if (!work) return;
 
   bool zero = true;
   const int q = ri.x;
@@ -137,6 +130,22 @@ __global__ void __launch_bounds__(kCombineThreads) sdpa_combine_kernel(AttnArgs 
 #pragma unroll
     for (int k = 0; k < PER; k += 2) *reinterpret_cast<uint32_t*>(dst + k) = 0u;
   }
+}
+
+// A grid of at most 8 CTAs per SM (a full SM's worth of warps) walks the (row, head) pairs,
+// so that a call with many rows and nothing to merge does not pay for launching a CTA per 8
+// pairs.
+template <int D>
+__global__ void __launch_bounds__(kCombineThreads) sdpa_combine_kernel(AttnArgs A) {
+  const Workspace& W = A.ws;
+  // independent loads, issued together: whether there is work and the routes' unit counts
+  const int64_t work = W.hdr->combine_work;
+  const int64_t U1 = W.hdr->units[kRouteSplitk], U2 = W.hdr->units[kRoutePrefill];
+  if (!work) return;
+  const int lane = threadIdx.x & 31;
+  const int64_t n = A.T * A.Hq, stride = (int64_t)gridDim.x * (kCombineThreads / 32);
+  for (int64_t gw = ((int64_t)blockIdx.x * kCombineThreads + threadIdx.x) >> 5; gw < n; gw += stride)
+    combine_row<D>(A, gw, lane, U1, U2);
 }
 
 template __global__ void sdpa_combine_kernel<64>(AttnArgs);

@@ -173,7 +173,7 @@ extern "C" sdpa_status sdpa_varlen_splitk_static(
   }
   if (e == cudaSuccess && T > 0) {
     void* args[] = {(void*)&aa};
-    const int64_t blocks = (T * Hq * 32 + 255) / 256;
+    const int64_t blocks = std::min<int64_t>((T * Hq * 32 + 255) / 256, 8 * (int64_t)sd.sms);
     e = cudaLaunchKernel(combine_kernel_ptr(D), dim3((unsigned)blocks), dim3(256), args, 0, s);
   }
   if (e != cudaSuccess) {

@@ -85,17 +85,17 @@ KERNEL_SOURCES = {
 # when it was taken.  A kernel whose sources hash differently now reports traffic null until
 # the capture is repeated.
 NCU_TRAFFIC = {
-    "prefill_d128": (1237094656 + 65428480, "prefill", "fa5647a7b80fc120"),  # sdpa_prefill_pair_kernel<128>
-    "prefill_d64": (9902080 + 512, "prefill", "fa5647a7b80fc120"),  # sdpa_prefill_pair_kernel<64>
-    "prefill_d256": (334974464 + 46728192, "prefill", "fa5647a7b80fc120"),  # sdpa_prefill_kernel<256>
-    "ring_prefill": (15016704 + 176128, "prefill", "fa5647a7b80fc120"),  # sdpa_prefill_pair_kernel<128>
-    "tiny": (158976 + 0, "splitk", "b2ea96bb9d5f324b"),  # sdpa_splitk_kernel<64> (tiny calls take the split-K route)
-    "decode": (141723136 + 3245568, "splitk", "b2ea96bb9d5f324b"),  # sdpa_splitk_kernel<128>
-    "decode_append": (141721856 + 3546880, "splitk", "b2ea96bb9d5f324b"),
-    "mixed": (285227776 + 10821888, "splitk", "b2ea96bb9d5f324b"),  # both calls
-    "mixed_modes": (219486464 + 8172800, "splitk", "b2ea96bb9d5f324b"),
+    "prefill_d128": (1207549440 + 65541888, "prefill", "f575124805b4cbdc"),  # sdpa_prefill_pair_kernel<128>
+    "prefill_d64": (9903616 + 512, "prefill", "f575124805b4cbdc"),  # sdpa_prefill_pair_kernel<64>
+    "prefill_d256": (334566912 + 47162368, "prefill", "f575124805b4cbdc"),  # sdpa_prefill_kernel<256>
+    "ring_prefill": (14966016 + 0, "prefill", "f575124805b4cbdc"),  # sdpa_prefill_pair_kernel<128>
+    "tiny": (159744 + 0, "splitk", "2caeca622bd8363d"),  # sdpa_splitk_kernel<64> (tiny calls take the split-K route)
+    "decode": (141723648 + 3188224, "splitk", "2caeca622bd8363d"),  # sdpa_splitk_kernel<128>
+    "decode_append": (141728000 + 3187456, "splitk", "2caeca622bd8363d"),
+    "mixed": (285199872 + 11369472, "splitk", "2caeca622bd8363d"),  # both calls
+    "mixed_modes": (220047104 + 8420096, "splitk", "2caeca622bd8363d"),
     # sdpa_clone_kernel: writes still dirty in L2 when the kernel ends are not counted
-    "seq_clone": (134238720 + 84515072, "clone", "429f90f2e11ceea7"),
+    "seq_clone": (134241280 + 84925696, "clone", "c9b82a90a0e5fff4"),
 }
 
 

@@ -75,8 +75,9 @@ CSRC = os.path.join(ROOT, "varlen_gqa_attention_gb300", "csrc")
 # the sources each kernel is built from (their hash ties a traffic figure to the code it was
 # measured on)
 KERNEL_SOURCES = {
-    "prefill": ["prefill.cu", "prefill_pair.cu", "tc.cuh", "common.cuh"],
-    "splitk": ["splitk.cu", "common.cuh"],
+    # the scheduler decides what the attention kernels read and write (pieces, partial slots)
+    "prefill": ["prefill.cu", "prefill_pair.cu", "tc.cuh", "common.cuh", "sched.cu"],
+    "splitk": ["splitk.cu", "common.cuh", "sched.cu"],
     "clone": ["append.cu", "common.cuh"],
 }
 # DRAM bytes (read + write) of the dominant kernel per step, from one ncu capture of the same
@@ -85,15 +86,15 @@ KERNEL_SOURCES = {
 # when it was taken.  A kernel whose sources hash differently now reports traffic null until
 # the capture is repeated.
 NCU_TRAFFIC = {
-    "prefill_d128": (1207549440 + 65541888, "prefill", "f575124805b4cbdc"),  # sdpa_prefill_pair_kernel<128>
-    "prefill_d64": (9903616 + 512, "prefill", "f575124805b4cbdc"),  # sdpa_prefill_pair_kernel<64>
-    "prefill_d256": (334566912 + 47162368, "prefill", "f575124805b4cbdc"),  # sdpa_prefill_kernel<256>
-    "ring_prefill": (14966016 + 0, "prefill", "f575124805b4cbdc"),  # sdpa_prefill_pair_kernel<128>
-    "tiny": (159744 + 0, "splitk", "2caeca622bd8363d"),  # sdpa_splitk_kernel<64> (tiny calls take the split-K route)
-    "decode": (141723648 + 3188224, "splitk", "2caeca622bd8363d"),  # sdpa_splitk_kernel<128>
-    "decode_append": (141728000 + 3187456, "splitk", "2caeca622bd8363d"),
-    "mixed": (285199872 + 11369472, "splitk", "2caeca622bd8363d"),  # both calls
-    "mixed_modes": (220047104 + 8420096, "splitk", "2caeca622bd8363d"),
+    "prefill_d128": (1207549440 + 65541888, "prefill", "91780631a32d4b44"),  # sdpa_prefill_pair_kernel<128>
+    "prefill_d64": (9903616 + 512, "prefill", "91780631a32d4b44"),  # sdpa_prefill_pair_kernel<64>
+    "prefill_d256": (334566912 + 47162368, "prefill", "91780631a32d4b44"),  # sdpa_prefill_kernel<256>
+    "ring_prefill": (14966016 + 0, "prefill", "91780631a32d4b44"),  # sdpa_prefill_pair_kernel<128>
+    "tiny": (159744 + 0, "splitk", "e448effc74ee4957"),  # sdpa_splitk_kernel<64> (tiny calls take the split-K route)
+    "decode": (141723648 + 3188224, "splitk", "e448effc74ee4957"),  # sdpa_splitk_kernel<128>
+    "decode_append": (141728000 + 3187456, "splitk", "e448effc74ee4957"),
+    "mixed": (285199872 + 11369472, "splitk", "e448effc74ee4957"),  # both calls
+    "mixed_modes": (220047104 + 8420096, "splitk", "e448effc74ee4957"),
     # sdpa_clone_kernel: writes still dirty in L2 when the kernel ends are not counted
     "seq_clone": (134241280 + 84925696, "clone", "c9b82a90a0e5fff4"),
 }

@@ -629,7 +629,6 @@ __global__ void __launch_bounds__(kSchedThreads) sdpa_sched_kernel(SchedArgs A) 
     if (k <= s_np[q]) {
       W.hdr->phase_base[q][k] = s_pb[q][k];
       W.hdr->phase_unit0[q][k] = s_pu0[q][k];
-
     }
   }
   if (threadIdx.x < 2) {
@@ -843,7 +842,6 @@ __global__ void __launch_bounds__(kSchedThreads) sdpa_sched_small_kernel(SchedAr
     if (k <= s_np[hq]) {
       W.hdr->phase_base[hq][k] = s_pb[hq][k];
       W.hdr->phase_unit0[hq][k] = s_pu0[hq][k];
-
     }
   }
   if (i < 2) {

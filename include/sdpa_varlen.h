@@ -66,7 +66,9 @@ typedef enum sdpa_status {
 #define SDPA_DEV_TIMEOUT 32   /* a bounded device wait gave up; the output is unspecified */
 
 /* Route policy (process-wide).  AUTO sends segments with q_len * (Hq / Hkv) >= 128 to the
- * tensor-memory prefill kernel and the rest to the split-K kernel; the other two force
+ * tensor-memory prefill kernel when the call's such segments hold at least 2^30 of work
+ * (sum of packed rows * needed key span, times Hkv * D: below it that kernel's fixed cost
+ * outweighs its speed), and everything else to the split-K kernel; the other two force
  * every segment onto one kernel (used to compare the kernels against each other). */
 #define SDPA_ROUTE_AUTO 0
 #define SDPA_ROUTE_SPLITK 1
